@@ -1,0 +1,680 @@
+/*
+ * dsv4_oracle.c -- plain, slow CPU reference for DeepSeek-V4 compressed sparse
+ * attention at decode.  TEST INFRASTRUCTURE ONLY (see dsv4_oracle.h): the
+ * product path never includes, links or calls it.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no -ffast-math).
+ * -ffp-contract=off matters: without it gcc on aarch64 fuses a*b+c and the fp32
+ * operation sequence the cache bytes are defined by would change.
+ *
+ * Every function states the passage it follows.  Readings of passages that are
+ * silent or ambiguous are marked "Reading:".
+ */
+#include "dsv4_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ========================================================================= */
+/* Number formats                                                            */
+/* ========================================================================= */
+
+/* bf16 is the top half of an IEEE binary32; widening is exact. */
+float or_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to the nearest bf16, ties to even (the usual IEEE rule).
+ * [vLLM-classes] "CSA layer Compressor": the RoPE half of a cache entry is
+ * stored as bfloat16. */
+uint16_t or_f32_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)            /* NaN stays NaN (quiet) */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16;
+    uint32_t rest = u & 0xffffu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1u;                                   /* may carry into inf: correct */
+    return (uint16_t)keep;
+}
+
+/* OCP FP8 E4M3 ("e4m3fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, largest finite 448.  Normal codes are
+ * (1 + m/8) * 2^(e-7); exponent field 0 gives the subnormals m * 2^-9.
+ * [vLLM-classes] "CSA layer Compressor": the NoPE part is stored as FP8 E4M3. */
+double or_e4m3_to_f64(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + (double)m, e - 10);
+    return s ? -v : v;
+}
+
+/* Encode to E4M3: the nearest of the 127 non-negative finite codes, ties to
+ * the even code, magnitudes past 448 saturate to 448 ("satfinite").  The
+ * positive codes 0x00..0x7e increase monotonically in value, so the two
+ * candidates are found by bisection: lo = the largest code not above |x|,
+ * hi = lo + 1. */
+uint8_t or_f32_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e);
+    int lo = 0, hi = 0x7e;               /* invariant: value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (or_e4m3_to_f64((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double dlo = a - or_e4m3_to_f64((uint8_t)lo);
+    double dhi = or_e4m3_to_f64((uint8_t)hi) - a;
+    int best = (dlo < dhi) ? lo : (dhi < dlo) ? hi : ((lo & 1) == 0 ? lo : hi);
+    return (uint8_t)(sign | best);
+}
+
+void or_f32_to_e4m3_n(long long n, const float* x, uint8_t* out)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = or_f32_to_e4m3(x[i]);
+}
+
+void or_f32_to_bf16_n(long long n, const float* x, uint16_t* out)
+{
+    for (long long i = 0; i < n; ++i)
+        out[i] = or_f32_to_bf16(x[i]);
+}
+
+/* UE8M0 block scale: an unsigned power-of-two exponent stored as e + 127.
+ * [vLLM-classes] "CSA layer Compressor" (cache block layout: UE8M0 scales) and
+ * [MLA-to-CSA] 6.2 (UE8M0 FP8 quantisation).
+ * Reading: the pages do not say how e is chosen.  We take the smallest power
+ * of two that keeps the block's largest magnitude within E4M3's 448, so no
+ * value saturates; e is clamped to [-127, 127] (the byte then lies in 0..254,
+ * 255 being the format's NaN).  An all-zero block takes e = 0. */
+int or_ue8m0_exponent(float amax)
+{
+    if (!(amax > 0.0f))
+        return 0;
+    int e = -127;
+    while (e < 127 && (double)amax > 448.0 * ldexp(1.0, e))
+        ++e;
+    return e;
+}
+
+/* The compressor's exponential, fp32 in, fp32 out, with every operation an
+ * IEEE-rounded fp32 add or multiply (no fused multiply-add):
+ *   Cody & Waite argument reduction (W. J. Cody, W. Waite, "Software Manual
+ *   for the Elementary Functions", 1980): n = rint(x / ln2),
+ *   r = (x - n*LN2_HI) - n*LN2_LO with LN2_HI = ln2 cut to 16 significant bits
+ *   (so n*LN2_HI is exact for |n| < 256) and LN2_LO = fp32(ln2 - LN2_HI);
+ *   then e^r by its Taylor series to degree 7 in Horner form (|r| <= ln2/2,
+ *   truncation error < 6e-9 relative), and the result scaled by 2^n.
+ * Inputs below -87 return 0 (e^-87 is at the bottom of the normal range);
+ * the compressor only evaluates it at score - max <= 0.
+ * Reading: the pages fix a softmax over the window but not how exp is
+ * evaluated; this definition is used so the FP8 bytes are defined exactly. */
+float or_expf(float x)
+{
+    const float LOG2E = 1.44269504088896340736f;
+    const float LN2_HI = 0.693145751953125f;          /* 45426 / 65536 */
+    const float LN2_LO = 1.42860682030941723212e-6f;  /* ln2 - LN2_HI */
+    const float C[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f,
+                        1.0f / 720.0f, 1.0f / 5040.0f};
+    if (x < -87.0f)
+        return 0.0f;
+    if (x > 88.0f)
+        x = 88.0f;
+    float t = x * LOG2E;
+    float n = rintf(t);
+    float nh = n * LN2_HI;
+    float nl = n * LN2_LO;
+    float r = x - nh;
+    r = r - nl;
+    float p = C[7];
+    for (int k = 6; k >= 0; --k) {
+        float rp = r * p;
+        p = C[k] + rp;
+    }
+    int ni = (int)n;                      /* in [-126, 127] */
+    uint32_t bits = (uint32_t)(ni + 127) << 23;
+    float two_n;
+    memcpy(&two_n, &bits, sizeof two_n);
+    return p * two_n;
+}
+
+/* ========================================================================= */
+/* Layer type and IndexCache schedule                                        */
+/* ========================================================================= */
+
+/* [vLLM-V4-attn] "compress_ratio: the three layer types": every layer reads
+ * compress_ratios[layer], takes max(1, r); <= 1 is swaonly, 4 is c4a (overlap
+ * compressor + indexer), 128 is c128a (compressor, top-k from metadata).  The
+ * compressor asserts ratio in {4, 128}, so any other ratio is unsupported. */
+int or_layer_type(int compress_ratio)
+{
+    int r = compress_ratio < 1 ? 1 : compress_ratio;
+    if (r == 1 || r == 4 || r == 128)
+        return r;
+    return -1;
+}
+
+/* [IndexCache] section 2: for a c4 layer, indexer_seq_idx = number of c4
+ * layers before it; skip_topk = indexer_seq_idx % freq != 0, only when
+ * use_index_cache is on.  A pattern string, when given, takes precedence: its
+ * first character must be 'F'; 'S' at the corresponding position means reuse;
+ * layers past the end of the string compute.
+ * Reading: "corresponding position" is the layer's indexer_seq_idx (its rank
+ * among c4 layers), the same counter the frequency rule uses.
+ * Returns 0, or -1 for an invalid frequency or pattern. */
+int or_index_schedule(const int* ratios, int n_layers, int use_index_cache, int freq,
+                      const char* pattern, uint8_t* skip_topk)
+{
+    if (n_layers < 0)
+        return -1;
+    if (pattern) {
+        if (pattern[0] != 'F')
+            return -1;
+        for (const char* c = pattern; *c; ++c)
+            if (*c != 'F' && *c != 'S')
+                return -1;
+    } else if (use_index_cache && freq < 1) {
+        return -1;
+    }
+    int plen = pattern ? (int)strlen(pattern) : 0;
+    int seq_idx = 0;
+    for (int l = 0; l < n_layers; ++l) {
+        int r = ratios[l] < 1 ? 1 : ratios[l];
+        skip_topk[l] = 0;
+        if (r == 4) {
+            if (use_index_cache) {
+                if (pattern)
+                    skip_topk[l] = (seq_idx < plen && pattern[seq_idx] == 'S') ? 1 : 0;
+                else
+                    skip_topk[l] = (seq_idx % freq != 0) ? 1 : 0;
+            }
+            ++seq_idx;
+        }
+    }
+    return 0;
+}
+
+/* ========================================================================= */
+/* Cache byte accounting                                                     */
+/* ========================================================================= */
+
+/* [MLA-to-CSA] 5.5 (SWA cache format): nope fp8 bytes + rope bf16 bytes +
+ * nope/64 UE8M0 scale bytes padded to 8 (448 + 128 + 7 + 1 = 584).  With the
+ * 512-latent geometry the same rule gives 512 + 128 + 8 = 648. */
+int or_mla_entry_bytes(int nope_dim, int rope_dim)
+{
+    int scale_bytes = (nope_dim / 64 + 7) / 8 * 8;
+    return nope_dim + 2 * rope_dim + scale_bytes;
+}
+
+/* [vLLM-classes] DeepseekV4Indexer: head_dim + head_dim // quant_block * 4
+ * bytes, quant_block = 128: 128 fp8 + one fp32 scale = 132. */
+int or_idx_entry_bytes(int head_dim) { return head_dim + head_dim / 128 * 4; }
+
+/* ========================================================================= */
+/* RoPE table                                                                */
+/* ========================================================================= */
+
+/* [vLLM-classes] DeepseekCompressor.forward comment: cos_sin_cache is
+ * [max_pos, rope_head_dim], first half cos, second half sin, one value per
+ * rotated pair.  Angle of pair i at position pos: pos * theta^(-2i/rope_dim).
+ * Built in double and rounded once to fp32. */
+void or_rope_table(int max_pos, int rope_dim, double theta, float* out)
+{
+    int half = rope_dim / 2;
+    for (int pos = 0; pos < max_pos; ++pos) {
+        for (int i = 0; i < half; ++i) {
+            double freq = pow(theta, -2.0 * (double)i / (double)rope_dim);
+            double ang = (double)pos * freq;
+            out[(long long)pos * rope_dim + i] = (float)cos(ang);
+            out[(long long)pos * rope_dim + half + i] = (float)sin(ang);
+        }
+    }
+}
+
+/* ========================================================================= */
+/* Compressor                                                                */
+/* ========================================================================= */
+
+/* Pooled (pre-norm) vector of the compressed entry emitted at boundary token p
+ * of one sequence.
+ *
+ * kv_score holds, for positions 0..p of the sequence, the bf16 projection row
+ * [kv block 0 | kv block 1 | score block 0 | score block 1] (coff blocks of d
+ * each; [vLLM-classes] "CSA layer Compressor": "kv block0, kv block1, score
+ * block0, score block1").  ape is [ratio][coff*d] fp32.
+ *
+ * Steps, following [vLLM-classes] DeepseekCompressor / save_partial_states and
+ * "CSA layer Compressor", [vLLM-V4-attn] "Compressor: ratio 4 vs 128" and
+ * [MLA-to-CSA] 5.1 / 5.2:
+ *  - ratio 4 uses overlap (coff = 2): the window is the 8 tokens p-7..p; the
+ *    old group p-7..p-4 contributes its block 0 (a), the new group p-3..p its
+ *    block 1 (b) (the C_Comp formula's [Z_a + B_a; Z_b + B_b] stacking and the
+ *    pos=3 / pos=7 table).  Ratio 128 has coff = 1: the window is the 128
+ *    tokens p-127..p, block 0.
+ *  - Tokens at negative positions are left out (pos >= 0 mask at the first
+ *    boundary).
+ *  - state values: kv = bf16 -> fp32 (exact); score = fp32(bf16 score +
+ *    ape[t % ratio]) -- the APE addition fused into the state save.
+ *  - per channel c, softmax over the window rows of the score, weights applied
+ *    to the kv rows and summed ("Softmax_row(...)^T (.) C").
+ * Reading: the softmax runs per channel across the window tokens.  fp32 ops
+ * in this order: m = max score; e_t = or_expf(score_t - m); num += e_t * kv_t;
+ * den += e_t (ascending t, each op rounded); y = num / den.
+ * Returns 0, or -1 if p is not a boundary ((p + 1) % ratio != 0). */
+int or_compress_pool(int ratio, int d, const uint16_t* kv_score, long long row_stride,
+                     const float* ape, int p, float* y)
+{
+    if (ratio != 4 && ratio != 128)
+        return -1;
+    if ((p + 1) % ratio != 0)
+        return -1;
+    int coff = (ratio == 4) ? 2 : 1;
+    int win = coff * ratio;
+    for (int c = 0; c < d; ++c) {
+        float sc[128], kv[128];
+        int n = 0;
+        for (int t = p - win + 1; t <= p; ++t) {
+            if (t < 0)
+                continue;
+            int blk = (coff == 2 && t <= p - ratio) ? 0 : coff - 1;
+            const uint16_t* row = kv_score + (long long)t * row_stride;
+            float kvv = or_bf16_to_f32(row[blk * d + c]);
+            float s = or_bf16_to_f32(row[coff * d + blk * d + c]);
+            float a = ape[(long long)(t % ratio) * coff * d + blk * d + c];
+            sc[n] = s + a;
+            kv[n] = kvv;
+            ++n;
+        }
+        float m = sc[0];
+        for (int i = 1; i < n; ++i)
+            if (sc[i] > m)
+                m = sc[i];
+        float num = 0.0f, den = 0.0f;
+        for (int i = 0; i < n; ++i) {
+            float diff = sc[i] - m;
+            float e = or_expf(diff);
+            float ek = e * kv[i];
+            num = num + ek;
+            den = den + e;
+        }
+        y[c] = num / den;
+    }
+    return 0;
+}
+
+/* RMSNorm over the d channels, weight w ([vLLM-classes] DeepseekCompressor:
+ * self.norm = RMSNorm(head_dim, eps); "compress -> RMSNorm -> RoPE").
+ * Reading (precision): the mean square is accumulated in double and rounded
+ * once to fp32; then inv = 1 / sqrt(ms + eps) and z = (y * inv) * w, each an
+ * IEEE-rounded fp32 operation. */
+void or_rmsnorm(const float* y, int d, const float* w, float eps, float* z)
+{
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c)
+        ss += (double)y[c] * (double)y[c];
+    float ms = (float)(ss / (double)d);
+    float root = sqrtf(ms + eps);
+    float inv = 1.0f / root;
+    for (int c = 0; c < d; ++c) {
+        float t = y[c] * inv;
+        z[c] = t * w[c];
+    }
+}
+
+/* GPT-J style (interleaved pairs, not split-half) forward rotation of the
+ * rope_dim values at x, pair i = (x[2i], x[2i+1]) with cos = row[i],
+ * sin = row[rope_dim/2 + i]  ([vLLM-classes] DeepseekCompressor.forward RoPE
+ * comment).  Each product and the sum/difference are separately rounded. */
+void or_rope_gptj(float* x, int rope_dim, const float* cos_sin_row)
+{
+    int half = rope_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        float x0 = x[2 * i], x1 = x[2 * i + 1];
+        float c = cos_sin_row[i], s = cos_sin_row[half + i];
+        float a = x0 * c, b = x1 * s, e = x0 * s, f = x1 * c;
+        x[2 * i] = a - b;
+        x[2 * i + 1] = e + f;
+    }
+}
+
+/* Main (MLA) cache entry: FP8 E4M3 of the nope dims with one UE8M0 scale per
+ * 64 dims, bf16 RoPE dims ([vLLM-classes] "CSA layer Compressor": nope -> FP8
+ * quant blocks + scale, rope -> bf16; [MLA-to-CSA] 5.5 / 6.2).
+ * data = nope fp8 codes then rope bf16 (little-endian); scales = 8 bytes
+ * (nope/64 used, rest 0).  code = E4M3(z * 2^-e), the scaling exact. */
+void or_quant_mla(const float* z, int nope_dim, int rope_dim, uint8_t* data, uint8_t* scales)
+{
+    memset(scales, 0, 8);
+    for (int b = 0; b < nope_dim / 64; ++b) {
+        float amax = 0.0f;
+        for (int c = 0; c < 64; ++c) {
+            float a = fabsf(z[b * 64 + c]);
+            if (a > amax)
+                amax = a;
+        }
+        int e = or_ue8m0_exponent(amax);
+        float mult = (float)ldexp(1.0, -e);
+        for (int c = 0; c < 64; ++c)
+            data[b * 64 + c] = or_f32_to_e4m3(z[b * 64 + c] * mult);
+        scales[b] = (uint8_t)(e + 127);
+    }
+    for (int i = 0; i < rope_dim; ++i) {
+        uint16_t h = or_f32_to_bf16(z[nope_dim + i]);
+        data[nope_dim + 2 * i] = (uint8_t)(h & 0xff);
+        data[nope_dim + 2 * i + 1] = (uint8_t)(h >> 8);
+    }
+}
+
+/* Indexer cache entry: all d (=128) dims in FP8 E4M3 with one fp32 scale
+ * ([vLLM-classes] DeepseekV4Indexer: "128 fp8 + 4 fp32 scale = 132").
+ * Reading: scale = amax / 448 (IEEE fp32 division; 1 if the row is all zero),
+ * code = E4M3(z / scale). */
+void or_quant_idx(const float* z, int d, uint8_t* data, float* scale)
+{
+    float amax = 0.0f;
+    for (int c = 0; c < d; ++c) {
+        float a = fabsf(z[c]);
+        if (a > amax)
+            amax = a;
+    }
+    float s = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    for (int c = 0; c < d; ++c)
+        data[c] = or_f32_to_e4m3(z[c] / s);
+    *scale = s;
+}
+
+/* Row-batched forms of or_quant_mla / or_quant_idx (n rows of d floats). */
+void or_quant_mla_rows(long long n, const float* z, int nope_dim, int rope_dim, uint8_t* data,
+                       uint8_t* scales)
+{
+    int d = nope_dim + rope_dim, db = nope_dim + 2 * rope_dim;
+    for (long long i = 0; i < n; ++i)
+        or_quant_mla(z + i * d, nope_dim, rope_dim, data + i * db, scales + i * 8);
+}
+
+void or_quant_idx_rows(long long n, const float* z, int d, uint8_t* data, float* scale)
+{
+    for (long long i = 0; i < n; ++i)
+        or_quant_idx(z + i * d, d, data + i * d, scale + i);
+}
+
+/* Run the compressor over positions 0..n_tokens-1 of one sequence and emit
+ * every compressed entry in slot order: slot j at boundary p = ratio*j +
+ * ratio - 1 ([MLA-to-CSA] 6.3: is_valid = (pos + 1) % ratio == 0,
+ * pos_after_compress = pos // ratio).  The pooled vector is RMS-normalised,
+ * its last rope_dim dims rotated at position (p // ratio) * ratio
+ * ([vLLM-V4-attn] "Compressor"; [MLA-to-CSA] 5.1: anchor 4j for slot j) and
+ * quantised.
+ * kind 0 = main cache (d = nope + rope; out_data rows of nope + 2*rope bytes,
+ * out_scale rows of 8 bytes); kind 1 = indexer cache (d = nope + rope, usually
+ * 64 + 64; out_data rows of d bytes, out_scale rows of one fp32).
+ * Returns the number of entries written, or -1. */
+int or_compress_stream(int kind, int ratio, int n_tokens, const uint16_t* kv_score,
+                       long long row_stride, const float* ape, const float* rms_w, float eps,
+                       const float* cos_sin, int rope_dim, int nope_dim,
+                       uint8_t* out_data, uint8_t* out_scale)
+{
+    int d = nope_dim + rope_dim;
+    float* y = (float*)malloc(sizeof(float) * (size_t)d);
+    float* z = (float*)malloc(sizeof(float) * (size_t)d);
+    int n_out = 0;
+    for (int p = 0; p < n_tokens; ++p) {
+        if ((p + 1) % ratio != 0)
+            continue;
+        if (or_compress_pool(ratio, d, kv_score, row_stride, ape, p, y) != 0) {
+            n_out = -1;
+            break;
+        }
+        or_rmsnorm(y, d, rms_w, eps, z);
+        int rope_pos = (p / ratio) * ratio;
+        or_rope_gptj(z + nope_dim, rope_dim, cos_sin + (long long)rope_pos * rope_dim);
+        if (kind == 0) {
+            int eb = nope_dim + 2 * rope_dim;
+            or_quant_mla(z, nope_dim, rope_dim, out_data + (long long)n_out * eb,
+                         out_scale + (long long)n_out * 8);
+        } else {
+            float s;
+            or_quant_idx(z, d, out_data + (long long)n_out * d, &s);
+            memcpy(out_scale + (long long)n_out * 4, &s, 4);
+        }
+        ++n_out;
+    }
+    free(y);
+    free(z);
+    return n_out;
+}
+
+/* Write entries 0..n_entries-1 (slot order) of one sequence into a paged
+ * cache.  Slot j lives in page block_table[j / page], row j % page
+ * ([MLA-to-CSA] 6.3 slot mapping).  Page layout ([vLLM-classes] "CSA layer
+ * Compressor": data plane of page*entry bytes, then the scale plane):
+ *   kind 0: [page][nope + 2*rope] data, then [page][8] UE8M0 scale bytes;
+ *   kind 1: [page][d] fp8 data, then [page] fp32 scales (d = nope + rope). */
+void or_page_write(int kind, int nope_dim, int rope_dim, int page, const int* block_table,
+                   int n_entries, const uint8_t* data, const uint8_t* scale, uint8_t* cache)
+{
+    int data_b = (kind == 0) ? nope_dim + 2 * rope_dim : nope_dim + rope_dim;
+    int scale_b = (kind == 0) ? 8 : 4;
+    long long page_b = (long long)page * (data_b + scale_b);
+    for (int j = 0; j < n_entries; ++j) {
+        uint8_t* base = cache + (long long)block_table[j / page] * page_b;
+        int r = j % page;
+        memcpy(base + (long long)r * data_b, data + (long long)j * data_b, (size_t)data_b);
+        memcpy(base + (long long)page * data_b + (long long)r * scale_b,
+               scale + (long long)j * scale_b, (size_t)scale_b);
+    }
+}
+
+/* ========================================================================= */
+/* Lightning indexer and top-k                                               */
+/* ========================================================================= */
+
+/* I_s = sum_j w_j * ReLU(q_j . k_s) over the n_c causal compressed slots
+ * ([vLLM-classes] SparseAttnIndexer formula; [V4-internals] section 2;
+ * [MLA-to-CSA] 5.1).  One key per slot is shared by all heads.  The key is
+ * the FP8 row times its fp32 scale; the scale is positive, so it factors out
+ * of the ReLU: I_s = scale_s * sum_j w_j * ReLU(q_j . k8_s).
+ * Reading: any per-head q scale is already folded into w by the caller.
+ * FP8 products are exact in double, so are the 128-term dots. */
+void or_indexer_logits(const uint8_t* q_fp8, const float* w, int n_heads, int d,
+                       const uint8_t* cache, const int* block_table, int page, int n_c,
+                       double* out)
+{
+    long long page_b = (long long)page * (d + 4);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)n_heads * (size_t)d);
+    for (int i = 0; i < n_heads * d; ++i)
+        qd[i] = or_e4m3_to_f64(q_fp8[i]);
+    double kd[512];
+    for (int s = 0; s < n_c; ++s) {
+        const uint8_t* base = cache + (long long)block_table[s / page] * page_b;
+        int r = s % page;
+        const uint8_t* k = base + (long long)r * d;
+        float scale;
+        memcpy(&scale, base + (long long)page * d + (long long)r * 4, 4);
+        for (int c = 0; c < d; ++c)
+            kd[c] = or_e4m3_to_f64(k[c]);
+        double acc = 0.0;
+        for (int j = 0; j < n_heads; ++j) {
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += qd[(long long)j * d + c] * kd[c];
+            acc += (double)w[j] * (dot > 0.0 ? dot : 0.0);
+        }
+        out[s] = (double)scale * acc;
+    }
+    free(qd);
+}
+
+typedef struct { double v; int i; } or_scored;
+
+static int cmp_score_desc(const void* a, const void* b)
+{
+    const or_scored* x = (const or_scored*)a;
+    const or_scored* y = (const or_scored*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->i < y->i) ? -1 : (x->i > y->i);
+}
+
+static int cmp_int(const void* a, const void* b)
+{
+    int x = *(const int*)a, y = *(const int*)b;
+    return (x > y) - (x < y);
+}
+
+/* Per-query top-k ([vLLM-V4-attn] "Indexer, C4A and C128A top-k";
+ * [V4-internals] section 6: indices plus lengths).
+ * Reading: order by score descending, lower slot first on equal scores; keep
+ * min(k, n) slots; report them in ascending slot order, padded with -1;
+ * length = min(k, n). */
+int or_topk(const double* logits, int n, int k, int* out_idx, int* out_len)
+{
+    if (n < 0 || k < 0)
+        return -1;
+    or_scored* v = (or_scored*)malloc(sizeof(or_scored) * (size_t)(n > 0 ? n : 1));
+    for (int i = 0; i < n; ++i) {
+        v[i].v = logits[i];
+        v[i].i = i;
+    }
+    qsort(v, (size_t)n, sizeof(or_scored), cmp_score_desc);
+    int len = n < k ? n : k;
+    for (int i = 0; i < len; ++i)
+        out_idx[i] = v[i].i;
+    qsort(out_idx, (size_t)len, sizeof(int), cmp_int);
+    for (int i = len; i < k; ++i)
+        out_idx[i] = -1;
+    *out_len = len;
+    free(v);
+    return 0;
+}
+
+/* ========================================================================= */
+/* Attention                                                                 */
+/* ========================================================================= */
+
+/* Dense multi-query attention in double: every head attends to all n_keys
+ * key rows (dk dims); the value is the first dv dims of the key row
+ * ([MLA-to-CSA] 2.2 "matrix absorption": decode attends directly over the
+ * cached latent vector, MQA-style).  s = scale * q.k; softmax over keys;
+ * out = sum_t P_t * key_t[0:dv]; lse = max + log(sum exp(s - max)) (natural
+ * log). */
+void or_dense_attention(const double* q, int n_heads, const double* keys, int n_keys,
+                        int dk, int dv, double scale, double* out, double* lse)
+{
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1));
+    for (int h = 0; h < n_heads; ++h) {
+        const double* qh = q + (long long)h * dk;
+        double m = -INFINITY;
+        for (int t = 0; t < n_keys; ++t) {
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c)
+                dot += qh[c] * keys[(long long)t * dk + c];
+            s[t] = scale * dot;
+            if (s[t] > m)
+                m = s[t];
+        }
+        double den = 0.0;
+        for (int t = 0; t < n_keys; ++t) {
+            s[t] = exp(s[t] - m);
+            den += s[t];
+        }
+        for (int v = 0; v < dv; ++v) {
+            double acc = 0.0;
+            for (int t = 0; t < n_keys; ++t)
+                acc += s[t] * keys[(long long)t * dk + v];
+            out[(long long)h * dv + v] = (n_keys > 0) ? acc / den : 0.0;
+        }
+        if (lse)
+            lse[h] = (n_keys > 0) ? m + log(den) : -INFINITY;
+    }
+    free(s);
+}
+
+/* Key rows a decode query attends to, dequantised to double
+ * ([vLLM-V4-attn] "Indexer, C4A and C128A top-k": FlashMLA takes the SWA
+ * indices and the compressed top-k indices together; [V4-internals] section
+ * 2: KV_actual = selected history || recent window):
+ *  1. the compressed slots idx[0..len) of this sequence (logical slot ids,
+ *     mapped through comp_bt); value = fp8 * 2^(scale byte - 127) for the
+ *     nope dims, bf16 for the rope dims;
+ *  2. the raw SWA tokens max(0, p - window + 1) .. p, bf16 rows of
+ *     nope + rope values, mapped through swa_bt (pages of `page` tokens).
+ * Reading: no de-duplication between the two sets.  comp_cache may be NULL
+ * when len == 0 (swaonly).  Returns the number of key rows. */
+int or_gather_keys(int nope_dim, int rope_dim, int page,
+                   const uint8_t* comp_cache, const int* comp_bt, const int* idx, int len,
+                   const uint16_t* swa_cache, const int* swa_bt, int p, int window,
+                   double* keys)
+{
+    int dk = nope_dim + rope_dim;
+    int data_b = nope_dim + 2 * rope_dim;
+    long long cpage_b = (long long)page * (data_b + 8);
+    int n = 0;
+    for (int i = 0; i < len; ++i) {
+        int slot = idx[i];
+        const uint8_t* base = comp_cache + (long long)comp_bt[slot / page] * cpage_b;
+        int r = slot % page;
+        const uint8_t* row = base + (long long)r * data_b;
+        const uint8_t* sc = base + (long long)page * data_b + (long long)r * 8;
+        double* k = keys + (long long)n * dk;
+        for (int c = 0; c < nope_dim; ++c)
+            k[c] = or_e4m3_to_f64(row[c]) * ldexp(1.0, (int)sc[c / 64] - 127);
+        for (int i2 = 0; i2 < rope_dim; ++i2) {
+            uint16_t h = (uint16_t)(row[nope_dim + 2 * i2] | (row[nope_dim + 2 * i2 + 1] << 8));
+            k[nope_dim + i2] = (double)or_bf16_to_f32(h);
+        }
+        ++n;
+    }
+    int t0 = p - window + 1 < 0 ? 0 : p - window + 1;
+    for (int t = t0; t <= p; ++t) {
+        const uint16_t* row = swa_cache + ((long long)swa_bt[t / page] * page + t % page) * dk;
+        double* k = keys + (long long)n * dk;
+        for (int c = 0; c < dk; ++c)
+            k[c] = (double)or_bf16_to_f32(row[c]);
+        ++n;
+    }
+    return n;
+}
+
+/* Sparse absorbed-MQA decode for one query token at position p: gather the
+ * key set (or_gather_keys) and attend densely over it with the 576-dim key,
+ * the value being its first nope_dim dims (the latent)
+ * ([vLLM-classes] _forward_decode; [MLA-to-CSA] 2.2, 5.1).
+ * q is bf16 [n_heads][nope + rope]; out is [n_heads][nope] in double.
+ * Returns the number of keys attended. */
+int or_sparse_mla(const uint16_t* q, int n_heads, int nope_dim, int rope_dim, int page,
+                  const uint8_t* comp_cache, const int* comp_bt, const int* idx, int len,
+                  const uint16_t* swa_cache, const int* swa_bt, int p, int window,
+                  double scale, double* out, double* lse)
+{
+    int dk = nope_dim + rope_dim;
+    int max_keys = len + window;
+    double* keys = (double*)malloc(sizeof(double) * (size_t)max_keys * (size_t)dk);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)n_heads * (size_t)dk);
+    for (int i = 0; i < n_heads * dk; ++i)
+        qd[i] = (double)or_bf16_to_f32(q[i]);
+    int n = or_gather_keys(nope_dim, rope_dim, page, comp_cache, comp_bt, idx, len, swa_cache,
+                           swa_bt, p, window, keys);
+    or_dense_attention(qd, n_heads, keys, n, dk, nope_dim, scale, out, lse);
+    free(keys);
+    free(qd);
+    return n;
+}
