@@ -1,0 +1,288 @@
+"""Thin ctypes binding of libdsv4 (include/dsv4.h): argument marshalling only.
+
+Every step of the decode path runs in the CUDA library; this module turns
+torch tensors into device pointers and the current torch stream into a
+cudaStream_t.  If the library is not built it raises: there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsv4.so")
+
+SWAONLY, C4A, C128A = 1, 4, 128
+CACHE_MLA, CACHE_IDX = 0, 1
+
+OK, ERR_INVALID, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
+DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+NOPE_DIM, ROPE_DIM, HEAD_DIM, V_DIM, IDX_DIM, PAGE, WINDOW = 512, 64, 576, 512, 128, 64, 128
+MLA_PAGE_BYTES = 64 * 648
+IDX_PAGE_BYTES = 64 * 132
+SWA_PAGE_BYTES = 64 * 576 * 2
+
+EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
+            "dsv4_index_schedule", "dsv4_rope_table", "dsv4_read_device_status",
+            "dsv4_plan_create", "dsv4_plan_destroy", "dsv4_plan_workspace_bytes",
+            "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
+            "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait"]
+
+
+class Dsv4Error(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+        self.status = status
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int), ("idx_heads", ctypes.c_int), ("window", ctypes.c_int),
+                ("softmax_scale", ctypes.c_float)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("layer_type", ctypes.c_int), ("batch", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("idx_heads", ctypes.c_int), ("topk", ctypes.c_int), ("max_ctx", ctypes.c_int),
+                ("max_slots", ctypes.c_int), ("idx_ctas_per_seq", ctypes.c_int),
+                ("mla_splits", ctypes.c_int), ("mla_head_groups", ctypes.c_int),
+                ("mla_keys_per_split", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+                ("launches_indexer", ctypes.c_int), ("launches_mla", ctypes.c_int)]
+
+
+class CompressArgs(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("ratio", ctypes.c_int), ("num_tokens", ctypes.c_int),
+                ("num_seqs", ctypes.c_int), ("one_token_per_seq", ctypes.c_int),
+                ("kv_score_dev", ctypes.c_void_p), ("kv_score_stride", ctypes.c_longlong),
+                ("positions_dev", ctypes.c_void_p), ("seq_dev", ctypes.c_void_p),
+                ("ape_dev", ctypes.c_void_p), ("rms_weight_dev", ctypes.c_void_p),
+                ("rms_eps", ctypes.c_float), ("cos_sin_dev", ctypes.c_void_p),
+                ("max_pos", ctypes.c_int), ("state_dev", ctypes.c_void_p),
+                ("cache_dev", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("block_table_dev", ctypes.c_void_p), ("bt_stride", ctypes.c_int),
+                ("status_dev", ctypes.c_void_p)]
+
+
+class InsertRowsArgs(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("num_rows", ctypes.c_int), ("rows_dev", ctypes.c_void_p),
+                ("seq_dev", ctypes.c_void_p), ("slot_dev", ctypes.c_void_p),
+                ("cache_dev", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("block_table_dev", ctypes.c_void_p), ("bt_stride", ctypes.c_int),
+                ("num_seqs", ctypes.c_int), ("status_dev", ctypes.c_void_p)]
+
+
+class IndexerArgs(ctypes.Structure):
+    _fields_ = [("q_fp8_dev", ctypes.c_void_p), ("weights_dev", ctypes.c_void_p),
+                ("idx_cache_dev", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("block_table_dev", ctypes.c_void_p), ("bt_stride", ctypes.c_int),
+                ("ctx_len_dev", ctypes.c_void_p), ("out_idx_dev", ctypes.c_void_p),
+                ("out_stride", ctypes.c_int), ("out_len_dev", ctypes.c_void_p),
+                ("status_dev", ctypes.c_void_p)]
+
+
+class MlaArgs(ctypes.Structure):
+    _fields_ = [("q_dev", ctypes.c_void_p), ("swa_cache_dev", ctypes.c_void_p),
+                ("swa_num_pages", ctypes.c_int), ("swa_block_table_dev", ctypes.c_void_p),
+                ("swa_bt_stride", ctypes.c_int), ("comp_cache_dev", ctypes.c_void_p),
+                ("comp_num_pages", ctypes.c_int), ("comp_block_table_dev", ctypes.c_void_p),
+                ("comp_bt_stride", ctypes.c_int), ("topk_idx_dev", ctypes.c_void_p),
+                ("topk_stride", ctypes.c_int), ("topk_len_dev", ctypes.c_void_p),
+                ("ctx_len_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
+                ("lse_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libdsv4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libdsv4.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    st = ctypes.c_int
+    vp = ctypes.c_void_p
+    L.dsv4_version.restype = ctypes.c_int
+    L.dsv4_status_string.restype = ctypes.c_char_p
+    L.dsv4_status_string.argtypes = [st]
+    L.dsv4_layer_type_from_ratio.restype = st
+    L.dsv4_layer_type_from_ratio.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.dsv4_index_schedule.restype = st
+    L.dsv4_index_schedule.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_char_p, ctypes.POINTER(ctypes.c_ubyte)]
+    L.dsv4_rope_table.restype = st
+    L.dsv4_rope_table.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_double]
+    L.dsv4_read_device_status.restype = st
+    L.dsv4_read_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+    L.dsv4_plan_create.restype = st
+    L.dsv4_plan_create.argtypes = [ctypes.c_int, ctypes.POINTER(Geom), ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.POINTER(vp)]
+    L.dsv4_plan_destroy.restype = None
+    L.dsv4_plan_destroy.argtypes = [vp]
+    L.dsv4_plan_workspace_bytes.restype = ctypes.c_size_t
+    L.dsv4_plan_workspace_bytes.argtypes = [vp]
+    L.dsv4_plan_get_info.restype = st
+    L.dsv4_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    L.dsv4_compress_insert.restype = st
+    L.dsv4_compress_insert.argtypes = [ctypes.POINTER(CompressArgs), vp]
+    L.dsv4_cache_insert_rows.restype = st
+    L.dsv4_cache_insert_rows.argtypes = [ctypes.POINTER(InsertRowsArgs), vp]
+    L.dsv4_indexer_topk.restype = st
+    L.dsv4_indexer_topk.argtypes = [vp, ctypes.POINTER(IndexerArgs), vp, ctypes.c_size_t, vp]
+    L.dsv4_sparse_mla_decode.restype = st
+    L.dsv4_sparse_mla_decode.argtypes = [vp, ctypes.POINTER(MlaArgs), vp, ctypes.c_size_t, vp]
+    L.dsv4_selftest_bounded_wait.restype = st
+    L.dsv4_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
+    _lib = L
+    return L
+
+
+def status_string(s):
+    return lib().dsv4_status_string(int(s)).decode()
+
+
+def _check(status, what):
+    if status != OK:
+        raise Dsv4Error(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def version():
+    return lib().dsv4_version()
+
+
+def layer_type_from_ratio(ratio):
+    out = ctypes.c_int(0)
+    _check(lib().dsv4_layer_type_from_ratio(int(ratio), ctypes.byref(out)), "layer_type_from_ratio")
+    return out.value
+
+
+def index_schedule(ratios, use_index_cache=True, freq=2, pattern=None):
+    n = len(ratios)
+    arr = (ctypes.c_int * max(n, 1))(*[int(r) for r in ratios])
+    out = (ctypes.c_ubyte * max(n, 1))()
+    _check(lib().dsv4_index_schedule(arr, n, int(bool(use_index_cache)), int(freq),
+                                     pattern.encode() if pattern is not None else None, out),
+           "index_schedule")
+    return [int(out[i]) for i in range(n)]
+
+
+def rope_table(max_pos, rope_dim=ROPE_DIM, theta=10000.0):
+    """Host fp32 tensor [max_pos, rope_dim] (copy it to the GPU yourself)."""
+    t = torch.empty((max_pos, rope_dim), dtype=torch.float32)
+    _check(lib().dsv4_rope_table(ctypes.cast(t.data_ptr(), ctypes.POINTER(ctypes.c_float)), max_pos,
+                                 rope_dim, float(theta)), "rope_table")
+    return t
+
+
+def read_device_status(status_dev, stream=None):
+    bits = ctypes.c_int(0)
+    st = lib().dsv4_read_device_status(_ptr(status_dev), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def selftest_bounded_wait(status_dev, spin_limit, stream=None):
+    _check(lib().dsv4_selftest_bounded_wait(_ptr(status_dev), int(spin_limit), _stream(stream)),
+           "selftest_bounded_wait")
+
+
+class Plan:
+    """One plan per layer type, reused by every layer of that type in a step."""
+
+    def __init__(self, layer_type, n_heads, batch, topk, max_ctx, idx_heads=64, window=WINDOW,
+                 softmax_scale=HEAD_DIM ** -0.5):
+        self.geom = Geom(int(n_heads), int(idx_heads), int(window), float(softmax_scale))
+        h = ctypes.c_void_p()
+        _check(lib().dsv4_plan_create(int(layer_type), ctypes.byref(self.geom), int(batch), int(topk),
+                                      int(max_ctx), ctypes.byref(h)), "plan_create")
+        self.handle = h
+        self.layer_type = int(layer_type)
+
+    @property
+    def workspace_bytes(self):
+        return int(lib().dsv4_plan_workspace_bytes(self.handle))
+
+    def info(self):
+        i = PlanInfo()
+        _check(lib().dsv4_plan_get_info(self.handle, ctypes.byref(i)), "plan_get_info")
+        return {f: getattr(i, f) for f, _ in PlanInfo._fields_}
+
+    def workspace(self, device="cuda"):
+        return torch.empty(max(self.workspace_bytes, 1), dtype=torch.uint8, device=device)
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.dsv4_plan_destroy(self.handle)
+            self.handle = None
+
+
+def compress_insert(kind, ratio, kv_score, positions, seqs, ape, rms_weight, rms_eps, cos_sin,
+                    state, cache, block_table, num_seqs, one_token_per_seq=True, status=None,
+                    stream=None):
+    """Compressor state update + compressed-cache insert for the tokens in kv_score
+    (bf16 [T, 2*coff*d]); see dsv4_compress_insert."""
+    a = CompressArgs(int(kind), int(ratio), int(kv_score.shape[0]), int(num_seqs),
+                     int(bool(one_token_per_seq)), _ptr(kv_score), int(kv_score.stride(0)),
+                     _ptr(positions), _ptr(seqs), _ptr(ape), _ptr(rms_weight), float(rms_eps),
+                     _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(state), _ptr(cache),
+                     int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                     _ptr(block_table), int(block_table.shape[1]), _ptr(status))
+    _check(lib().dsv4_compress_insert(ctypes.byref(a), _stream(stream)), "compress_insert")
+
+
+def cache_insert_rows(kind, rows, seqs, slots, cache, block_table, status=None, stream=None):
+    a = InsertRowsArgs(int(kind), int(rows.shape[0]), _ptr(rows), _ptr(seqs), _ptr(slots),
+                       _ptr(cache),
+                       int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                       _ptr(block_table), int(block_table.shape[1]), int(block_table.shape[0]),
+                       _ptr(status))
+    _check(lib().dsv4_cache_insert_rows(ctypes.byref(a), _stream(stream)), "cache_insert_rows")
+
+
+def indexer_topk(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx, out_len, workspace,
+                 status=None, stream=None):
+    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // IDX_PAGE_BYTES),
+                    _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
+                    int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
+    _check(lib().dsv4_indexer_topk(plan.handle, ctypes.byref(a), _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream)), "indexer_topk")
+
+
+def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspace, comp_cache=None,
+                      comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None,
+                      stream=None):
+    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // SWA_PAGE_BYTES),
+                _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
+                int(_nbytes(comp_cache) // MLA_PAGE_BYTES) if comp_cache is not None else 0,
+                _ptr(comp_block_table),
+                int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
+                _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
+                _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status))
+    _check(lib().dsv4_sparse_mla_decode(plan.handle, ctypes.byref(a), _ptr(workspace),
+                                        workspace.numel(), _stream(stream)), "sparse_mla_decode")

@@ -1,0 +1,385 @@
+// compress.cu -- token-level Compressor -> RMSNorm -> RoPE -> FP8 -> paged insert.
+//
+// Follows DeepseekCompressor.forward / save_partial_states and "CSA layer
+// Compressor" of the "DeepseekV4Attention" class walkthrough, "Compressor:
+// ratio 4 vs 128" of "DeepSeek V4 attention in vLLM", and sections 5.1, 5.2,
+// 6.3 of "From MLA to CSA + HCA".
+//
+// One CTA per token, d/2 threads, thread i owns channels 2i and 2i+1
+// (main cache d = 576: 288 threads = 9 warps, warp w < 8 owns nope block w of
+// 64 dims, warp 8 the rope dims; indexer d = 128: 64 threads).  The per-token
+// state row is [kv block 0..coff-1 | score block 0..coff-1] in fp32; the
+// window of a boundary token is read from the per-sequence ring (and, in a
+// multi-token call, from this call's own inputs).  Work per entry is tiny and
+// bound by the state reads; it runs on the CUDA cores, no contraction.
+#include "dsv4_common.cuh"
+
+namespace dsv4 {
+
+struct CompressParams {
+    const uint16_t* kv_score;
+    long long kv_stride;
+    const int* positions;
+    const int* seqs;
+    const float* ape;
+    const float* rms_w;
+    float eps;
+    const float* cos_sin;
+    int max_pos;
+    float* state;
+    uint8_t* cache;
+    int num_pages;
+    const int* bt;
+    int bt_stride;
+    int num_tokens;
+    int num_seqs;
+    int* status;
+};
+
+// Per-block double reduction of the RMSNorm sum of squares (any order: the
+// double sum is rounded once to fp32 afterwards).
+template <int NT>
+__device__ __forceinline__ double block_sum_d(double v, double* red)
+{
+    constexpr int NW = NT / 32;
+    v = warp_sum_d(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    double s = 0.0;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) s += red[i];
+    return s;
+}
+
+// Quantise the normalised, rotated vector (this thread's channels c0, c0+1)
+// into a main-cache entry: E4M3 nope with one UE8M0 byte per 64 dims, bf16
+// rope.  Called by all 288 threads.
+__device__ __forceinline__ void store_mla_entry(float z0, float z1, int c0, uint8_t* data_row,
+                                                uint8_t* scale_row)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < kNope / 64) {
+        const float amax = warp_max(fmaxf(fabsf(z0), fabsf(z1)));
+        const int e = ue8m0_exponent(amax);
+        const float mult = exp2i(-e);
+        const uint16_t codes = f32x2_to_e4m3x2(__fmul_rn(z0, mult), __fmul_rn(z1, mult));
+        *reinterpret_cast<uint16_t*>(data_row + c0) = codes;
+        if (lane == 0) scale_row[warp] = static_cast<uint8_t>(e + 127);
+    } else {
+        const uint32_t pk = static_cast<uint32_t>(f32_to_bf16_bits(z0)) |
+                            (static_cast<uint32_t>(f32_to_bf16_bits(z1)) << 16);
+        *reinterpret_cast<uint32_t*>(data_row + kNope + 2 * (c0 - kNope)) = pk;
+    }
+}
+
+// Indexer entry: E4M3 of all 128 dims, one fp32 scale = amax / 448.
+// Called by all 64 threads.
+__device__ __forceinline__ void store_idx_entry(float z0, float z1, int c0, uint8_t* data_row,
+                                                float* scale_ptr, float* red)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float amax = warp_max(fmaxf(fabsf(z0), fabsf(z1)));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = fmaxf(red[0], red[1]);
+    const float s = (amax > 0.0f) ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const uint16_t codes = f32x2_to_e4m3x2(__fdiv_rn(z0, s), __fdiv_rn(z1, s));
+    *reinterpret_cast<uint16_t*>(data_row + c0) = codes;
+    if (threadIdx.x == 0) *scale_ptr = s;
+}
+
+// Resolve the page of logical slot j of sequence seq; nullptr (and a status
+// bit) when the table entry is out of range.
+template <bool IDX>
+__device__ __forceinline__ uint8_t* entry_page(const CompressParams& P, int seq, int j)
+{
+    const int pi = j / kPage;
+    if (pi >= P.bt_stride) {
+        flag(P.status, DSV4_DEV_BAD_PAGE);
+        return nullptr;
+    }
+    const int pg = P.bt[static_cast<long long>(seq) * P.bt_stride + pi];
+    if (pg < 0 || pg >= P.num_pages) {
+        flag(P.status, DSV4_DEV_BAD_PAGE);
+        return nullptr;
+    }
+    return P.cache + static_cast<long long>(pg) * (IDX ? kIdxPage : kMlaPage);
+}
+
+// The state values (kv, score + ape) of one token for this thread's two
+// channels of block blk, straight from the projection input.
+template <int D, int COFF>
+__device__ __forceinline__ void token_values(const CompressParams& P, int t, int pos, int blk,
+                                             int c0, float2& kv, float2& sc, int ratio)
+{
+    const uint16_t* row = P.kv_score + static_cast<long long>(t) * P.kv_stride;
+    kv = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(row + blk * D + c0));
+    const float2 s = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(row + COFF * D + blk * D + c0));
+    const float2 a = *reinterpret_cast<const float2*>(
+        P.ape + static_cast<long long>(pos % ratio) * COFF * D + blk * D + c0);
+    sc = make_float2(__fadd_rn(s.x, a.x), __fadd_rn(s.y, a.y));
+}
+
+// Compress kernel.  FUSED: each sequence has at most one token in the call;
+// the token's state row is written here too.  Otherwise (multi-token calls)
+// window rows inside the call come from the inputs and the ring is written
+// by state_write_kernel afterwards.
+template <int D, int RATIO, bool IDX, bool FUSED>
+__global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
+{
+    constexpr int COFF = (RATIO == 4) ? 2 : 1;
+    constexpr int W = COFF * RATIO;
+    constexpr int ROW = 2 * COFF * D;
+    constexpr int NT = D / 2;
+    constexpr int NOPE = IDX ? kIdx - kRope : kNope;
+    __shared__ double red_d[NT / 32];
+    __shared__ float red_f[2];
+
+    const int t = blockIdx.x;
+    const int c0 = 2 * threadIdx.x;
+    const int seq = P.seqs[t];
+    const int p = P.positions[t];
+    if (seq < 0 || seq >= P.num_seqs || p < 0) {
+        if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+        return;
+    }
+    if (!FUSED && t > 0 && P.seqs[t - 1] == seq && P.positions[t - 1] != p - 1) {
+        if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_POSITION);
+        return;
+    }
+    float* ring = P.state + static_cast<long long>(seq) * W * ROW;
+
+    // This token's own values (block coff-1 is the "new" block of a window).
+    float2 own_kv[COFF], own_sc[COFF];
+#pragma unroll
+    for (int b = 0; b < COFF; ++b) token_values<D, COFF>(P, t, p, b, c0, own_kv[b], own_sc[b], RATIO);
+
+    if (FUSED) {
+        float* dst = ring + static_cast<long long>(p % W) * ROW;
+#pragma unroll
+        for (int b = 0; b < COFF; ++b) {
+            *reinterpret_cast<float2*>(dst + b * D + c0) = own_kv[b];
+            *reinterpret_cast<float2*>(dst + COFF * D + b * D + c0) = own_sc[b];
+        }
+    }
+    if ((p + 1) % RATIO != 0) return;
+
+    // Window rows s = p-W+1 .. p (s >= 0); block 0 for the old group of a
+    // ratio-4 window (s <= p - 4), the last block otherwise.
+    auto fetch = [&](int s, float2& kv, float2& sc) {
+        const int blk = (COFF == 2 && s <= p - RATIO) ? 0 : COFF - 1;
+        if (s == p) {
+            kv = own_kv[COFF - 1];
+            sc = own_sc[COFF - 1];
+            return;
+        }
+        if (!FUSED) {
+            const int ts = t - (p - s);
+            if (ts >= 0 && P.seqs[ts] == seq && P.positions[ts] == s) {
+                token_values<D, COFF>(P, ts, s, blk, c0, kv, sc, RATIO);
+                return;
+            }
+        }
+        const float* src = ring + static_cast<long long>(s % W) * ROW;
+        kv = *reinterpret_cast<const float2*>(src + blk * D + c0);
+        sc = *reinterpret_cast<const float2*>(src + COFF * D + blk * D + c0);
+    };
+    const int s0 = (p - W + 1) < 0 ? 0 : p - W + 1;
+    float m0 = -INFINITY, m1 = -INFINITY;
+    for (int s = s0; s <= p; ++s) {
+        float2 kv, sc;
+        fetch(s, kv, sc);
+        m0 = fmaxf(m0, sc.x);
+        m1 = fmaxf(m1, sc.y);
+    }
+    float n0 = 0.f, n1 = 0.f, d0 = 0.f, d1 = 0.f;
+    for (int s = s0; s <= p; ++s) {
+        float2 kv, sc;
+        fetch(s, kv, sc);
+        const float e0 = cw_expf(__fsub_rn(sc.x, m0));
+        const float e1 = cw_expf(__fsub_rn(sc.y, m1));
+        n0 = __fadd_rn(n0, __fmul_rn(e0, kv.x));
+        n1 = __fadd_rn(n1, __fmul_rn(e1, kv.y));
+        d0 = __fadd_rn(d0, e0);
+        d1 = __fadd_rn(d1, e1);
+    }
+    const float y0 = __fdiv_rn(n0, d0), y1 = __fdiv_rn(n1, d1);
+
+    // RMSNorm: mean square accumulated in double, rounded once.
+    const double ss = block_sum_d<NT>(static_cast<double>(y0) * y0 + static_cast<double>(y1) * y1, red_d);
+    const float ms = __double2float_rn(ss / static_cast<double>(D));
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, P.eps)));
+    const float2 w = *reinterpret_cast<const float2*>(P.rms_w + c0);
+    float z0 = __fmul_rn(__fmul_rn(y0, inv), w.x);
+    float z1 = __fmul_rn(__fmul_rn(y1, inv), w.y);
+
+    // GPT-J RoPE on the last 64 dims at the slot's anchor position.
+    if (c0 >= NOPE) {
+        const int rp = (p / RATIO) * RATIO;
+        const int pair = (c0 - NOPE) >> 1;
+        if (rp < P.max_pos) {
+            const float cs = P.cos_sin[static_cast<long long>(rp) * kRope + pair];
+            const float sn = P.cos_sin[static_cast<long long>(rp) * kRope + kRope / 2 + pair];
+            const float r0 = __fsub_rn(__fmul_rn(z0, cs), __fmul_rn(z1, sn));
+            const float r1 = __fadd_rn(__fmul_rn(z0, sn), __fmul_rn(z1, cs));
+            z0 = r0;
+            z1 = r1;
+        } else {
+            flag(P.status, DSV4_DEV_BAD_POSITION);
+        }
+    }
+
+    const int j = p / RATIO;
+    uint8_t* page = entry_page<IDX>(P, seq, j);
+    const int r = j % kPage;
+    if (IDX) {
+        if (page == nullptr) return;   // uniform across the CTA
+        store_idx_entry(z0, z1, c0, page + r * kIdx,
+                        reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
+    } else {
+        if (page == nullptr) return;
+        store_mla_entry(z0, z1, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
+    }
+}
+
+// Multi-token calls: write the ring rows of the last W tokens of every
+// sequence (earlier tokens of the call are never read again).
+template <int D, int RATIO>
+__global__ void __launch_bounds__(D / 2) state_write_kernel(CompressParams P)
+{
+    constexpr int COFF = (RATIO == 4) ? 2 : 1;
+    constexpr int W = COFF * RATIO;
+    constexpr int ROW = 2 * COFF * D;
+    const int t = blockIdx.x;
+    const int c0 = 2 * threadIdx.x;
+    const int seq = P.seqs[t];
+    const int p = P.positions[t];
+    if (seq < 0 || seq >= P.num_seqs || p < 0) return;
+    if (t + W < P.num_tokens && P.seqs[t + W] == seq) return;   // superseded in this call
+    float* dst = P.state + (static_cast<long long>(seq) * W + p % W) * ROW;
+#pragma unroll
+    for (int b = 0; b < COFF; ++b) {
+        float2 kv, sc;
+        token_values<D, COFF>(P, t, p, b, c0, kv, sc, RATIO);
+        *reinterpret_cast<float2*>(dst + b * D + c0) = kv;
+        *reinterpret_cast<float2*>(dst + COFF * D + b * D + c0) = sc;
+    }
+}
+
+// Quantise-and-insert of given fp32 rows (no pooling / norm / rope).
+template <int D, bool IDX>
+__global__ void __launch_bounds__(D / 2) insert_rows_kernel(const float* rows, const int* seqs,
+                                                            const int* slots, CompressParams P)
+{
+    __shared__ float red_f[2];
+    const int i = blockIdx.x;
+    const int c0 = 2 * threadIdx.x;
+    const int seq = seqs[i], j = slots[i];
+    if (seq < 0 || seq >= P.num_seqs || j < 0) {
+        if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+        return;
+    }
+    const float2 z = *reinterpret_cast<const float2*>(rows + static_cast<long long>(i) * D + c0);
+    uint8_t* page = entry_page<IDX>(P, seq, j);
+    if (page == nullptr) return;
+    const int r = j % kPage;
+    if (IDX)
+        store_idx_entry(z.x, z.y, c0, page + r * kIdx,
+                        reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
+    else
+        store_mla_entry(z.x, z.y, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
+}
+
+template <int D, int RATIO, bool IDX>
+static cudaError_t launch_compress(const CompressParams& P, bool fused, cudaStream_t st)
+{
+    if (P.num_tokens == 0) return cudaSuccess;
+    if (fused) {
+        compress_kernel<D, RATIO, IDX, true><<<P.num_tokens, D / 2, 0, st>>>(P);
+        return cudaGetLastError();
+    }
+    compress_kernel<D, RATIO, IDX, false><<<P.num_tokens, D / 2, 0, st>>>(P);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    state_write_kernel<D, RATIO><<<P.num_tokens, D / 2, 0, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace dsv4
+
+using namespace dsv4;
+
+extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_stream_t stream)
+{
+    if (a == nullptr) return DSV4_ERR_INVALID;
+    if (a->num_tokens < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
+        return DSV4_ERR_INVALID;
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (a->ratio != 4 && a->ratio != 128) return DSV4_ERR_UNSUPPORTED;
+    if (a->kind == DSV4_CACHE_IDX && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
+    if (a->num_tokens == 0) return DSV4_OK;
+    if (!a->kv_score_dev || !a->positions_dev || !a->seq_dev || !a->ape_dev || !a->rms_weight_dev ||
+        !a->cos_sin_dev || !a->state_dev || !a->cache_dev || !a->block_table_dev)
+        return DSV4_ERR_INVALID;
+    const int d = (a->kind == DSV4_CACHE_MLA) ? kHead : kIdx;
+    const int coff = (a->ratio == 4) ? 2 : 1;
+    if (a->kv_score_stride < 2LL * coff * d || (a->kv_score_stride & 1)) return DSV4_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(a->kv_score_dev) & 3) || (reinterpret_cast<uintptr_t>(a->cache_dev) & 15))
+        return DSV4_ERR_SHAPE;
+
+    CompressParams P;
+    P.kv_score = static_cast<const uint16_t*>(a->kv_score_dev);
+    P.kv_stride = a->kv_score_stride;
+    P.positions = a->positions_dev;
+    P.seqs = a->seq_dev;
+    P.ape = a->ape_dev;
+    P.rms_w = a->rms_weight_dev;
+    P.eps = a->rms_eps;
+    P.cos_sin = a->cos_sin_dev;
+    P.max_pos = a->max_pos;
+    P.state = a->state_dev;
+    P.cache = static_cast<uint8_t*>(a->cache_dev);
+    P.num_pages = a->num_pages;
+    P.bt = a->block_table_dev;
+    P.bt_stride = a->bt_stride;
+    P.num_tokens = a->num_tokens;
+    P.num_seqs = a->num_seqs;
+    P.status = a->status_dev;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool fused = a->one_token_per_seq != 0;
+    cudaError_t e;
+    if (a->kind == DSV4_CACHE_IDX)
+        e = launch_compress<kIdx, 4, true>(P, fused, st);
+    else if (a->ratio == 4)
+        e = launch_compress<kHead, 4, false>(P, fused, st);
+    else
+        e = launch_compress<kHead, 128, false>(P, fused, st);
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, dsv4_stream_t stream)
+{
+    if (a == nullptr) return DSV4_ERR_INVALID;
+    if (a->num_rows < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
+        return DSV4_ERR_INVALID;
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (a->num_rows == 0) return DSV4_OK;
+    if (!a->rows_dev || !a->seq_dev || !a->slot_dev || !a->cache_dev || !a->block_table_dev)
+        return DSV4_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(a->rows_dev) & 7) || (reinterpret_cast<uintptr_t>(a->cache_dev) & 15))
+        return DSV4_ERR_SHAPE;
+    CompressParams P{};
+    P.cache = static_cast<uint8_t*>(a->cache_dev);
+    P.num_pages = a->num_pages;
+    P.bt = a->block_table_dev;
+    P.bt_stride = a->bt_stride;
+    P.num_seqs = a->num_seqs;
+    P.status = a->status_dev;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (a->kind == DSV4_CACHE_IDX)
+        insert_rows_kernel<kIdx, true><<<a->num_rows, kIdx / 2, 0, st>>>(a->rows_dev, a->seq_dev, a->slot_dev, P);
+    else
+        insert_rows_kernel<kHead, false><<<a->num_rows, kHead / 2, 0, st>>>(a->rows_dev, a->seq_dev, a->slot_dev, P);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}

@@ -1,0 +1,28 @@
+// plan.h -- the per-layer-type plan (host object) and its workspace layout.
+#pragma once
+
+#include <stddef.h>
+
+#include "dsv4.h"
+
+struct dsv4_plan {
+    dsv4_layer_type type;
+    dsv4_geom geom;
+    int batch;
+    int topk;
+    int max_ctx;
+    int max_slots;           // compressed slots per sequence at max_ctx
+    int max_keys;            // topk + window
+    int idx_ctas_per_seq;    // indexer split over slots
+    int mla_head_groups;     // ceil(n_heads / 64)
+    int mla_splits;          // key splits per (sequence, head group)
+    int mla_keys_per_split;
+    size_t ws_logits_off;    // fp32 [batch][max_slots] indexer logits
+    size_t ws_partial_off;   // fp32 attention partials
+    size_t ws_partial_bytes;
+    size_t ws_bytes;
+};
+
+namespace dsv4 {
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}

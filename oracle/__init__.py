@@ -256,14 +256,20 @@ def compress_stream(kind, ratio, kv_score_bf16, ape, rms_w, eps, cos_sin, nope_d
     return data, scale
 
 
-def page_bytes(kind, page=64, nope_dim=512, rope_dim=64):
+def _nope(kind, nope_dim):
+    return nope_dim if nope_dim is not None else (512 if kind == MLA_KIND else 64)
+
+
+def page_bytes(kind, page=64, nope_dim=None, rope_dim=64):
+    nope_dim = _nope(kind, nope_dim)
     if kind == MLA_KIND:
         return page * (nope_dim + 2 * rope_dim + 8)
     return page * (nope_dim + rope_dim + 4)
 
 
-def page_write(kind, cache, block_table_row, data, scale, page=64, nope_dim=512, rope_dim=64):
+def page_write(kind, cache, block_table_row, data, scale, page=64, nope_dim=None, rope_dim=64):
     """Write a sequence's entries (slot order) into the paged byte array ``cache`` in place."""
+    nope_dim = _nope(kind, nope_dim)
     assert cache.dtype == np.uint8 and cache.flags.c_contiguous
     bt = _c(block_table_row, np.int32)
     data = _c(data, np.uint8)

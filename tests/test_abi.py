@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and its host-side utilities and validation behave."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from deepseek_v4_compressed_gb300 import binding as B
+from deepseek_v4_compressed_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dsv4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsv4_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(B.LIB_PATH)
+    syms = declared_symbols()
+    assert len(syms) >= 15
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(B.EXPORTED) <= set(syms)
+    assert B.version() == 1
+
+
+def test_layer_type_from_ratio_matches_oracle():
+    for r in [0, 1, 4, 128]:
+        assert B.layer_type_from_ratio(r) == oracle.layer_type(r)
+    for r in [2, 8, 64]:
+        with pytest.raises(B.Dsv4Error) as e:
+            B.layer_type_from_ratio(r)
+        assert e.value.status == B.ERR_UNSUPPORTED
+
+
+def test_index_schedule_matches_oracle():
+    ratios = synth.mixed_stack_ratios()
+    for use, freq, pat in [(True, 2, None), (True, 1, None), (False, 2, None), (True, 3, None),
+                           (True, 2, "FSSF"), (True, 2, "F")]:
+        assert B.index_schedule(ratios, use, freq, pat) == list(oracle.index_schedule(ratios, use, freq, pat))
+    for pat in ["SF", "FX", ""]:
+        with pytest.raises(B.Dsv4Error):
+            B.index_schedule(ratios, True, 2, pat)
+
+
+def test_rope_table_bitwise_equals_oracle():
+    ours = B.rope_table(4096, 64, 10000.0).numpy()
+    assert np.array_equal(ours, oracle.rope_table(4096, 64, 10000.0))
+
+
+def test_plan_validation_and_info():
+    p = B.Plan(B.C4A, n_heads=64, batch=32, topk=512, max_ctx=32768, idx_heads=64)
+    info = p.info()
+    assert info["max_slots"] == 8192 and info["topk"] == 512 and info["batch"] == 32
+    assert p.workspace_bytes >= 32 * 8192 * 4
+    assert p.workspace_bytes % 256 == 0
+    assert B.Plan(B.SWAONLY, 8, 1, 0, 100).info()["max_slots"] == 0
+    assert B.Plan(B.C128A, 64, 64, 512, 131072).info()["max_slots"] == 1024
+    for kwargs, status in [(dict(n_heads=0), B.ERR_UNSUPPORTED), (dict(n_heads=129), B.ERR_UNSUPPORTED),
+                           (dict(window=64), B.ERR_UNSUPPORTED), (dict(idx_heads=65), B.ERR_UNSUPPORTED),
+                           (dict(topk=0), B.ERR_INVALID), (dict(batch=0), B.ERR_INVALID)]:
+        args = dict(layer_type=B.C4A, n_heads=64, batch=4, topk=64, max_ctx=1024, idx_heads=64)
+        args.update(kwargs)
+        with pytest.raises(B.Dsv4Error) as e:
+            B.Plan(**args)
+        assert e.value.status == status, kwargs
+
+
+def test_entry_points_reject_null_arguments_without_gpu():
+    lib = B.lib()
+    a = B.CompressArgs()
+    a.kind, a.ratio, a.num_tokens, a.num_seqs = 0, 4, 1, 1
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_INVALID
+    a.ratio = 8
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_UNSUPPORTED
+    a.kind, a.ratio = 1, 128
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_UNSUPPORTED
+    assert lib.dsv4_compress_insert(None, None) == B.ERR_INVALID
+    p = B.Plan(B.C4A, 8, 1, 32, 512, idx_heads=4)
+    ia = B.IndexerArgs()
+    assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), None, 0, None) in (B.ERR_SHAPE, B.ERR_INVALID)
+    ma = B.MlaArgs()
+    assert lib.dsv4_sparse_mla_decode(p.handle, ctypes.byref(ma), None, 0, None) in (B.ERR_SHAPE, B.ERR_INVALID)
+    sp = B.Plan(B.SWAONLY, 8, 1, 0, 512)
+    assert lib.dsv4_indexer_topk(sp.handle, ctypes.byref(ia), None, 0, None) == B.ERR_SHAPE
+    assert lib.dsv4_read_device_status(None, None, None) == B.ERR_INVALID
+    assert B.status_string(B.ERR_TIMEOUT).startswith("device-side bounded wait")

@@ -1,0 +1,166 @@
+"""GPU parity of dsv4_compress_insert / dsv4_cache_insert_rows: cache bytes must
+equal the oracle's bit for bit."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_compressed_gb300 import binding as B
+from deepseek_v4_compressed_gb300 import synth
+
+from _util import bf16_bits, bits_tensor, dev
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+def make_stream(kind, ratio, n_tok, seed, w_ones=False):
+    g = synth.rng(seed)
+    d = 576 if kind == B.CACHE_MLA else 128
+    coff = 2 if ratio == 4 else 1
+    ks = bf16_bits(synth.normal(g, (n_tok, 2 * coff * d)))
+    ape = synth.normal(g, (ratio, coff * d), 0.1)
+    w = np.ones(d, np.float32) if w_ones else synth.uniform(g, d, 0.5, 1.5)
+    return ks, ape, w
+
+
+def entries_from_pages(kind, cache, bt_row, n):
+    """Read entries 0..n-1 (slot order) back out of the paged bytes."""
+    data_b, sc_b = (640, 8) if kind == B.CACHE_MLA else (128, 4)
+    if n == 0:
+        return np.zeros((0, data_b), np.uint8), np.zeros((0, sc_b), np.uint8)
+    pages = cache.reshape(-1, 64 * (data_b + sc_b))
+    data = np.stack([pages[bt_row[j // 64], (j % 64) * data_b:(j % 64 + 1) * data_b] for j in range(n)])
+    sc = np.stack([pages[bt_row[j // 64], 64 * data_b + (j % 64) * sc_b: 64 * data_b + (j % 64 + 1) * sc_b]
+                   for j in range(n)])
+    return data, sc
+
+
+def run_gpu_streams(kind, ratio, streams, chunks, cos_sin):
+    """streams: list of (kv_score bits [T_b, row], ape, w) per sequence -- all sequences
+    share ape / w (one layer).  chunks: per-step token counts per sequence (list of
+    lists) or None for one token per step.  Returns per-sequence cache entries."""
+    nseq = len(streams)
+    d = 576 if kind == B.CACHE_MLA else 128
+    coff = 2 if ratio == 4 else 1
+    ape, w = streams[0][1], streams[0][2]
+    n_ent = [s[0].shape[0] // ratio for s in streams]
+    pps = max(1, (max(n_ent) + 63) // 64)
+    g = synth.rng(99)
+    bt = synth.page_tables(g, nseq, pps, extra_pages=2)
+    page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
+    cache = torch.zeros((nseq * pps + 2) * page_b, dtype=torch.uint8, device="cuda")
+    state = torch.zeros((nseq, coff * ratio, 2 * coff * d), dtype=torch.float32, device="cuda")
+    t_ape, t_w, t_cs, t_bt = dev(ape), dev(w), dev(cos_sin), dev(bt)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t_ks = [bits_tensor(s[0]) for s in streams]
+    pos = [0] * nseq
+    step = 0
+    while any(pos[b] < streams[b][0].shape[0] for b in range(nseq)):
+        rows, ps, sq = [], [], []
+        for b in range(nseq):
+            n_b = streams[b][0].shape[0]
+            if pos[b] >= n_b:
+                continue
+            take = 1 if chunks is None else chunks[b][step % len(chunks[b])]
+            take = min(take, n_b - pos[b])
+            rows.append(t_ks[b][pos[b]:pos[b] + take])
+            ps += list(range(pos[b], pos[b] + take))
+            sq += [b] * take
+            pos[b] += take
+        kv = torch.cat(rows, 0).contiguous()
+        one = len(sq) == len(set(sq))
+        B.compress_insert(kind, ratio, kv, dev(np.array(ps, np.int32)), dev(np.array(sq, np.int32)),
+                          t_ape, t_w, EPS, t_cs, state, cache, t_bt, nseq, one_token_per_seq=one,
+                          status=status)
+        step += 1
+    torch.cuda.synchronize()
+    st, bits = B.read_device_status(status)
+    assert st == B.OK, bits
+    host = cache.cpu().numpy()
+    return [entries_from_pages(kind, host, bt[b], n_ent[b]) for b in range(nseq)]
+
+
+def oracle_entries(kind, ratio, ks, ape, w, cos_sin):
+    nope = 512 if kind == B.CACHE_MLA else 64
+    data, sc = oracle.compress_stream(kind, ratio, ks, ape, w, EPS, cos_sin, nope_dim=nope)
+    if kind == B.CACHE_IDX:
+        sc = sc.view(np.uint8).reshape(-1, 4)
+    return data, sc
+
+
+def assert_bytes_equal(got, want, what):
+    gd, gs = got
+    wd, ws = want
+    assert gd.shape == wd.shape, what
+    bad = np.nonzero(np.any(gd != wd, axis=1) | np.any(gs != ws, axis=1))[0]
+    assert bad.size == 0, "%s: %d of %d entries differ, first %s" % (what, bad.size, gd.shape[0], bad[:8])
+
+
+@pytest.mark.parametrize("kind,ratio,n_tok", [(B.CACHE_MLA, 4, 512), (B.CACHE_IDX, 4, 512),
+                                              (B.CACHE_MLA, 128, 384)])
+def test_decode_stream_bit_exact(kind, ratio, n_tok):
+    ks, ape, w = make_stream(kind, ratio, n_tok, seed=kind * 10 + ratio, w_ones=(ratio == 4))
+    cs = oracle.rope_table(n_tok, 64)
+    got = run_gpu_streams(kind, ratio, [(ks, ape, w)], None, cs)[0]
+    assert_bytes_equal(got, oracle_entries(kind, ratio, ks, ape, w, cs), "decode stream")
+
+
+@pytest.mark.parametrize("kind,ratio", [(B.CACHE_MLA, 4), (B.CACHE_IDX, 4), (B.CACHE_MLA, 128)])
+def test_chunked_stream_bit_exact(kind, ratio):
+    n_tok = 700 if ratio == 4 else 600
+    ks, ape, w = make_stream(kind, ratio, n_tok, seed=77 + ratio)
+    cs = oracle.rope_table(n_tok, 64)
+    chunks = [[1, 3, 7, 16, 2, 64, 5, 200, 9]]   # spans ring-size chunks (200 > 128)
+    got = run_gpu_streams(kind, ratio, [(ks, ape, w)], chunks, cs)[0]
+    assert_bytes_equal(got, oracle_entries(kind, ratio, ks, ape, w, cs), "chunked stream")
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_batched_sequences_bit_exact(ratio):
+    lens = [13, 200, 517, 3] if ratio == 4 else [130, 300, 256]
+    ks0, ape, w = make_stream(B.CACHE_MLA, ratio, 1, seed=5)
+    streams = []
+    for i, L in enumerate(lens):
+        ks, _, _ = make_stream(B.CACHE_MLA, ratio, L, seed=500 + i)
+        streams.append((ks, ape, w))
+    cs = oracle.rope_table(max(lens), 64)
+    for chunks in [None, [[1, 2, 3]] * len(lens)]:
+        got = run_gpu_streams(B.CACHE_MLA, ratio, streams, chunks, cs)
+        for b, (ks, _, _) in enumerate(streams):
+            if ks.shape[0] >= ratio:
+                assert_bytes_equal(got[b], oracle_entries(B.CACHE_MLA, ratio, ks, ape, w, cs),
+                                   "seq %d" % b)
+
+
+@pytest.mark.parametrize("kind", [B.CACHE_MLA, B.CACHE_IDX])
+def test_insert_rows_bit_exact(kind):
+    g = synth.rng(31 + kind)
+    d = 576 if kind == B.CACHE_MLA else 128
+    n = 300
+    rows = synth.normal(g, (n, d), 1.0)
+    rows *= (10.0 ** g.uniform(-6, 3, size=(n, 1))).astype(np.float32)
+    rows[0] = 0.0
+    rows[1, :64] = 1e-30
+    rows[2, :64] = 448.0
+    nseq = 2
+    pps = 4
+    bt = synth.page_tables(g, nseq, pps)
+    seqs = np.array([i % nseq for i in range(n)], np.int32)
+    slots = np.array([i // nseq for i in range(n)], np.int32)
+    page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
+    cache = torch.zeros(nseq * pps * page_b, dtype=torch.uint8, device="cuda")
+    B.cache_insert_rows(kind, dev(rows), dev(seqs), dev(slots), cache, dev(bt))
+    host = cache.cpu().numpy()
+    if kind == B.CACHE_MLA:
+        wd, ws = oracle.quant_mla_rows(rows)
+    else:
+        wd, wsf = oracle.quant_idx_rows(rows)
+        ws = wsf.view(np.uint8).reshape(-1, 4)
+    for b in range(nseq):
+        sel = seqs == b
+        got = entries_from_pages(kind, host, bt[b], int(sel.sum()))
+        assert_bytes_equal(got, (wd[sel], ws[sel]), "insert rows seq %d" % b)

@@ -1,0 +1,78 @@
+"""GPU parity of dsv4_indexer_topk: index sets equal the oracle's, except slots
+whose oracle score lies within 1e-3 relative of the k-th score."""
+import numpy as np
+import pytest
+import torch
+
+from deepseek_v4_compressed_gb300 import binding as B
+
+from _util import check_topk, make_decode_inputs, oracle_indexer
+
+pytestmark = pytest.mark.gpu
+
+
+def run_indexer(d, max_ctx=None, seqs=None):
+    plan = B.Plan(B.C4A, d.n_heads, d.batch, d.topk, int(max_ctx or d.ctx.max()), idx_heads=d.idx_heads)
+    ws = plan.workspace()
+    out_idx = torch.full((d.batch, d.topk), -7, dtype=torch.int32, device="cuda")
+    out_len = torch.full((d.batch,), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.indexer_topk(plan, d.t["qi"], d.t["w"], d.t["idx"], d.t["idx_bt"], d.t["ctx"], out_idx, out_len, ws,
+                   status=status)
+    torch.cuda.synchronize()
+    st, bits = B.read_device_status(status)
+    assert st == B.OK, bits
+    return out_idx.cpu().numpy(), out_len.cpu().numpy()
+
+
+def check_all(d, idx, ln, seqs=None):
+    tolerated = 0
+    for b in (range(d.batch) if seqs is None else seqs):
+        tolerated += check_topk(idx[b], int(ln[b]), oracle_indexer(d, b), d.topk)
+    return tolerated
+
+
+def test_tiny_c4a():
+    d = make_decode_inputs(4, 1, 512, 8, 4, 32, seed=0, with_comp=False)
+    idx, ln = run_indexer(d)
+    assert ln[0] == 32
+    check_all(d, idx, ln)
+
+
+def test_ragged_contexts_and_short_sequences():
+    # n_c = 0, 1, 25, 64 (= k), 512, 1250: covers n_c <= k, a ragged last tile and empty
+    ctx = np.array([3, 4, 100, 256, 2049, 5000], np.int32)
+    d = make_decode_inputs(4, len(ctx), ctx, 8, 64, 64, seed=21, with_comp=False)
+    idx, ln = run_indexer(d)
+    assert list(ln) == [0, 1, 25, 64, 64, 64]
+    check_all(d, idx, ln)
+
+
+def test_c4a_32k_batch32_full_size():
+    d = make_decode_inputs(4, 32, 32768, 64, 64, 512, seed=1, with_comp=False)
+    idx, ln = run_indexer(d)
+    assert np.all(ln == 512)
+    tol = check_all(d, idx, ln)
+    print("near-tie slots tolerated:", tol)
+
+
+def test_plan_max_ctx_larger_than_batch_contexts():
+    ctx = np.array([1000, 4001, 16], np.int32)
+    d = make_decode_inputs(4, 3, ctx, 8, 16, 128, seed=22, with_comp=False)
+    idx, ln = run_indexer(d, max_ctx=70000)
+    check_all(d, idx, ln)
+
+
+def test_long_c4a_1m_full_size():
+    d = make_decode_inputs(4, 4, 1048576, 8, 64, 2048, seed=4, with_comp=False)
+    idx, ln = run_indexer(d)
+    assert np.all(ln == 2048)
+    check_all(d, idx, ln)
+
+
+def test_deterministic_across_runs():
+    d = make_decode_inputs(4, 8, 20000, 8, 64, 256, seed=23, with_comp=False)
+    first = run_indexer(d)
+    for _ in range(5):
+        again = run_indexer(d)
+        assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
