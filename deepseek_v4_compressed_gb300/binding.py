@@ -286,3 +286,16 @@ def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspa
                 _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status))
     _check(lib().dsv4_sparse_mla_decode(plan.handle, ctypes.byref(a), _ptr(workspace),
                                         workspace.numel(), _stream(stream)), "sparse_mla_decode")
+
+
+def indexer_topk_noalloc(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx, out_len,
+                         status=None, stream=None):
+    """dsv4_indexer_topk_noalloc: the indexer without a caller workspace (scratch in a
+    4 MiB device array the library owns; overlapping calls race on it)."""
+    f = lib().dsv4_indexer_topk_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.POINTER(IndexerArgs), ctypes.c_void_p]
+    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // IDX_PAGE_BYTES),
+                    _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
+                    int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
+    _check(f(plan.handle, ctypes.byref(a), _stream(stream)), "indexer_topk_noalloc")

@@ -305,6 +305,28 @@ typedef struct dsv4_indexer_args {
 dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_indexer_args* args,
                               void* workspace_dev, size_t workspace_bytes, dsv4_stream_t stream);
 
+/* Allocation-free variant of dsv4_indexer_topk.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory or own a workspace -- e.g. a plugin inside a serving engine
+ * whose allocator owns every device allocation, or a restricted deployment
+ * where cudaMalloc is not permitted.  It computes exactly what
+ * dsv4_indexer_topk computes, but the per-query logits live in a file-scope
+ * device array of 4 MiB that every GPU loading the library holds until the
+ * process exits; no call allocates or frees memory.
+ *   - Limit: the plan's workspace (batch x max_slots fp32 logits, 256-byte
+ *     aligned) must fit in 4 MiB, e.g. batch 32 at context 131072 or batch 4
+ *     at context 1,048,576; larger plans return DSV4_ERR_UNSUPPORTED and
+ *     launch nothing.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array: calls whose executions overlap on the
+ *     GPU (other streams, other host threads) race on it.  Nothing in it has
+ *     to start at zero; each call writes every logit it reads.
+ * Arguments and errors otherwise as dsv4_indexer_topk. */
+dsv4_status dsv4_indexer_topk_noalloc(const dsv4_plan* plan, const dsv4_indexer_args* args,
+                                      dsv4_stream_t stream);
+
 /* ---- (3) sparse MLA decode --------------------------------------------------- */
 
 /* [vLLM-classes] _forward_decode (SWA indices plus the compressed top-k,
