@@ -3,10 +3,58 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "dsv4_common.cuh"
 #include "plan.h"
+#include "tmap.h"
 
 using namespace dsv4;
+
+namespace dsv4 {
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle)
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (fn == nullptr) return false;
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    const CUresult r = fn(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
+}  // namespace dsv4
 
 extern "C" int dsv4_version(void) { return DSV4_VERSION; }
 
@@ -121,7 +169,15 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
     p->max_ctx = max_ctx;
     p->max_slots = (type == DSV4_C4A) ? max_ctx / 4 : (type == DSV4_C128A ? max_ctx / 128 : 0);
     p->max_keys = p->topk + g->window;
-    p->idx_ctas_per_seq = (type == DSV4_C4A) ? (p->max_slots + 127) / 128 : 0;
+    if (type == DSV4_C4A) {
+        // indexer: 128-slot tiles spread so about three CTAs per SM stay resident
+        const int tiles = (p->max_slots + 127) / 128;
+        const int target = 3 * sm_count();
+        int per_seq = (target + batch - 1) / batch;
+        per_seq = per_seq < 1 ? 1 : (per_seq > tiles ? tiles : per_seq);
+        p->idx_tiles_per_cta = tiles > 0 ? (tiles + per_seq - 1) / per_seq : 1;
+        p->idx_ctas_per_seq = tiles > 0 ? (tiles + p->idx_tiles_per_cta - 1) / p->idx_tiles_per_cta : 0;
+    }
     p->mla_head_groups = (g->n_heads + 63) / 64;
     p->mla_splits = 1;
     p->mla_keys_per_split = p->max_keys;

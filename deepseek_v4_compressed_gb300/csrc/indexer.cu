@@ -7,58 +7,201 @@
 // C4A and C128A top-k", "DeepSeek V4 attention in vLLM").
 #include "dsv4_common.cuh"
 #include "plan.h"
+#include "tc_common.cuh"
+#include "tmap.h"
 
 namespace dsv4 {
 
 // ---------------------------------------------------------------------------
-// Logits on the CUDA cores: one thread per slot, q in shared memory.
+// Logits on the tensor cores.  Per 128-slot tile (two 64-entry pages, each a
+// contiguous 8 KB plane of FP8 rows), one tcgen05.mma kind::f8f6f4 chain
+// D[128 slots x N heads] = K_tile[128 x 128] * Q^T[128 x N] (fp32 in TMEM),
+// then each of 128 epilogue threads turns its slot's row of D into
+// I_s = scale_s * sum_j w_j * max(D_sj, 0).
+//   warp 4: TMA producer (query once, then two page loads per tile, 3-stage ring)
+//   warp 5: MMA issuer (4 MMAs of K=32 per tile, double-buffered accumulator)
+//   warps 0-3: epilogue (TMEM lane = slot row)
+// Memory-bound: 132 bytes of cache per slot against 2 * 128 * N flops.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) indexer_logits_simt(
-    const uint8_t* __restrict__ q_fp8, const float* __restrict__ w, int H,
-    const uint8_t* __restrict__ cache, int num_pages, const int* __restrict__ bt, int bt_stride,
-    const int* __restrict__ ctx_len, float* __restrict__ logits, int max_slots, int* status)
+constexpr int kIdxTileSlots = 128;
+constexpr int kIdxStages = 3;
+constexpr int kIdxTileBytes = kIdxTileSlots * kIdx;       // 16 KB
+constexpr int kIdxQBytes = 64 * kIdx;                     // query tile, N <= 64 rows
+constexpr int kIdxThreads = 192;
+constexpr int kIdxTmemCols = 128;                         // 2 accumulators x 64 columns
+constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + 1024 /* barriers etc */ + 1024 /* align */;
+
+struct IdxTcParams {
+    const uint8_t* cache;
+    int num_pages;
+    const int* bt;
+    int bt_stride;
+    const int* ctx_len;
+    const float* w;
+    int H;
+    int n_pad;
+    float* logits;
+    int max_slots;
+    int tiles_per_cta;
+    int* status;
+};
+
+__global__ void __launch_bounds__(kIdxThreads, 1)
+indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_q,
+                  IdxTcParams P)
 {
-    __shared__ float qs[DSV4_MAX_IDX_HEADS * kIdx];
-    __shared__ float ws[DSV4_MAX_IDX_HEADS];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_tiles = smem;
+    uint8_t* q_tile = smem + kIdxStages * kIdxTileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_tile + kIdxQBytes);
+    uint64_t* full = bars;                        // [kIdxStages]
+    uint64_t* empty = bars + kIdxStages;          // [kIdxStages]
+    uint64_t* acc_full = bars + 2 * kIdxStages;   // [2]
+    uint64_t* acc_empty = acc_full + 2;           // [2]
+    uint64_t* q_bar = acc_empty + 2;
+    float* w_s = reinterpret_cast<float*>(q_bar + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_s + 64);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
     const int b = blockIdx.y;
-    int n_c = ctx_len[b] / 4;
-    if (n_c > max_slots) n_c = max_slots;
-    if (static_cast<int>(blockIdx.x) * 128 >= n_c) return;
-    const uint8_t* qb = q_fp8 + static_cast<long long>(b) * H * kIdx;
-    for (int i = threadIdx.x; i < H * kIdx; i += blockDim.x) qs[i] = e4m3_to_f32(qb[i]);
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ws[i] = w[static_cast<long long>(b) * H + i];
+    int n_c = P.ctx_len[b] / 4;
+    if (n_c > P.max_slots) n_c = P.max_slots;
+    if (n_c < 0) n_c = 0;
+    const int n_tiles = (n_c + kIdxTileSlots - 1) / kIdxTileSlots;
+    const int t_begin = blockIdx.x * P.tiles_per_cta;
+    const int t_end = min(n_tiles, t_begin + P.tiles_per_cta);
+    if (t_begin >= t_end) return;                 // uniform: nothing allocated yet
+    const int n_my = t_end - t_begin;
+    const int n_pages = (n_c + kPage - 1) / kPage;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kIdxStages; ++i) {
+            tc::mbar_init(tc::smem_u32(&full[i]), 1);
+            tc::mbar_init(tc::smem_u32(&empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
+            tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
+        }
+        tc::mbar_init(tc::smem_u32(q_bar), 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (threadIdx.x < 64) w_s[threadIdx.x] = (threadIdx.x < P.H) ? P.w[static_cast<long long>(b) * P.H + threadIdx.x] : 0.f;
+    if (warp == 0) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kIdxTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
     __syncthreads();
-    const int s = blockIdx.x * 128 + threadIdx.x;
-    if (s >= n_c) return;
-    const int pi = s / kPage;
-    int pg = (pi < bt_stride) ? bt[static_cast<long long>(b) * bt_stride + pi] : -1;
-    if (pg < 0 || pg >= num_pages) {
-        flag(status, DSV4_DEV_BAD_PAGE);
-        logits[static_cast<long long>(b) * max_slots + s] = -INFINITY;
-        return;
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int issued = 0;   // tiles whose loads were issued (producer only)
+    int consumed = 0; // tiles whose stage the MMA released (MMA thread only)
+
+    if (warp == 4) {
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm_cache);
+            tc::prefetch_tensormap(&tm_q);
+            tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
+            tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
+            for (int i = 0; i < n_my; ++i) {
+                const int st = i % kIdxStages;
+                const uint32_t ph = (i / kIdxStages) & 1;
+                if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status)) break;
+                const int tile = t_begin + i;
+                int pg[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int pi = min(2 * tile + h, n_pages - 1);
+                    int v = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                    if (v < 0 || v >= P.num_pages) {
+                        flag(P.status, DSV4_DEV_BAD_PAGE);
+                        v = P.num_pages;          // out of the map: TMA fills zeros
+                    }
+                    pg[h] = v;
+                }
+                const uint32_t dst = tc::smem_u32(a_tiles + st * kIdxTileBytes);
+                tc::mbar_arrive_expect_tx(tc::smem_u32(&full[st]), kIdxTileBytes);
+                tc::tma_load_3d(dst, &tm_cache, tc::smem_u32(&full[st]), 0, 0, pg[0]);
+                tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, tc::smem_u32(&full[st]), 0, 0, pg[1]);
+                issued = i + 1;
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc(128, P.n_pad, tc::kFmtE4M3, tc::kFmtE4M3);
+            const uint64_t b_desc = tc::desc_kmajor_sw128(tc::smem_u32(q_tile));
+            if (tc::mbar_wait(tc::smem_u32(q_bar), 0, abort_flag, P.status)) {
+                for (int i = 0; i < n_my; ++i) {
+                    const int st = i % kIdxStages;
+                    const uint32_t ph = (i / kIdxStages) & 1;
+                    const int ab = i & 1;
+                    const uint32_t aph = (i >> 1) & 1;
+                    if (!tc::mbar_wait(tc::smem_u32(&full[st]), ph, abort_flag, P.status)) break;
+                    if (i >= 2 && !tc::mbar_wait(tc::smem_u32(&acc_empty[ab]), aph ^ 1, abort_flag, P.status)) break;
+                    tc::tc_fence_after();
+                    const uint64_t a_desc = tc::desc_kmajor_sw128(tc::smem_u32(a_tiles + st * kIdxTileBytes));
+                    const uint32_t d = tmem + ab * 64;
+#pragma unroll
+                    for (int k = 0; k < kIdx / 32; ++k)   // K = 32 FP8 (32 bytes) per instruction
+                        tc::mma_f8f6f4(d, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    tc::mma_commit(tc::smem_u32(&empty[st]));
+                    tc::mma_commit(tc::smem_u32(&acc_full[ab]));
+                    consumed = i + 1;
+                }
+            }
+        }
+    } else {
+        const int row = warp * 32 + lane;
+        for (int i = 0; i < n_my; ++i) {
+            const int ab = i & 1;
+            const uint32_t aph = (i >> 1) & 1;
+            if (!tc::mbar_wait(tc::smem_u32(&acc_full[ab]), aph, abort_flag, P.status)) break;
+            tc::tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + ab * 64;
+            float v0[32], v1[32];
+            tc::tmem_ld32(taddr, v0);
+            if (P.n_pad > 32) tc::tmem_ld32(taddr + 32, v1);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acc_empty[ab]));
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc += (j < P.H) ? w_s[j] * fmaxf(v0[j], 0.f) : 0.f;
+            if (P.n_pad > 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
+            }
+            const int s = (t_begin + i) * kIdxTileSlots + row;
+            if (s < n_c) {
+                const int pi = s / kPage;
+                const int pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                float out = -INFINITY;
+                if (pg >= 0 && pg < P.num_pages)
+                    out = acc * reinterpret_cast<const float*>(P.cache + static_cast<long long>(pg) * kIdxPage +
+                                                               kPage * kIdx)[s % kPage];
+                P.logits[static_cast<long long>(b) * P.max_slots + s] = out;
+            }
+        }
     }
-    const uint8_t* page = cache + static_cast<long long>(pg) * kIdxPage;
-    const int r = s % kPage;
-    float k[kIdx];
-    const uint4* src = reinterpret_cast<const uint4*>(page + r * kIdx);
-#pragma unroll
-    for (int v = 0; v < kIdx / 16; ++v) {
-        uint4 u = src[v];
-        const uint32_t words[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) k[v * 16 + q * 4 + bb] = e4m3_to_f32((words[q] >> (8 * bb)) & 0xff);
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp == 4 && lane == 0) {
+        // let this CTA's own copies land before its shared memory is released
+        for (int i = consumed > 0 ? consumed : 0; i < issued; ++i) {
+            volatile int no_abort = 0;
+            tc::mbar_wait(tc::smem_u32(&full[i % kIdxStages]), (i / kIdxStages) & 1, &no_abort, nullptr);
+        }
     }
-    const float scale = reinterpret_cast<const float*>(page + kPage * kIdx)[r];
-    float acc = 0.f;
-    for (int j = 0; j < H; ++j) {
-        float dot = 0.f;
-#pragma unroll
-        for (int c = 0; c < kIdx; ++c) dot = fmaf(qs[j * kIdx + c], k[c], dot);
-        acc = fmaf(ws[j], fmaxf(dot, 0.f), acc);
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kIdxTmemCols);
     }
-    logits[static_cast<long long>(b) * max_slots + s] = scale * acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -229,13 +372,45 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_logits_off);
     const int B = plan->batch, H = plan->geom.idx_heads;
-    dim3 grid((plan->max_slots + 127) / 128, B);
-    indexer_logits_simt<<<grid, 128, 0, st>>>(
-        static_cast<const uint8_t*>(a->q_fp8_dev), a->weights_dev, H,
-        static_cast<const uint8_t*>(a->idx_cache_dev), a->num_pages, a->block_table_dev, a->bt_stride,
-        a->ctx_len_dev, logits, plan->max_slots, a->status_dev);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return DSV4_ERR_CUDA;
+    if (plan->idx_ctas_per_seq > 0) {
+        CUtensorMap tm_cache, tm_q;
+        const uint64_t cdims[3] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(kPage),
+                                   static_cast<uint64_t>(a->num_pages)};
+        const uint64_t cstr[2] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(kIdxPage)};
+        const uint32_t cbox[3] = {static_cast<uint32_t>(kIdx), static_cast<uint32_t>(kPage), 1};
+        const int n_pad = H <= 16 ? 16 : (H + 15) / 16 * 16;
+        const uint64_t qdims[2] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(B) * H};
+        const uint64_t qstr[1] = {static_cast<uint64_t>(kIdx)};
+        const uint32_t qbox[2] = {static_cast<uint32_t>(kIdx), static_cast<uint32_t>(n_pad)};
+        if (!encode_tmap(&tm_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a->idx_cache_dev, cdims, cstr, cbox,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a->q_fp8_dev, qdims, qstr, qbox,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return DSV4_ERR_CUDA;
+        IdxTcParams P;
+        P.cache = static_cast<const uint8_t*>(a->idx_cache_dev);
+        P.num_pages = a->num_pages;
+        P.bt = a->block_table_dev;
+        P.bt_stride = a->bt_stride;
+        P.ctx_len = a->ctx_len_dev;
+        P.w = a->weights_dev;
+        P.H = H;
+        P.n_pad = n_pad;
+        P.logits = logits;
+        P.max_slots = plan->max_slots;
+        P.tiles_per_cta = plan->idx_tiles_per_cta;
+        P.status = a->status_dev;
+        static bool tc_attr = false;
+        if (!tc_attr) {
+            cudaFuncSetAttribute(indexer_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem);
+            tc_attr = true;
+        }
+        dim3 grid(plan->idx_ctas_per_seq, B);
+        indexer_logits_tc<<<grid, kIdxThreads, kIdxSmem, st>>>(tm_cache, tm_q, P);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return DSV4_ERR_CUDA;
+    }
+    cudaError_t e;
     const int smem_keys = plan->max_slots <= kTopkSmemKeys ? plan->max_slots : 0;
     const size_t smem = static_cast<size_t>(smem_keys) * 4;
     static bool attr_set = false;
