@@ -179,8 +179,16 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
         p->idx_ctas_per_seq = tiles > 0 ? (tiles + p->idx_tiles_per_cta - 1) / p->idx_tiles_per_cta : 0;
     }
     p->mla_head_groups = (g->n_heads + 63) / 64;
-    p->mla_splits = 1;
-    p->mla_keys_per_split = p->max_keys;
+    // attention: the keys of a (sequence, head group) are split over a cluster
+    // of 1, 2, 4 or 8 CTAs, the largest that keeps every CTA on its own SM
+    {
+        const int units = batch * p->mla_head_groups;
+        const int sms = sm_count();
+        int c = 8;
+        while (c > 1 && units * c > sms) c >>= 1;
+        p->mla_splits = c;
+        p->mla_keys_per_split = (p->max_keys + c - 1) / c;
+    }
     size_t off = 0;
     p->ws_logits_off = off;
     if (type == DSV4_C4A) off += align256(static_cast<size_t>(batch) * p->max_slots * sizeof(float));
@@ -213,7 +221,7 @@ extern "C" dsv4_status dsv4_plan_get_info(const dsv4_plan* p, dsv4_plan_info* in
     info->mla_keys_per_split = p->mla_keys_per_split;
     info->workspace_bytes = p->ws_bytes;
     info->launches_indexer = (p->type == DSV4_C4A) ? 2 : 0;
-    info->launches_mla = 1;
+    info->launches_mla = 1;   // one cluster launch; partials merge through DSMEM
     return DSV4_OK;
 }
 

@@ -8,6 +8,8 @@
 // cached latent in section 2.2 of "From MLA to CSA + HCA".
 #include "dsv4_common.cuh"
 #include "plan.h"
+#include "tc_common.cuh"
+#include "tmap.h"
 
 namespace dsv4 {
 
@@ -76,105 +78,422 @@ __device__ __forceinline__ bool key_ref(const MlaParams& P, int b, int i, int n_
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core version: CTA = (head group of 8, sequence), 256 threads; keys in
-// chunks of 32 dequantised into shared memory; online softmax per head.
+// Tensor-core decode attention (tcgen05, TMEM accumulators).
+//
+// CTA = (rank r of a cluster of C CTAs, sequence b x 64-head group g).  The C
+// CTAs of a cluster split the sequence's keys (selected compressed slots then
+// the SWA window) into contiguous ranges, each CTA walks its range in 32-key
+// tiles with an online softmax, and the partial results are merged through
+// distributed shared memory -- no partials in HBM, no combine kernel.
+//
+//   S  = Q K^T     tcgen05.mma kind::f16, M = 128 head rows (64 real; the
+//                  padding rows alias neighbouring shared memory and are never
+//                  read back), N = 32 keys, K = 576 (36 instructions);
+//                  double-buffered in TMEM columns [0, 64).
+//   O^T += V^T P^T M = 128 value dims (4 blocks cover the 512 latent dims),
+//                  N = 64 heads, K = 32 keys; V^T is the same swizzled K tile
+//                  read as an MN-major operand; O^T lives in TMEM [64, 320).
+// Warps: 0-3 softmax (lanes 0-63 = heads) and O^T correction (all lanes);
+// 4-7 producers: gather and dequantise key rows (FP8 * 2^e -> bf16, exact) into
+// the 128-byte-swizzled tile; 8 MMA issuer (and the Q load by TMA).
 // ---------------------------------------------------------------------------
-constexpr int kSimtHeads = 8;
-constexpr int kSimtKeys = 32;
-constexpr int kSimtRow = kHead + 1;   // padded row (bank-conflict free column reads)
+constexpr int kTcKeys = 32;
+constexpr int kTcStages = 3;
+constexpr int kTcQChunk = 64 * 128;                        // 64 head rows x 64 dims (bf16)
+constexpr int kTcQBytes = 9 * kTcQChunk;                   // 73728
+constexpr int kTcKChunk = kTcKeys * 128;                   // 32 key rows x 64 dims
+constexpr int kTcKBytes = 9 * kTcKChunk;                   // 36864 per stage
+constexpr int kTcPBytes = 64 * 128;                        // 64 head rows x 32 keys (rows padded to 128 B)
+constexpr int kTcThreads = 288;
+constexpr int kTcTmemCols = 512;
+constexpr int kTcOCol = 64;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTcQBytes;
+constexpr int kOffP = kOffK + kTcStages * kTcKBytes;
+constexpr int kOffMisc = kOffP + 2 * kTcPBytes;
+constexpr int kMiscBytes = 4096;
+constexpr int kTcSmem = kOffMisc + kMiscBytes + 1024;
+constexpr int kStageO = 0;                                 // epilogue: fp32 [64 heads][512] (reuses Q/K space)
+static_assert(64 * 512 * 4 <= kOffP, "staging must fit in the Q/K space");
 
-__global__ void __launch_bounds__(256) mla_decode_simt(MlaParams P)
+struct MlaTcParams {
+    MlaParams base;
+    int head_groups;
+    int cluster;
+};
+
+__device__ __forceinline__ float ex2_approx(float x)
 {
-    extern __shared__ float smem[];
-    float* qs = smem;                              // [8][576]
-    float* ks = qs + kSimtHeads * kHead;           // [32][577]
-    float* ps = ks + kSimtKeys * kSimtRow;         // [8][32]
-    __shared__ float s_m[kSimtHeads], s_l[kSimtHeads], s_alpha[kSimtHeads];
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-    const int b = blockIdx.y;
-    const int h0 = blockIdx.x * kSimtHeads;
-    const int nh = min(kSimtHeads, P.H - h0);
-    const int tid = threadIdx.x;
+// 16 FP8 codes scaled by 2^e -> 16 bf16 (exact: 4 significant bits fit).
+__device__ __forceinline__ void dequant16(const uint4 w, float mult, uint4& lo, uint4& hi)
+{
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((in[i] >> (16 * h)) & 0xffff);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x * mult, f.y * mult);
+            out[2 * i + h] = *reinterpret_cast<const uint32_t*>(&bb);
+        }
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+__device__ __forceinline__ float ue8m0_mult(uint32_t byte)
+{
+    const int e = static_cast<int>(byte) - 127;
+    return e >= -126 ? exp2i(e) : exp2i(-126) * 0.5f;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, MlaTcParams T)
+{
+    const MlaParams& P = T.base;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_s = smem + kOffQ;
+    uint8_t* k_s = smem + kOffK;
+    uint8_t* p_s = smem + kOffP;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffMisc);
+    uint64_t* kv_full = bars;          // [3] producers -> MMA
+    uint64_t* kv_empty = bars + 3;     // [3] MMA -> producers
+    uint64_t* s_full = bars + 6;       // [2] MMA -> softmax
+    uint64_t* p_full = bars + 8;       // [2] softmax -> MMA (P written, S read, O^T corrected)
+    uint64_t* pv_done = bars + 10;     // [2] MMA -> softmax
+    uint64_t* q_full = bars + 12;
+    uint64_t* sync4 = bars + 13;       // [2] the four softmax warps meet once per tile
+    float* sm_m = reinterpret_cast<float*>(bars + 16);   // [64] running max (log2 domain)
+    float* sm_l = sm_m + 64;                              // [64] running sum
+    float* sm_alpha = sm_l + 64;                          // [64] correction factors of this tile
+    float* red_w = sm_alpha + 64;                         // [8][64] merge weights
+    float* red_invl = red_w + 8 * 64;                     // [64]
+    int* sm_any = reinterpret_cast<int*>(red_invl + 64);  // [2][4]
+    volatile int* abort_flag = sm_any + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm_any + 9);
+
+    const int rank = blockIdx.x;
+    const int b = blockIdx.y / T.head_groups, g = blockIdx.y % T.head_groups;
+    const int h0 = g * 64;
+    const int nh = min(64, P.H - h0);
     const int p = P.ctx_len[b] - 1;
-    const int n_comp = P.idx_len ? max(0, P.idx_len[b]) : 0;
+    const int n_comp = P.idx_len ? min(max(P.idx_len[b], 0), P.idx_stride) : 0;
     const int t0 = max(0, p - P.window + 1);
     const int n_keys = n_comp + (p >= 0 ? p - t0 + 1 : 0);
+    const int per = (n_keys + T.cluster - 1) / T.cluster;
+    const int k0 = min(n_keys, rank * per), k1 = min(n_keys, k0 + per);
+    const int n_tiles = (k1 - k0 + kTcKeys - 1) / kTcKeys;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float scale_log2 = P.scale * 1.4426950408889634f;
 
-    for (int i = tid; i < kSimtHeads * kHead; i += 256) {
-        const int h = i / kHead;
-        qs[i] = (h < nh) ? bf16_bits_to_f32(P.q[(static_cast<long long>(b) * P.H + h0 + h) * kHead + i % kHead]) : 0.f;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; ++i) {
+            tc::mbar_init(tc::smem_u32(&kv_full[i]), 4);
+            tc::mbar_init(tc::smem_u32(&kv_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(tc::smem_u32(&s_full[i]), 1);
+            tc::mbar_init(tc::smem_u32(&p_full[i]), 4);
+            tc::mbar_init(tc::smem_u32(&pv_done[i]), 1);
+        }
+        tc::mbar_init(tc::smem_u32(q_full), 1);
+        tc::mbar_init(tc::smem_u32(&sync4[0]), 4);
+        tc::mbar_init(tc::smem_u32(&sync4[1]), 4);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
     }
-    if (tid < kSimtHeads) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
+    if (threadIdx.x < 64) {
+        sm_m[threadIdx.x] = -INFINITY;
+        sm_l[threadIdx.x] = 0.f;
     }
-    // thread owns head hh = tid / 32 and dims v = lane + 32 * u (u < 16)
-    const int hh = tid >> 5, lane = tid & 31;
-    float acc[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    if (warp == 0) {
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTcTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
     __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    for (int base = 0; base < n_keys; base += kSimtKeys) {
-        const int nk = min(kSimtKeys, n_keys - base);
-        // stage keys: 32 rows x 576 values, 8 warps x 4 rows
-        for (int kk = tid >> 5; kk < kSimtKeys; kk += 8) {
-            float* dst = ks + kk * kSimtRow;
-            KeyRef kr;
-            const bool ok = kk < nk && key_ref(P, b, base + kk, n_comp, t0, kr);
-            if (!ok) {
-                for (int c = lane; c < kHead; c += 32) dst[c] = 0.f;
-                continue;
-            }
-            if (kr.comp) {
-                for (int c = lane; c < kNope; c += 32)
-                    dst[c] = e4m3_to_f32(kr.row[c]) * exp2i(static_cast<int>(kr.scales[c >> 6]) - 127);
-                const uint16_t* rope = reinterpret_cast<const uint16_t*>(kr.row + kNope);
-                for (int c = lane; c < kRope; c += 32) dst[kNope + c] = bf16_bits_to_f32(rope[c]);
-            } else {
-                const uint16_t* row = reinterpret_cast<const uint16_t*>(kr.row);
-                for (int c = lane; c < kHead; c += 32) dst[c] = bf16_bits_to_f32(row[c]);
-            }
-        }
-        __syncthreads();
-        // scores: thread (hh, key lane)
-        float s = -INFINITY;
-        if (lane < nk && hh < nh) {
-            float dot = 0.f;
-            const float* qr = qs + hh * kHead;
-            const float* kr = ks + lane * kSimtRow;
-            for (int c = 0; c < kHead; ++c) dot = fmaf(qr[c], kr[c], dot);
-            s = dot * P.scale;
-        }
-        const float cmax = warp_max(s);
-        const float m_old = s_m[hh];
-        const float m_new = fmaxf(m_old, cmax);
-        const float pexp = (s == -INFINITY) ? 0.f : __expf(s - m_new);
-        const float csum = warp_sum(pexp);
-        ps[hh * kSimtKeys + lane] = pexp;
-        const float alpha = (m_old == -INFINITY) ? 0.f : __expf(m_old - m_new);
-        __syncthreads();
-        if (lane == 0) {
-            s_m[hh] = m_new;
-            s_l[hh] = s_l[hh] * alpha + csum;
-        }
+    if (n_tiles > 0) {
+        if (warp == 8) {
+            // ------------------------------------------------------------ MMA
+            if (lane == 0) {
+                tc::prefetch_tensormap(&tm_q);
+                tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), kTcQBytes);
+                for (int c = 0; c < 9; ++c)
+                    tc::tma_load_2d(tc::smem_u32(q_s + c * kTcQChunk), &tm_q, tc::smem_u32(q_full), c * 64,
+                                    b * P.H + h0);
+                const uint32_t id_qk = tc::idesc(128, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
+                const uint32_t id_pv = tc::idesc(128, 64, tc::kFmtBF16, tc::kFmtBF16, true, false);
+                bool ok = tc::mbar_wait(tc::smem_u32(q_full), 0, abort_flag, P.status);
+                for (int t = 0; ok && t <= n_tiles; ++t) {
+                    if (t < n_tiles) {
+                        const int st = t % kTcStages;
+                        if (!tc::mbar_wait(tc::smem_u32(&kv_full[st]), (t / kTcStages) & 1, abort_flag, P.status)) break;
+                        tc::tc_fence_after();
+                        const uint32_t d = tmem + (t & 1) * kTcKeys;
+                        const uint32_t kb = tc::smem_u32(k_s + st * kTcKBytes);
+#pragma unroll 1
+                        for (int c = 0; c < 9; ++c) {
+                            const uint64_t ad = tc::desc_kmajor_sw128(tc::smem_u32(q_s + c * kTcQChunk));
+                            const uint64_t bd = tc::desc_kmajor_sw128(kb + c * kTcKChunk);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int v = lane + 32 * u;
-            float a = acc[u] * alpha;
-            for (int kk = 0; kk < nk; ++kk) a = fmaf(ps[hh * kSimtKeys + kk], ks[kk * kSimtRow + v], a);
-            acc[u] = a;
+                            for (int k = 0; k < 4; ++k)
+                                tc::mma_f16(d, ad + 2 * k, bd + 2 * k, id_qk, (c | k) != 0 ? 1u : 0u);
+                        }
+                        tc::mma_commit(tc::smem_u32(&s_full[t & 1]));
+                    }
+                    if (t >= 1) {
+                        const int u = t - 1;
+                        const int ust = u % kTcStages;
+                        if (!tc::mbar_wait(tc::smem_u32(&p_full[u & 1]), (u >> 1) & 1, abort_flag, P.status)) break;
+                        tc::tc_fence_after();
+                        const uint32_t kb = tc::smem_u32(k_s + ust * kTcKBytes);
+                        const uint64_t pd = tc::desc_kmajor_sw128(tc::smem_u32(p_s + (u & 1) * kTcPBytes));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 2; ++j)
+                                tc::mma_f16(tmem + kTcOCol + i * 64,
+                                            tc::desc_mnmajor_sw128(kb + 2 * i * kTcKChunk + j * 2048, kTcKChunk, 1024),
+                                            pd + 2 * j, id_pv, (u > 0 || j > 0) ? 1u : 0u);
+                        tc::mma_commit(tc::smem_u32(&kv_empty[ust]));
+                        tc::mma_commit(tc::smem_u32(&pv_done[u & 1]));
+                    }
+                }
+            }
+        } else if (warp >= 4) {
+            // ------------------------------------------------------ producers
+            const int pt = threadIdx.x - 128;
+            const int r = pt >> 2, sub = pt & 3, sw = r & 7;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % kTcStages;
+                if (t >= kTcStages &&
+                    !tc::mbar_wait(tc::smem_u32(&kv_empty[st]), ((t / kTcStages) & 1) ^ 1, abort_flag, P.status))
+                    break;
+                uint8_t* kst = k_s + st * kTcKBytes;
+                const int key = k0 + t * kTcKeys + r;
+                KeyRef kr;
+                const bool valid = key < k1 && key_ref(P, b, key, n_comp, t0, kr);
+                if (valid && kr.comp) {
+                    const uint4* src = reinterpret_cast<const uint4*>(kr.row);
+                    uint4 d[10];
+#pragma unroll
+                    for (int i = 0; i < 10; ++i) d[i] = __ldg(src + sub + 4 * i);
+                    const uint2 sc = *reinterpret_cast<const uint2*>(kr.scales);
+#pragma unroll
+                    for (int i = 0; i < 10; ++i) {
+                        const int u = sub + 4 * i;            // 16-byte unit of the 640-byte row
+                        if (u < 32) {
+                            const uint32_t byte = ((u >> 2) < 4 ? (sc.x >> (8 * (u >> 2))) : (sc.y >> (8 * ((u >> 2) - 4)))) & 0xff;
+                            uint4 lo, hi;
+                            dequant16(d[i], ue8m0_mult(byte), lo, hi);
+                            const int c = u >> 2, w0 = 2 * (u & 3);
+                            *reinterpret_cast<uint4*>(kst + c * kTcKChunk + r * 128 + ((w0 ^ sw) << 4)) = lo;
+                            *reinterpret_cast<uint4*>(kst + c * kTcKChunk + r * 128 + (((w0 + 1) ^ sw) << 4)) = hi;
+                        } else {
+                            const int w = u - 32;                 // rope: 8 bf16 per unit, chunk 8
+                            *reinterpret_cast<uint4*>(kst + 8 * kTcKChunk + r * 128 + ((w ^ sw) << 4)) = d[i];
+                        }
+                    }
+                } else if (valid) {
+                    const uint4* src = reinterpret_cast<const uint4*>(kr.row);
+                    uint4 d[18];
+#pragma unroll
+                    for (int i = 0; i < 18; ++i) d[i] = __ldg(src + sub + 4 * i);
+#pragma unroll
+                    for (int i = 0; i < 18; ++i) {
+                        const int w = sub + 4 * i;                // 8 bf16 per unit: chunk w/8, unit w%8
+                        *reinterpret_cast<uint4*>(kst + (w >> 3) * kTcKChunk + r * 128 + (((w & 7) ^ sw) << 4)) = d[i];
+                    }
+                } else {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int i = 0; i < 18; ++i) {
+                        const int w = sub + 4 * i;
+                        *reinterpret_cast<uint4*>(kst + (w >> 3) * kTcKChunk + r * 128 + (((w & 7) ^ sw) << 4)) = z;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[st]));
+            }
+        } else {
+            // ------------------------------------------- softmax + O correction
+            const bool real = warp < 2;                   // TMEM lanes 0-63 hold the head rows
+            const int h = warp * 32 + lane;
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int sb = t & 1;
+                if (!tc::mbar_wait(tc::smem_u32(&s_full[sb]), (t >> 1) & 1, abort_flag, P.status)) break;
+                tc::tc_fence_after();
+                const int nvalid = min(kTcKeys, k1 - (k0 + t * kTcKeys));
+                float s[32];
+                float mx = -INFINITY;
+                if (real) {
+                    tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + sb * kTcKeys, s);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        s[j] = (j < nvalid) ? s[j] * scale_log2 : -INFINITY;
+                        mx = fmaxf(mx, s[j]);
+                    }
+                }
+                const float m_new = fmaxf(m, mx);
+                const bool need = real && (m_new > m + 8.0f);
+                const float m_use = need ? m_new : m;
+                uint32_t pk[16];
+                float rowsum = 0.f;
+                if (real) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float e0 = (j < nvalid) ? ex2_approx(s[j] - m_use) : 0.f;
+                        const float e1 = (j + 1 < nvalid) ? ex2_approx(s[j + 1] - m_use) : 0.f;
+                        const __nv_bfloat162 bb = __floats2bfloat162_rn(e0, e1);
+                        const float2 rb = __bfloat1622float2(bb);
+                        rowsum += rb.x + rb.y;
+                        pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
+                    }
+                }
+                if (t >= 1 && !tc::mbar_wait(tc::smem_u32(&pv_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag, P.status))
+                    break;
+                const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
+                if (real) sm_alpha[h] = alpha;
+                const int any_w = __any_sync(0xffffffffu, need);
+                if (lane == 0) sm_any[sb * 4 + warp] = any_w;
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sync4[sb]));
+                if (!tc::mbar_wait(tc::smem_u32(&sync4[sb]), (t >> 1) & 1, abort_flag, P.status)) break;
+                const bool any = (sm_any[sb * 4 + 0] | sm_any[sb * 4 + 1] | sm_any[sb * 4 + 2] | sm_any[sb * 4 + 3]) != 0;
+                if (any && t >= 1) {
+                    tc::tc_fence_after();
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i) {
+#pragma unroll 1
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kTcOCol + i * 64 + half * 32;
+                            float o[32];
+                            tc::tmem_ld32(ta, o);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] *= sm_alpha[half * 32 + j];
+                            tc::tmem_st32(ta, o);
+                        }
+                    }
+                    tc::tmem_st_wait();
+                }
+                if (real) {
+                    l = l * alpha + rowsum;
+                    m = m_use;
+                    uint8_t* prow = p_s + sb * kTcPBytes + h * 128;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4*>(prow + ((u ^ (h & 7)) << 4)) =
+                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&p_full[sb]));
+            }
+            if (real) {
+                sm_m[h] = m;
+                sm_l[h] = l;
+            }
+            tc::mbar_wait(tc::smem_u32(&pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1, abort_flag, P.status);
+            tc::tc_fence_before();
         }
-        __syncthreads();
     }
-    if (hh < nh) {
-        const float l = s_l[hh];
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        uint16_t* o = P.out + (static_cast<long long>(b) * P.H + h0 + hh) * kV;
+
+    // ------------------------------------------------------------- epilogue
+    __syncthreads();
+    tc::tc_fence_after();
+    float* stage_o = reinterpret_cast<float*>(smem + kStageO);    // [64 heads][512]
+    if (n_tiles > 0 && !*abort_flag) {
+        if (warp < 8) {
+            const int q4 = warp & 3;
+#pragma unroll 1
+            for (int bi = 0; bi < 2; ++bi) {
+                const int i = (warp >> 2) * 2 + bi;
+                const int v = i * 128 + q4 * 32 + lane;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float o[32];
+                    tc::tmem_ld32(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + kTcOCol + i * 64 + half * 32, o);
+                    tc::tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) o[lane + 32 * u] = f32_to_bf16_bits(acc[u] * inv);
-        if (P.lse && lane == 0)
-            P.lse[static_cast<long long>(b) * P.H + h0 + hh] = (l > 0.f) ? s_m[hh] + logf(l) : -INFINITY;
+                    for (int j = 0; j < 32; ++j) stage_o[(half * 32 + j) * 512 + v] = o[j];
+                }
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < 64 * 512; i += kTcThreads) stage_o[i] = 0.f;
+        if (threadIdx.x < 64) {
+            sm_m[threadIdx.x] = -INFINITY;
+            sm_l[threadIdx.x] = 0.f;
+        }
+    }
+    __syncthreads();
+    tc::cluster_sync();
+    const int C = T.cluster;
+    if (threadIdx.x < 64) {
+        const int hh = threadIdx.x;
+        float mq[8], lq[8];
+        float M = -INFINITY;
+        for (int q = 0; q < C; ++q) {
+            mq[q] = tc::ld_cluster_f32(tc::map_to_rank(tc::smem_u32(sm_m + hh), q));
+            lq[q] = tc::ld_cluster_f32(tc::map_to_rank(tc::smem_u32(sm_l + hh), q));
+            M = fmaxf(M, mq[q]);
+        }
+        float L = 0.f;
+        for (int q = 0; q < C; ++q) {
+            const float wq = (mq[q] == -INFINITY) ? 0.f : exp2f(mq[q] - M);
+            red_w[q * 64 + hh] = wq;
+            L += wq * lq[q];
+        }
+        red_invl[hh] = L > 0.f ? 1.0f / L : 0.f;
+        if (rank == 0 && hh < nh && P.lse)
+            P.lse[static_cast<long long>(b) * P.H + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    const int VS = kV / C;                  // value dims merged by this CTA
+    const int per_h = VS / 4;
+    for (int it = threadIdx.x; it < nh * per_h; it += kTcThreads) {
+        const int hh = it / per_h;
+        const int v = rank * VS + (it % per_h) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t local = tc::smem_u32(stage_o + hh * 512 + v);
+        for (int q = 0; q < C; ++q) {
+            const float wq = red_w[q * 64 + hh];
+            const float4 x = tc::ld_cluster_v4(tc::map_to_rank(local, q));
+            acc.x += wq * x.x;
+            acc.y += wq * x.y;
+            acc.z += wq * x.z;
+            acc.w += wq * x.w;
+        }
+        const float il = red_invl[hh];
+        const __nv_bfloat162 o01 = __floats2bfloat162_rn(acc.x * il, acc.y * il);
+        const __nv_bfloat162 o23 = __floats2bfloat162_rn(acc.z * il, acc.w * il);
+        uint2 pk2;
+        pk2.x = *reinterpret_cast<const uint32_t*>(&o01);
+        pk2.y = *reinterpret_cast<const uint32_t*>(&o23);
+        *reinterpret_cast<uint2*>(P.out + (static_cast<long long>(b) * P.H + h0 + hh) * kV + v) = pk2;
+    }
+    tc::cluster_sync();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTcTmemCols);
     }
 }
 
@@ -215,13 +534,37 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     P.scale = plan->geom.softmax_scale;
     P.status = a->status_dev;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t smem = sizeof(float) * (kSimtHeads * kHead + kSimtKeys * kSimtRow + kSimtHeads * kSimtKeys);
+    MlaTcParams T;
+    T.base = P;
+    T.head_groups = plan->mla_head_groups;
+    T.cluster = plan->mla_splits;
+    CUtensorMap tm_q;
+    const uint64_t qdims[2] = {static_cast<uint64_t>(kHead), static_cast<uint64_t>(plan->batch) * P.H};
+    const uint64_t qstr[1] = {static_cast<uint64_t>(kHead) * 2};
+    const uint32_t qbox[2] = {64, 64};
+    if ((reinterpret_cast<uintptr_t>(a->q_dev) & 15) || (reinterpret_cast<uintptr_t>(a->swa_cache_dev) & 15) ||
+        (sparse && (reinterpret_cast<uintptr_t>(a->comp_cache_dev) & 15)))
+        return DSV4_ERR_SHAPE;
+    if (!encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->q_dev, qdims, qstr, qbox,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return DSV4_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(mla_decode_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        cudaFuncSetAttribute(mla_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         attr_set = true;
     }
-    dim3 grid((P.H + kSimtHeads - 1) / kSimtHeads, plan->batch);
-    mla_decode_simt<<<grid, 256, smem, st>>>(P);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T.cluster, plan->batch * T.head_groups, 1);
+    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = T.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_tc, tm_q, T);
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
