@@ -160,6 +160,7 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
     if (!(g->softmax_scale > 0.0f)) return DSV4_ERR_INVALID;
     if (type == DSV4_C4A && (g->idx_heads < 1 || g->idx_heads > DSV4_MAX_IDX_HEADS)) return DSV4_ERR_UNSUPPORTED;
     if (type != DSV4_SWAONLY && topk < 1) return DSV4_ERR_INVALID;
+    if (topk + g->window > 8 * 1024) return DSV4_ERR_UNSUPPORTED;   // 8 CTAs x 1024 keys
     dsv4_plan* p = static_cast<dsv4_plan*>(calloc(1, sizeof(dsv4_plan)));
     if (p == nullptr) return DSV4_ERR_INVALID;
     p->type = type;
@@ -186,12 +187,14 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
         const int sms = sm_count();
         int c = 8;
         while (c > 1 && units * c > sms) c >>= 1;
+        while (c < 8 && (p->max_keys + c - 1) / c > 1024) c <<= 1;   // a CTA owns at most 1024 keys
         p->mla_splits = c;
         p->mla_keys_per_split = (p->max_keys + c - 1) / c;
     }
     size_t off = 0;
     p->ws_logits_off = off;
-    if (type == DSV4_C4A) off += align256(static_cast<size_t>(batch) * p->max_slots * sizeof(float));
+    p->logits_stride = (p->max_slots + 3) & ~3;
+    if (type == DSV4_C4A) off += align256(static_cast<size_t>(batch) * p->logits_stride * sizeof(float));
     p->ws_partial_off = off;
     p->ws_partial_bytes = 0;
     off += p->ws_partial_bytes;

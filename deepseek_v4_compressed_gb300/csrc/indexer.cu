@@ -29,7 +29,9 @@ constexpr int kIdxTileBytes = kIdxTileSlots * kIdx;       // 16 KB
 constexpr int kIdxQBytes = 64 * kIdx;                     // query tile, N <= 64 rows
 constexpr int kIdxThreads = 192;
 constexpr int kIdxTmemCols = 128;                         // 2 accumulators x 64 columns
-constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + 1024 /* barriers etc */ + 1024 /* align */;
+constexpr int kIdxScaleBytes = 2 * kPage * 4;                // scale planes of the tile's two pages
+constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
+                         2048 /* barriers etc */ + 1024 /* align */;
 
 struct IdxTcParams {
     const uint8_t* cache;
@@ -41,6 +43,7 @@ struct IdxTcParams {
     int H;
     int n_pad;
     float* logits;
+    int logits_stride;
     int max_slots;
     int tiles_per_cta;
     int* status;
@@ -54,7 +57,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_tiles = smem;
     uint8_t* q_tile = smem + kIdxStages * kIdxTileBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(q_tile + kIdxQBytes);
+    float* scales_s = reinterpret_cast<float*>(q_tile + kIdxQBytes);   // [stage][128 slots]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_tile + kIdxQBytes + kIdxStages * kIdxScaleBytes);
     uint64_t* full = bars;                        // [kIdxStages]
     uint64_t* empty = bars + kIdxStages;          // [kIdxStages]
     uint64_t* acc_full = bars + 2 * kIdxStages;   // [2]
@@ -79,7 +83,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < kIdxStages; ++i) {
             tc::mbar_init(tc::smem_u32(&full[i]), 1);
-            tc::mbar_init(tc::smem_u32(&empty[i]), 1);
+            tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (scales read)
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
@@ -112,20 +116,26 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                 const uint32_t ph = (i / kIdxStages) & 1;
                 if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status)) break;
                 const int tile = t_begin + i;
-                int pg[2];
+                int pg[2], spg[2];
                 for (int h = 0; h < 2; ++h) {
                     const int pi = min(2 * tile + h, n_pages - 1);
                     int v = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                    spg[h] = v;
                     if (v < 0 || v >= P.num_pages) {
                         flag(P.status, DSV4_DEV_BAD_PAGE);
                         v = P.num_pages;          // out of the map: TMA fills zeros
+                        spg[h] = 0;               // scales from a valid page (the row's data is zero)
                     }
                     pg[h] = v;
                 }
                 const uint32_t dst = tc::smem_u32(a_tiles + st * kIdxTileBytes);
-                tc::mbar_arrive_expect_tx(tc::smem_u32(&full[st]), kIdxTileBytes);
-                tc::tma_load_3d(dst, &tm_cache, tc::smem_u32(&full[st]), 0, 0, pg[0]);
-                tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, tc::smem_u32(&full[st]), 0, 0, pg[1]);
+                const uint32_t fb = tc::smem_u32(&full[st]);
+                tc::mbar_arrive_expect_tx(fb, kIdxTileBytes + kIdxScaleBytes);
+                tc::tma_load_3d(dst, &tm_cache, fb, 0, 0, pg[0]);
+                tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, fb, 0, 0, pg[1]);
+                for (int h = 0; h < 2; ++h)
+                    tc::bulk_load(tc::smem_u32(scales_s + st * 128 + h * kPage),
+                                  P.cache + static_cast<long long>(spg[h]) * kIdxPage + kPage * kIdx, kPage * 4, fb);
                 issued = i + 1;
             }
         }
@@ -175,16 +185,16 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
             }
+            // the stage's scales: its full barrier cannot have moved on, since
+            // the stage is only refilled after this warp releases it below
+            const int st = i % kIdxStages;
+            float scale = 0.f;
+            if (tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status))
+                scale = scales_s[st * 128 + row];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
             const int s = (t_begin + i) * kIdxTileSlots + row;
-            if (s < n_c) {
-                const int pi = s / kPage;
-                const int pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
-                float out = -INFINITY;
-                if (pg >= 0 && pg < P.num_pages)
-                    out = acc * reinterpret_cast<const float*>(P.cache + static_cast<long long>(pg) * kIdxPage +
-                                                               kPage * kIdx)[s % kPage];
-                P.logits[static_cast<long long>(b) * P.max_slots + s] = out;
-            }
+            if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc * scale;
         }
     }
 
@@ -205,151 +215,179 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// Top-k by radix select: one CTA per query.  Keys are the order-preserving
-// uint32 images of the logits; four 8-bit passes find the k-th largest key K*
-// and how many of the keys equal to K* to take (lowest slots first); a final
-// ordered compaction writes the selected slots in ascending order.
+// Top-k: one CTA per query.  Keys are the order-preserving uint32 images of
+// the logits, taken relative to their minimum so the radix digits start at the
+// data's own range: up to three passes of 11-bit digits (2048-bin shared
+// histograms) narrow the k-th largest key down to its bin; a pass stops early
+// once the bin holding the k-th key is taken whole.  Keys equal to the final
+// threshold are taken lowest slot first; an ordered compaction writes the k
+// slots in ascending order.
 // ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkSmemKeys = 32768;   // keys staged in shared memory up to this many
+constexpr int kTopkThreads = 512;
+constexpr int kTopkBins = 2048;
+constexpr int kTopkSmemKeys = 49152;   // keys staged in shared memory up to this many (192 KB)
 
-__device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
+// Exclusive scan of one int per thread over the CTA; also returns the total.
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int& total)
 {
+    constexpr int NW = kTopkThreads / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) warp_tot[warp] = x;
+    if (lane == 31) scratch[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int t = (lane < kTopkThreads / 32) ? warp_tot[lane] : 0;
+        const int t = (lane < NW) ? scratch[lane] : 0;
         int u = t;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, u, o);
+            const int y = __shfl_up_sync(0xffffffffu, u, o);
             if (lane >= o) u += y;
         }
-        warp_tot[lane] = u - t;          // exclusive prefix of warp totals
-        if (lane == 31) warp_tot[32] = u;
+        scratch[lane] = u - t;
+        if (lane == 31) scratch[32] = u;
     }
     __syncthreads();
-    total = warp_tot[32];
-    const int r = warp_tot[warp] + x - v;
+    total = scratch[32];
+    const int r = scratch[warp] + x - v;
     __syncthreads();
     return r;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_radix_kernel(
-    const float* __restrict__ logits, int max_slots, const int* __restrict__ ctx_len, int k,
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(
+    const float* __restrict__ logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
     int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len, int smem_keys)
 {
     extern __shared__ uint32_t skeys[];
-    __shared__ int hist[256];
-    __shared__ int warp_tot[33];
-    __shared__ uint32_t s_prefix, s_mask;
-    __shared__ int s_remaining;
+    __shared__ int hist[kTopkBins];
+    __shared__ int scratch[33];
+    __shared__ uint32_t s_min, s_max, s_prefix;
+    __shared__ int s_lo, s_hi, s_rem, s_done;
 
     const int b = blockIdx.x;
     int n = ctx_len[b] / 4;
-    if (n > max_slots) n = max_slots;
-    if (n < 0) n = 0;
+    n = n < 0 ? 0 : (n > max_slots ? max_slots : n);
     int* orow = out_idx + static_cast<long long>(b) * out_stride;
-    const float* lrow = logits + static_cast<long long>(b) * max_slots;
+    const float* lrow = logits + static_cast<long long>(b) * row_stride;
     if (n <= k) {
         for (int i = threadIdx.x; i < k; i += blockDim.x) orow[i] = (i < n) ? i : -1;
         if (threadIdx.x == 0) out_len[b] = n;
         return;
     }
     const bool in_smem = n <= smem_keys;
-    if (in_smem)
-        for (int i = threadIdx.x; i < n; i += blockDim.x) skeys[i] = f32_order_key(lrow[i]);
-    auto key_at = [&](int i) -> uint32_t { return in_smem ? skeys[i] : f32_order_key(lrow[i]); };
-    if (threadIdx.x == 0) {
-        s_prefix = 0;
-        s_mask = 0;
-        s_remaining = k;
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    // vectorised load (rows are 16-byte aligned: row_stride is a multiple of 4)
+    const int n4 = n >> 2;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const float4 v = reinterpret_cast<const float4*>(lrow)[i];
+        const uint32_t k0 = f32_order_key(v.x), k1 = f32_order_key(v.y), k2 = f32_order_key(v.z),
+                       k3 = f32_order_key(v.w);
+        kmin = min(min(kmin, k0), min(min(k1, k2), k3));
+        kmax = max(max(kmax, k0), max(max(k1, k2), k3));
+        if (in_smem) reinterpret_cast<uint4*>(skeys)[i] = make_uint4(k0, k1, k2, k3);
+    }
+    for (int i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) {
+        const uint32_t kk = f32_order_key(lrow[i]);
+        kmin = min(kmin, kk);
+        kmax = max(kmax, kk);
+        if (in_smem) skeys[i] = kk;
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if ((threadIdx.x & 31) == 0) {
+        scratch[threadIdx.x >> 5] = static_cast<int>(kmin);
+        hist[threadIdx.x >> 5] = static_cast<int>(kmax);
     }
     __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t mn = 0xffffffffu, mx = 0u;
+        for (int w = 0; w < kTopkThreads / 32; ++w) {
+            mn = min(mn, static_cast<uint32_t>(scratch[w]));
+            mx = max(mx, static_cast<uint32_t>(hist[w]));
+        }
+        s_min = mn;
+        s_max = mx;
+        const uint32_t range = mx - mn;
+        s_hi = range ? 32 - __clz(range) : 0;   // offsets (key - min) fit in s_hi bits
+        s_lo = s_hi;
+        s_prefix = 0;
+        s_rem = k;
+        s_done = (range == 0);
+    }
+    __syncthreads();
+    const uint32_t base = s_min;
+    auto key_at = [&](int i) -> uint32_t { return in_smem ? skeys[i] : f32_order_key(lrow[i]); };
 
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    while (!s_done) {
+        const int hi = s_hi;
+        const int lo = hi > 11 ? hi - 11 : 0;
+        const uint32_t prefix = s_prefix;
+        const int rem = s_rem;
+        for (int i = threadIdx.x; i < kTopkBins; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        const uint32_t prefix = s_prefix, mask = s_mask;
-        const int lane = threadIdx.x & 31;
-        // warp-aggregated histogram (most keys share their top byte)
-        for (int base = 0; base < n; base += blockDim.x) {
-            const int i = base + threadIdx.x;
-            int digit = -1;
-            if (i < n) {
-                const uint32_t key = key_at(i);
-                if ((key & mask) == prefix) digit = (key >> shift) & 0xff;
-            }
-            const unsigned peers = __match_any_sync(0xffffffffu, digit);
-            if (digit >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint32_t off = key_at(i) - base;
+            if (hi >= 32 || (off >> hi) == (prefix >> hi)) atomicAdd(&hist[(off >> lo) & (kTopkBins - 1)], 1);
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
-            // lane l scans bins 255-8l .. 248-8l (descending digits)
-            int local = 0;
+        // bins from the top: thread t sums bins 2047-4t .. 2044-4t
+        int c[4];
+        int local = 0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) local += hist[255 - 8 * lane - q];
-            int incl = local;
+        for (int q = 0; q < 4; ++q) {
+            c[q] = hist[kTopkBins - 1 - 4 * threadIdx.x - q];
+            local += c[q];
+        }
+        int tot;
+        const int before = block_excl_scan(local, scratch, tot);
+        if (before < rem && rem <= before + local) {
+            int cum = before;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int before = incl - local;
-            const int rem = s_remaining;
-            const bool mine = before < rem && rem <= incl;
-            const unsigned who = __ballot_sync(0xffffffffu, mine);
-            if (mine && lane == __ffs(who) - 1) {
-                int cum = before;
-                for (int q = 0; q < 8; ++q) {
-                    const int d = 255 - 8 * lane - q;
-                    if (cum + hist[d] >= rem) {
-                        s_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-                        s_mask = mask | (0xffu << shift);
-                        s_remaining = rem - cum;
-                        break;
-                    }
-                    cum += hist[d];
+            for (int q = 0; q < 4; ++q) {
+                if (cum + c[q] >= rem) {
+                    const uint32_t d = kTopkBins - 1 - 4 * threadIdx.x - q;
+                    s_prefix = prefix | (d << lo);
+                    s_rem = rem - cum;
+                    s_lo = lo;
+                    s_hi = lo;
+                    s_done = (lo == 0) || (cum + c[q] == rem);
+                    break;
                 }
+                cum += c[q];
             }
         }
         __syncthreads();
     }
-    const uint32_t kstar = s_prefix;
-    const int take_eq = s_remaining;   // keys equal to K* to take, lowest slots first
+    const int lo = s_lo;
+    const uint32_t thr = s_prefix >> lo;   // digit prefix of the threshold bin
+    const int take_eq = s_rem;             // keys of the threshold bin to take, lowest slot first
 
-    // Ordered compaction: thread i owns a contiguous chunk of slots.
     const int chunk = (n + blockDim.x - 1) / blockDim.x;
-    const int lo = threadIdx.x * chunk;
-    const int hi = min(n, lo + chunk);
+    const int i0 = threadIdx.x * chunk;
+    const int i1 = min(n, i0 + chunk);
     int gt = 0, eq = 0;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t key = key_at(i);
-        gt += key > kstar;
-        eq += key == kstar;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t d = (key_at(i) - base) >> lo;
+        gt += d > thr;
+        eq += d == thr;
     }
     int tot;
-    const int gt_before = block_excl_scan(gt, warp_tot, tot);
-    const int eq_before = block_excl_scan(eq, warp_tot, tot);
+    const int gt_before = block_excl_scan(gt, scratch, tot);
+    const int eq_before = block_excl_scan(eq, scratch, tot);
     int g = gt_before, e = eq_before;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t key = key_at(i);
-        bool sel = false;
-        if (key > kstar) {
-            sel = true;
-        } else if (key == kstar) {
-            sel = e < take_eq;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t d = (key_at(i) - base) >> lo;
+        if (d > thr) {
+            orow[g + min(e, take_eq)] = i;
+            ++g;
+        } else if (d == thr) {
+            if (e < take_eq) orow[g + e] = i;
+            ++e;
         }
-        if (sel) orow[g + min(e, take_eq)] = i;
-        g += key > kstar;
-        e += key == kstar;
     }
     if (threadIdx.x == 0) out_len[b] = k;
 }
@@ -397,6 +435,7 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         P.H = H;
         P.n_pad = n_pad;
         P.logits = logits;
+        P.logits_stride = plan->logits_stride;
         P.max_slots = plan->max_slots;
         P.tiles_per_cta = plan->idx_tiles_per_cta;
         P.status = a->status_dev;
@@ -415,13 +454,12 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
     const size_t smem = static_cast<size_t>(smem_keys) * 4;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(topk_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTopkSmemKeys * 4);
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemKeys * 4);
         attr_set = true;
     }
-    topk_radix_kernel<<<B, kTopkThreads, smem, st>>>(logits, plan->max_slots, a->ctx_len_dev, plan->topk,
-                                                      a->out_idx_dev, a->out_stride, a->out_len_dev,
-                                                      smem_keys);
+    topk_kernel<<<B, kTopkThreads, smem, st>>>(logits, plan->logits_stride, plan->max_slots, a->ctx_len_dev,
+                                               plan->topk, a->out_idx_dev, a->out_stride, a->out_len_dev,
+                                               smem_keys);
     e = cudaGetLastError();
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

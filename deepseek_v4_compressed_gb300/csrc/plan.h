@@ -18,7 +18,8 @@ struct dsv4_plan {
     int mla_head_groups;     // ceil(n_heads / 64)
     int mla_splits;          // key splits per (sequence, head group)
     int mla_keys_per_split;
-    size_t ws_logits_off;    // fp32 [batch][max_slots] indexer logits
+    int logits_stride;       // floats per logits row (max_slots rounded up to 4)
+    size_t ws_logits_off;    // fp32 [batch][logits_stride] indexer logits
     size_t ws_partial_off;   // fp32 attention partials
     size_t ws_partial_bytes;
     size_t ws_bytes;
