@@ -27,7 +27,8 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_index_schedule", "dsv4_rope_table", "dsv4_read_device_status",
             "dsv4_plan_create", "dsv4_plan_destroy", "dsv4_plan_workspace_bytes",
             "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
-            "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait"]
+            "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
+            "dsv4_selftest_key_dequant"]
 
 
 class Dsv4Error(RuntimeError):
@@ -136,6 +137,8 @@ def lib():
     L.dsv4_sparse_mla_decode.argtypes = [vp, ctypes.POINTER(MlaArgs), vp, ctypes.c_size_t, vp]
     L.dsv4_selftest_bounded_wait.restype = st
     L.dsv4_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
+    L.dsv4_selftest_key_dequant.restype = st
+    L.dsv4_selftest_key_dequant.argtypes = [vp, vp]
     _lib = L
     return L
 
@@ -205,6 +208,12 @@ def read_device_status(status_dev, stream=None):
     bits = ctypes.c_int(0)
     st = lib().dsv4_read_device_status(_ptr(status_dev), _stream(stream), ctypes.byref(bits))
     return st, bits.value
+
+
+def selftest_key_dequant(out_dev, stream=None):
+    """Every (E4M3 code, UE8M0 scale byte) through the decode kernel's key
+    conversion; out_dev: uint16 [65536] receives the bf16 bits."""
+    _check(lib().dsv4_selftest_key_dequant(_ptr(out_dev), _stream(stream)), "selftest_key_dequant")
 
 
 def selftest_bounded_wait(status_dev, spin_limit, stream=None):

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     extern __shared__ uint32_t skeys[];
     __shared__ int hist[kTopkBins];
     __shared__ int scratch[33];
-    __shared__ uint32_t s_min, s_max, s_prefix;
+    __shared__ uint32_t s_min, s_prefix;
     __shared__ int s_lo, s_hi, s_rem, s_done;
 
     const int b = blockIdx.x;
@@ -310,7 +310,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
             mx = max(mx, static_cast<uint32_t>(hist[w]));
         }
         s_min = mn;
-        s_max = mx;
         const uint32_t range = mx - mn;
         s_hi = range ? 32 - __clz(range) : 0;   // offsets (key - min) fit in s_hi bits
         s_lo = s_hi;

@@ -35,90 +35,63 @@ struct MlaParams {
     int* status;
 };
 
-// Row pointer of key i of sequence b (compressed keys first, then the SWA
-// window).  Returns false (and flags) for an out-of-range index or page.
-struct KeyRef {
-    const uint8_t* row;     // compressed: 640 data bytes; SWA: 576 bf16
-    const uint8_t* scales;  // compressed only
-    bool comp;
-};
-
-__device__ __forceinline__ bool key_ref(const MlaParams& P, int b, int i, int n_comp, int t0, KeyRef& k)
-{
-    if (i < n_comp) {
-        const int slot = P.idx[static_cast<long long>(b) * P.idx_stride + i];
-        const int pi = slot / kPage;
-        if (slot < 0 || pi >= P.comp_bt_stride) {
-            flag(P.status, DSV4_DEV_BAD_INDEX);
-            return false;
-        }
-        const int pg = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + pi];
-        if (pg < 0 || pg >= P.comp_pages) {
-            flag(P.status, DSV4_DEV_BAD_PAGE);
-            return false;
-        }
-        const uint8_t* page = P.comp + static_cast<long long>(pg) * kMlaPage;
-        const int r = slot % kPage;
-        k.row = page + r * kMlaData;
-        k.scales = page + kPage * kMlaData + r * 8;
-        k.comp = true;
-        return true;
-    }
-    const int t = t0 + (i - n_comp);
-    const int pi = t / kPage;
-    const int pg = (pi < P.swa_bt_stride) ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + pi] : -1;
-    if (pg < 0 || pg >= P.swa_pages) {
-        flag(P.status, DSV4_DEV_BAD_PAGE);
-        return false;
-    }
-    k.row = P.swa + static_cast<long long>(pg) * kSwaPage + (t % kPage) * (kHead * 2);
-    k.scales = nullptr;
-    k.comp = false;
-    return true;
-}
-
 // ---------------------------------------------------------------------------
 // Tensor-core decode attention (tcgen05, TMEM accumulators).
 //
-// CTA = (rank r of a cluster of C CTAs, sequence b x 64-head group g).  The C
-// CTAs of a cluster split the sequence's keys (selected compressed slots then
-// the SWA window) into contiguous ranges, each CTA walks its range in 32-key
-// tiles with an online softmax, and the partial results are merged through
-// distributed shared memory -- no partials in HBM, no combine kernel.
+// CTA = (rank r of a cluster of C CTAs, sequence b x 64-head group g).  The
+// keys of a sequence come as 64-key tiles: first the SWA window as whole
+// 64-token cache pages (rows outside the window masked), then the selected
+// compressed slots in list order (rows past the selection masked).  Tile j of
+// that list belongs to CTA j mod C.  Each CTA runs an online softmax over its
+// tiles; then every CTA pushes each 512/C-dim slice of its unnormalised O,
+// with its running max and sum, into the shared memory of the CTA that owns
+// the slice, which combines the C parts and stores the output -- no partials
+// in HBM, no combine kernel.
 //
-//   S  = Q K^T     tcgen05.mma kind::f16, M = 64 head rows (row r lands in
-//                  TMEM lane 32*(r/16) + r%16), N = 32 keys, K = 576 (36
-//                  instructions); double-buffered in TMEM columns [0, 64).
-//   O^T += V^T P^T M = 128 value dims (4 blocks cover the 512 latent dims),
-//                  N = 64 heads, K = 32 keys; V^T is the same swizzled K tile
-//                  read as an MN-major operand; O^T lives in TMEM [64, 320).
-// Warps: 0-3 softmax (lanes 0-15 of each = 16 heads) and O^T correction (all lanes);
-// 4-7 producers: gather and dequantise key rows (FP8 * 2^e -> bf16, exact) into
-// the 128-byte-swizzled tile; 8 MMA issuer (and the Q load by TMA).
+//   S  = Q K^T      kind::f16, M = 64 head rows (row r in TMEM lane
+//                   32*(r/16) + r%16), N = 64 keys, K = 576: 36 MMAs per
+//                   tile, double-buffered in TMEM columns [0, 128).
+//   O^T += V^T P^T  M = 128 value dims (4 blocks), N = 64 heads, K = 64 keys:
+//                   V^T is the key tile read as an MN-major operand; O^T sits
+//                   in TMEM columns [128, 384).
+// A single thread issues one tcgen05.mma about every 20 ns whatever its shape
+// (up to N = 64), so the tile is as wide as two bf16 tiles and Q fit in
+// shared memory.  Once QK(t) is done the tile's RoPE chunk is free; P(t)
+// (bf16, 64 heads x 64 keys) is written there, so P is double-buffered with
+// the stages.
+// Warps 0-3: softmax (lanes 0-15 = 16 heads each) and O^T correction; warps
+// 4-11: producers (window pages by TMA; compressed rows loaded into registers
+// one tile ahead and dequantised into the swizzled tile); warp 12: Q load and
+// QK issue; warp 13: PV issue (two issuers keep PV(t) off QK(t+1)'s path).
 // ---------------------------------------------------------------------------
-constexpr int kTcKeys = 32;
-constexpr int kTcStages = 2;                               // bf16 key tiles (MMA operands)
-constexpr int kTcRawStages = 2;                            // raw FP8 rows landing from TMA bulk copies
+constexpr int kTcKeys = 64;
+constexpr int kTcStages = 2;
 constexpr int kTcQChunk = 64 * 128;                        // 64 head rows x 64 dims (bf16)
 constexpr int kTcQBytes = 9 * kTcQChunk;                   // 73728
-constexpr int kTcKChunk = kTcKeys * 128;                   // 32 key rows x 64 dims
-constexpr int kTcKBytes = 9 * kTcKChunk;                   // 36864 per stage
-constexpr int kTcRawBytes = kTcKeys * kMlaData;            // 32 rows x 640 B
-constexpr int kTcPBytes = 64 * 128;                        // 64 head rows x 32 keys (rows padded to 128 B)
-constexpr int kTcMaxKeys = 1024;                           // keys one CTA can own (its pointer table)
-constexpr int kTcThreads = 288;
+constexpr int kTcKChunk = kTcKeys * 128;                   // 64 key rows x 64 dims
+constexpr int kTcKBytes = 9 * kTcKChunk;                   // 73728 per stage
+constexpr int kTcMaxCompTiles = 16;                        // compressed tiles one CTA can own
+constexpr int kTcProdWarps = 8;
+constexpr int kTcMmaWarp = 4 + kTcProdWarps;               // 12: Q load, QK issue
+constexpr int kTcPvWarp = kTcMmaWarp + 1;                  // 13: PV issue
+constexpr int kTcThreads = 32 * (kTcPvWarp + 1);           // 448
+constexpr int kTcMaxTiles = 24;                            // per-tile PV completion barriers
 constexpr int kTcTmemCols = 512;
-constexpr int kTcOCol = 64;
+constexpr int kTcOCol = 128;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTcQBytes;
-constexpr int kOffRaw = kOffK + kTcStages * kTcKBytes;
-constexpr int kOffP = kOffRaw + kTcRawStages * kTcRawBytes;
-constexpr int kOffTab = kOffP + 2 * kTcPBytes;
-constexpr int kOffMisc = kOffTab + kTcMaxKeys * 16;
-constexpr int kMiscBytes = 4096;
-constexpr int kTcSmem = kOffMisc + kMiscBytes + 1024;
-constexpr int kStageO = 0;                                 // epilogue: fp32 [64 heads][512] (reuses Q/K space)
-static_assert(64 * 512 * 4 <= kOffRaw, "staging must fit in the Q/K space");
+constexpr int kOffMisc = kOffK + kTcStages * kTcKBytes;    // 221184
+constexpr int kMiscBytes = 2048;
+constexpr int kTcSmem = kOffMisc + kMiscBytes + 1024;      // + alignment slack of the dynamic base
+// epilogue buffers (in the Q / K space once the main loop is over): a slice
+// is bf16 [512/C dims][64 heads] (16-byte head groups swizzled by dim) plus
+// fp32 [64][2] running max and sum; receive slots [C], send slots [C], merge
+// weights [8][64] and 1 / L [64]
+constexpr int kSliceMax = (kV / 1) * 128 + 512;
+constexpr int kOffRecv = 0;
+constexpr int kOffSend = 64 * kV * 2 + 8 * 512;
+constexpr int kOffWeights = 2 * kOffSend;
+static_assert(kOffWeights + 9 * 64 * 4 <= kOffMisc, "epilogue buffers fit in the Q / K space");
 static_assert(kTcSmem <= 232448, "shared memory budget");
 
 struct MlaTcParams {
@@ -135,32 +108,39 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
-// 16 FP8 E4M3 codes times 2^E -> 16 bf16.  Each code's 7 magnitude bits go to
-// bit 20 of an fp32 word and its sign to bit 31: the word's value is the code's
-// value times 2^-120 (exponent field 0 gives exactly the scaled subnormals).
-// Two exact power-of-two multiplies restore 2^(E+120); the product has at most
-// 4 significant bits, so its upper 16 bits are the bf16 (exact for every
-// result in the normal range).  Integer and FMA pipes only.
-__device__ __forceinline__ uint32_t code_f32_bits(uint32_t byte)
+// 16 FP8 E4M3 codes times 2^E -> 16 bf16, E = scale_byte - 127 (UE8M0).
+// Placing a code's 7 magnitude bits at bits 4-10 of a bf16 and its sign at
+// bit 15 gives a bf16 whose value is the code's value times 2^-120 (exponent
+// field 0 gives exactly the scaled subnormal codes).  Multiplying by 2^(E+120)
+// in one or two exact power-of-two steps restores the value; results in the
+// bf16 normal range are exact.  Integer and bf16x2 pipes only.
+__device__ __forceinline__ __nv_bfloat162 e4m3_pair_scaled(uint32_t t)   // t: codes in bytes 1 and 3
 {
-    return ((byte & 0x7fu) << 20) | ((byte & 0x80u) << 24);
+    const uint32_t v = ((t >> 4) & 0x07f007f0u) | (t & 0x80008000u);
+    return *reinterpret_cast<const __nv_bfloat162*>(&v);
 }
 
 __device__ __forceinline__ void dequant16(const uint4 w, uint32_t scale_byte, uint4& lo, uint4& hi)
 {
-    const int k = static_cast<int>(scale_byte) - 7;          // E + 120, E = byte - 127
+    const int k = static_cast<int>(scale_byte) - 7;          // E + 120, in [-7, 248]
     const int ka = k < 127 ? k : 127;
-    const float ma = __int_as_float((ka + 127) << 23);        // 2^ka, ka in [-7, 127]
-    const float mb = __int_as_float((k - ka + 127) << 23);    // 2^(k-ka) >= 1
+    const uint32_t ba = static_cast<uint32_t>(ka + 127) << 7;        // bf16 2^ka
+    const uint32_t bb = static_cast<uint32_t>(k - ka + 127) << 7;    // bf16 2^(k - ka)
+    const uint32_t ma2 = ba | (ba << 16), mb2 = bb | (bb << 16);
+    const __nv_bfloat162 ma = *reinterpret_cast<const __nv_bfloat162*>(&ma2);
+    const __nv_bfloat162 mb = *reinterpret_cast<const __nv_bfloat162*>(&mb2);
     const uint32_t in[4] = {w.x, w.y, w.z, w.w};
     uint32_t out[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float f[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) f[c] = __uint_as_float(code_f32_bits((in[i] >> (8 * c)) & 0xffu)) * ma * mb;
-        out[2 * i] = __byte_perm(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632);
-        out[2 * i + 1] = __byte_perm(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632);
+        __nv_bfloat162 x0 = __hmul2(e4m3_pair_scaled(__byte_perm(in[i], 0u, 0x1404)), ma);   // codes 0, 1
+        __nv_bfloat162 x1 = __hmul2(e4m3_pair_scaled(__byte_perm(in[i], 0u, 0x3424)), ma);   // codes 2, 3
+        if (k > 127) {
+            x0 = __hmul2(x0, mb);
+            x1 = __hmul2(x1, mb);
+        }
+        out[2 * i] = *reinterpret_cast<const uint32_t*>(&x0);
+        out[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&x1);
     }
     lo = make_uint4(out[0], out[1], out[2], out[3]);
     hi = make_uint4(out[4], out[5], out[6], out[7]);
@@ -179,6 +159,22 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
     return ok != 0;
 }
 
+__device__ __forceinline__ uint4 ldg_stream_v4(const uint8_t* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u8(const uint8_t* p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_swa, MlaTcParams T)
 {
@@ -187,49 +183,39 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_s = smem + kOffQ;
     uint8_t* k_s = smem + kOffK;
-    uint8_t* p_s = smem + kOffP;
-    uint8_t* raw_s = smem + kOffRaw;
-    uint4* table = reinterpret_cast<uint4*>(smem + kOffTab);   // per owned compressed row: pointer | flags, scales
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffMisc);
-    uint64_t* kv_full = bars;          // [2] producers -> MMA (tile in its stage)
+    uint64_t* kv_full = bars;          // [2] producers (8 warps; window tiles: + TMA bytes) -> MMA
     uint64_t* kv_empty = bars + 2;     // [2] MMA -> producers (stage read by QK and PV)
-    uint64_t* swa_full = bars + 4;     // [2] TMA tensor loads of a window tile landed
-    uint64_t* s_full = bars + 6;       // [2] MMA -> softmax
-    uint64_t* p_full = bars + 8;       // [2] softmax -> MMA (P written, S read, O^T corrected)
-    uint64_t* pv_done = bars + 10;     // [2] MMA -> softmax
-    uint64_t* q_full = bars + 12;
-    uint64_t* sync4 = bars + 13;       // [2] the four softmax warps meet once per tile
-    uint64_t* table_ready = bars + 15;
-    float* sm_m = reinterpret_cast<float*>(bars + 32);   // [64] running max (log2 domain)
+    uint64_t* s_full = bars + 4;       // [2] MMA -> softmax
+    uint64_t* p_full = bars + 6;       // [2] softmax (4 warps) -> MMA: P written, S read, O^T corrected
+    uint64_t* q_full = bars + 8;
+    uint64_t* sync4 = bars + 9;        // [2] the four softmax warps meet once per tile
+    uint64_t* recv_full = bars + 11;   // epilogue: the C - 1 peer slices have landed (bytes)
+    uint64_t* pv_done = bars + 12;     // [kTcMaxTiles] PV(u) complete (one phase each)
+    float* sm_m = reinterpret_cast<float*>(bars + 12 + kTcMaxTiles);   // [64] running max (log2 domain)
     float* sm_l = sm_m + 64;                              // [64] running sum
-    float* sm_alpha = sm_l + 64;                          // [64] correction factors of this tile
-    float* red_w = sm_alpha + 64;                         // [8][64] merge weights
-    float* red_invl = red_w + 8 * 64;                     // [64]
-    int* sm_any = reinterpret_cast<int*>(red_invl + 64);  // [2][4]
+    float* sm_alpha = sm_l + 64;                          // [2][64] correction factors (by tile parity)
+    int* sm_any = reinterpret_cast<int*>(sm_alpha + 128); // [2][4]
     volatile int* abort_flag = sm_any + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm_any + 9);
 
-    const int rank = blockIdx.x;
+    const int rank = blockIdx.x;                          // the cluster spans gridDim.x
     const int b = blockIdx.y / T.head_groups, g_head = blockIdx.y % T.head_groups;
     const int h0 = g_head * 64;
     const int nh = min(64, P.H - h0);
     const int p = P.ctx_len[b] - 1;
     const int n_comp = P.idx_len ? min(max(P.idx_len[b], 0), T.topk) : 0;
     const int t0 = max(0, p - P.window + 1);
-    // Tiles of 32 keys: first the window, in 32-token-aligned blocks A0..A1
-    // (rows outside [t0, p] masked), then the compressed keys in slot-list order
-    // (rows past n_comp masked).  Tile g belongs to CTA g % C of the cluster,
-    // so every CTA starts with its window tiles.
     const int C = T.cluster;
-    const int A0 = t0 >> 5;
-    const int n_swa_t = p >= 0 ? (p >> 5) - A0 + 1 : 0;
+    const int pg0 = t0 >> 6;                              // first window page (64 tokens)
+    const int n_swa_t = p >= 0 ? (p >> 6) - pg0 + 1 : 0;
     const int n_comp_t = (n_comp + kTcKeys - 1) / kTcKeys;
     const int n_glob = n_swa_t + n_comp_t;
     const int n_swa_mine = n_swa_t > rank ? (n_swa_t - rank + C - 1) / C : 0;
     int n_tiles = n_glob > rank ? (n_glob - rank + C - 1) / C : 0;
-    if (n_tiles - n_swa_mine > kTcMaxKeys / kTcKeys) {
+    if (n_tiles - n_swa_mine > kTcMaxCompTiles || n_tiles > kTcMaxTiles) {
         if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
-        n_tiles = n_swa_mine + kTcMaxKeys / kTcKeys;
+        n_tiles = min(n_swa_mine + kTcMaxCompTiles, kTcMaxTiles);
     }
     const int n_comp_mine = n_tiles - n_swa_mine;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -237,16 +223,15 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(tc::smem_u32(&kv_full[i]), 4);
+            tc::mbar_init(tc::smem_u32(&kv_full[i]), kTcProdWarps);
             tc::mbar_init(tc::smem_u32(&kv_empty[i]), 1);
-            tc::mbar_init(tc::smem_u32(&swa_full[i]), 1);
             tc::mbar_init(tc::smem_u32(&s_full[i]), 1);
-            tc::mbar_init(tc::smem_u32(&p_full[i]), 4);
-            tc::mbar_init(tc::smem_u32(&pv_done[i]), 1);
             tc::mbar_init(tc::smem_u32(&sync4[i]), 4);
+            tc::mbar_init(tc::smem_u32(&p_full[i]), 4);
         }
+        for (int i = 0; i < kTcMaxTiles; ++i) tc::mbar_init(tc::smem_u32(&pv_done[i]), 1);
         tc::mbar_init(tc::smem_u32(q_full), 1);
-        tc::mbar_init(tc::smem_u32(table_ready), 4);
+        tc::mbar_init(tc::smem_u32(recv_full), 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -254,7 +239,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         sm_m[threadIdx.x] = -INFINITY;
         sm_l[threadIdx.x] = 0.f;
     }
-    if (warp == 0) {
+    if (warp == kTcMmaWarp) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), kTcTmemCols);
         tc::tmem_relinquish();
     }
@@ -264,222 +249,193 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tmem = *tmem_slot;
 
     if (n_tiles > 0) {
-        if (warp == 8) {
-            // ------------------------------------------------------------ MMA
-            // S(t) = Q K(t)^T with M = 64 (the head rows; D row r in TMEM lane
-            // 32*(r/16) + r%16) and O^T += V(u)^T P(u)^T, issued as soon as each
-            // is ready: QK(t) needs tile t loaded and S buffer t%2 read out
-            // (PV(t-2) issued); PV(u) needs P(u).
+        if (warp == kTcMmaWarp) {
+            // ------------------------------------------------------- QK issue
+            // QK(t) needs tile t loaded and S buffer t%2 read out by the
+            // softmax (P(t-2) written).
             if (lane == 0) {
                 tc::prefetch_tensormap(&tm_q);
+                tc::prefetch_tensormap(&tm_swa);
                 tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), kTcQBytes);
                 for (int c = 0; c < 9; ++c)
                     tc::tma_load_2d(tc::smem_u32(q_s + c * kTcQChunk), &tm_q, tc::smem_u32(q_full), c * 64,
                                     b * P.H + h0);
-                const uint32_t id_qk = tc::idesc(64, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
-                const uint32_t id_pv = tc::idesc(128, 64, tc::kFmtBF16, tc::kFmtBF16, true, false);
+                constexpr uint32_t id_qk = tc::idesc(64, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
                 bool ok = tc::mbar_wait(tc::smem_u32(q_full), 0, abort_flag, P.status);
-                int next_qk = 0, next_pv = 0;
-                uint64_t t_idle = 0;
-                while (ok && next_pv < n_tiles) {
-                    bool did = false;
-                    if (next_qk < n_tiles && next_qk <= next_pv + 1 &&
-                        tc::mbar_test(tc::smem_u32(&kv_full[next_qk & 1]), (next_qk >> 1) & 1)) {
-                        const int t = next_qk;
-                        tc::tc_fence_after();
-                        const uint32_t d = tmem + (t & 1) * kTcKeys;
-                        const uint32_t kb = tc::smem_u32(k_s + (t & 1) * kTcKBytes);
-#pragma unroll 1
-                        for (int c = 0; c < 9; ++c) {
-                            const uint64_t ad = tc::desc_kmajor_sw128(tc::smem_u32(q_s + c * kTcQChunk));
-                            const uint64_t bd = tc::desc_kmajor_sw128(kb + c * kTcKChunk);
+                const uint64_t qd = tc::desc_kmajor_sw128(tc::smem_u32(q_s));
+                for (int t = 0; ok && t < n_tiles; ++t) {
+                    ok = tc::mbar_wait(tc::smem_u32(&kv_full[t & 1]), (t >> 1) & 1, abort_flag, P.status);
+                    if (ok && t >= 2)
+                        ok = tc::mbar_wait(tc::smem_u32(&p_full[t & 1]), ((t - 2) >> 1) & 1, abort_flag, P.status);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint32_t d = tmem + (t & 1) * kTcKeys;
+                    const uint64_t kd = tc::desc_kmajor_sw128(tc::smem_u32(k_s + (t & 1) * kTcKBytes));
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                tc::mma_f16(d, ad + 2 * k, bd + 2 * k, id_qk, (c | k) != 0 ? 1u : 0u);
-                        }
-                        tc::mma_commit(tc::smem_u32(&s_full[t & 1]));
-                        ++next_qk;
-                        did = true;
-                    }
-                    if (next_pv < next_qk &&
-                        tc::mbar_test(tc::smem_u32(&p_full[next_pv & 1]), (next_pv >> 1) & 1)) {
-                        const int u = next_pv;
-                        tc::tc_fence_after();
-                        const uint32_t kb = tc::smem_u32(k_s + (u & 1) * kTcKBytes);
-                        const uint64_t pd = tc::desc_kmajor_sw128(tc::smem_u32(p_s + (u & 1) * kTcPBytes));
+                    for (int c = 0; c < 9; ++c)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc::mma_f16(d, qd + (c * kTcQChunk >> 4) + 2 * k, kd + (c * kTcKChunk >> 4) + 2 * k,
+                                        id_qk, (c | k) != 0 ? 1u : 0u);
+                    tc::mma_commit(tc::smem_u32(&s_full[t & 1]));
+                }
+            }
+        } else if (warp == kTcPvWarp) {
+            // ------------------------------------------------------- PV issue
+            // O^T += V^T P^T once P(u) is written (in the RoPE chunk of tile u).
+            if (lane == 0) {
+                constexpr uint32_t id_pv = tc::idesc(128, 64, tc::kFmtBF16, tc::kFmtBF16, true, false);
+                for (int u = 0; u < n_tiles; ++u) {
+                    if (!tc::mbar_wait(tc::smem_u32(&p_full[u & 1]), (u >> 1) & 1, abort_flag, P.status)) break;
+                    tc::tc_fence_after();
+                    const uint32_t kb = tc::smem_u32(k_s + (u & 1) * kTcKBytes);
+                    const uint64_t pd = tc::desc_kmajor_sw128(kb + 8 * kTcKChunk);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-#pragma unroll
-                            for (int j = 0; j < 2; ++j)
-                                tc::mma_f16(tmem + kTcOCol + i * 64,
-                                            tc::desc_mnmajor_sw128(kb + 2 * i * kTcKChunk + j * 2048, kTcKChunk, 1024),
-                                            pd + 2 * j, id_pv, (u > 0 || j > 0) ? 1u : 0u);
-                        tc::mma_commit(tc::smem_u32(&kv_empty[u & 1]));
-                        tc::mma_commit(tc::smem_u32(&pv_done[u & 1]));
-                        ++next_pv;
-                        did = true;
-                    }
-                    if (did) {
-                        t_idle = 0;
-                    } else if (*abort_flag) {
-                        ok = false;
-                    } else {
-                        // with one event possible, sleep on it (the wait returns when
-                        // it completes); with both possible, keep polling
-                        const bool qk_possible = next_qk < n_tiles && next_qk <= next_pv + 1;
-                        const bool pv_possible = next_pv < next_qk;
-                        if (pv_possible && !qk_possible)
-                            mbar_try_wait_hint(tc::smem_u32(&p_full[next_pv & 1]), (next_pv >> 1) & 1, 1000);
-                        else if (qk_possible && !pv_possible)
-                            mbar_try_wait_hint(tc::smem_u32(&kv_full[next_qk & 1]), (next_qk >> 1) & 1, 1000);
-                        const uint64_t now = tc::global_timer_ns();
-                        if (t_idle == 0) t_idle = now;
-                        else if (now - t_idle > tc::kWaitNs) {
-                            *abort_flag = 1;
-                            flag(P.status, DSV4_DEV_TIMEOUT);
-                            ok = false;
-                        }
-                    }
+                            tc::mma_f16(tmem + kTcOCol + i * 64,
+                                        tc::desc_mnmajor_sw128(kb + 2 * i * kTcKChunk + j * 2048, kTcKChunk, 1024),
+                                        pd + 2 * j, id_pv, (u > 0 || j > 0) ? 1u : 0u);
+                    tc::mma_commit(tc::smem_u32(&kv_empty[u & 1]));
+                    tc::mma_commit(tc::smem_u32(&pv_done[u]));
                 }
             }
         } else if (warp >= 4) {
-            // ------------------------------------------------------ producers
-            const int pt = threadIdx.x - 128;
-            const int pw = warp - 4;                           // producer warp: rows pw, pw + 4, ... of a tile
-            const int n_ckeys = n_comp_mine * kTcKeys;
-            // 1. pointer table of the owned compressed rows (row e: tile
-            //    e / 32 of this CTA's compressed tiles, slot-list key 32 ct + e % 32);
-            //    all index, block-table and scale loads of a phase issued together
+            // ------------------------------------------------------ producers (warps 4-11)
+            // Producer warp pw owns rows pw + 8k (k = 0..7) of every tile.
+            const int pw = warp - 4;
+            // Row table, spread over the lanes: lane l holds row pw + 8 (l % 8) of
+            // compressed tiles 4q + l / 8 (q = 0..3) as page * 64 + row (-1:
+            // padding or unreadable).  Index loads, then block-table loads, each
+            // issued together.
+            int ent[4];
             {
-                constexpr int kPer = kTcMaxKeys / 128;
-                int slot[kPer];
-                int pg[kPer];
+                int slot[4], pg[4];
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    const int e = pt + 128 * i;
-                    slot[i] = -1;
-                    if (e < n_ckeys) {
-                        const int ct = rank + (n_swa_mine + (e >> 5)) * C - n_swa_t;
-                        const int key = ct * kTcKeys + (e & 31);
-                        if (key < n_comp) slot[i] = P.idx[static_cast<long long>(b) * P.idx_stride + key];
+                for (int q = 0; q < 4; ++q) {
+                    const int jc = 4 * q + (lane >> 3);
+                    slot[q] = -1;
+                    if (jc < n_comp_mine) {
+                        const int ct = rank + (n_swa_mine + jc) * C - n_swa_t;
+                        const int key = ct * kTcKeys + pw + 8 * (lane & 7);
+                        if (key < n_comp) slot[q] = P.idx[static_cast<long long>(b) * P.idx_stride + key];
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    pg[i] = -1;
-                    if (slot[i] >= 0 && (slot[i] >> 6) < P.comp_bt_stride)
-                        pg[i] = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + (slot[i] >> 6)];
-                    else if (slot[i] != -1)
+                for (int q = 0; q < 4; ++q) {
+                    pg[q] = -2;
+                    if (slot[q] >= 0 && (slot[q] >> 6) < P.comp_bt_stride)
+                        pg[q] = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + (slot[q] >> 6)];
+                    else if (slot[q] != -1)
                         flag(P.status, DSV4_DEV_BAD_INDEX);
                 }
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    const int e = pt + 128 * i;
-                    if (e >= n_ckeys) continue;
-                    uint64_t ent = 0;
-                    uint2 sc = make_uint2(0, 0);
-                    if (pg[i] >= 0 && pg[i] < P.comp_pages) {
-                        const uint8_t* page = P.comp + static_cast<long long>(pg[i]) * kMlaPage;
-                        const int r = slot[i] & (kPage - 1);
-                        ent = reinterpret_cast<uint64_t>(page + r * kMlaData) | 3u;
-                        sc = *reinterpret_cast<const uint2*>(page + kPage * kMlaData + r * 8);
-                    } else if (slot[i] >= 0) {
-                        flag(P.status, DSV4_DEV_BAD_PAGE);
+                for (int q = 0; q < 4; ++q) {
+                    ent[q] = -1;
+                    if (pg[q] != -2) {
+                        if (pg[q] >= 0 && pg[q] < P.comp_pages) ent[q] = pg[q] * kPage + (slot[q] & (kPage - 1));
+                        else flag(P.status, DSV4_DEV_BAD_PAGE);
                     }
-                    table[e] = make_uint4(static_cast<uint32_t>(ent), static_cast<uint32_t>(ent >> 32), sc.x, sc.y);
                 }
             }
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(table_ready));
-            bool ok = tc::mbar_wait(tc::smem_u32(table_ready), 0, abort_flag, P.status);
-            // 2. compressed rows of tile jc: each lane copies its 16-byte units of
-            //    its warp's rows (units lane and 32 + lane) into the raw stage,
-            //    the same units it converts later (no cross-thread handoff)
-            auto issue_comp = [&](int jc) {
-                uint8_t* rbase = raw_s + (jc & 1) * kTcRawBytes;
+            // raw data of one compressed tile, loaded one tile ahead of its use:
+            // nope unit `lane` (16 codes) of rows pw + 8k with its scale byte,
+            // rope unit lane % 8 of rows pw + 8 (lane / 8) and pw + 8 (lane / 8 + 4)
+            uint4 rn[8];
+            uint32_t rs[8];
+            uint4 rr[2];
+            auto fetch = [&](int jc) {
+                const int q = jc >> 2;
+                const int e_src = q == 0 ? ent[0] : (q == 1 ? ent[1] : (q == 2 ? ent[2] : ent[3]));
+                const int base = (jc & 3) * 8;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int r = pw + 4 * kk;
-                    const uint4 e = table[jc * kTcKeys + r];
-                    if ((e.x & 3u) != 3u) continue;
-                    const uint8_t* src = reinterpret_cast<const uint8_t*>((static_cast<uint64_t>(e.y) << 32 | e.x) & ~uint64_t(15));
-                    tc::cp_async16(tc::smem_u32(rbase + r * kMlaData + lane * 16), src + lane * 16);
-                    if (lane < 8) tc::cp_async16(tc::smem_u32(rbase + r * kMlaData + kNope + lane * 16), src + kNope + lane * 16);
+                for (int k = 0; k < 8; ++k) {
+                    const int e = __shfl_sync(0xffffffffu, e_src, base + k);
+                    rn[k] = make_uint4(0, 0, 0, 0);
+                    rs[k] = 127;
+                    if (e >= 0) {
+                        const uint8_t* page = P.comp + static_cast<long long>(e >> 6) * kMlaPage;
+                        rn[k] = ldg_stream_v4(page + (e & 63) * kMlaData + lane * 16);
+                        rs[k] = ldg_stream_u8(page + kPage * kMlaData + (e & 63) * 8 + (lane >> 2));
+                    }
                 }
-                tc::cp_async_commit();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int e = __shfl_sync(0xffffffffu, e_src, base + (lane >> 3) + 4 * hh);
+                    rr[hh] = make_uint4(0, 0, 0, 0);
+                    if (e >= 0)
+                        rr[hh] = ldg_stream_v4(P.comp + static_cast<long long>(e >> 6) * kMlaPage + (e & 63) * kMlaData +
+                                               kNope + (lane & 7) * 16);
+                }
             };
-            if (ok && n_comp_mine > 0) issue_comp(0);
-            if (ok && n_comp_mine > 1) issue_comp(1);
-            for (int i = 0; ok && i < n_tiles; ++i) {
+            // dequantise into the 128-byte-swizzled tile (row r, 16-byte unit u
+            // of 64-dim chunk c at c * kTcKChunk + r * 128 + ((u ^ (r & 7)) << 4);
+            // r & 7 == pw for every row of this warp).  Lanes of odd chunks store
+            // their two units in the other order, which halves bank conflicts.
+            auto convert = [&](uint8_t* kp) {
+                const int w0 = 2 * (lane & 3);
+                const int flip = (lane >> 2) & 1;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = pw + 8 * k;
+                    uint4 lo, hi;
+                    dequant16(rn[k], rs[k], lo, hi);
+                    uint8_t* row = kp + (lane >> 2) * kTcKChunk + r * 128;
+                    const uint4 first = flip ? hi : lo;
+                    const uint4 second = flip ? lo : hi;
+                    *reinterpret_cast<uint4*>(row + (((w0 + flip) ^ pw) << 4)) = first;
+                    *reinterpret_cast<uint4*>(row + (((w0 + 1 - flip) ^ pw) << 4)) = second;
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = pw + 8 * ((lane >> 3) + 4 * hh);
+                    *reinterpret_cast<uint4*>(kp + 8 * kTcKChunk + r * 128 + (((lane & 7) ^ pw) << 4)) = rr[hh];
+                }
+            };
+            // the first compressed tile's rows are requested once the window pages
+            // are on their way (their table loads overlap the window tiles)
+            if (n_swa_mine == 0 && n_comp_mine > 0) fetch(0);
+            for (int i = 0; i < n_tiles; ++i) {
                 const int kst = i & 1;
                 uint8_t* kp = k_s + kst * kTcKBytes;
                 if (i >= kTcStages &&
                     !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status))
                     break;
                 if (i < n_swa_mine) {
-                    // window tile: nine TMA tensor loads (64 dims x 32 tokens each)
-                    // land it swizzled; nothing to convert
-                    if (pt == 0) {
-                        const int a = A0 + rank + i * C;
-                        const int tok = a * kTcKeys;
-                        int pg = ((tok >> 6) < P.swa_bt_stride) ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + (tok >> 6)] : -1;
-                        if (pg < 0 || pg >= P.swa_pages) {
-                            flag(P.status, DSV4_DEV_BAD_PAGE);
-                            pg = -1;                               // outside the map: the load reads zeros
+                    // window page: nine TMA tensor loads (64 dims x 64 tokens) land it
+                    // swizzled; an unreadable page reads zeros (negative coordinate)
+                    if (pw == 0) {
+                        if (lane == 0) {
+                            const int lp = pg0 + rank + i * C;
+                            int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + lp] : -1;
+                            if (pg < 0 || pg >= P.swa_pages) {
+                                flag(P.status, DSV4_DEV_BAD_PAGE);
+                                pg = -1;
+                            }
+                            const uint32_t bar = tc::smem_u32(&kv_full[kst]);
+                            tc::mbar_arrive_expect_tx(bar, kTcKBytes);
+                            for (int c = 0; c < 9; ++c)
+                                tc::tma_load_3d(tc::smem_u32(kp + c * kTcKChunk), &tm_swa, bar, c * 64, 0, pg);
                         }
-                        const uint32_t bar = tc::smem_u32(&swa_full[kst]);
-                        tc::mbar_arrive_expect_tx(bar, kTcKBytes);
-                        for (int c = 0; c < 9; ++c)
-                            tc::tma_load_3d(tc::smem_u32(kp + c * kTcKChunk), &tm_swa, bar, c * 64, tok & 63, pg);
+                    } else if (lane == 0) {
+                        tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
                     }
-                    if (!tc::mbar_wait(tc::smem_u32(&swa_full[kst]), (i >> 1) & 1, abort_flag, P.status)) break;
+                    if (i == n_swa_mine - 1 && n_comp_mine > 0) fetch(0);
                 } else {
                     const int jc = i - n_swa_mine;
-                    if (jc + 1 < n_comp_mine) asm volatile("cp.async.wait_group 1;" ::: "memory");
-                    else asm volatile("cp.async.wait_group 0;" ::: "memory");
-                    const uint8_t* rbase = raw_s + (jc & 1) * kTcRawBytes;
-#pragma unroll 2
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const int r = pw + 4 * kk;
-                        const uint4 e = table[jc * kTcKeys + r];
-                        const int sw = r & 7;
-                        if ((e.x & 3u) == 3u) {
-                            // lane: nope unit lane (dims 16 lane.., UE8M0 block lane/4);
-                            // lanes 0-7: rope unit (bf16, copied)
-                            const int blk = lane >> 2;
-                            const uint32_t byte = (blk < 4 ? (e.z >> (8 * blk)) : (e.w >> (8 * (blk - 4)))) & 0xffu;
-                            uint4 lo, hi;
-                            dequant16(*reinterpret_cast<const uint4*>(rbase + r * kMlaData + lane * 16), byte, lo, hi);
-                            const int w0 = 2 * (lane & 3);
-                            uint8_t* row = kp + blk * kTcKChunk + r * 128;
-                            *reinterpret_cast<uint4*>(row + ((w0 ^ sw) << 4)) = lo;
-                            *reinterpret_cast<uint4*>(row + (((w0 + 1) ^ sw) << 4)) = hi;
-                            if (lane < 8)
-                                *reinterpret_cast<uint4*>(kp + 8 * kTcKChunk + r * 128 + ((lane ^ sw) << 4)) =
-                                    *reinterpret_cast<const uint4*>(rbase + r * kMlaData + kNope + lane * 16);
-                        } else {
-                            // padding or unreadable row: zeros (masked in the softmax)
-#pragma unroll
-                            for (int q = 0; q < 3; ++q) {
-                                const int w = lane + 32 * q;
-                                if (w < 72)
-                                    *reinterpret_cast<uint4*>(kp + (w >> 3) * kTcKChunk + r * 128 + (((w & 7) ^ sw) << 4)) =
-                                        make_uint4(0, 0, 0, 0);
-                            }
-                        }
-                    }
-                    if (jc + 2 < n_comp_mine) issue_comp(jc + 2);
+                    convert(kp);
                     tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
+                    if (jc + 1 < n_comp_mine) fetch(jc + 1);
                 }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
             }
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
         } else {
             // ------------------------------------------- softmax + O correction
             const bool real = lane < 16;                  // S row h = 16*warp + lane sits in lane 32*warp + lane
             const int h = warp * 16 + (lane & 15);
+            const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
             float m = -INFINITY, l = 0.f;
             for (int t = 0; t < n_tiles; ++t) {
                 const int sb = t & 1;
@@ -489,20 +445,21 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int gt = rank + t * C;
                 int lo_r, hi_r;
                 if (gt < n_swa_t) {
-                    const int tok0 = (A0 + gt) * kTcKeys;
+                    const int tok0 = (pg0 + gt) * kPage;
                     lo_r = max(0, t0 - tok0);
                     hi_r = min(kTcKeys, p - tok0 + 1);
                 } else {
                     lo_r = 0;
                     hi_r = min(kTcKeys, n_comp - (gt - n_swa_t) * kTcKeys);
                 }
-                float s[32];
-                float mx = -INFINITY;
-                tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + sb * kTcKeys, s);
+                float s[64];
+                tc::tmem_ld32(tmem + lane_base + sb * kTcKeys, *reinterpret_cast<float(*)[32]>(s));
+                tc::tmem_ld32(tmem + lane_base + sb * kTcKeys + 32, *reinterpret_cast<float(*)[32]>(s + 32));
                 tc::tmem_ld_wait();
+                float mx = -INFINITY;
                 if (real) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < 64; ++j) {
                         s[j] = (j >= lo_r && j < hi_r) ? s[j] * scale_log2 : -INFINITY;
                         mx = fmaxf(mx, s[j]);
                     }
@@ -510,11 +467,11 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const float m_new = fmaxf(m, mx);
                 const bool need = real && (m_new > m + 8.0f);
                 const float m_use = need ? m_new : m;
-                uint32_t pk[16];
+                uint32_t pk[32];
                 float rowsum = 0.f;
                 if (real) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
+                    for (int j = 0; j < 64; j += 2) {
                         const float e0 = (j >= lo_r && j < hi_r) ? ex2_approx(s[j] - m_use) : 0.f;
                         const float e1 = (j + 1 >= lo_r && j + 1 < hi_r) ? ex2_approx(s[j + 1] - m_use) : 0.f;
                         const __nv_bfloat162 bb = __floats2bfloat162_rn(e0, e1);
@@ -523,10 +480,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
                     }
                 }
-                if (t >= 1 && !tc::mbar_wait(tc::smem_u32(&pv_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag, P.status))
-                    break;
                 const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
-                if (real) sm_alpha[h] = alpha;
+                if (real) sm_alpha[sb * 64 + h] = alpha;
                 const int any_w = __any_sync(0xffffffffu, need);
                 if (lane == 0) sm_any[sb * 4 + warp] = any_w;
                 __threadfence_block();
@@ -535,17 +490,19 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (!tc::mbar_wait(tc::smem_u32(&sync4[sb]), (t >> 1) & 1, abort_flag, P.status)) break;
                 const bool any = (sm_any[sb * 4 + 0] | sm_any[sb * 4 + 1] | sm_any[sb * 4 + 2] | sm_any[sb * 4 + 3]) != 0;
                 if (any && t >= 1) {
+                    // rescale O^T once PV(t-1) (and so every earlier PV) is complete
+                    if (!tc::mbar_wait(tc::smem_u32(&pv_done[t - 1]), 0, abort_flag, P.status)) break;
                     tc::tc_fence_after();
 #pragma unroll 1
                     for (int i = 0; i < 4; ++i) {
 #pragma unroll 1
                         for (int half = 0; half < 2; ++half) {
-                            const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kTcOCol + i * 64 + half * 32;
+                            const uint32_t ta = tmem + lane_base + kTcOCol + i * 64 + half * 32;
                             float o[32];
                             tc::tmem_ld32(ta, o);
                             tc::tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] *= sm_alpha[half * 32 + j];
+                            for (int j = 0; j < 32; ++j) o[j] *= sm_alpha[sb * 64 + half * 32 + j];
                             tc::tmem_st32(ta, o);
                         }
                     }
@@ -554,9 +511,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (real) {
                     l = l * alpha + rowsum;
                     m = m_use;
-                    uint8_t* prow = p_s + sb * kTcPBytes + h * 128;
+                    uint8_t* prow = k_s + sb * kTcKBytes + 8 * kTcKChunk + h * 128;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < 8; ++u)
                         *reinterpret_cast<uint4*>(prow + ((u ^ (h & 7)) << 4)) =
                             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
@@ -569,41 +526,75 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 sm_m[h] = m;
                 sm_l[h] = l;
             }
-            tc::mbar_wait(tc::smem_u32(&pv_done[(n_tiles - 1) & 1]), ((n_tiles - 1) >> 1) & 1, abort_flag, P.status);
+            tc::mbar_wait(tc::smem_u32(&pv_done[n_tiles - 1]), 0, abort_flag, P.status);
             tc::tc_fence_before();
         }
     }
 
     // ------------------------------------------------------------- epilogue
+    // 1. every CTA is past its main loop (its shared memory is free to receive)
     __syncthreads();
     tc::tc_fence_after();
-    float* stage_o = reinterpret_cast<float*>(smem + kStageO);    // [64 heads][512]
-    if (n_tiles > 0 && !*abort_flag) {
-        if (warp < 8) {
-            const int q4 = warp & 3;
+    const int DS = kV / C;                                  // value dims combined by each CTA
+    const int slice = DS * 128 + 512;                       // bytes of one slice
+    uint8_t* recv = smem + kOffRecv;                        // [C] slices from every CTA (own one written here)
+    uint8_t* send = smem + kOffSend;                        // [C] slices for the peers
+    float* mw = reinterpret_cast<float*>(smem + kOffWeights);   // [8][64] weights, then [64] 1 / L
+    if (threadIdx.x == 0)
+        tc::mbar_arrive_expect_tx(tc::smem_u32(recv_full), static_cast<uint32_t>((C - 1) * slice));
+    __syncwarp();
+    tc::cluster_arrive_release();
+    // 2. stage: O^T dim d (TMEM lane) belongs to CTA d / DS; the unnormalised
+    // partial is rounded to bf16 (half the distributed shared memory traffic)
+    const bool have = n_tiles > 0 && !*abort_flag;
+    if (warp < 8) {
+        const int q4 = warp & 3;
 #pragma unroll 1
-            for (int bi = 0; bi < 2; ++bi) {
-                const int i = (warp >> 2) * 2 + bi;
-                const int v = i * 128 + q4 * 32 + lane;
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    float o[32];
-                    tc::tmem_ld32(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + kTcOCol + i * 64 + half * 32, o);
-                    tc::tmem_ld_wait();
+        for (int bi = 0; bi < 2; ++bi) {
+            const int i = (warp >> 2) * 2 + bi;
+            const int d = i * 128 + q4 * 32 + lane;
+            const int dst = d / DS, dl = d - dst * DS;
+            float o[64];
+            if (have) {
+                const uint32_t ta = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + kTcOCol + i * 64;
+                tc::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(o));
+                tc::tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+                tc::tmem_ld_wait();
+            } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) stage_o[(half * 32 + j) * 512 + v] = o[j];
+                for (int j = 0; j < 64; ++j) o[j] = 0.f;
+            }
+            uint8_t* row = (dst == rank ? recv + rank * slice : send + dst * slice) + dl * 128;
+#pragma unroll
+            for (int hc = 0; hc < 8; ++hc) {
+                uint32_t w[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * hc + 2 * c], o[8 * hc + 2 * c + 1]);
+                    w[c] = *reinterpret_cast<const uint32_t*>(&v2);
                 }
+                *reinterpret_cast<uint4*>(row + ((hc ^ (dl & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
-    } else {
-        for (int i = threadIdx.x; i < 64 * 512; i += kTcThreads) stage_o[i] = 0.f;
-        if (threadIdx.x < 64) {
-            sm_m[threadIdx.x] = -INFINITY;
-            sm_l[threadIdx.x] = 0.f;
-        }
+    } else if (warp < 10) {
+        const int hh = threadIdx.x - 256;
+        const float2 ml = have ? make_float2(sm_m[hh], sm_l[hh]) : make_float2(-INFINITY, 0.f);
+        for (int q = 0; q < C; ++q)
+            *reinterpret_cast<float2*>((q == rank ? recv + rank * slice : send + q * slice) + DS * 128 + hh * 8) = ml;
     }
+    tc::fence_proxy_async_smem();
     __syncthreads();
-    tc::cluster_sync();
+    // 3. one bulk copy per peer, once every peer is past its main loop
+    tc::cluster_wait_acquire();
+    if (threadIdx.x < C && threadIdx.x != rank) {
+        const int q = threadIdx.x;
+        tc::bulk_s2s(tc::map_to_rank(tc::smem_u32(recv + rank * slice), q), tc::smem_u32(send + q * slice),
+                     static_cast<uint32_t>(slice), tc::map_to_rank(tc::smem_u32(recv_full), q));
+    }
+    // 4. combine this CTA's slice (bounded wait, also after an abort)
+    const bool got = tc::mbar_wait_cluster(tc::smem_u32(recv_full), 0, P.status);
+    __syncwarp();
+    tc::cluster_arrive_release();                           // the peers' copies into this CTA have landed
     if (threadIdx.x < 64) {
         const int hh = threadIdx.x;
         float mq[8], lq[8];
@@ -613,59 +604,98 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mq[q] = -INFINITY;
             lq[q] = 0.f;
             if (q < C) {
-                mq[q] = tc::ld_cluster_f32(tc::map_to_rank(tc::smem_u32(sm_m + hh), q));
-                lq[q] = tc::ld_cluster_f32(tc::map_to_rank(tc::smem_u32(sm_l + hh), q));
+                const float2 ml = *reinterpret_cast<const float2*>(recv + q * slice + DS * 128 + hh * 8);
+                mq[q] = ml.x;
+                lq[q] = ml.y;
             }
+            M = fmaxf(M, mq[q]);
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) M = fmaxf(M, mq[q]);
         float L = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (q < C) {
                 const float wq = (mq[q] == -INFINITY) ? 0.f : exp2f(mq[q] - M);
-                red_w[q * 64 + hh] = wq;
+                mw[q * 64 + hh] = wq;
                 L += wq * lq[q];
             }
         }
-        red_invl[hh] = L > 0.f ? 1.0f / L : 0.f;
+        mw[8 * 64 + hh] = L > 0.f ? 1.0f / L : 0.f;
         if (rank == 0 && hh < nh && P.lse)
             P.lse[static_cast<long long>(b) * P.H + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
+    tc::tc_fence_before();
     __syncthreads();
-    const int VS = kV / C;                  // value dims merged by this CTA
-    const int per_h = VS / 4;
-    for (int it = threadIdx.x; it < nh * per_h; it += kTcThreads) {
-        const int hh = it / per_h;
-        const int v = rank * VS + (it % per_h) * 4;
-        const uint32_t local = tc::smem_u32(stage_o + hh * 512 + v);
-        float4 x[8];
+    if (got) {
+        // item = 8 dims x 8 heads: 8 swizzled 16-byte rows per source, then
+        // 8 output rows of 8 dims (16-byte stores)
+        for (int it = threadIdx.x; it < DS; it += kTcThreads) {
+            const int d8 = it % (DS / 8), hc = it / (DS / 8);
+            float acc[8][8];                                // [dim][head]
 #pragma unroll
-        for (int q = 0; q < 8; ++q)                   // all remote loads in flight together
-            if (q < C) x[q] = tc::ld_cluster_v4(tc::map_to_rank(local, q));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q < C) {
-                const float wq = red_w[q * 64 + hh];
-                acc.x += wq * x[q].x;
-                acc.y += wq * x[q].y;
-                acc.z += wq * x[q].z;
-                acc.w += wq * x[q].w;
+                for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+            for (int q = 0; q < C; ++q) {
+                float wv[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) wv[c] = mw[q * 64 + 8 * hc + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int dl = 8 * d8 + r;
+                    const uint4 x = *reinterpret_cast<const uint4*>(recv + q * slice + dl * 128 + ((hc ^ (dl & 7)) << 4));
+                    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[c]));
+                        acc[r][2 * c] += wv[2 * c] * f.x;
+                        acc[r][2 * c + 1] += wv[2 * c + 1] * f.y;
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int hh = 8 * hc + c;
+                if (hh < nh) {
+                    const float il = mw[8 * 64 + hh];
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int r = 0; r < 8; r += 2) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[r][c] * il, acc[r + 1][c] * il);
+                        pk[r >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+                    }
+                    *reinterpret_cast<uint4*>(P.out + (static_cast<long long>(b) * P.H + h0 + hh) * kV + rank * DS + 8 * d8) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
             }
         }
-        const float il = red_invl[hh];
-        const __nv_bfloat162 o01 = __floats2bfloat162_rn(acc.x * il, acc.y * il);
-        const __nv_bfloat162 o23 = __floats2bfloat162_rn(acc.z * il, acc.w * il);
-        uint2 pk2;
-        pk2.x = *reinterpret_cast<const uint32_t*>(&o01);
-        pk2.y = *reinterpret_cast<const uint32_t*>(&o23);
-        *reinterpret_cast<uint2*>(P.out + (static_cast<long long>(b) * P.H + h0 + hh) * kV + v) = pk2;
     }
-    tc::cluster_sync();
-    if (warp == 0) {
+    __syncwarp();
+    tc::cluster_wait_acquire();                             // every peer has received this CTA's copies
+    if (warp == kTcMmaWarp) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
+// Every (code, scale byte) pair through the key conversion of the decode
+// kernel: out[s * 256 + c] = bf16 bits of code c times 2^(s - 127).
+__global__ void key_dequant_selftest_kernel(uint16_t* out)
+{
+    const int s = blockIdx.x;                 // scale byte
+    const int g = threadIdx.x;                // 16 groups of 16 codes
+    uint32_t wv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c0 = g * 16 + 4 * i;
+        wv[i] = c0 | ((c0 + 1) << 8) | ((c0 + 2) << 16) | ((c0 + 3) << 24);
+    }
+    uint4 lo, hi;
+    dequant16(make_uint4(wv[0], wv[1], wv[2], wv[3]), static_cast<uint32_t>(s), lo, hi);
+    const uint32_t o[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        out[s * 256 + g * 16 + 2 * i] = static_cast<uint16_t>(o[i] & 0xffffu);
+        out[s * 256 + g * 16 + 2 * i + 1] = static_cast<uint16_t>(o[i] >> 16);
     }
 }
 
@@ -716,6 +746,7 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     const uint64_t qstr[1] = {static_cast<uint64_t>(kHead) * 2};
     const uint32_t qbox[2] = {64, 64};
     if ((reinterpret_cast<uintptr_t>(a->q_dev) & 15) || (reinterpret_cast<uintptr_t>(a->swa_cache_dev) & 15) ||
+        (reinterpret_cast<uintptr_t>(a->out_dev) & 15) ||
         (sparse && (reinterpret_cast<uintptr_t>(a->comp_cache_dev) & 15)))
         return DSV4_ERR_SHAPE;
     if (!encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->q_dev, qdims, qstr, qbox,
@@ -748,4 +779,12 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_tc, tm_q, tm_swa, T);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" dsv4_status dsv4_selftest_key_dequant(void* out_dev, dsv4_stream_t stream)
+{
+    if (out_dev == nullptr) return DSV4_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(out_dev) & 1) return DSV4_ERR_SHAPE;
+    key_dequant_selftest_kernel<<<256, 16, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<uint16_t*>(out_dev));
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

@@ -71,6 +71,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: pairs with remote release arrivals.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Every wait is bounded: past kWaitNs (wall clock) or once another role has
 // set the CTA's abort word, it gives up, sets the abort word and the device
 // status bit, and returns false so the caller can unwind.
@@ -90,6 +104,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+
+// Bounded wait for a phase completed by arrivals from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitNs) {
+            flag(status, DSV4_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ---- TMA ----------------------------------------------------------------------
@@ -244,6 +271,68 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Split cluster barrier: every thread of every CTA arrives (release), and
+// later waits (acquire) for all arrivals of the phase.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Asynchronous store into (possibly another CTA's) shared memory; completion
+// is counted in bytes on the destination CTA's mbarrier `bar` (both addresses
+// are shared::cluster addresses of the destination CTA).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr), "f"(a), "f"(b), "r"(bar)
+                 : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into (another) CTA's shared memory
+// of the cluster; completion counted in bytes on the destination's mbarrier.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+
+// Plain (weak) stores into another CTA's shared memory.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.

@@ -342,7 +342,8 @@ dsv4_status dsv4_indexer_topk_noalloc(const dsv4_plan* plan, const dsv4_indexer_
  *   out[b][h] = sum P * key[0:512] (bf16), lse[b][h] = max s + ln sum e^(s - max).
  * swaonly plans ignore the compressed cache and indices (may be NULL).
  *
- * q_dev: bf16 [batch][n_heads][576]; out_dev: bf16 [batch][n_heads][512];
+ * q_dev: bf16 [batch][n_heads][576]; out_dev: bf16 [batch][n_heads][512]
+ * (q_dev, out_dev and both caches 16-byte aligned, else DSV4_ERR_SHAPE);
  * lse_dev: fp32 [batch][n_heads] or NULL.
  * swa_cache_dev / swa_block_table_dev: SWA pages; comp_cache_dev /
  * comp_block_table_dev: compressed pages; topk_idx_dev: int32
@@ -377,6 +378,15 @@ dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_mla_args* a
  * `spin_limit` polls, so a test can see the bounded-wait path set
  * DSV4_DEV_TIMEOUT in *status_dev and return (the context stays usable). */
 dsv4_status dsv4_selftest_bounded_wait(int* status_dev, int spin_limit, dsv4_stream_t stream);
+
+/* Run the decode kernel's key conversion (FP8 E4M3 code times 2^(s - 127),
+ * s a UE8M0 scale byte, to bf16) over every code c and scale byte s:
+ * out_dev: uint16 [256 * 256], out[s * 256 + c] = the bf16 bits.  Lets a test
+ * check the conversion exhaustively against the definition of the two formats
+ * (section "FP8 Quant" of the compressor walkthrough: E4M3 codes with one
+ * power-of-two scale per 64 dims).  Errors: DSV4_ERR_INVALID (NULL),
+ * DSV4_ERR_SHAPE (misaligned), DSV4_ERR_CUDA (launch). */
+dsv4_status dsv4_selftest_key_dequant(void* out_dev, dsv4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -113,3 +113,31 @@ def test_zero_output_fails_the_tolerance():
     check_attention(out[0], ref)
     with pytest.raises(AssertionError):
         check_attention(np.zeros_like(out[0]), ref)
+
+
+def test_key_dequant_every_code_and_scale():
+    """The decode kernel's key conversion (E4M3 code x 2^(s-127) -> bf16) for all
+    256 codes and 256 scale bytes: bit-exact against the oracle's decode of the
+    two formats wherever the result is a normal bf16, zero or infinite; results
+    below the bf16 normal range only need the right sign and a magnitude below
+    2^-126.  The two NaN codes are never written and are left out."""
+    out = torch.zeros(65536, dtype=torch.int16, device="cuda")
+    B.selftest_key_dequant(out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16).reshape(256, 256)
+    vals = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    nan = np.isnan(vals)            # 0x7f / 0xff: never written (the quantiser saturates)
+    assert nan.sum() == 2
+    vals = np.where(nan, 0.0, vals)
+    for s in range(256):
+        v = vals * (2.0 ** (s - 127))
+        small = ((v != 0) & (np.abs(v) < 2.0 ** -126)) | nan
+        with np.errstate(over="ignore"):
+            exp = oracle.f32_to_bf16(v.astype(np.float32))
+        ok = (got[s] == exp) | small
+        assert ok.all(), (s, np.nonzero(~ok)[0][:8], got[s][~ok][:8], exp[~ok][:8])
+        tiny = small & ~nan
+        if tiny.any():
+            g = oracle.bf16_to_f32(got[s][tiny])
+            assert np.all(np.abs(g) < 2.0 ** -126)
+            assert np.all((np.signbit(g) == np.signbit(v[tiny])) | (g == 0))
