@@ -54,7 +54,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                   IdxTcParams P)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = tc::align1024_shared(smem_raw);
     uint8_t* a_tiles = smem;
     uint8_t* q_tile = smem + kIdxStages * kIdxTileBytes;
     float* scales_s = reinterpret_cast<float*>(q_tile + kIdxQBytes);   // [stage][128 slots]

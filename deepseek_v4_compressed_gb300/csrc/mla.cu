@@ -180,7 +180,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 {
     const MlaParams& P = T.base;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = tc::align1024_shared(smem_raw);
     uint8_t* q_s = smem + kOffQ;
     uint8_t* k_s = smem + kOffK;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffMisc);
@@ -433,7 +433,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
         } else {
             // ------------------------------------------- softmax + O correction
-            const bool real = lane < 16;                  // S row h = 16*warp + lane sits in lane 32*warp + lane
+            // Head h = 16*warp + lane % 16 (S row in TMEM lane 32*warp + lane % 16);
+            // lanes 0-15 take keys 0-31 of the tile, lanes 16-31 keys 32-63.
+            const int half = lane >> 4;
             const int h = warp * 16 + (lane & 15);
             const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
             float m = -INFINITY, l = 0.f;
@@ -441,7 +443,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int sb = t & 1;
                 if (!tc::mbar_wait(tc::smem_u32(&s_full[sb]), (t >> 1) & 1, abort_flag, P.status)) break;
                 tc::tc_fence_after();
-                // rows of this tile that are keys of the query
+                // rows of this tile that are keys of the query, relative to this half
                 const int gt = rank + t * C;
                 int lo_r, hi_r;
                 if (gt < n_swa_t) {
@@ -452,36 +454,35 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     lo_r = 0;
                     hi_r = min(kTcKeys, n_comp - (gt - n_swa_t) * kTcKeys);
                 }
-                float s[64];
-                tc::tmem_ld32(tmem + lane_base + sb * kTcKeys, *reinterpret_cast<float(*)[32]>(s));
-                tc::tmem_ld32(tmem + lane_base + sb * kTcKeys + 32, *reinterpret_cast<float(*)[32]>(s + 32));
+                lo_r -= 32 * half;
+                hi_r -= 32 * half;
+                float s[32];
+                tc::tmem_ld16x2_32(tmem + lane_base + sb * kTcKeys, s);
                 tc::tmem_ld_wait();
                 float mx = -INFINITY;
-                if (real) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        s[j] = (j >= lo_r && j < hi_r) ? s[j] * scale_log2 : -INFINITY;
-                        mx = fmaxf(mx, s[j]);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = (j >= lo_r && j < hi_r) ? s[j] * scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[j]);
                 }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m, mx);
-                const bool need = real && (m_new > m + 8.0f);
+                const bool need = m_new > m + 8.0f;
                 const float m_use = need ? m_new : m;
-                uint32_t pk[32];
+                uint32_t pk[16];
                 float rowsum = 0.f;
-                if (real) {
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const float e0 = (j >= lo_r && j < hi_r) ? ex2_approx(s[j] - m_use) : 0.f;
-                        const float e1 = (j + 1 >= lo_r && j + 1 < hi_r) ? ex2_approx(s[j + 1] - m_use) : 0.f;
-                        const __nv_bfloat162 bb = __floats2bfloat162_rn(e0, e1);
-                        const float2 rb = __bfloat1622float2(bb);
-                        rowsum += rb.x + rb.y;
-                        pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
-                    }
+                for (int j = 0; j < 32; j += 2) {
+                    const float e0 = (j >= lo_r && j < hi_r) ? ex2_approx(s[j] - m_use) : 0.f;
+                    const float e1 = (j + 1 >= lo_r && j + 1 < hi_r) ? ex2_approx(s[j + 1] - m_use) : 0.f;
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(e0, e1);
+                    const float2 rb = __bfloat1622float2(bb);
+                    rowsum += rb.x + rb.y;
+                    pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
+                rowsum += __shfl_xor_sync(0xffffffffu, rowsum, 16);
                 const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
-                if (real) sm_alpha[sb * 64 + h] = alpha;
+                if (half == 0) sm_alpha[sb * 64 + h] = alpha;
                 const int any_w = __any_sync(0xffffffffu, need);
                 if (lane == 0) sm_any[sb * 4 + warp] = any_w;
                 __threadfence_block();
@@ -494,35 +495,30 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!tc::mbar_wait(tc::smem_u32(&pv_done[t - 1]), 0, abort_flag, P.status)) break;
                     tc::tc_fence_after();
 #pragma unroll 1
-                    for (int i = 0; i < 4; ++i) {
-#pragma unroll 1
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t ta = tmem + lane_base + kTcOCol + i * 64 + half * 32;
-                            float o[32];
-                            tc::tmem_ld32(ta, o);
-                            tc::tmem_ld_wait();
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t ta = tmem + lane_base + kTcOCol + i * 32;
+                        float o[32];
+                        tc::tmem_ld32(ta, o);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] *= sm_alpha[sb * 64 + half * 32 + j];
-                            tc::tmem_st32(ta, o);
-                        }
+                        for (int j = 0; j < 32; ++j) o[j] *= sm_alpha[sb * 64 + (i & 1) * 32 + j];
+                        tc::tmem_st32(ta, o);
                     }
                     tc::tmem_st_wait();
                 }
-                if (real) {
-                    l = l * alpha + rowsum;
-                    m = m_use;
-                    uint8_t* prow = k_s + sb * kTcKBytes + 8 * kTcKChunk + h * 128;
+                l = l * alpha + rowsum;
+                m = m_use;
+                uint8_t* prow = k_s + sb * kTcKBytes + 8 * kTcKChunk + h * 128;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<uint4*>(prow + ((u ^ (h & 7)) << 4)) =
-                            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4*>(prow + (((4 * half + u) ^ (h & 7)) << 4)) =
+                        make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(tc::smem_u32(&p_full[sb]));
             }
-            if (real) {
+            if (half == 0) {
                 sm_m[h] = m;
                 sm_l[h] = l;
             }
@@ -614,7 +610,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (q < C) {
-                const float wq = (mq[q] == -INFINITY) ? 0.f : exp2f(mq[q] - M);
+                const float wq = (mq[q] == -INFINITY) ? 0.f : ex2_approx(mq[q] - M);
                 mw[q * 64 + hh] = wq;
                 L += wq * lq[q];
             }
@@ -626,47 +622,29 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tc::tc_fence_before();
     __syncthreads();
     if (got) {
-        // item = 8 dims x 8 heads: 8 swizzled 16-byte rows per source, then
-        // 8 output rows of 8 dims (16-byte stores)
-        for (int it = threadIdx.x; it < DS; it += kTcThreads) {
-            const int d8 = it % (DS / 8), hc = it / (DS / 8);
-            float acc[8][8];                                // [dim][head]
+        // item = (dim, 8 heads): consecutive threads take consecutive dims
+        for (int it = threadIdx.x; it < DS * 8; it += kTcThreads) {
+            const int dl = it % DS, hc = it / DS;
+            float acc[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+            for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+#pragma unroll 1
             for (int q = 0; q < C; ++q) {
-                float wv[8];
+                const uint4 x = *reinterpret_cast<const uint4*>(recv + q * slice + dl * 128 + ((hc ^ (dl & 7)) << 4));
+                const float4 w0 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc);
+                const float4 w1 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc + 4);
+                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int c = 0; c < 8; ++c) wv[c] = mw[q * 64 + 8 * hc + c];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int dl = 8 * d8 + r;
-                    const uint4 x = *reinterpret_cast<const uint4*>(recv + q * slice + dl * 128 + ((hc ^ (dl & 7)) << 4));
-                    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[c]));
-                        acc[r][2 * c] += wv[2 * c] * f.x;
-                        acc[r][2 * c + 1] += wv[2 * c + 1] * f.y;
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    acc[2 * c] += wv[2 * c] * __uint_as_float(xw[c] << 16);
+                    acc[2 * c + 1] += wv[2 * c + 1] * __uint_as_float(xw[c] & 0xffff0000u);
                 }
             }
+            uint16_t* o = P.out + (static_cast<long long>(b) * P.H + h0 + 8 * hc) * kV + rank * DS + dl;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int hh = 8 * hc + c;
-                if (hh < nh) {
-                    const float il = mw[8 * 64 + hh];
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int r = 0; r < 8; r += 2) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[r][c] * il, acc[r + 1][c] * il);
-                        pk[r >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
-                    }
-                    *reinterpret_cast<uint4*>(P.out + (static_cast<long long>(b) * P.H + h0 + hh) * kV + rank * DS + 8 * d8) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
-            }
+            for (int c = 0; c < 8; ++c)
+                if (8 * hc + c < nh) o[c * kV] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * mw[8 * 64 + 8 * hc + c]));
         }
     }
     __syncwarp();

@@ -236,6 +236,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 TMEM lanes (from the warp's base lane) x 32 columns, twice: threads
+// 0-15 read lane t at columns [c, c + 32), threads 16-31 read lane t - 16 at
+// columns [c + 32, c + 64).  Suits M = 64 accumulators, whose rows sit in 16
+// lanes of each 32-lane quadrant.
+__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], 32;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
@@ -259,6 +279,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 1024-byte aligned start inside the dynamic shared-memory array.  Derived by
+// pointer arithmetic on the array itself (no integer round trip), so every
+// access through it stays a shared-memory access rather than a generic one.
+__device__ __forceinline__ uint8_t* align1024_shared(uint8_t* base)
+{
+    return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
 
 // ---- thread-block clusters / distributed shared memory ----------------------
 __device__ __forceinline__ uint32_t cluster_ctarank()
