@@ -171,10 +171,10 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
     p->max_slots = (type == DSV4_C4A) ? max_ctx / 4 : (type == DSV4_C128A ? max_ctx / 128 : 0);
     p->max_keys = p->topk + g->window;
     if (type == DSV4_C4A) {
-        // indexer: 128-slot tiles spread so about three CTAs per SM stay resident
+        // indexer: 128-slot tiles; a sequence's tiles are split over at most
+        // SMs / batch CTAs (one CTA per SM), each streaming its share
         const int tiles = (p->max_slots + 127) / 128;
-        const int target = 3 * sm_count();
-        int per_seq = (target + batch - 1) / batch;
+        int per_seq = sm_count() / batch;
         per_seq = per_seq < 1 ? 1 : (per_seq > tiles ? tiles : per_seq);
         p->idx_tiles_per_cta = tiles > 0 ? (tiles + per_seq - 1) / per_seq : 1;
         p->idx_ctas_per_seq = tiles > 0 ? (tiles + p->idx_tiles_per_cta - 1) / p->idx_tiles_per_cta : 0;

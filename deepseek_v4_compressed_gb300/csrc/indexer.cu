@@ -18,17 +18,21 @@ namespace dsv4 {
 // D[128 slots x N heads] = K_tile[128 x 128] * Q^T[128 x N] (fp32 in TMEM),
 // then each of 128 epilogue threads turns its slot's row of D into
 // I_s = scale_s * sum_j w_j * max(D_sj, 0).
-//   warp 4: TMA producer (query once, then two page loads per tile, 3-stage ring)
-//   warp 5: MMA issuer (4 MMAs of K=32 per tile, double-buffered accumulator)
-//   warps 0-3: epilogue (TMEM lane = slot row)
+//   warp 8: TMA producer (query once, then two page loads per tile, 6-stage ring)
+//   warp 9: MMA issuer (4 MMAs of K=32 per tile, 4 accumulators)
+//   warps 0-3 / 4-7: epilogue of the even / odd tiles (TMEM lane = slot row)
+// One CTA per SM: CTAs of kernels that allocate tensor memory start one
+// after another on an SM, so the work of a sequence is split over at most
+// SMs / batch CTAs that each stream many tiles.
 // Memory-bound: 132 bytes of cache per slot against 2 * 128 * N flops.
 // ---------------------------------------------------------------------------
 constexpr int kIdxTileSlots = 128;
-constexpr int kIdxStages = 3;
+constexpr int kIdxStages = 6;
+constexpr int kIdxAcc = 4;
 constexpr int kIdxTileBytes = kIdxTileSlots * kIdx;       // 16 KB
 constexpr int kIdxQBytes = 64 * kIdx;                     // query tile, N <= 64 rows
-constexpr int kIdxThreads = 192;
-constexpr int kIdxTmemCols = 128;                         // 2 accumulators x 64 columns
+constexpr int kIdxThreads = 320;
+constexpr int kIdxTmemCols = kIdxAcc * 64;                // 4 accumulators x 64 columns
 constexpr int kIdxScaleBytes = 2 * kPage * 4;                // scale planes of the tile's two pages
 constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
                          2048 /* barriers etc */ + 1024 /* align */;
@@ -53,6 +57,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_q,
                   IdxTcParams P)
 {
+    // the top-k kernel that follows may be scheduled now; it waits for this
+    // grid's completion before reading the logits
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = tc::align1024_shared(smem_raw);
     uint8_t* a_tiles = smem;
@@ -61,10 +68,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     uint64_t* bars = reinterpret_cast<uint64_t*>(q_tile + kIdxQBytes + kIdxStages * kIdxScaleBytes);
     uint64_t* full = bars;                        // [kIdxStages]
     uint64_t* empty = bars + kIdxStages;          // [kIdxStages]
-    uint64_t* acc_full = bars + 2 * kIdxStages;   // [2]
-    uint64_t* acc_empty = acc_full + 2;           // [2]
-    uint64_t* q_bar = acc_empty + 2;
-    float* w_s = reinterpret_cast<float*>(q_bar + 1);
+    uint64_t* acc_full = bars + 2 * kIdxStages;   // [kIdxAcc]
+    uint64_t* acc_empty = acc_full + kIdxAcc;     // [kIdxAcc]
+    uint64_t* q_bar = acc_empty + kIdxAcc;
+    float* w_s = reinterpret_cast<float*>(bars + 32);            // [64], 16-byte aligned, zero past H
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_s + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -85,7 +92,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             tc::mbar_init(tc::smem_u32(&full[i]), 1);
             tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (scales read)
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kIdxAcc; ++i) {
             tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
             tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
         }
@@ -105,41 +112,54 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     int issued = 0;   // tiles whose loads were issued (producer only)
     int consumed = 0; // tiles whose stage the MMA released (MMA thread only)
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             tc::prefetch_tensormap(&tm_cache);
             tc::prefetch_tensormap(&tm_q);
             tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
             tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
-            for (int i = 0; i < n_my; ++i) {
+        }
+        int pgl = -1;     // lane l: page id of page l of the current group of 16 tiles
+        for (int i = 0; i < n_my; ++i) {
+            if ((i & 15) == 0) {
+                // the page ids of the next 16 tiles, loaded by the lanes at once
+                const int gp = 2 * (t_begin + i) + lane;
+                pgl = -1;
+                if (2 * i + lane < 2 * n_my) {
+                    const int pi = min(gp, n_pages - 1);
+                    pgl = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                    if (pgl < 0 || pgl >= P.num_pages) {
+                        flag(P.status, DSV4_DEV_BAD_PAGE);
+                        pgl = -1;
+                    }
+                }
+            }
+            const int v0 = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15));
+            const int v1 = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15) + 1);
+            bool go = true;
+            if (lane == 0) {
                 const int st = i % kIdxStages;
                 const uint32_t ph = (i / kIdxStages) & 1;
-                if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status)) break;
-                const int tile = t_begin + i;
-                int pg[2], spg[2];
-                for (int h = 0; h < 2; ++h) {
-                    const int pi = min(2 * tile + h, n_pages - 1);
-                    int v = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
-                    spg[h] = v;
-                    if (v < 0 || v >= P.num_pages) {
-                        flag(P.status, DSV4_DEV_BAD_PAGE);
-                        v = P.num_pages;          // out of the map: TMA fills zeros
-                        spg[h] = 0;               // scales from a valid page (the row's data is zero)
-                    }
-                    pg[h] = v;
+                if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status)) {
+                    go = false;
+                } else {
+                    const int pg[2] = {v0 < 0 ? P.num_pages : v0, v1 < 0 ? P.num_pages : v1};  // unreadable: zeros
+                    const int spg[2] = {v0 < 0 ? 0 : v0, v1 < 0 ? 0 : v1};  // scales from a valid page
+                    const uint32_t dst = tc::smem_u32(a_tiles + st * kIdxTileBytes);
+                    const uint32_t fb = tc::smem_u32(&full[st]);
+                    tc::mbar_arrive_expect_tx(fb, kIdxTileBytes + kIdxScaleBytes);
+                    tc::tma_load_3d(dst, &tm_cache, fb, 0, 0, pg[0]);
+                    tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, fb, 0, 0, pg[1]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tc::bulk_load(tc::smem_u32(scales_s + st * 128 + h * kPage),
+                                      P.cache + static_cast<long long>(spg[h]) * kIdxPage + kPage * kIdx, kPage * 4, fb);
+                    issued = i + 1;
                 }
-                const uint32_t dst = tc::smem_u32(a_tiles + st * kIdxTileBytes);
-                const uint32_t fb = tc::smem_u32(&full[st]);
-                tc::mbar_arrive_expect_tx(fb, kIdxTileBytes + kIdxScaleBytes);
-                tc::tma_load_3d(dst, &tm_cache, fb, 0, 0, pg[0]);
-                tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, fb, 0, 0, pg[1]);
-                for (int h = 0; h < 2; ++h)
-                    tc::bulk_load(tc::smem_u32(scales_s + st * 128 + h * kPage),
-                                  P.cache + static_cast<long long>(spg[h]) * kIdxPage + kPage * kIdx, kPage * 4, fb);
-                issued = i + 1;
             }
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc(128, P.n_pad, tc::kFmtE4M3, tc::kFmtE4M3);
             const uint64_t b_desc = tc::desc_kmajor_sw128(tc::smem_u32(q_tile));
@@ -147,10 +167,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                 for (int i = 0; i < n_my; ++i) {
                     const int st = i % kIdxStages;
                     const uint32_t ph = (i / kIdxStages) & 1;
-                    const int ab = i & 1;
-                    const uint32_t aph = (i >> 1) & 1;
+                    const int ab = i % kIdxAcc;
+                    const uint32_t aph = (i / kIdxAcc) & 1;
                     if (!tc::mbar_wait(tc::smem_u32(&full[st]), ph, abort_flag, P.status)) break;
-                    if (i >= 2 && !tc::mbar_wait(tc::smem_u32(&acc_empty[ab]), aph ^ 1, abort_flag, P.status)) break;
+                    if (i >= kIdxAcc && !tc::mbar_wait(tc::smem_u32(&acc_empty[ab]), aph ^ 1, abort_flag, P.status)) break;
                     tc::tc_fence_after();
                     const uint64_t a_desc = tc::desc_kmajor_sw128(tc::smem_u32(a_tiles + st * kIdxTileBytes));
                     const uint32_t d = tmem + ab * 64;
@@ -164,13 +184,16 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             }
         }
     } else {
-        const int row = warp * 32 + lane;
-        for (int i = 0; i < n_my; ++i) {
-            const int ab = i & 1;
-            const uint32_t aph = (i >> 1) & 1;
+        // epilogue group (warps 0-3 or 4-7) takes every other tile
+        const int grp = warp >> 2;
+        const int q4 = warp & 3;
+        const int row = q4 * 32 + lane;
+        for (int i = grp; i < n_my; i += 2) {
+            const int ab = i % kIdxAcc;
+            const uint32_t aph = (i / kIdxAcc) & 1;
             if (!tc::mbar_wait(tc::smem_u32(&acc_full[ab]), aph, abort_flag, P.status)) break;
             tc::tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + ab * 64;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + ab * 64;
             float v0[32], v1[32];
             tc::tmem_ld32(taddr, v0);
             if (P.n_pad > 32) tc::tmem_ld32(taddr + 32, v1);
@@ -179,14 +202,27 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acc_empty[ab]));
             float acc = 0.f;
+            if (P.n_pad == 64) {
+                // weights past H are zero and every column is a real accumulator
+                const float4* w4 = reinterpret_cast<const float4*>(w_s);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc += (j < P.H) ? w_s[j] * fmaxf(v0[j], 0.f) : 0.f;
-            if (P.n_pad > 32) {
+                for (int j = 0; j < 8; ++j) {
+                    const float4 a = w4[j], c = w4[j + 8];
+                    acc += a.x * fmaxf(v0[4 * j], 0.f) + a.y * fmaxf(v0[4 * j + 1], 0.f) +
+                           a.z * fmaxf(v0[4 * j + 2], 0.f) + a.w * fmaxf(v0[4 * j + 3], 0.f);
+                    acc += c.x * fmaxf(v1[4 * j], 0.f) + c.y * fmaxf(v1[4 * j + 1], 0.f) +
+                           c.z * fmaxf(v1[4 * j + 2], 0.f) + c.w * fmaxf(v1[4 * j + 3], 0.f);
+                }
+            } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
+                for (int j = 0; j < 32; ++j) acc += (j < P.H) ? w_s[j] * fmaxf(v0[j], 0.f) : 0.f;
+                if (P.n_pad > 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
+                }
             }
             // the stage's scales: its full barrier cannot have moved on, since
-            // the stage is only refilled after this warp releases it below
+            // the stage is only refilled after this group releases it below
             const int st = i % kIdxStages;
             float scale = 0.f;
             if (tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status))
@@ -200,7 +236,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
 
     tc::tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp == 4 && lane == 0) {
+    if (*abort_flag && warp == 8 && lane == 0) {
         // let this CTA's own copies land before its shared memory is released
         for (int i = consumed > 0 ? consumed : 0; i < issued; ++i) {
             volatile int no_abort = 0;
@@ -391,6 +427,237 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     if (threadIdx.x == 0) out_len[b] = k;
 }
 
+// Rows of at most 8192 slots: every thread keeps 16 consecutive keys in
+// registers.  An 11-bit digit pass over (key - row minimum) finds the bin of
+// the k-th largest key; that bin's keys go to a list (up to 2048; else the
+// passes stay on the registers with one 256-bin histogram per warp), and
+// 8-bit passes over the list finish the threshold.  The same ordered
+// compaction writes the k slots in ascending order.
+constexpr int kTopkSmallPer = 16;
+constexpr int kTopkSmallMax = kTopkThreads * kTopkSmallPer;   // 8192
+constexpr int kTopkList = 2048;                                 // threshold-bin keys kept in a list
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
+    const float* __restrict__ logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
+    int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len)
+{
+    constexpr int NW = kTopkThreads / 32;
+    constexpr int kClear = (NW * 256) / kTopkThreads;   // histogram words each thread clears
+    __shared__ int wh[NW][256];
+    __shared__ int hist1[kTopkBins];
+    __shared__ uint32_t list[kTopkList];
+    __shared__ int scratch[33];
+    __shared__ uint32_t s_max[NW], s_mins[NW], s_prefix;
+    __shared__ int s_shift, s_rem, s_done;
+
+    // the logits were produced by the previous kernel of this call
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = threadIdx.x * kTopkSmallPer;
+    const float* lrow = logits + static_cast<long long>(b) * row_stride;
+    // the row is allocated up to max_slots: load it together with the length
+    float v[kTopkSmallPer];
+#pragma unroll
+    for (int j = 0; j < kTopkSmallPer / 4; ++j) {
+        const int i = i0 + 4 * j;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i + 3 < max_slots) {
+            f = *reinterpret_cast<const float4*>(lrow + i);   // row_stride and i are multiples of 4
+        } else {
+            if (i < max_slots) f.x = lrow[i];
+            if (i + 1 < max_slots) f.y = lrow[i + 1];
+            if (i + 2 < max_slots) f.z = lrow[i + 2];
+        }
+        v[4 * j] = f.x;
+        v[4 * j + 1] = f.y;
+        v[4 * j + 2] = f.z;
+        v[4 * j + 3] = f.w;
+    }
+    int n = ctx_len[b] / 4;
+    n = n < 0 ? 0 : (n > max_slots ? max_slots : n);
+    int* orow = out_idx + static_cast<long long>(b) * out_stride;
+    if (n <= k) {
+        for (int i = threadIdx.x; i < k; i += blockDim.x) orow[i] = (i < n) ? i : -1;
+        if (threadIdx.x == 0) out_len[b] = n;
+        return;
+    }
+    uint32_t off[kTopkSmallPer];
+    uint32_t vm = 0;                                  // bit e: slot i0 + e exists
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int e = 0; e < kTopkSmallPer; ++e) {
+        off[e] = f32_order_key(v[e]);
+        if (i0 + e < n) {
+            vm |= 1u << e;
+            mn = min(mn, off[e]);
+            mx = max(mx, off[e]);
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        s_mins[warp] = mn;
+        s_max[warp] = mx;
+    }
+#pragma unroll
+    for (int q = 0; q < kClear; ++q) (&wh[0][0])[threadIdx.x * kClear + q] = 0;
+#pragma unroll
+    for (int q = 0; q < kTopkBins / kTopkThreads; ++q) hist1[threadIdx.x * (kTopkBins / kTopkThreads) + q] = 0;
+    __syncthreads();
+    uint32_t base = 0xffffffffu, top = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        base = min(base, s_mins[w]);
+        top = max(top, s_max[w]);
+    }
+    const uint32_t range = top - base;
+    int shift = range ? 32 - __clz(range) : 0;        // offsets fit in `shift` bits
+    uint32_t prefix = 0;
+    int rem = k;
+    bool done = (range == 0);
+#pragma unroll
+    for (int e = 0; e < kTopkSmallPer; ++e) off[e] = ((vm >> e) & 1u) ? off[e] - base : 0u;
+
+    // pass 1: 11-bit digits over the whole range, one shared histogram
+    if (!done) {
+        const int lo1 = shift > 11 ? shift - 11 : 0;
+#pragma unroll
+        for (int e = 0; e < kTopkSmallPer; ++e)
+            if ((vm >> e) & 1u) atomicAdd(&hist1[off[e] >> lo1], 1);
+        __syncthreads();
+        int c[4];
+        int local = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            c[q] = hist1[kTopkBins - 1 - 4 * threadIdx.x - q];
+            local += c[q];
+        }
+        int tot1;
+        const int before = block_excl_scan(local, scratch, tot1);
+        if (before < rem && rem <= before + local) {
+            int cum = before;
+            bool found = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (!found && cum + c[q] >= rem) {
+                    const uint32_t d = kTopkBins - 1 - 4 * threadIdx.x - q;
+                    s_prefix = d << lo1;
+                    s_rem = rem - cum;
+                    s_shift = lo1;
+                    s_done = (lo1 == 0) || (cum + c[q] == rem);
+                    found = true;
+                }
+                cum += c[q];
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        rem = s_rem;
+        shift = s_shift;
+        done = s_done;
+    }
+    // the keys of the threshold bin go to a list; 8-bit passes run over it
+    int m = 0;
+    if (!done) {
+        int nc = 0;
+#pragma unroll
+        for (int e = 0; e < kTopkSmallPer; ++e) nc += (((vm >> e) & 1u) && (off[e] >> shift) == (prefix >> shift)) ? 1 : 0;
+        int tot2;
+        int pos = block_excl_scan(nc, scratch, tot2);
+        m = tot2;
+        if (m <= kTopkList) {
+#pragma unroll
+            for (int e = 0; e < kTopkSmallPer; ++e)
+                if (((vm >> e) & 1u) && (off[e] >> shift) == (prefix >> shift)) list[pos++] = off[e];
+        }
+        __syncthreads();
+    }
+    const bool use_list = m <= kTopkList;
+    while (!done) {
+        const int lo = shift > 8 ? shift - 8 : 0;
+        if (use_list) {
+            for (int i = threadIdx.x; i < m; i += kTopkThreads) {
+                const uint32_t o = list[i];
+                if (shift >= 32 || (o >> shift) == (prefix >> shift)) atomicAdd(&wh[0][(o >> lo) & 255u], 1);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kTopkSmallPer; ++e) {
+                const bool cand = ((vm >> e) & 1u) && (shift >= 32 || (off[e] >> shift) == (prefix >> shift));
+                if (cand) atomicAdd(&wh[warp][(off[e] >> lo) & 255u], 1);
+            }
+        }
+        __syncthreads();
+        // digit 255 - t for t < 256: the count over all warps, then a scan from the top
+        int cnt = 0;
+        if (threadIdx.x < 256) {
+            if (use_list) {
+                cnt = wh[0][255 - threadIdx.x];
+            } else {
+#pragma unroll
+                for (int w = 0; w < NW; ++w) cnt += wh[w][255 - threadIdx.x];
+            }
+        }
+        int x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31 && warp < 8) scratch[warp] = x;
+        __syncthreads();
+        // every histogram read is done: clear for the next pass
+#pragma unroll
+        for (int q = 0; q < kClear; ++q) (&wh[0][0])[threadIdx.x * kClear + q] = 0;
+        if (threadIdx.x < 256) {
+            int before = x - cnt;
+            for (int w = 0; w < warp; ++w) before += scratch[w];
+            if (before < rem && rem <= before + cnt) {
+                s_prefix = prefix | (static_cast<uint32_t>(255 - threadIdx.x) << lo);
+                s_rem = rem - before;
+                s_shift = lo;
+                s_done = (lo == 0) || (before + cnt == rem);
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        rem = s_rem;
+        shift = s_shift;
+        done = s_done;
+    }
+    const int lo = shift;
+    const uint32_t thr = prefix >> lo;     // digit prefix of the threshold bin
+    const int take_eq = rem;               // keys of that bin to take, lowest slot first
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int e = 0; e < kTopkSmallPer; ++e) {
+        if ((vm >> e) & 1u) {
+            const uint32_t d = off[e] >> lo;
+            gt += d > thr;
+            eq += d == thr;
+        }
+    }
+    int tot;
+    const int gt_before = block_excl_scan(gt, scratch, tot);
+    const int eq_before = block_excl_scan(eq, scratch, tot);
+    int g = gt_before, e2 = eq_before;
+#pragma unroll
+    for (int e = 0; e < kTopkSmallPer; ++e) {
+        if ((vm >> e) & 1u) {
+            const uint32_t d = off[e] >> lo;
+            if (d > thr) {
+                orow[g + min(e2, take_eq)] = i0 + e;
+                ++g;
+            } else if (d == thr) {
+                if (e2 < take_eq) orow[g + e2] = i0 + e;
+                ++e2;
+            }
+        }
+    }
+    if (threadIdx.x == 0) out_len[b] = k;
+}
+
 }  // namespace dsv4
 
 using namespace dsv4;
@@ -441,6 +708,9 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         static bool tc_attr = false;
         if (!tc_attr) {
             cudaFuncSetAttribute(indexer_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem);
+            // the whole unified L1 as shared memory: three CTAs per SM
+            cudaFuncSetAttribute(indexer_logits_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
             tc_attr = true;
         }
         dim3 grid(plan->idx_ctas_per_seq, B);
@@ -449,6 +719,24 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         if (e != cudaSuccess) return DSV4_ERR_CUDA;
     }
     cudaError_t e;
+    if (plan->max_slots <= kTopkSmallMax) {
+        // programmatic dependent launch: the top-k CTAs may be scheduled while the
+        // logits kernel drains; they wait (griddepcontrol.wait) before reading it
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(B, 1, 1);
+        cfg.blockDim = dim3(kTopkThreads, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = plan->idx_ctas_per_seq > 0 ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, topk_small_kernel, static_cast<const float*>(logits), plan->logits_stride,
+                               plan->max_slots, a->ctx_len_dev, plan->topk, a->out_idx_dev, a->out_stride,
+                               a->out_len_dev);
+        return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    }
     const int smem_keys = plan->max_slots <= kTopkSmemKeys ? plan->max_slots : 0;
     const size_t smem = static_cast<size_t>(smem_keys) * 4;
     static bool attr_set = false;
