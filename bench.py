@@ -81,7 +81,7 @@ def algorithmic_bytes(w, ctx):
     indexer = B * (n_c * 132 + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
     mla = B * (k * 648 + 128 * 1152 + k * 4 + 4 + H * 576 * 2 + H * 512 * 2 + H * 4
                + (k + 2) * 4)
-    return dict(compress_main=comp_main, compress_idx=comp_idx, indexer=indexer, mla=mla,
+    return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla,
                 total=comp_main + comp_idx + indexer + mla)
 
 
@@ -234,19 +234,20 @@ class GpuBench:
         self.topk_len = torch.empty((Bsz,), dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.info = self.plan.info()
-        self.launches_per_step = 2 + self.info["launches_indexer"] + self.info["launches_mla"]
+        self.launches_per_step = 1 + self.info["launches_indexer"] + self.info["launches_mla"]
 
-    # one layer-step: the four library calls
+    # one layer-step: the three library calls (both compressor streams in one launch)
     def stage_calls(self, r, j):
         Bd, L = self.Bd, self.layers[r]
         Bsz = self.w["batch"]
         return [
-            lambda: Bd.compress_insert(Bd.CACHE_MLA, 4, L.kv_main[j], self.pos[j], L.seqs, L.ape_main,
-                                       L.rms_main, 1e-6, self.cos_sin, L.state_main, L.comp, L.comp_bt, Bsz,
-                                       True, self.status),
-            lambda: Bd.compress_insert(Bd.CACHE_IDX, 4, L.kv_idx[j], self.pos[j], L.seqs, L.ape_idx,
-                                       L.rms_idx, 1e-6, self.cos_sin, L.state_idx, L.idx, L.idx_bt, Bsz,
-                                       True, self.status),
+            lambda: Bd.compress_insert_pair(
+                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=L.kv_main[j], positions=self.pos[j], seqs=L.seqs,
+                     ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=self.cos_sin,
+                     state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=self.status),
+                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=L.kv_idx[j], positions=self.pos[j], seqs=L.seqs,
+                     ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=self.cos_sin,
+                     state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=self.status)),
             lambda: Bd.indexer_topk(self.plan, L.qi[j], L.wts[j], L.idx, L.idx_bt, self.ctx[j], self.topk_idx,
                                     self.topk_len, self.ws, self.status),
             lambda: Bd.sparse_mla_decode(self.plan, L.q[j], L.swa, L.swa_bt, self.ctx[j], L.out, self.ws,
@@ -323,10 +324,13 @@ def run_e2e(bench, steps, warmup):
             d_w.copy_(hin["wts"], non_blocking=True)
             d_pos.copy_(hin["pos"], non_blocking=True)
             d_ctx.copy_(hin["ctx"], non_blocking=True)
-            Bd.compress_insert(Bd.CACHE_MLA, 4, d_kv_main, d_pos, L.seqs, L.ape_main, L.rms_main, 1e-6,
-                               bench.cos_sin, L.state_main, L.comp, L.comp_bt, Bsz, True, bench.status)
-            Bd.compress_insert(Bd.CACHE_IDX, 4, d_kv_idx, d_pos, L.seqs, L.ape_idx, L.rms_idx, 1e-6,
-                               bench.cos_sin, L.state_idx, L.idx, L.idx_bt, Bsz, True, bench.status)
+            Bd.compress_insert_pair(
+                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=d_kv_main, positions=d_pos, seqs=L.seqs,
+                     ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=bench.cos_sin,
+                     state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=bench.status),
+                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=d_kv_idx, positions=d_pos, seqs=L.seqs,
+                     ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=bench.cos_sin,
+                     state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=bench.status))
             Bd.indexer_topk(bench.plan, d_qi, d_w, L.idx, L.idx_bt, d_ctx, bench.topk_idx, bench.topk_len,
                             bench.ws, bench.status)
             Bd.sparse_mla_decode(bench.plan, d_q, L.swa, L.swa_bt, d_ctx, L.out, bench.ws, comp_cache=L.comp,
@@ -355,39 +359,27 @@ def run_e2e(bench, steps, warmup):
 
 
 def stage_times(bench, n):
-    """Average device time of each stage over n live steps (CUDA events inside a
-    captured replay of the same workload)."""
-    names = ["compress_main", "compress_idx", "indexer_topk", "sparse_mla"]
-    try:
-        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)] for _ in range(n)]
-        g = bench.capture(n, ev)
-        g.replay()
+    """Average device time of each stage: the stage's library call alone, n
+    launches over the rotated layer instances in one captured graph, timed
+    with CUDA events around the replay (inside the full step, programmatic
+    dependent launch overlaps the stages, so their sum exceeds a step)."""
+    names = ["compress", "indexer_topk", "sparse_mla"]
+    out = {}
+    for s, nm in enumerate(names):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for r, j in bench.step_order(n):
+                bench.stage_calls(r, j)[s]()
+        gr.replay()
         torch.cuda.synchronize()
-        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gr.replay()
+        b.record()
         torch.cuda.synchronize()
-        out = {}
-        for s, nm in enumerate(names):
-            out[nm] = sum(ev[i][s].elapsed_time(ev[i][s + 1]) for i in range(n)) / n
-        out["method"] = "events inside the captured step sequence"
-        return out
-    except TypeError:
-        # no external graph events in this torch: time each stage alone in a graph
-        out = {}
-        for s, nm in enumerate(names):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr):
-                for r, j in bench.step_order(n):
-                    bench.stage_calls(r, j)[s]()
-            gr.replay()
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            gr.replay()
-            b.record()
-            torch.cuda.synchronize()
-            out[nm] = a.elapsed_time(b) / n
-        out["method"] = "each stage alone in a captured graph"
-        return out
+        out[nm] = a.elapsed_time(b) / n
+    out["method"] = "each stage alone, n launches over the rotated layers in one captured graph"
+    return out
 
 
 def load_peaks():
@@ -581,15 +573,13 @@ def main():
     B = w["batch"]
     value = world * B * K / (ms / 1e3)
     peak, peak_kind = load_peaks()
-    # roofline of the stage with the largest time share
-    stage_bytes = {"compress_main": ab["compress_main"], "compress_idx": ab["compress_idx"],
-                   "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
-    dom = max(stage_bytes, key=lambda s: stages[s])
+    # roofline of the dominant kernel: the sparse MLA decode kernel, the one
+    # single-kernel stage with the largest time (the indexer stage is two
+    # kernels, the logits kernel and the top-k kernel)
+    stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
+    dom = "sparse_mla"
     achieved = stage_bytes[dom] / (stages[dom] / 1e3) / 1e9
-    srcs = {"indexer_topk": ["deepseek_v4_compressed_gb300/csrc/indexer.cu"],
-            "sparse_mla": ["deepseek_v4_compressed_gb300/csrc/mla.cu"],
-            "compress_main": ["deepseek_v4_compressed_gb300/csrc/compress.cu"],
-            "compress_idx": ["deepseek_v4_compressed_gb300/csrc/compress.cu"]}[dom]
+    srcs = ["deepseek_v4_compressed_gb300/csrc/mla.cu"]
     rec = TRAFFIC_RECORD.get(dom)
     traffic = rec["bytes_per_launch"] if rec and rec["src_sha"] == src_digest(srcs) else None
     line = {
@@ -603,7 +593,7 @@ def main():
                          "visits of one layer)" % (bench.R, bench.R * ab["total"] / 1e6),
                    "timing": "CUDA graph replay of the K steps, CUDA events on the launch stream",
                    "parallelism": "replicas x%d" % world},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": "mla_decode_tc (dsv4_sparse_mla_decode)", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
                      "algorithmic_bytes_per_launch": stage_bytes[dom]},

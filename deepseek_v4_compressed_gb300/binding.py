@@ -28,7 +28,7 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_plan_create", "dsv4_plan_destroy", "dsv4_plan_workspace_bytes",
             "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
             "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
-            "dsv4_selftest_key_dequant"]
+            "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair"]
 
 
 class Dsv4Error(RuntimeError):
@@ -137,6 +137,8 @@ def lib():
     L.dsv4_sparse_mla_decode.argtypes = [vp, ctypes.POINTER(MlaArgs), vp, ctypes.c_size_t, vp]
     L.dsv4_selftest_bounded_wait.restype = st
     L.dsv4_selftest_bounded_wait.argtypes = [vp, ctypes.c_int, vp]
+    L.dsv4_compress_insert_pair.restype = st
+    L.dsv4_compress_insert_pair.argtypes = [ctypes.POINTER(CompressArgs), ctypes.POINTER(CompressArgs), vp]
     L.dsv4_selftest_key_dequant.restype = st
     L.dsv4_selftest_key_dequant.argtypes = [vp, vp]
     _lib = L
@@ -263,6 +265,27 @@ def compress_insert(kind, ratio, kv_score, positions, seqs, ape, rms_weight, rms
                      int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
                      _ptr(block_table), int(block_table.shape[1]), _ptr(status))
     _check(lib().dsv4_compress_insert(ctypes.byref(a), _stream(stream)), "compress_insert")
+
+
+def _compress_args(kind, ratio, kv_score, positions, seqs, ape, rms_weight, rms_eps, cos_sin, state, cache,
+                   block_table, num_seqs, one_token_per_seq, status):
+    return CompressArgs(int(kind), int(ratio), int(kv_score.shape[0]), int(num_seqs),
+                        int(bool(one_token_per_seq)), _ptr(kv_score), int(kv_score.stride(0)),
+                        _ptr(positions), _ptr(seqs), _ptr(ape), _ptr(rms_weight), float(rms_eps),
+                        _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(state), _ptr(cache),
+                        int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                        _ptr(block_table), int(block_table.shape[1]), _ptr(status))
+
+
+def compress_insert_pair(main, idx, stream=None):
+    """Both compressor streams of a layer in one launch (decode: one token per
+    sequence).  main / idx: dicts with the compress_insert arguments (kind,
+    ratio, kv_score, positions, seqs, ape, rms_weight, rms_eps, cos_sin,
+    state, cache, block_table, num_seqs, status); see dsv4_compress_insert_pair."""
+    am = _compress_args(one_token_per_seq=True, **main)
+    ai = _compress_args(one_token_per_seq=True, **idx)
+    _check(lib().dsv4_compress_insert_pair(ctypes.byref(am), ctypes.byref(ai), _stream(stream)),
+           "compress_insert_pair")
 
 
 def cache_insert_rows(kind, rows, seqs, slots, cache, block_table, status=None, stream=None):

@@ -126,7 +126,7 @@ __device__ __forceinline__ void token_values(const CompressParams& P, int t, int
 // window rows inside the call come from the inputs and the ring is written
 // by state_write_kernel afterwards.
 template <int D, int RATIO, bool IDX, bool FUSED>
-__global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
+__device__ __forceinline__ void compress_token(const CompressParams& P, const int t)
 {
     constexpr int COFF = (RATIO == 4) ? 2 : 1;
     constexpr int W = COFF * RATIO;
@@ -136,7 +136,6 @@ __global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
     __shared__ double red_d[NT / 32];
     __shared__ float red_f[2];
 
-    const int t = blockIdx.x;
     const int c0 = 2 * threadIdx.x;
     const int seq = P.seqs[t];
     const int p = P.positions[t];
@@ -245,6 +244,29 @@ __global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
 
 // Multi-token calls: write the ring rows of the last W tokens of every
 // sequence (earlier tokens of the call are never read again).
+// A dependent kernel launched behind this one (programmatic dependent
+// launch) may be scheduled at once; it waits for this grid before reading
+// what it writes.
+template <int D, int RATIO, bool IDX, bool FUSED>
+__global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    compress_token<D, RATIO, IDX, FUSED>(P, blockIdx.x);
+}
+
+// The main (d = 576) and indexer (d = 128) streams of a layer in one launch,
+// one token per sequence: blocks [0, main tokens) take the main entries,
+// the rest the indexer entries with their first 64 threads.
+template <int RATIO>
+__global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
+        compress_token<kHead, RATIO, false, true>(Pm, blockIdx.x);
+    else if (threadIdx.x < kIdx / 2)
+        compress_token<kIdx, 4, true, true>(Pi, blockIdx.x - Pm.num_tokens);
+}
+
 template <int D, int RATIO>
 __global__ void __launch_bounds__(D / 2) state_write_kernel(CompressParams P)
 {
@@ -310,7 +332,8 @@ static cudaError_t launch_compress(const CompressParams& P, bool fused, cudaStre
 
 using namespace dsv4;
 
-extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_stream_t stream)
+// Validate a call's arguments and fill the kernel parameters.
+static dsv4_status compress_params(const dsv4_compress_args* a, CompressParams& P)
 {
     if (a == nullptr) return DSV4_ERR_INVALID;
     if (a->num_tokens < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
@@ -318,17 +341,16 @@ extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_st
     if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
     if (a->ratio != 4 && a->ratio != 128) return DSV4_ERR_UNSUPPORTED;
     if (a->kind == DSV4_CACHE_IDX && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
-    if (a->num_tokens == 0) return DSV4_OK;
-    if (!a->kv_score_dev || !a->positions_dev || !a->seq_dev || !a->ape_dev || !a->rms_weight_dev ||
-        !a->cos_sin_dev || !a->state_dev || !a->cache_dev || !a->block_table_dev)
+    if (a->num_tokens > 0 &&
+        (!a->kv_score_dev || !a->positions_dev || !a->seq_dev || !a->ape_dev || !a->rms_weight_dev ||
+         !a->cos_sin_dev || !a->state_dev || !a->cache_dev || !a->block_table_dev))
         return DSV4_ERR_INVALID;
     const int d = (a->kind == DSV4_CACHE_MLA) ? kHead : kIdx;
     const int coff = (a->ratio == 4) ? 2 : 1;
-    if (a->kv_score_stride < 2LL * coff * d || (a->kv_score_stride & 1)) return DSV4_ERR_SHAPE;
+    if (a->num_tokens > 0 && (a->kv_score_stride < 2LL * coff * d || (a->kv_score_stride & 1)))
+        return DSV4_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(a->kv_score_dev) & 3) || (reinterpret_cast<uintptr_t>(a->cache_dev) & 15))
         return DSV4_ERR_SHAPE;
-
-    CompressParams P;
     P.kv_score = static_cast<const uint16_t*>(a->kv_score_dev);
     P.kv_stride = a->kv_score_stride;
     P.positions = a->positions_dev;
@@ -346,6 +368,15 @@ extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_st
     P.num_tokens = a->num_tokens;
     P.num_seqs = a->num_seqs;
     P.status = a->status_dev;
+    return DSV4_OK;
+}
+
+extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_stream_t stream)
+{
+    CompressParams P;
+    const dsv4_status s = compress_params(a, P);
+    if (s != DSV4_OK) return s;
+    if (a->num_tokens == 0) return DSV4_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool fused = a->one_token_per_seq != 0;
     cudaError_t e;
@@ -356,6 +387,26 @@ extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_st
     else
         e = launch_compress<kHead, 128, false>(P, fused, st);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_args,
+                                                 const dsv4_compress_args* idx_args, dsv4_stream_t stream)
+{
+    CompressParams Pm, Pi;
+    dsv4_status s = compress_params(main_args, Pm);
+    if (s != DSV4_OK) return s;
+    s = compress_params(idx_args, Pi);
+    if (s != DSV4_OK) return s;
+    if (main_args->kind != DSV4_CACHE_MLA || idx_args->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (!main_args->one_token_per_seq || !idx_args->one_token_per_seq) return DSV4_ERR_INVALID;
+    const int n = Pm.num_tokens + Pi.num_tokens;
+    if (n == 0) return DSV4_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (main_args->ratio == 4)
+        compress_pair_kernel<4><<<n, kHead / 2, 0, st>>>(Pm, Pi);
+    else
+        compress_pair_kernel<128><<<n, kHead / 2, 0, st>>>(Pm, Pi);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
 extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, dsv4_stream_t stream)

@@ -119,6 +119,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
             tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
         }
+        // the cache may have been written by the kernel before this one, which
+        // this kernel may overlap (programmatic dependent launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         int pgl = -1;     // lane l: page id of page l of the current group of 16 tiles
         for (int i = 0; i < n_my; ++i) {
             if ((i & 15) == 0) {
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
     int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len, int smem_keys)
 {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint32_t skeys[];
     __shared__ int hist[kTopkBins];
     __shared__ int scratch[33];
@@ -450,7 +454,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     __shared__ uint32_t s_max[NW], s_mins[NW], s_prefix;
     __shared__ int s_shift, s_rem, s_done;
 
-    // the logits were produced by the previous kernel of this call
+    // the attention kernel that follows may be scheduled now (it waits for
+    // this grid before reading the selection); the logits were produced by
+    // the previous kernel of this call
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -713,9 +720,17 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
                                  cudaSharedmemCarveoutMaxShared);
             tc_attr = true;
         }
-        dim3 grid(plan->idx_ctas_per_seq, B);
-        indexer_logits_tc<<<grid, kIdxThreads, kIdxSmem, st>>>(tm_cache, tm_q, P);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(plan->idx_ctas_per_seq, B, 1);
+        cfg.blockDim = dim3(kIdxThreads, 1, 1);
+        cfg.dynamicSmemBytes = kIdxSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, indexer_logits_tc, tm_cache, tm_q, P);
         if (e != cudaSuccess) return DSV4_ERR_CUDA;
     }
     cudaError_t e;

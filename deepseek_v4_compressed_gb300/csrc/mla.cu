@@ -204,20 +204,29 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int h0 = g_head * 64;
     const int nh = min(64, P.H - h0);
     const int p = P.ctx_len[b] - 1;
-    const int n_comp = P.idx_len ? min(max(P.idx_len[b], 0), T.topk) : 0;
     const int t0 = max(0, p - P.window + 1);
     const int C = T.cluster;
     const int pg0 = t0 >> 6;                              // first window page (64 tokens)
     const int n_swa_t = p >= 0 ? (p >> 6) - pg0 + 1 : 0;
-    const int n_comp_t = (n_comp + kTcKeys - 1) / kTcKeys;
-    const int n_glob = n_swa_t + n_comp_t;
-    const int n_swa_mine = n_swa_t > rank ? (n_swa_t - rank + C - 1) / C : 0;
-    int n_tiles = n_glob > rank ? (n_glob - rank + C - 1) / C : 0;
-    if (n_tiles - n_swa_mine > kTcMaxCompTiles || n_tiles > kTcMaxTiles) {
-        if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
-        n_tiles = min(n_swa_mine + kTcMaxCompTiles, kTcMaxTiles);
-    }
-    const int n_comp_mine = n_tiles - n_swa_mine;
+    const int n_swa_mine = min(n_swa_t > rank ? (n_swa_t - rank + C - 1) / C : 0, kTcMaxTiles);
+    // The selected slots come from the kernel launched before this one, which
+    // this kernel may overlap (programmatic dependent launch): n_comp and the
+    // tile counts are read after griddepcontrol.wait, by every thread once,
+    // when it first needs them.  The window tiles need none of it.
+    int n_comp = 0, n_tiles = n_swa_mine, n_comp_mine = 0;
+    bool resolved = false;
+    auto resolve = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        n_comp = P.idx_len ? min(max(P.idx_len[b], 0), T.topk) : 0;
+        const int n_glob = n_swa_t + (n_comp + kTcKeys - 1) / kTcKeys;
+        n_tiles = n_glob > rank ? (n_glob - rank + C - 1) / C : 0;
+        if (n_tiles - n_swa_mine > kTcMaxCompTiles || n_tiles > kTcMaxTiles) {
+            if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+            n_tiles = min(n_swa_mine + kTcMaxCompTiles, kTcMaxTiles);
+        }
+        n_comp_mine = n_tiles - n_swa_mine;
+        resolved = true;
+    };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float scale_log2 = P.scale * 1.4426950408889634f;
 
@@ -248,7 +257,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (n_tiles > 0) {
+    {
         if (warp == kTcMmaWarp) {
             // ------------------------------------------------------- QK issue
             // QK(t) needs tile t loaded and S buffer t%2 read out by the
@@ -263,7 +272,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 constexpr uint32_t id_qk = tc::idesc(64, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
                 bool ok = tc::mbar_wait(tc::smem_u32(q_full), 0, abort_flag, P.status);
                 const uint64_t qd = tc::desc_kmajor_sw128(tc::smem_u32(q_s));
-                for (int t = 0; ok && t < n_tiles; ++t) {
+                for (int t = 0; ok; ++t) {
+                    if (t == n_swa_mine) resolve();
+                    if (t >= n_tiles) break;
                     ok = tc::mbar_wait(tc::smem_u32(&kv_full[t & 1]), (t >> 1) & 1, abort_flag, P.status);
                     if (ok && t >= 2)
                         ok = tc::mbar_wait(tc::smem_u32(&p_full[t & 1]), ((t - 2) >> 1) & 1, abort_flag, P.status);
@@ -285,7 +296,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // O^T += V^T P^T once P(u) is written (in the RoPE chunk of tile u).
             if (lane == 0) {
                 constexpr uint32_t id_pv = tc::idesc(128, 64, tc::kFmtBF16, tc::kFmtBF16, true, false);
-                for (int u = 0; u < n_tiles; ++u) {
+                for (int u = 0;; ++u) {
+                    if (u == n_swa_mine) resolve();
+                    if (u >= n_tiles) break;
                     if (!tc::mbar_wait(tc::smem_u32(&p_full[u & 1]), (u >> 1) & 1, abort_flag, P.status)) break;
                     tc::tc_fence_after();
                     const uint32_t kb = tc::smem_u32(k_s + (u & 1) * kTcKBytes);
@@ -309,8 +322,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // compressed tiles 4q + l / 8 (q = 0..3) as page * 64 + row (-1:
             // padding or unreadable).  Index loads, then block-table loads, each
             // issued together.
-            int ent[4];
-            {
+            int ent[4] = {-1, -1, -1, -1};
+            auto build_table = [&]() {
                 int slot[4], pg[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -338,7 +351,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         else flag(P.status, DSV4_DEV_BAD_PAGE);
                     }
                 }
-            }
+            };
             // raw data of one compressed tile, loaded one tile ahead of its use:
             // nope unit `lane` (16 codes) of rows pw + 8k with its scale byte,
             // rope unit lane % 8 of rows pw + 8 (lane / 8) and pw + 8 (lane / 8 + 4)
@@ -393,43 +406,54 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     *reinterpret_cast<uint4*>(kp + 8 * kTcKChunk + r * 128 + (((lane & 7) ^ pw) << 4)) = rr[hh];
                 }
             };
-            // the first compressed tile's rows are requested once the window pages
-            // are on their way (their table loads overlap the window tiles)
-            if (n_swa_mine == 0 && n_comp_mine > 0) fetch(0);
-            for (int i = 0; i < n_tiles; ++i) {
+            // window pages first: they need nothing from the kernel before
+            int i = 0;
+            bool ok = true;
+            for (; i < n_swa_mine; ++i) {
+                const int kst = i & 1;
+                uint8_t* kp = k_s + kst * kTcKBytes;
+                if (i >= kTcStages &&
+                    !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+                // nine TMA tensor loads (64 dims x 64 tokens) land the page swizzled;
+                // an unreadable page reads zeros (negative coordinate)
+                if (pw == 0) {
+                    if (lane == 0) {
+                        const int lp = pg0 + rank + i * C;
+                        int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + lp] : -1;
+                        if (pg < 0 || pg >= P.swa_pages) {
+                            flag(P.status, DSV4_DEV_BAD_PAGE);
+                            pg = -1;
+                        }
+                        const uint32_t bar = tc::smem_u32(&kv_full[kst]);
+                        tc::mbar_arrive_expect_tx(bar, kTcKBytes);
+                        for (int c = 0; c < 9; ++c)
+                            tc::tma_load_3d(tc::smem_u32(kp + c * kTcKChunk), &tm_swa, bar, c * 64, 0, pg);
+                    }
+                } else if (lane == 0) {
+                    tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
+                }
+            }
+            // then the selected slots: row table, first rows, compressed tiles
+            resolve();
+            if (ok) {
+                build_table();
+                if (n_comp_mine > 0) fetch(0);
+            }
+            for (; ok && i < n_tiles; ++i) {
                 const int kst = i & 1;
                 uint8_t* kp = k_s + kst * kTcKBytes;
                 if (i >= kTcStages &&
                     !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status))
                     break;
-                if (i < n_swa_mine) {
-                    // window page: nine TMA tensor loads (64 dims x 64 tokens) land it
-                    // swizzled; an unreadable page reads zeros (negative coordinate)
-                    if (pw == 0) {
-                        if (lane == 0) {
-                            const int lp = pg0 + rank + i * C;
-                            int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + lp] : -1;
-                            if (pg < 0 || pg >= P.swa_pages) {
-                                flag(P.status, DSV4_DEV_BAD_PAGE);
-                                pg = -1;
-                            }
-                            const uint32_t bar = tc::smem_u32(&kv_full[kst]);
-                            tc::mbar_arrive_expect_tx(bar, kTcKBytes);
-                            for (int c = 0; c < 9; ++c)
-                                tc::tma_load_3d(tc::smem_u32(kp + c * kTcKChunk), &tm_swa, bar, c * 64, 0, pg);
-                        }
-                    } else if (lane == 0) {
-                        tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
-                    }
-                    if (i == n_swa_mine - 1 && n_comp_mine > 0) fetch(0);
-                } else {
-                    const int jc = i - n_swa_mine;
-                    convert(kp);
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
-                    if (jc + 1 < n_comp_mine) fetch(jc + 1);
-                }
+                const int jc = i - n_swa_mine;
+                convert(kp);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
+                if (jc + 1 < n_comp_mine) fetch(jc + 1);
             }
         } else {
             // ------------------------------------------- softmax + O correction
@@ -439,7 +463,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int h = warp * 16 + (lane & 15);
             const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
             float m = -INFINITY, l = 0.f;
-            for (int t = 0; t < n_tiles; ++t) {
+            for (int t = 0;; ++t) {
+                if (t == n_swa_mine) resolve();
+                if (t >= n_tiles) break;
                 const int sb = t & 1;
                 if (!tc::mbar_wait(tc::smem_u32(&s_full[sb]), (t >> 1) & 1, abort_flag, P.status)) break;
                 tc::tc_fence_after();
@@ -522,10 +548,11 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 sm_m[h] = m;
                 sm_l[h] = l;
             }
-            tc::mbar_wait(tc::smem_u32(&pv_done[n_tiles - 1]), 0, abort_flag, P.status);
+            if (n_tiles > 0) tc::mbar_wait(tc::smem_u32(&pv_done[n_tiles - 1]), 0, abort_flag, P.status);
             tc::tc_fence_before();
         }
     }
+    if (!resolved) resolve();                                // lanes that ran no loop
 
     // ------------------------------------------------------------- epilogue
     // 1. every CTA is past its main loop (its shared memory is free to receive)
@@ -748,13 +775,18 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = kTcSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = T.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: behind a kernel that allows it (the
+    // top-k), the window tiles run while it finishes; the selected slots are
+    // read after griddepcontrol.wait
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_tc, tm_q, tm_swa, T);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

@@ -245,6 +245,15 @@ typedef struct dsv4_compress_args {
 
 dsv4_status dsv4_compress_insert(const dsv4_compress_args* args, dsv4_stream_t stream);
 
+/* Both compressor streams of a layer in one launch, for decode steps:
+ * main_args (DSV4_CACHE_MLA, ratio 4 or 128) and idx_args (DSV4_CACHE_IDX,
+ * ratio 4), each with one_token_per_seq set.  Same effect, arguments and
+ * errors as the two dsv4_compress_insert calls (DSV4_ERR_INVALID also for a
+ * wrong kind or a call without one_token_per_seq); the two streams touch
+ * disjoint state and caches, so their entries are computed side by side. */
+dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_args, const dsv4_compress_args* idx_args,
+                                      dsv4_stream_t stream);
+
 /* Quantise already-final rows into the cache format and insert them: the
  * quantise-and-insert tail of dsv4_compress_insert on its own (no pooling,
  * normalisation or rotation), for filling caches with given entries.

@@ -82,6 +82,15 @@ def test_entry_points_reject_null_arguments_without_gpu():
     a.kind, a.ratio = 1, 128
     assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_UNSUPPORTED
     assert lib.dsv4_compress_insert(None, None) == B.ERR_INVALID
+    assert lib.dsv4_compress_insert_pair(None, None, None) == B.ERR_INVALID
+    m = B.CompressArgs()
+    m.kind, m.ratio, m.num_tokens, m.num_seqs, m.one_token_per_seq = 0, 4, 0, 1, 1
+    i = B.CompressArgs()
+    i.kind, i.ratio, i.num_tokens, i.num_seqs, i.one_token_per_seq = 1, 4, 0, 1, 1
+    assert lib.dsv4_compress_insert_pair(ctypes.byref(m), ctypes.byref(i), None) == B.OK      # nothing to do
+    assert lib.dsv4_compress_insert_pair(ctypes.byref(i), ctypes.byref(m), None) == B.ERR_INVALID   # kinds swapped
+    m.one_token_per_seq = 0
+    assert lib.dsv4_compress_insert_pair(ctypes.byref(m), ctypes.byref(i), None) == B.ERR_INVALID
     p = B.Plan(B.C4A, 8, 1, 32, 512, idx_heads=4)
     ia = B.IndexerArgs()
     assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), None, 0, None) in (B.ERR_SHAPE, B.ERR_INVALID)

@@ -164,3 +164,51 @@ def test_insert_rows_bit_exact(kind):
         sel = seqs == b
         got = entries_from_pages(kind, host, bt[b], int(sel.sum()))
         assert_bytes_equal(got, (wd[sel], ws[sel]), "insert rows seq %d" % b)
+
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_pair_launch_bit_exact(ratio):
+    """dsv4_compress_insert_pair (main + indexer streams in one launch, one token
+    per sequence per step) writes the same bytes as the oracle for both caches."""
+    lens = [300, 129, 517] if ratio == 4 else [300, 256, 384]
+    nseq = len(lens)
+    cs = oracle.rope_table(max(lens), 64)
+    t_cs = dev(cs)
+    kinds = {"main": (B.CACHE_MLA, ratio, 576), "idx": (B.CACHE_IDX, 4, 128)}
+    setup = {}
+    for name, (kind, r, d) in kinds.items():
+        coff = 2 if r == 4 else 1
+        _, ape, w = make_stream(kind, r, 1, seed=900 + kind)
+        streams = [make_stream(kind, r, L, seed=910 + 7 * kind + i)[0] for i, L in enumerate(lens)]
+        n_ent = max(L // r for L in lens)
+        pps = max(1, (n_ent + 63) // 64)
+        bt = synth.page_tables(synth.rng(40 + kind), nseq, pps, extra_pages=1)
+        page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
+        setup[name] = dict(kind=kind, ratio=r, ape=ape, w=w, streams=streams, bt=bt,
+                           t_ks=[bits_tensor(s) for s in streams],
+                           cache=torch.zeros((nseq * pps + 1) * page_b, dtype=torch.uint8, device="cuda"),
+                           state=torch.zeros((nseq, coff * r, 2 * coff * d), dtype=torch.float32, device="cuda"),
+                           t_ape=dev(ape), t_w=dev(w), t_bt=dev(bt))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for step in range(max(lens)):
+        live = [b for b in range(nseq) if step < lens[b]]
+        pos = dev(np.full(len(live), step, np.int32))
+        seqs = dev(np.array(live, np.int32))
+        args = {}
+        for name, st in setup.items():
+            kv = torch.cat([st["t_ks"][b][step:step + 1] for b in live], 0).contiguous()
+            args[name] = dict(kind=st["kind"], ratio=st["ratio"], kv_score=kv, positions=pos, seqs=seqs,
+                              ape=st["t_ape"], rms_weight=st["t_w"], rms_eps=EPS, cos_sin=t_cs,
+                              state=st["state"], cache=st["cache"], block_table=st["t_bt"], num_seqs=nseq,
+                              status=status)
+        B.compress_insert_pair(args["main"], args["idx"])
+    torch.cuda.synchronize()
+    s, bits = B.read_device_status(status)
+    assert s == B.OK, bits
+    for name, st in setup.items():
+        host = st["cache"].cpu().numpy()
+        for b in range(nseq):
+            n = lens[b] // st["ratio"]
+            got = entries_from_pages(st["kind"], host, st["bt"][b], n)
+            want = oracle_entries(st["kind"], st["ratio"], st["streams"][b], st["ape"], st["w"], cs)
+            assert_bytes_equal(got, want, "%s seq %d" % (name, b))
