@@ -18,7 +18,8 @@ namespace dsv4 {
 // D[128 slots x N heads] = K_tile[128 x 128] * Q^T[128 x N] (fp32 in TMEM),
 // then each of 128 epilogue threads turns its slot's row of D into
 // I_s = scale_s * sum_j w_j * max(D_sj, 0).
-//   warp 8: TMA producer (query once, then two page loads per tile, 6-stage ring)
+//   warps 8, 10: TMA producers of the even / odd tiles (query once, then two
+//            page loads per tile, 6-stage ring)
 //   warp 9: MMA issuer (4 MMAs of K=32 per tile, 4 accumulators)
 //   warps 0-3 / 4-7: epilogue of the even / odd tiles (TMEM lane = slot row)
 // One CTA per SM: CTAs of kernels that allocate tensor memory start one
@@ -31,9 +32,9 @@ constexpr int kIdxStages = 6;
 constexpr int kIdxAcc = 4;
 constexpr int kIdxTileBytes = kIdxTileSlots * kIdx;       // 16 KB
 constexpr int kIdxQBytes = 64 * kIdx;                     // query tile, N <= 64 rows
-constexpr int kIdxThreads = 320;
+constexpr int kIdxThreads = 352;
 constexpr int kIdxTmemCols = kIdxAcc * 64;                // 4 accumulators x 64 columns
-constexpr int kIdxScaleBytes = 2 * kPage * 4;                // scale planes of the tile's two pages
+constexpr int kIdxScaleBytes = 16;                           // the tile's two page ids (+ padding)
 constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
                          2048 /* barriers etc */ + 1024 /* align */;
 
@@ -64,7 +65,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     uint8_t* smem = tc::align1024_shared(smem_raw);
     uint8_t* a_tiles = smem;
     uint8_t* q_tile = smem + kIdxStages * kIdxTileBytes;
-    float* scales_s = reinterpret_cast<float*>(q_tile + kIdxQBytes);   // [stage][128 slots]
+    int* stage_pages = reinterpret_cast<int*>(q_tile + kIdxQBytes);    // [stage][2] page ids of the tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(q_tile + kIdxQBytes + kIdxStages * kIdxScaleBytes);
     uint64_t* full = bars;                        // [kIdxStages]
     uint64_t* empty = bars + kIdxStages;          // [kIdxStages]
@@ -90,7 +91,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < kIdxStages; ++i) {
             tc::mbar_init(tc::smem_u32(&full[i]), 1);
-            tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (scales read)
+            tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (page ids read)
         }
         for (int i = 0; i < kIdxAcc; ++i) {
             tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
@@ -112,55 +113,55 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     int issued = 0;   // tiles whose loads were issued (producer only)
     int consumed = 0; // tiles whose stage the MMA released (MMA thread only)
 
-    if (warp == 8) {
-        if (lane == 0) {
+    if (warp == 8 || warp == 10) {
+        const int pgrp = warp == 8 ? 0 : 1;       // this producer's tiles: i = pgrp, pgrp + 2, ...
+        if (lane == 0 && pgrp == 0) {
             tc::prefetch_tensormap(&tm_cache);
             tc::prefetch_tensormap(&tm_q);
             tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
             tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
         }
+        // lane l: page id of page l of the group of 16 tiles starting at tile i,
+        // loaded by the lanes at once
+        auto page_group = [&](int i) {
+            int pg = -1;
+            if (2 * i + lane < 2 * n_my) {
+                const int pi = min(2 * (t_begin + i) + lane, n_pages - 1);
+                pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                if (pg < 0 || pg >= P.num_pages) {
+                    flag(P.status, DSV4_DEV_BAD_PAGE);
+                    pg = -1;
+                }
+            }
+            return pg;
+        };
+        int pgl = page_group(0);
         // the cache may have been written by the kernel before this one, which
         // this kernel may overlap (programmatic dependent launch)
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        int pgl = -1;     // lane l: page id of page l of the current group of 16 tiles
-        for (int i = 0; i < n_my; ++i) {
-            if ((i & 15) == 0) {
-                // the page ids of the next 16 tiles, loaded by the lanes at once
-                const int gp = 2 * (t_begin + i) + lane;
-                pgl = -1;
-                if (2 * i + lane < 2 * n_my) {
-                    const int pi = min(gp, n_pages - 1);
-                    pgl = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
-                    if (pgl < 0 || pgl >= P.num_pages) {
-                        flag(P.status, DSV4_DEV_BAD_PAGE);
-                        pgl = -1;
-                    }
-                }
-            }
-            const int v0 = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15));
-            const int v1 = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15) + 1);
-            bool go = true;
+        for (int i = pgrp; i < n_my; i += 2) {
+            if (i >= 16 && (i & 15) < 2) pgl = page_group(i & ~15);
+            const int v = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15) + (lane & 1));   // this lane's page
+            const int st = i % kIdxStages;
+            const uint32_t fb = tc::smem_u32(&full[st]);
+            int go = 1;
             if (lane == 0) {
-                const int st = i % kIdxStages;
                 const uint32_t ph = (i / kIdxStages) & 1;
-                if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status)) {
-                    go = false;
-                } else {
-                    const int pg[2] = {v0 < 0 ? P.num_pages : v0, v1 < 0 ? P.num_pages : v1};  // unreadable: zeros
-                    const int spg[2] = {v0 < 0 ? 0 : v0, v1 < 0 ? 0 : v1};  // scales from a valid page
-                    const uint32_t dst = tc::smem_u32(a_tiles + st * kIdxTileBytes);
-                    const uint32_t fb = tc::smem_u32(&full[st]);
-                    tc::mbar_arrive_expect_tx(fb, kIdxTileBytes + kIdxScaleBytes);
-                    tc::tma_load_3d(dst, &tm_cache, fb, 0, 0, pg[0]);
-                    tc::tma_load_3d(dst + kIdxTileBytes / 2, &tm_cache, fb, 0, 0, pg[1]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tc::bulk_load(tc::smem_u32(scales_s + st * 128 + h * kPage),
-                                      P.cache + static_cast<long long>(spg[h]) * kIdxPage + kPage * kIdx, kPage * 4, fb);
-                    issued = i + 1;
-                }
+                if (i >= kIdxStages && !tc::mbar_wait(tc::smem_u32(&empty[st]), ph ^ 1, abort_flag, P.status))
+                    go = 0;
             }
-            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            // the tile's page ids go to stage_pages (the epilogue reads the
+            // scales straight from those pages) before the phase is armed
+            if (lane < 2) stage_pages[st * 2 + lane] = v < 0 ? 0 : v;   // scales from a valid page
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_expect_tx(fb, kIdxTileBytes);
+            __syncwarp();
+            // lanes 0-1: the two pages' rows (TMA tensor loads)
+            if (lane < 2)
+                tc::tma_load_3d(tc::smem_u32(a_tiles + st * kIdxTileBytes + lane * (kIdxTileBytes / 2)), &tm_cache, fb,
+                                0, 0, v < 0 ? P.num_pages : v);          // unreadable page: outside the map, zeros
+            if (lane == 0) issued = i + 1;
         }
     } else if (warp == 9) {
         if (lane == 0) {
@@ -194,6 +195,15 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         for (int i = grp; i < n_my; i += 2) {
             const int ab = i % kIdxAcc;
             const uint32_t aph = (i / kIdxAcc) & 1;
+            const int st = i % kIdxStages;
+            // the tile's rows have landed: its page ids are known; this row's
+            // scale comes straight from its page (in flight during the MMA)
+            if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) break;
+            const float scale = *reinterpret_cast<const float*>(
+                P.cache + static_cast<long long>(stage_pages[st * 2 + (row >> 6)]) * kIdxPage + kPage * kIdx +
+                (row & (kPage - 1)) * 4);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
             if (!tc::mbar_wait(tc::smem_u32(&acc_full[ab]), aph, abort_flag, P.status)) break;
             tc::tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + ab * 64;
@@ -224,14 +234,6 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                     for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
                 }
             }
-            // the stage's scales: its full barrier cannot have moved on, since
-            // the stage is only refilled after this group releases it below
-            const int st = i % kIdxStages;
-            float scale = 0.f;
-            if (tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status))
-                scale = scales_s[st * 128 + row];
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
             const int s = (t_begin + i) * kIdxTileSlots + row;
             if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc * scale;
         }
@@ -239,9 +241,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
 
     tc::tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp == 8 && lane == 0) {
+    if (*abort_flag && (warp == 8 || warp == 10) && lane == 0) {
         // let this CTA's own copies land before its shared memory is released
         for (int i = consumed > 0 ? consumed : 0; i < issued; ++i) {
+            if ((i & 1) != (warp == 8 ? 0 : 1)) continue;
             volatile int no_abort = 0;
             tc::mbar_wait(tc::smem_u32(&full[i % kIdxStages]), (i / kIdxStages) & 1, &no_abort, nullptr);
         }
