@@ -434,12 +434,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     if (threadIdx.x == 0) out_len[b] = k;
 }
 
-// Rows of at most 8192 slots: every thread keeps 16 consecutive keys in
-// registers.  An 11-bit digit pass over (key - row minimum) finds the bin of
-// the k-th largest key; that bin's keys go to a list (up to 2048; else the
-// passes stay on the registers with one 256-bin histogram per warp), and
-// 8-bit passes over the list finish the threshold.  The same ordered
-// compaction writes the k slots in ascending order.
+// Rows of at most 8192 slots, one CTA of 16 warps per row: warp w keeps
+// slots 512 w + 32 j + lane (j = 0..15) in registers, so every step but
+// three block-wide exchanges runs on warp votes.  An 11-bit digit pass over
+// (key - row minimum) finds the bin of the k-th largest key; the keys of
+// that bin (usually a handful) are ranked by one warp, or narrowed by 8-bit
+// passes when there are more than 32; the slots above the threshold, and the
+// lowest-slot ones equal to it, are written in ascending order.
 constexpr int kTopkSmallPer = 16;
 constexpr int kTopkSmallMax = kTopkThreads * kTopkSmallPer;   // 8192
 constexpr int kTopkList = 2048;                                 // threshold-bin keys kept in a list
@@ -449,13 +450,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len)
 {
     constexpr int NW = kTopkThreads / 32;
-    constexpr int kClear = (NW * 256) / kTopkThreads;   // histogram words each thread clears
-    __shared__ int wh[NW][256];
     __shared__ int hist1[kTopkBins];
+    __shared__ int hist2[256];
     __shared__ uint32_t list[kTopkList];
     __shared__ int scratch[33];
-    __shared__ uint32_t s_max[NW], s_mins[NW], s_prefix;
-    __shared__ int s_shift, s_rem, s_done;
+    __shared__ uint32_t s_wmin[NW], s_wmax[NW];
+    __shared__ int s_wgt[NW], s_weq[NW];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_shift, s_rem, s_done, s_m;
 
     // the attention kernel that follows may be scheduled now (it waits for
     // this grid before reading the selection); the logits were produced by
@@ -464,26 +466,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i0 = threadIdx.x * kTopkSmallPer;
+    const int base_slot = warp * 512 + lane;             // slot of row j: base_slot + 32 j
     const float* lrow = logits + static_cast<long long>(b) * row_stride;
     // the row is allocated up to max_slots: load it together with the length
     float v[kTopkSmallPer];
 #pragma unroll
-    for (int j = 0; j < kTopkSmallPer / 4; ++j) {
-        const int i = i0 + 4 * j;
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i + 3 < max_slots) {
-            f = *reinterpret_cast<const float4*>(lrow + i);   // row_stride and i are multiples of 4
-        } else {
-            if (i < max_slots) f.x = lrow[i];
-            if (i + 1 < max_slots) f.y = lrow[i + 1];
-            if (i + 2 < max_slots) f.z = lrow[i + 2];
-        }
-        v[4 * j] = f.x;
-        v[4 * j + 1] = f.y;
-        v[4 * j + 2] = f.z;
-        v[4 * j + 3] = f.w;
-    }
+    for (int j = 0; j < kTopkSmallPer; ++j) v[j] = (base_slot + 32 * j < max_slots) ? lrow[base_slot + 32 * j] : 0.f;
     int n = ctx_len[b] / 4;
     n = n < 0 ? 0 : (n > max_slots ? max_slots : n);
     int* orow = out_idx + static_cast<long long>(b) * out_stride;
@@ -493,49 +481,49 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
         return;
     }
     uint32_t off[kTopkSmallPer];
-    uint32_t vm = 0;                                  // bit e: slot i0 + e exists
+    uint32_t vm = 0;                                     // bit j: slot of row j exists
     uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
-    for (int e = 0; e < kTopkSmallPer; ++e) {
-        off[e] = f32_order_key(v[e]);
-        if (i0 + e < n) {
-            vm |= 1u << e;
-            mn = min(mn, off[e]);
-            mx = max(mx, off[e]);
+    for (int j = 0; j < kTopkSmallPer; ++j) {
+        off[j] = f32_order_key(v[j]);
+        if (base_slot + 32 * j < n) {
+            vm |= 1u << j;
+            mn = min(mn, off[j]);
+            mx = max(mx, off[j]);
         }
     }
     mn = __reduce_min_sync(0xffffffffu, mn);
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0) {
-        s_mins[warp] = mn;
-        s_max[warp] = mx;
+        s_wmin[warp] = mn;
+        s_wmax[warp] = mx;
     }
 #pragma unroll
-    for (int q = 0; q < kClear; ++q) (&wh[0][0])[threadIdx.x * kClear + q] = 0;
-#pragma unroll
     for (int q = 0; q < kTopkBins / kTopkThreads; ++q) hist1[threadIdx.x * (kTopkBins / kTopkThreads) + q] = 0;
-    __syncthreads();
+    if (threadIdx.x < 256) hist2[threadIdx.x] = 0;
+    __syncthreads();                                                   // (1)
     uint32_t base = 0xffffffffu, top = 0u;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-        base = min(base, s_mins[w]);
-        top = max(top, s_max[w]);
+        base = min(base, s_wmin[w]);
+        top = max(top, s_wmax[w]);
     }
     const uint32_t range = top - base;
-    int shift = range ? 32 - __clz(range) : 0;        // offsets fit in `shift` bits
+    int shift = range ? 32 - __clz(range) : 0;           // offsets fit in `shift` bits
     uint32_t prefix = 0;
     int rem = k;
     bool done = (range == 0);
 #pragma unroll
-    for (int e = 0; e < kTopkSmallPer; ++e) off[e] = ((vm >> e) & 1u) ? off[e] - base : 0u;
+    for (int j = 0; j < kTopkSmallPer; ++j) off[j] = ((vm >> j) & 1u) ? off[j] - base : 0u;
 
-    // pass 1: 11-bit digits over the whole range, one shared histogram
+    // pass 1: 11-bit digits over the whole range
+    int m = 0;                                           // keys in the threshold bin
     if (!done) {
         const int lo1 = shift > 11 ? shift - 11 : 0;
 #pragma unroll
-        for (int e = 0; e < kTopkSmallPer; ++e)
-            if ((vm >> e) & 1u) atomicAdd(&hist1[off[e] >> lo1], 1);
-        __syncthreads();
+        for (int j = 0; j < kTopkSmallPer; ++j)
+            if ((vm >> j) & 1u) atomicAdd(&hist1[off[j] >> lo1], 1);
+        __syncthreads();                                               // (2)
         int c[4];
         int local = 0;
 #pragma unroll
@@ -544,71 +532,91 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
             local += c[q];
         }
         int tot1;
-        const int before = block_excl_scan(local, scratch, tot1);
+        const int before = block_excl_scan(local, scratch, tot1);     // (3, 4, 5)
         if (before < rem && rem <= before + local) {
             int cum = before;
             bool found = false;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (!found && cum + c[q] >= rem) {
-                    const uint32_t d = kTopkBins - 1 - 4 * threadIdx.x - q;
-                    s_prefix = d << lo1;
+                    s_prefix = static_cast<uint32_t>(kTopkBins - 1 - 4 * threadIdx.x - q) << lo1;
                     s_rem = rem - cum;
                     s_shift = lo1;
                     s_done = (lo1 == 0) || (cum + c[q] == rem);
+                    s_m = c[q];
                     found = true;
                 }
                 cum += c[q];
             }
         }
-        __syncthreads();
+        __syncthreads();                                               // (6)
         prefix = s_prefix;
         rem = s_rem;
         shift = s_shift;
         done = s_done;
+        m = s_m;
     }
-    // the keys of the threshold bin go to a list; 8-bit passes run over it
-    int m = 0;
-    if (!done) {
-        int nc = 0;
+    // the threshold bin's keys go to a list (warp-aggregated positions)
+    if (!done && m <= kTopkList) {
+        if (threadIdx.x == 0) s_m = 0;
+        __syncthreads();
 #pragma unroll
-        for (int e = 0; e < kTopkSmallPer; ++e) nc += (((vm >> e) & 1u) && (off[e] >> shift) == (prefix >> shift)) ? 1 : 0;
-        int tot2;
-        int pos = block_excl_scan(nc, scratch, tot2);
-        m = tot2;
-        if (m <= kTopkList) {
-#pragma unroll
-            for (int e = 0; e < kTopkSmallPer; ++e)
-                if (((vm >> e) & 1u) && (off[e] >> shift) == (prefix >> shift)) list[pos++] = off[e];
+        for (int j = 0; j < kTopkSmallPer; ++j) {
+            const bool cand = ((vm >> j) & 1u) && (off[j] >> shift) == (prefix >> shift);
+            const uint32_t bal = __ballot_sync(0xffffffffu, cand);
+            if (bal) {
+                int pos = 0;
+                if (lane == 0) pos = atomicAdd(&s_m, __popc(bal));
+                pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+                if (cand) list[pos] = off[j];
+            }
         }
         __syncthreads();
+        if (m <= 32) {
+            // one warp ranks the bin's keys: T = the rem-th largest, and how
+            // many keys equal to T are taken
+            if (warp == 0) {
+                const uint32_t c = lane < m ? list[lane] : 0u;
+                int gt = 0, eq = 0;
+                for (int i = 0; i < m; ++i) {
+                    const uint32_t o = __shfl_sync(0xffffffffu, c, i);
+                    gt += o > c;
+                    eq += o == c;
+                }
+                const bool is_t = lane < m && gt < rem && rem <= gt + eq;
+                const uint32_t bal = __ballot_sync(0xffffffffu, is_t);
+                if (lane == __ffs(bal) - 1) {
+                    s_prefix = c;
+                    s_rem = rem - gt;
+                    s_shift = 0;
+                    s_done = 1;
+                }
+            }
+            __syncthreads();
+            prefix = s_prefix;
+            rem = s_rem;
+            shift = s_shift;
+            done = true;
+        }
     }
+    // more than 32 keys in the bin: 8-bit passes (over the list, or over the
+    // registers when the bin holds more than the list)
     const bool use_list = m <= kTopkList;
     while (!done) {
         const int lo = shift > 8 ? shift - 8 : 0;
         if (use_list) {
             for (int i = threadIdx.x; i < m; i += kTopkThreads) {
                 const uint32_t o = list[i];
-                if (shift >= 32 || (o >> shift) == (prefix >> shift)) atomicAdd(&wh[0][(o >> lo) & 255u], 1);
+                if ((o >> shift) == (prefix >> shift)) atomicAdd(&hist2[(o >> lo) & 255u], 1);
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < kTopkSmallPer; ++e) {
-                const bool cand = ((vm >> e) & 1u) && (shift >= 32 || (off[e] >> shift) == (prefix >> shift));
-                if (cand) atomicAdd(&wh[warp][(off[e] >> lo) & 255u], 1);
-            }
+            for (int j = 0; j < kTopkSmallPer; ++j)
+                if (((vm >> j) & 1u) && (off[j] >> shift) == (prefix >> shift)) atomicAdd(&hist2[(off[j] >> lo) & 255u], 1);
         }
         __syncthreads();
-        // digit 255 - t for t < 256: the count over all warps, then a scan from the top
-        int cnt = 0;
-        if (threadIdx.x < 256) {
-            if (use_list) {
-                cnt = wh[0][255 - threadIdx.x];
-            } else {
-#pragma unroll
-                for (int w = 0; w < NW; ++w) cnt += wh[w][255 - threadIdx.x];
-            }
-        }
+        // digit 255 - t for t < 256, scanned from the top
+        const int cnt = threadIdx.x < 256 ? hist2[255 - threadIdx.x] : 0;
         int x = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -617,10 +625,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
         }
         if (lane == 31 && warp < 8) scratch[warp] = x;
         __syncthreads();
-        // every histogram read is done: clear for the next pass
-#pragma unroll
-        for (int q = 0; q < kClear; ++q) (&wh[0][0])[threadIdx.x * kClear + q] = 0;
         if (threadIdx.x < 256) {
+            hist2[255 - threadIdx.x] = 0;                 // every read of the histogram is done
             int before = x - cnt;
             for (int w = 0; w < warp; ++w) before += scratch[w];
             if (before < rem && rem <= before + cnt) {
@@ -636,34 +642,40 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
         shift = s_shift;
         done = s_done;
     }
+    // ordered compaction: slot order is (warp, row, lane)
     const int lo = shift;
     const uint32_t thr = prefix >> lo;     // digit prefix of the threshold bin
     const int take_eq = rem;               // keys of that bin to take, lowest slot first
-    int gt = 0, eq = 0;
+    uint32_t gtb[kTopkSmallPer], eqb[kTopkSmallPer];
+    int gtw = 0, eqw = 0;
 #pragma unroll
-    for (int e = 0; e < kTopkSmallPer; ++e) {
-        if ((vm >> e) & 1u) {
-            const uint32_t d = off[e] >> lo;
-            gt += d > thr;
-            eq += d == thr;
-        }
+    for (int j = 0; j < kTopkSmallPer; ++j) {
+        const bool valid = (vm >> j) & 1u;
+        const uint32_t d = off[j] >> lo;
+        gtb[j] = __ballot_sync(0xffffffffu, valid && d > thr);
+        eqb[j] = __ballot_sync(0xffffffffu, valid && d == thr);
+        gtw += __popc(gtb[j]);
+        eqw += __popc(eqb[j]);
     }
-    int tot;
-    const int gt_before = block_excl_scan(gt, scratch, tot);
-    const int eq_before = block_excl_scan(eq, scratch, tot);
-    int g = gt_before, e2 = eq_before;
+    if (lane == 0) {
+        s_wgt[warp] = gtw;
+        s_weq[warp] = eqw;
+    }
+    __syncthreads();
+    int g = 0, e = 0;
+    for (int w = 0; w < warp; ++w) {
+        g += s_wgt[w];
+        e += s_weq[w];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int e = 0; e < kTopkSmallPer; ++e) {
-        if ((vm >> e) & 1u) {
-            const uint32_t d = off[e] >> lo;
-            if (d > thr) {
-                orow[g + min(e2, take_eq)] = i0 + e;
-                ++g;
-            } else if (d == thr) {
-                if (e2 < take_eq) orow[g + e2] = i0 + e;
-                ++e2;
-            }
-        }
+    for (int j = 0; j < kTopkSmallPer; ++j) {
+        const int gr = g + __popc(gtb[j] & lt);
+        const int er = e + __popc(eqb[j] & lt);
+        if ((gtb[j] >> lane) & 1u) orow[gr + min(er, take_eq)] = base_slot + 32 * j;
+        else if (((eqb[j] >> lane) & 1u) && er < take_eq) orow[gr + er] = base_slot + 32 * j;
+        g += __popc(gtb[j]);
+        e += __popc(eqb[j]);
     }
     if (threadIdx.x == 0) out_len[b] = k;
 }
