@@ -188,7 +188,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             }
         }
     } else {
-        // epilogue group (warps 0-3 or 4-7) takes every other tile
+        // epilogue group (warps 0-3 or 4-7) takes every other tile; the scales it
+        // reads may come from the kernel before this one
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const int grp = warp >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
@@ -301,7 +303,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int& total)
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
-    const float* __restrict__ logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
+    const float* logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
     int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len, int smem_keys)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -446,7 +448,7 @@ constexpr int kTopkSmallMax = kTopkThreads * kTopkSmallPer;   // 8192
 constexpr int kTopkList = 2048;                                 // threshold-bin keys kept in a list
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
-    const float* __restrict__ logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
+    const float* logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k,
     int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len)
 {
     constexpr int NW = kTopkThreads / 32;
@@ -454,24 +456,35 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     __shared__ int hist2[256];
     __shared__ uint32_t list[kTopkList];
     __shared__ int scratch[33];
-    __shared__ uint32_t s_wmin[NW], s_wmax[NW];
-    __shared__ int s_wgt[NW], s_weq[NW];
+    __shared__ uint32_t s_min, s_max;
+    __shared__ __align__(16) int s_wgt[NW];
+    __shared__ __align__(16) int s_weq[NW];
     __shared__ uint32_t s_prefix;
-    __shared__ int s_shift, s_rem, s_done, s_m;
+    __shared__ int s_shift, s_rem, s_done, s_m, s_fill;
 
     // the attention kernel that follows may be scheduled now (it waits for
     // this grid before reading the selection); the logits were produced by
     // the previous kernel of this call
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int q = 0; q < kTopkBins / kTopkThreads; ++q) hist1[threadIdx.x * (kTopkBins / kTopkThreads) + q] = 0;
+    if (threadIdx.x < 256) hist2[threadIdx.x] = 0;
+    if (threadIdx.x == 0) {
+        s_min = 0xffffffffu;
+        s_max = 0u;
+        s_fill = 0;
+    }
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int base_slot = warp * 512 + lane;             // slot of row j: base_slot + 32 j
     const float* lrow = logits + static_cast<long long>(b) * row_stride;
     // the row is allocated up to max_slots: load it together with the length
     float v[kTopkSmallPer];
 #pragma unroll
-    for (int j = 0; j < kTopkSmallPer; ++j) v[j] = (base_slot + 32 * j < max_slots) ? lrow[base_slot + 32 * j] : 0.f;
+    for (int j = 0; j < kTopkSmallPer; ++j)   // written by the grid before: L2 loads, after the wait
+        v[j] = (base_slot + 32 * j < max_slots) ? __ldcg(lrow + base_slot + 32 * j) : 0.f;
     int n = ctx_len[b] / 4;
     n = n < 0 ? 0 : (n > max_slots ? max_slots : n);
     int* orow = out_idx + static_cast<long long>(b) * out_stride;
@@ -495,19 +508,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     mn = __reduce_min_sync(0xffffffffu, mn);
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0) {
-        s_wmin[warp] = mn;
-        s_wmax[warp] = mx;
+        atomicMin(&s_min, mn);
+        atomicMax(&s_max, mx);
     }
-#pragma unroll
-    for (int q = 0; q < kTopkBins / kTopkThreads; ++q) hist1[threadIdx.x * (kTopkBins / kTopkThreads) + q] = 0;
-    if (threadIdx.x < 256) hist2[threadIdx.x] = 0;
     __syncthreads();                                                   // (1)
-    uint32_t base = 0xffffffffu, top = 0u;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-        base = min(base, s_wmin[w]);
-        top = max(top, s_wmax[w]);
-    }
+    const uint32_t base = s_min, top = s_max;
     const uint32_t range = top - base;
     int shift = range ? 32 - __clz(range) : 0;           // offsets fit in `shift` bits
     uint32_t prefix = 0;
@@ -558,15 +563,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     }
     // the threshold bin's keys go to a list (warp-aggregated positions)
     if (!done && m <= kTopkList) {
-        if (threadIdx.x == 0) s_m = 0;
-        __syncthreads();
 #pragma unroll
         for (int j = 0; j < kTopkSmallPer; ++j) {
             const bool cand = ((vm >> j) & 1u) && (off[j] >> shift) == (prefix >> shift);
             const uint32_t bal = __ballot_sync(0xffffffffu, cand);
             if (bal) {
                 int pos = 0;
-                if (lane == 0) pos = atomicAdd(&s_m, __popc(bal));
+                if (lane == 0) pos = atomicAdd(&s_fill, __popc(bal));
                 pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(bal & ((1u << lane) - 1u));
                 if (cand) list[pos] = off[j];
             }
@@ -663,9 +666,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     }
     __syncthreads();
     int g = 0, e = 0;
-    for (int w = 0; w < warp; ++w) {
-        g += s_wgt[w];
-        e += s_weq[w];
+#pragma unroll
+    for (int q = 0; q < NW / 4; ++q) {
+        const int4 a4 = reinterpret_cast<const int4*>(s_wgt)[q];
+        const int4 b4 = reinterpret_cast<const int4*>(s_weq)[q];
+        g += (4 * q < warp ? a4.x : 0) + (4 * q + 1 < warp ? a4.y : 0) + (4 * q + 2 < warp ? a4.z : 0) +
+             (4 * q + 3 < warp ? a4.w : 0);
+        e += (4 * q < warp ? b4.x : 0) + (4 * q + 1 < warp ? b4.y : 0) + (4 * q + 2 < warp ? b4.z : 0) +
+             (4 * q + 3 < warp ? b4.w : 0);
     }
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll

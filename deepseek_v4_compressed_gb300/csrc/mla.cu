@@ -81,13 +81,13 @@ constexpr int kTcOCol = 128;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kTcQBytes;
 constexpr int kOffMisc = kOffK + kTcStages * kTcKBytes;    // 221184
-constexpr int kMiscBytes = 2048;
+constexpr int kMiscBytes = 2048 + 4 * 1024;                   // + the compressed block-table row
+constexpr int kBtSmem = 1024;                               // block-table entries kept in shared memory
 constexpr int kTcSmem = kOffMisc + kMiscBytes + 1024;      // + alignment slack of the dynamic base
 // epilogue buffers (in the Q / K space once the main loop is over): a slice
 // is bf16 [512/C dims][64 heads] (16-byte head groups swizzled by dim) plus
 // fp32 [64][2] running max and sum; receive slots [C], send slots [C], merge
 // weights [8][64] and 1 / L [64]
-constexpr int kSliceMax = (kV / 1) * 128 + 512;
 constexpr int kOffRecv = 0;
 constexpr int kOffSend = 64 * kV * 2 + 8 * 512;
 constexpr int kOffWeights = 2 * kOffSend;
@@ -192,12 +192,14 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint64_t* sync4 = bars + 9;        // [2] the four softmax warps meet once per tile
     uint64_t* recv_full = bars + 11;   // epilogue: the C - 1 peer slices have landed (bytes)
     uint64_t* pv_done = bars + 12;     // [kTcMaxTiles] PV(u) complete (one phase each)
-    float* sm_m = reinterpret_cast<float*>(bars + 12 + kTcMaxTiles);   // [64] running max (log2 domain)
+    float* sm_m = reinterpret_cast<float*>(bars + 13 + kTcMaxTiles);   // [64] running max (log2 domain)
     float* sm_l = sm_m + 64;                              // [64] running sum
     float* sm_alpha = sm_l + 64;                          // [2][64] correction factors (by tile parity)
     int* sm_any = reinterpret_cast<int*>(sm_alpha + 128); // [2][4]
     volatile int* abort_flag = sm_any + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm_any + 9);
+    int* bt_s = reinterpret_cast<int*>(smem + kOffMisc + 2048);  // [kBtSmem] this sequence's block-table row
+    uint64_t* bt_ready = bars + 12 + kTcMaxTiles;                 // producers: bt_s loaded
 
     const int rank = blockIdx.x;                          // the cluster spans gridDim.x
     const int b = blockIdx.y / T.head_groups, g_head = blockIdx.y % T.head_groups;
@@ -217,7 +219,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     bool resolved = false;
     auto resolve = [&]() {
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        n_comp = P.idx_len ? min(max(P.idx_len[b], 0), T.topk) : 0;
+        // written by the grid before: L2 loads after the wait
+        n_comp = P.idx_len ? min(max(__ldcg(P.idx_len + b), 0), T.topk) : 0;
         const int n_glob = n_swa_t + (n_comp + kTcKeys - 1) / kTcKeys;
         n_tiles = n_glob > rank ? (n_glob - rank + C - 1) / C : 0;
         if (n_tiles - n_swa_mine > kTcMaxCompTiles || n_tiles > kTcMaxTiles) {
@@ -239,6 +242,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc::mbar_init(tc::smem_u32(&p_full[i]), 4);
         }
         for (int i = 0; i < kTcMaxTiles; ++i) tc::mbar_init(tc::smem_u32(&pv_done[i]), 1);
+        tc::mbar_init(tc::smem_u32(bt_ready), kTcProdWarps);
         tc::mbar_init(tc::smem_u32(q_full), 1);
         tc::mbar_init(tc::smem_u32(recv_full), 1);
         *abort_flag = 0;
@@ -318,6 +322,14 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // ------------------------------------------------------ producers (warps 4-11)
             // Producer warp pw owns rows pw + 8k (k = 0..7) of every tile.
             const int pw = warp - 4;
+            // the sequence's compressed block-table row (a caller input) into
+            // shared memory while the window tiles run
+            const bool bt_smem = P.comp_bt != nullptr && P.comp_bt_stride <= kBtSmem;
+            if (bt_smem)
+                for (int i = threadIdx.x - 128; i < P.comp_bt_stride; i += 32 * kTcProdWarps)
+                    bt_s[i] = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + i];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(bt_ready));
             // Row table, spread over the lanes: lane l holds row pw + 8 (l % 8) of
             // compressed tiles 4q + l / 8 (q = 0..3) as page * 64 + row (-1:
             // padding or unreadable).  Index loads, then block-table loads, each
@@ -332,14 +344,15 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (jc < n_comp_mine) {
                         const int ct = rank + (n_swa_mine + jc) * C - n_swa_t;
                         const int key = ct * kTcKeys + pw + 8 * (lane & 7);
-                        if (key < n_comp) slot[q] = P.idx[static_cast<long long>(b) * P.idx_stride + key];
+                        if (key < n_comp) slot[q] = __ldcg(P.idx + static_cast<long long>(b) * P.idx_stride + key);
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     pg[q] = -2;
                     if (slot[q] >= 0 && (slot[q] >> 6) < P.comp_bt_stride)
-                        pg[q] = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + (slot[q] >> 6)];
+                        pg[q] = bt_smem ? bt_s[slot[q] >> 6]
+                                        : P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + (slot[q] >> 6)];
                     else if (slot[q] != -1)
                         flag(P.status, DSV4_DEV_BAD_INDEX);
                 }
@@ -438,6 +451,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             // then the selected slots: row table, first rows, compressed tiles
             resolve();
+            if (ok) ok = tc::mbar_wait(tc::smem_u32(bt_ready), 0, abort_flag, P.status);
             if (ok) {
                 build_table();
                 if (n_comp_mine > 0) fetch(0);
