@@ -159,19 +159,46 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
     return ok != 0;
 }
 
-__device__ __forceinline__ uint4 ldg_stream_v4(const uint8_t* p)
+// Loads that run only when `pred` holds and otherwise leave a default: the
+// default and the load are one predicated sequence, so nothing that reads the
+// result sits between one load and the next (a select after each load would
+// wait for it and serialise the gather).  p is not dereferenced when pred is
+// false.
+__device__ __forceinline__ uint4 ldg_stream_v4_if(const uint8_t* p, bool pred)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm volatile("{\n\t.reg .pred q;\n\t"
+                 "setp.ne.u32 q, %5, 0;\n\t"
+                 "mov.u32 %0, 0;\n\tmov.u32 %1, 0;\n\tmov.u32 %2, 0;\n\tmov.u32 %3, 0;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+                 : "=&r"(v.x), "=&r"(v.y), "=&r"(v.z), "=&r"(v.w)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred)));
     return v;
 }
 
-__device__ __forceinline__ uint32_t ldg_stream_u8(const uint8_t* p)
+__device__ __forceinline__ uint32_t ldg_stream_u8_if(const uint8_t* p, bool pred, uint32_t dflt)
 {
-    uint16_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    uint32_t v;
+    asm volatile("{\n\t.reg .pred q;\n\t.reg .u16 h;\n\t"
+                 "setp.ne.u32 q, %2, 0;\n\t"
+                 "mov.u32 %0, %3;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.u8 h, [%1];\n\t"
+                 "@q cvt.u32.u16 %0, h;\n\t}"
+                 : "=&r"(v)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred)), "r"(dflt));
+    return v;
+}
+
+// L2 load of an int written by the grid before this one, or dflt
+__device__ __forceinline__ int ldcg_s32_if(const int* p, bool pred, int dflt)
+{
+    int v;
+    asm volatile("{\n\t.reg .pred q;\n\t"
+                 "setp.ne.u32 q, %2, 0;\n\t"
+                 "mov.b32 %0, %3;\n\t"
+                 "@q ld.global.cg.b32 %0, [%1];\n\t}"
+                 : "=&r"(v)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred)), "r"(dflt));
     return v;
 }
 
@@ -335,17 +362,26 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // padding or unreadable).  Index loads, then block-table loads, each
             // issued together.
             int ent[4] = {-1, -1, -1, -1};
-            auto build_table = [&]() {
-                int slot[4], pg[4];
+            // The slots of every key this CTA could own (keys below top-k, all
+            // in bounds) are loaded before the count is known, so that the two
+            // loads overlap; keys at or past the count are dropped once it is.
+            int slot[4];
+            auto load_slots = [&]() {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int jc = 4 * q + (lane >> 3);
-                    slot[q] = -1;
-                    if (jc < n_comp_mine) {
-                        const int ct = rank + (n_swa_mine + jc) * C - n_swa_t;
-                        const int key = ct * kTcKeys + pw + 8 * (lane & 7);
-                        if (key < n_comp) slot[q] = __ldcg(P.idx + static_cast<long long>(b) * P.idx_stride + key);
-                    }
+                    const int key = (rank + (n_swa_mine + jc) * C - n_swa_t) * kTcKeys + pw + 8 * (lane & 7);
+                    slot[q] = ldcg_s32_if(P.idx + static_cast<long long>(b) * P.idx_stride + key,
+                                          P.idx_len != nullptr && key < T.topk, -1);
+                }
+            };
+            auto build_table = [&]() {
+                int pg[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int jc = 4 * q + (lane >> 3);
+                    const int key = (rank + (n_swa_mine + jc) * C - n_swa_t) * kTcKeys + pw + 8 * (lane & 7);
+                    if (jc >= n_comp_mine || key >= n_comp) slot[q] = -1;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -378,21 +414,16 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int e = __shfl_sync(0xffffffffu, e_src, base + k);
-                    rn[k] = make_uint4(0, 0, 0, 0);
-                    rs[k] = 127;
-                    if (e >= 0) {
-                        const uint8_t* page = P.comp + static_cast<long long>(e >> 6) * kMlaPage;
-                        rn[k] = ldg_stream_v4(page + (e & 63) * kMlaData + lane * 16);
-                        rs[k] = ldg_stream_u8(page + kPage * kMlaData + (e & 63) * 8 + (lane >> 2));
-                    }
+                    const uint8_t* page = P.comp + static_cast<long long>(e >> 6) * kMlaPage;
+                    rn[k] = ldg_stream_v4_if(page + (e & 63) * kMlaData + lane * 16, e >= 0);
+                    rs[k] = ldg_stream_u8_if(page + kPage * kMlaData + (e & 63) * 8 + (lane >> 2), e >= 0, 127);
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int e = __shfl_sync(0xffffffffu, e_src, base + (lane >> 3) + 4 * hh);
-                    rr[hh] = make_uint4(0, 0, 0, 0);
-                    if (e >= 0)
-                        rr[hh] = ldg_stream_v4(P.comp + static_cast<long long>(e >> 6) * kMlaPage + (e & 63) * kMlaData +
-                                               kNope + (lane & 7) * 16);
+                    rr[hh] = ldg_stream_v4_if(P.comp + static_cast<long long>(e >> 6) * kMlaPage + (e & 63) * kMlaData +
+                                                  kNope + (lane & 7) * 16,
+                                              e >= 0);
                 }
             };
             // dequantise into the 128-byte-swizzled tile (row r, 16-byte unit u
@@ -450,6 +481,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             // then the selected slots: row table, first rows, compressed tiles
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            load_slots();
             resolve();
             if (ok) ok = tc::mbar_wait(tc::smem_u32(bt_ready), 0, abort_flag, P.status);
             if (ok) {

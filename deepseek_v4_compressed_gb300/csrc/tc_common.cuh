@@ -109,6 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait for a phase completed by arrivals from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status)
 {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait_cluster(bar, parity)) {
         if (global_timer_ns() - t0 > kWaitNs) {
