@@ -38,9 +38,12 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = dict(name="c4a_32k_b32", batch=32, context=32768, n_heads=64, idx_heads=64, topk=512,
                 window=128, ratio=4)
 
-# DRAM bytes per launch from an ncu capture of the indexer stage, with the
-# sha256 of the sources it was taken on; reported as null once they change.
-TRAFFIC_RECORD = {}
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture (profiles/mla_decode_tc_c4a_32k_b32_traffic.md), with the sha256 of
+# the sources it was taken on; reported as null once they change.
+TRAFFIC_RECORD = {
+    "sparse_mla": {"bytes_per_launch": 19084032 + 0, "src_sha": "d91c13b7fa9b7a9b"},
+}
 
 
 # ----------------------------------------------------------------------------
