@@ -178,6 +178,9 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
         per_seq = per_seq < 1 ? 1 : (per_seq > tiles ? tiles : per_seq);
         p->idx_tiles_per_cta = tiles > 0 ? (tiles + per_seq - 1) / per_seq : 1;
         p->idx_ctas_per_seq = tiles > 0 ? (tiles + p->idx_tiles_per_cta - 1) / p->idx_tiles_per_cta : 0;
+        // the CTAs of a sequence form a cluster that also selects the top-k,
+        // when they fit one (at most 8 CTAs of at most 16 tiles each)
+        p->idx_fused_topk = p->idx_ctas_per_seq >= 1 && p->idx_ctas_per_seq <= 8 && p->idx_tiles_per_cta <= 16;
     }
     p->mla_head_groups = (g->n_heads + 63) / 64;
     // attention: the keys of a (sequence, head group) are split over a cluster
@@ -223,7 +226,7 @@ extern "C" dsv4_status dsv4_plan_get_info(const dsv4_plan* p, dsv4_plan_info* in
     info->mla_head_groups = p->mla_head_groups;
     info->mla_keys_per_split = p->mla_keys_per_split;
     info->workspace_bytes = p->ws_bytes;
-    info->launches_indexer = (p->type == DSV4_C4A) ? 2 : 0;
+    info->launches_indexer = (p->type == DSV4_C4A) ? (p->idx_fused_topk ? 1 : 2) : 0;
     info->launches_mla = 1;   // one cluster launch; partials merge through DSMEM
     return DSV4_OK;
 }

@@ -38,6 +38,183 @@ constexpr int kIdxScaleBytes = 16;                           // the tile's two p
 constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
                          2048 /* barriers etc */ + 1024 /* align */;
 
+// ---------------------------------------------------------------------------
+// Top-k inside the logits launch: the CTAs of a sequence form a cluster, CTA
+// r holding the logits of its consecutive slots [s0, s1) in shared memory.
+// The selection rule is the one of the single-CTA top-k below (keys relative
+// to the row minimum; digit passes from the top until the bin of the k-th
+// largest key is taken whole or is one key; keys equal to the threshold taken
+// lowest slot first; slots written in ascending order), here with 8-bit
+// digits and every count summed over the cluster: each CTA pushes its counts
+// into every CTA's shared memory (distributed shared memory stores) before a
+// cluster barrier, after which each CTA reads them locally and takes the same
+// decisions as the others.
+// ---------------------------------------------------------------------------
+constexpr int kCtkSlots = 16 * kIdxTileSlots;                        // slots per CTA at most
+constexpr int kCtkPer = (kCtkSlots + kIdxThreads - 1) / kIdxThreads;   // slots per thread (6)
+constexpr int kCtkMaxCluster = 8;
+struct CtkScratch {
+    uint32_t mm_in[kCtkMaxCluster][2];      // (min, max) key of CTA q's slots, pushed by q
+    int cnt_in[kCtkMaxCluster][2];          // CTA q's keys above / at the threshold, pushed by q
+    int hin[2][kCtkMaxCluster][256];        // CTA q's digit histogram, by pass parity, pushed by q
+    int hist[256];                          // this CTA's histogram of the current pass
+    uint32_t mm[2];                         // this CTA's min, max
+    uint32_t prefix;                        // the decisions, for the CTA's threads
+    int rem, lo, done;
+    int scan[16];
+};
+constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
+
+// Exclusive scan of one int per thread over the CTA (kIdxThreads threads).
+__device__ __forceinline__ int ctk_excl_scan(int v, int* scan, int& total)
+{
+    constexpr int NW = kIdxThreads / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scan[warp] = x;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const int t = scan[w];
+        before += w < warp ? t : 0;
+        total += t;
+    }
+    __syncthreads();
+    return before + x - v;
+}
+
+// Called by every thread of every CTA of the cluster once the CTA's logits
+// are in lg[0, s1 - s0), and after the cluster arrival that the kernel made
+// when it started (this function waits for it before its first push).
+// Writes the row's k slots (or, with at most k slots, all of them and -1
+// past) and its length.
+__device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, int C, int rank, int* orow,
+                             int* out_len, CtkScratch* S)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    tc::cluster_wait_acquire();                      // every CTA of the cluster has started
+    if (n_c <= k) {
+        for (int s = s0 + tid; s < s1; s += kIdxThreads) orow[s] = s;
+        if (rank == 0) {
+            for (int i = n_c + tid; i < k; i += kIdxThreads) orow[i] = -1;
+            if (tid == 0) *out_len = n_c;
+        }
+        return;
+    }
+    // this thread's consecutive slots [i0, i0 + nv) of the CTA's range
+    const int nl = max(0, s1 - s0);
+    const int chunk = (nl + kIdxThreads - 1) / kIdxThreads;
+    const int i0 = tid * chunk;
+    const int nv = max(0, min(chunk, nl - i0));
+    uint32_t key[kCtkPer];
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < kCtkPer; ++j) {
+        key[j] = j < nv ? f32_order_key(lg[i0 + j]) : 0u;
+        if (j < nv) {
+            mn = min(mn, key[j]);
+            mx = max(mx, key[j]);
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        atomicMin(&S->mm[0], mn);
+        atomicMax(&S->mm[1], mx);
+    }
+    __syncthreads();
+    if (tid < C) tc::st_cluster_u32x2(tc::map_to_rank(tc::smem_u32(&S->mm_in[rank][0]), tid), S->mm[0], S->mm[1]);
+    tc::cluster_arrive_release();                    // (a) min / max pushed
+    tc::cluster_wait_acquire();
+    uint32_t base = 0xffffffffu, top = 0u;
+    for (int q = 0; q < C; ++q) {
+        base = min(base, S->mm_in[q][0]);
+        top = max(top, S->mm_in[q][1]);
+    }
+    const uint32_t range = top - base;
+    const int shift = range ? 32 - __clz(range) : 0;     // (key - base) < 2^shift
+    // digit passes: pass 0 takes bits [lo, shift) of every key, later passes
+    // the next 8 bits of the keys still in the threshold bin
+    int lo = shift > 8 ? shift - 8 : 0;
+    int plo = 32;                                        // the bin is (key - base) >> plo == prefix >> plo
+    uint32_t prefix = 0;
+    int rem = k;
+    for (int pass = 0;; ++pass) {
+        const int p = pass & 1;
+        if (tid < 256) S->hist[tid] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kCtkPer; ++j) {
+            const uint32_t o = key[j] - base;
+            if (j < nv && (plo == 32 || (o >> plo) == (prefix >> plo))) atomicAdd(&S->hist[(o >> lo) & 255u], 1);
+        }
+        __syncthreads();
+        if (tid < 64) {
+            const uint4 h4 = *reinterpret_cast<const uint4*>(&S->hist[4 * tid]);
+            for (int q = 0; q < C; ++q)
+                tc::st_cluster_u32x4(tc::map_to_rank(tc::smem_u32(&S->hin[p][rank][4 * tid]), q), h4);
+        }
+        tc::cluster_arrive_release();                // (b) histograms pushed
+        tc::cluster_wait_acquire();
+        // digit 255 - tid, summed over the cluster, scanned from the top
+        int g = 0;
+        if (tid < 256)
+            for (int q = 0; q < C; ++q) g += S->hin[p][q][255 - tid];
+        int tot;
+        const int before = ctk_excl_scan(g, S->scan, tot);
+        if (tid < 256 && before < rem && rem <= before + g) {
+            S->prefix = prefix | (static_cast<uint32_t>(255 - tid) << lo);
+            S->rem = rem - before;
+            S->done = (lo == 0) || (g == rem - before);
+        }
+        __syncthreads();
+        prefix = S->prefix;
+        rem = S->rem;
+        plo = lo;
+        if (S->done) break;
+        lo = lo > 8 ? lo - 8 : 0;
+    }
+    // ordered compaction: keys above the threshold bin, and the first `rem`
+    // in it (lowest slot first), at their positions in the whole row
+    const uint32_t thr = prefix >> plo;
+    int gtn = 0, eqn = 0;
+#pragma unroll
+    for (int j = 0; j < kCtkPer; ++j) {
+        const uint32_t d = (key[j] - base) >> plo;
+        gtn += j < nv && d > thr;
+        eqn += j < nv && d == thr;
+    }
+    int tot;
+    const int before = ctk_excl_scan((gtn << 16) | eqn, S->scan, tot);   // counts < 2^16
+    if (tid < C) tc::st_cluster_u32x2(tc::map_to_rank(tc::smem_u32(&S->cnt_in[rank][0]), tid), tot >> 16, tot & 0xffff);
+    tc::cluster_arrive_release();                    // (c) counts pushed
+    tc::cluster_wait_acquire();
+    int gpos = before >> 16, epos = before & 0xffff;
+    for (int q = 0; q < rank; ++q) {
+        gpos += S->cnt_in[q][0];
+        epos += S->cnt_in[q][1];
+    }
+#pragma unroll
+    for (int j = 0; j < kCtkPer; ++j) {
+        const uint32_t d = (key[j] - base) >> plo;
+        if (j < nv && d > thr) {
+            orow[gpos + min(epos, rem)] = s0 + i0 + j;
+            ++gpos;
+        } else if (j < nv && d == thr) {
+            if (epos < rem) orow[gpos + epos] = s0 + i0 + j;
+            ++epos;
+        }
+    }
+    if (rank == 0 && tid == 0) *out_len = k;
+}
+
 struct IdxTcParams {
     const uint8_t* cache;
     int num_pages;
@@ -52,8 +229,14 @@ struct IdxTcParams {
     int max_slots;
     int tiles_per_cta;
     int* status;
+    // with the top-k in the launch: k, and the selection's rows
+    int k;
+    int* out_idx;
+    int out_stride;
+    int* out_len;
 };
 
+template <bool kFused>
 __global__ void __launch_bounds__(kIdxThreads, 1)
 indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_q,
                   IdxTcParams P)
@@ -75,6 +258,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     float* w_s = reinterpret_cast<float*>(bars + 32);            // [64], 16-byte aligned, zero past H
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_s + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // with the top-k in the launch: this CTA's logits, then the top-k scratch
+    float* lg_s = reinterpret_cast<float*>(smem + kIdxSmem - 1024);
+    CtkScratch* ctk = reinterpret_cast<CtkScratch*>(lg_s + kCtkSlots);
 
     const int b = blockIdx.y;
     int n_c = P.ctx_len[b] / 4;
@@ -83,8 +269,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     const int n_tiles = (n_c + kIdxTileSlots - 1) / kIdxTileSlots;
     const int t_begin = blockIdx.x * P.tiles_per_cta;
     const int t_end = min(n_tiles, t_begin + P.tiles_per_cta);
-    if (t_begin >= t_end) return;                 // uniform: nothing allocated yet
-    const int n_my = t_end - t_begin;
+    if (!kFused && t_begin >= t_end) return;      // uniform: nothing allocated yet
+    const int n_my = max(0, t_end - t_begin);
     const int n_pages = (n_c + kPage - 1) / kPage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -102,6 +288,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         tc::fence_barrier_init();
     }
     if (threadIdx.x < 64) w_s[threadIdx.x] = (threadIdx.x < P.H) ? P.w[static_cast<long long>(b) * P.H + threadIdx.x] : 0.f;
+    if (kFused && threadIdx.x == 0) {
+        ctk->mm[0] = 0xffffffffu;
+        ctk->mm[1] = 0u;
+    }
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), kIdxTmemCols);
         tc::tmem_relinquish();
@@ -110,6 +300,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (kFused) tc::cluster_arrive_relaxed();   // this CTA has started (the top-k waits for every CTA)
     int issued = 0;   // tiles whose loads were issued (producer only)
     int consumed = 0; // tiles whose stage the MMA released (MMA thread only)
 
@@ -237,7 +428,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                 }
             }
             const int s = (t_begin + i) * kIdxTileSlots + row;
-            if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc * scale;
+            if (kFused) lg_s[i * kIdxTileSlots + row] = acc * scale;
+            else if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc * scale;
         }
     }
 
@@ -256,6 +448,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kIdxTmemCols);
     }
+    if (kFused)
+        cluster_topk(lg_s, t_begin * kIdxTileSlots, min(t_end * kIdxTileSlots, n_c), n_c, P.k, static_cast<int>(gridDim.x),
+                     static_cast<int>(blockIdx.x), P.out_idx + static_cast<long long>(b) * P.out_stride,
+                     P.out_len + b, ctk);
 }
 
 // ---------------------------------------------------------------------------
@@ -735,26 +931,41 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         P.max_slots = plan->max_slots;
         P.tiles_per_cta = plan->idx_tiles_per_cta;
         P.status = a->status_dev;
+        P.k = plan->topk;
+        P.out_idx = a->out_idx_dev;
+        P.out_stride = a->out_stride;
+        P.out_len = a->out_len_dev;
+        const bool fused = plan->idx_fused_topk != 0;
         static bool tc_attr = false;
         if (!tc_attr) {
-            cudaFuncSetAttribute(indexer_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem);
-            // the whole unified L1 as shared memory: three CTAs per SM
-            cudaFuncSetAttribute(indexer_logits_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+            cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem);
+            cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmemFused);
+            // the whole unified L1 as shared memory
+            cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+            cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
             tc_attr = true;
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(plan->idx_ctas_per_seq, B, 1);
         cfg.blockDim = dim3(kIdxThreads, 1, 1);
-        cfg.dynamicSmemBytes = kIdxSmem;
+        cfg.dynamicSmemBytes = fused ? kIdxSmemFused : kIdxSmem;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
+        // with the top-k in the launch, a sequence's CTAs form one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = plan->idx_ctas_per_seq;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, indexer_logits_tc, tm_cache, tm_q, P);
+        cfg.numAttrs = fused ? 2 : 1;
+        cudaError_t e = fused ? cudaLaunchKernelEx(&cfg, indexer_logits_tc<true>, tm_cache, tm_q, P)
+                              : cudaLaunchKernelEx(&cfg, indexer_logits_tc<false>, tm_cache, tm_q, P);
         if (e != cudaSuccess) return DSV4_ERR_CUDA;
+        if (fused) return DSV4_OK;
     }
     cudaError_t e;
     if (plan->max_slots <= kTopkSmallMax) {

@@ -15,6 +15,7 @@ struct dsv4_plan {
     int max_keys;            // topk + window
     int idx_ctas_per_seq;    // indexer split over slots
     int idx_tiles_per_cta;   // 128-slot tiles per indexer CTA
+    int idx_fused_topk;      // the top-k runs inside the logits launch (one cluster per sequence)
     int mla_head_groups;     // ceil(n_heads / 64)
     int mla_splits;          // key splits per (sequence, head group)
     int mla_keys_per_split;

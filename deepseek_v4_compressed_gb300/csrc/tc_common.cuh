@@ -314,6 +314,29 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrival that orders nothing: for "every CTA of the cluster has started".
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32x2(uint32_t addr, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32x4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 // Asynchronous store into (possibly another CTA's) shared memory; completion
 // is counted in bytes on the destination CTA's mbarrier `bar` (both addresses
 // are shared::cluster addresses of the destination CTA).

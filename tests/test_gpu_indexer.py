@@ -56,6 +56,43 @@ def test_c4a_32k_batch32_full_size():
     print("near-tie slots tolerated:", tol)
 
 
+def _with_zero_weights(d, seqs):
+    """All-equal logits (zero head weights) for the given sequences: every
+    selection of k of them is a valid top-k."""
+    for b in seqs:
+        d.w[b] = 0.0
+        d.t["w"][b] = 0.0
+    return d
+
+
+def test_cluster_topk_ragged_batch32():
+    # a plan for 32 sequences of up to 32768 tokens takes the top-k inside the
+    # logits launch (clusters of 4 CTAs): n_c <= k, empty CTAs of a cluster,
+    # ragged last tiles, and all-equal rows (zero weights)
+    ctx = np.array([3, 4, 100, 2048, 2052, 5000, 32768, 8195, 20000, 4097, 131, 600] * 3, np.int32)[:32]
+    d = _with_zero_weights(make_decode_inputs(4, 32, ctx, 8, 64, 512, seed=31, with_comp=False), [7, 9, 30])
+    plan = B.Plan(B.C4A, d.n_heads, d.batch, d.topk, 32768, idx_heads=d.idx_heads)
+    assert plan.info()["launches_indexer"] == 1
+    idx, ln = run_indexer(d, max_ctx=32768)
+    assert list(ln) == [min(512, int(c) // 4) for c in ctx]
+    check_all(d, idx, ln)
+
+
+def test_cluster_topk_eight_ctas():
+    # 19 sequences of up to 8192 tokens: clusters of 8 CTAs of 2 tiles each
+    ctx = np.array([8192, 8000, 7777, 4096, 4100, 257, 1, 0, 6000, 8192, 5555, 3000, 2049, 1024, 999, 8190,
+                    7000, 6500, 12], np.int32)
+    d = _with_zero_weights(make_decode_inputs(4, 19, ctx, 8, 32, 256, seed=32, with_comp=False), [4])
+    plan = B.Plan(B.C4A, d.n_heads, d.batch, d.topk, 8192, idx_heads=d.idx_heads)
+    info = plan.info()
+    if info["idx_ctas_per_seq"] > 8:
+        pytest.skip("this GPU splits a sequence over more than 8 CTAs")
+    assert info["launches_indexer"] == 1
+    idx, ln = run_indexer(d, max_ctx=8192)
+    assert list(ln) == [min(256, int(c) // 4) for c in ctx]
+    check_all(d, idx, ln)
+
+
 def test_plan_max_ctx_larger_than_batch_contexts():
     ctx = np.array([1000, 4001, 16], np.int32)
     d = make_decode_inputs(4, 3, ctx, 8, 16, 128, seed=22, with_comp=False)
