@@ -261,6 +261,9 @@ template <int RATIO>
 __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched behind the previous kernel of the stream (programmatic
+    // dependent launch): its outputs may be this kernel's inputs
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
         compress_token<kHead, RATIO, false, true>(Pm, blockIdx.x);
     else if (threadIdx.x < kIdx / 2)
@@ -401,12 +404,21 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     if (!main_args->one_token_per_seq || !idx_args->one_token_per_seq) return DSV4_ERR_INVALID;
     const int n = Pm.num_tokens + Pi.num_tokens;
     if (n == 0) return DSV4_OK;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (main_args->ratio == 4)
-        compress_pair_kernel<4><<<n, kHead / 2, 0, st>>>(Pm, Pi);
-    else
-        compress_pair_kernel<128><<<n, kHead / 2, 0, st>>>(Pm, Pi);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    // programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel drains; they wait for it before reading anything
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n, 1, 1);
+    cfg.blockDim = dim3(kHead / 2, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = main_args->ratio == 4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4>, Pm, Pi)
+                                                : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128>, Pm, Pi);
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
 extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, dsv4_stream_t stream)
