@@ -285,62 +285,100 @@ class GpuBench:
 
 
 def make_pinned_inputs(bench):
-    """Host (pinned) copies of every per-step input, for the end-to-end run."""
+    """Host (pinned) inputs of every (layer, position) step, each step's seven
+    tensors packed in one block (one copy per step), with the byte offsets."""
+    names = ["kv_main", "kv_idx", "q", "qi", "wts", "pos", "ctx"]
+    def step_tensors(L, j):
+        return dict(kv_main=L.kv_main[j], kv_idx=L.kv_idx[j], q=L.q[j], qi=L.qi[j], wts=L.wts[j],
+                    pos=bench.pos[j], ctx=bench.ctx[j])
+    t0 = step_tensors(bench.layers[0], 0)
+    layout, off = {}, 0
+    for n in names:
+        nbytes = t0[n].numel() * t0[n].element_size()
+        layout[n] = (off, t0[n].dtype, tuple(t0[n].shape))
+        off += (nbytes + 255) // 256 * 256
+    total = off
     host = []
     for r in range(bench.R):
-        L = bench.layers[r]
         per = []
         for j in range(bench.P):
-            per.append(dict(kv_main=L.kv_main[j].cpu().pin_memory(), kv_idx=L.kv_idx[j].cpu().pin_memory(),
-                            q=L.q[j].cpu().pin_memory(), qi=L.qi[j].cpu().pin_memory(),
-                            wts=L.wts[j].cpu().pin_memory(), pos=bench.pos[j].cpu().pin_memory(),
-                            ctx=bench.ctx[j].cpu().pin_memory()))
+            blk = torch.empty(total, dtype=torch.uint8).pin_memory()
+            for n, t in step_tensors(bench.layers[r], j).items():
+                o, _, _ = layout[n]
+                raw = t.contiguous().view(torch.uint8).reshape(-1).cpu()
+                blk[o:o + raw.numel()].copy_(raw)
+            per.append(blk)
         host.append(per)
+    h2d = sum(t0[n].numel() * t0[n].element_size() for n in names)
     out_host = torch.empty((bench.w["batch"], bench.w["n_heads"], 512), dtype=torch.bfloat16).pin_memory()
     lse_host = torch.empty((bench.w["batch"], bench.w["n_heads"]), dtype=torch.float32).pin_memory()
-    return host, out_host, lse_host
+    return host, layout, total, h2d, out_host, lse_host
 
 
 def run_e2e(bench, steps, warmup):
     """The same steps through the public API with host buffers: every step copies
-    its inputs host->device and its output device->host inside the timed region."""
+    its inputs host->device and its output device->host inside the timed region.
+    As in a serving loop the copies run on their own streams, overlapped with the
+    previous step's kernels: a step's inputs go to one of two device blocks, its
+    kernels wait for them, and its output is read back once its kernels end."""
     Bd = bench.Bd
-    host, out_host, lse_host = make_pinned_inputs(bench)
-    Bsz, H, HI = bench.w["batch"], bench.w["n_heads"], bench.w["idx_heads"]
-    d_kv_main = torch.empty((Bsz, 4 * 576), dtype=torch.bfloat16, device=bench.device)
-    d_kv_idx = torch.empty((Bsz, 4 * 128), dtype=torch.bfloat16, device=bench.device)
-    d_q = torch.empty((Bsz, H, 576), dtype=torch.bfloat16, device=bench.device)
-    d_qi = torch.empty((Bsz, HI, 128), dtype=torch.uint8, device=bench.device)
-    d_w = torch.empty((Bsz, HI), dtype=torch.float32, device=bench.device)
-    d_pos = torch.empty((Bsz,), dtype=torch.int32, device=bench.device)
-    d_ctx = torch.empty((Bsz,), dtype=torch.int32, device=bench.device)
-    h2d = sum(t.numel() * t.element_size() for t in host[0][0].values())
+    host, layout, total, h2d, out_host, lse_host = make_pinned_inputs(bench)
+    Bsz = bench.w["batch"]
+    dblk = [torch.empty(total, dtype=torch.uint8, device=bench.device) for _ in range(2)]
+
+    def views(blk):
+        v = {}
+        for n, (o, dt, shp) in layout.items():
+            nbytes = int(torch.Size(shp).numel()) * torch.empty((), dtype=dt).element_size()
+            v[n] = blk[o:o + nbytes].view(dt).view(shp)
+        return v
+    dv = [views(b) for b in dblk]
     d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
+    s_in = torch.cuda.Stream(bench.device)
+    s_out = torch.cuda.Stream(bench.device)
 
     def steps_fn(n):
-        for r, j in bench.step_order(n):
-            L, hin = bench.layers[r], host[r][j]
-            d_kv_main.copy_(hin["kv_main"], non_blocking=True)
-            d_kv_idx.copy_(hin["kv_idx"], non_blocking=True)
-            d_q.copy_(hin["q"], non_blocking=True)
-            d_qi.copy_(hin["qi"], non_blocking=True)
-            d_w.copy_(hin["wts"], non_blocking=True)
-            d_pos.copy_(hin["pos"], non_blocking=True)
-            d_ctx.copy_(hin["ctx"], non_blocking=True)
+        s_c = torch.cuda.current_stream(bench.device)   # the kernels' stream (the capture stream in a capture)
+        s_in.wait_stream(s_c)
+        s_out.wait_stream(s_c)
+        read_done = [None, None]            # per device block: its last step's kernels
+        out_read = {}                       # per layer instance: its last read-back
+        for i, (r, j) in enumerate(bench.step_order(n)):
+            L, b = bench.layers[r], i % 2
+            with torch.cuda.stream(s_in):
+                if read_done[b] is not None:
+                    s_in.wait_event(read_done[b])
+                dblk[b].copy_(host[r][j], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_c.wait_event(ev_in)
+            if r in out_read:
+                s_c.wait_event(out_read[r])
+            d = dv[b]
             Bd.compress_insert_pair(
-                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=d_kv_main, positions=d_pos, seqs=L.seqs,
+                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=d["kv_main"], positions=d["pos"], seqs=L.seqs,
                      ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=bench.cos_sin,
                      state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=bench.status),
-                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=d_kv_idx, positions=d_pos, seqs=L.seqs,
+                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=d["kv_idx"], positions=d["pos"], seqs=L.seqs,
                      ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=bench.cos_sin,
                      state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=bench.status))
-            Bd.indexer_topk(bench.plan, d_qi, d_w, L.idx, L.idx_bt, d_ctx, bench.topk_idx, bench.topk_len,
-                            bench.ws, bench.status)
-            Bd.sparse_mla_decode(bench.plan, d_q, L.swa, L.swa_bt, d_ctx, L.out, bench.ws, comp_cache=L.comp,
+            Bd.indexer_topk(bench.plan, d["qi"], d["wts"], L.idx, L.idx_bt, d["ctx"], bench.topk_idx,
+                            bench.topk_len, bench.ws, bench.status)
+            Bd.sparse_mla_decode(bench.plan, d["q"], L.swa, L.swa_bt, d["ctx"], L.out, bench.ws, comp_cache=L.comp,
                                  comp_block_table=L.comp_bt, topk_idx=bench.topk_idx, topk_len=bench.topk_len,
                                  lse=L.lse, status=bench.status)
-            out_host.copy_(L.out, non_blocking=True)
-            lse_host.copy_(L.lse, non_blocking=True)
+            ev_c = torch.cuda.Event()
+            ev_c.record(s_c)
+            read_done[b] = ev_c
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c)
+                out_host.copy_(L.out, non_blocking=True)
+                lse_host.copy_(L.lse, non_blocking=True)
+                ev_o = torch.cuda.Event()
+                ev_o.record(s_out)
+            out_read[r] = ev_o
+        s_c.wait_stream(s_in)
+        s_c.wait_stream(s_out)
 
     steps_fn(warmup)
     torch.cuda.synchronize()
