@@ -89,6 +89,7 @@ constexpr int kTcSmem = kOffMisc + kMiscBytes + 1024;      // + alignment slack 
 // fp32 [64][2] running max and sum; receive slots [C], send slots [C], merge
 // weights [8][64] and 1 / L [64]
 constexpr int kOffRecv = 0;
+constexpr int kEpiParts = 4;                               // a slice moves in 4 parts (by dim), merged as they land
 constexpr int kOffSend = 64 * kV * 2 + 8 * 512;
 constexpr int kOffWeights = 2 * kOffSend;
 static_assert(kOffWeights + 9 * 64 * 4 <= kOffMisc, "epilogue buffers fit in the Q / K space");
@@ -217,9 +218,10 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint64_t* p_full = bars + 6;       // [2] softmax (4 warps) -> MMA: P written, S read, O^T corrected
     uint64_t* q_full = bars + 8;
     uint64_t* sync4 = bars + 9;        // [2] the four softmax warps meet once per tile
-    uint64_t* recv_full = bars + 11;   // epilogue: the C - 1 peer slices have landed (bytes)
+    uint64_t* recv_ml = bars + 11;     // epilogue: the C - 1 peers' running max and sum have landed (bytes)
     uint64_t* pv_done = bars + 12;     // [kTcMaxTiles] PV(u) complete (one phase each)
-    float* sm_m = reinterpret_cast<float*>(bars + 13 + kTcMaxTiles);   // [64] running max (log2 domain)
+    uint64_t* recv_part = bars + 13 + kTcMaxTiles;                // [kEpiParts] epilogue: part p of the peer slices
+    float* sm_m = reinterpret_cast<float*>(recv_part + kEpiParts); // [64] running max (log2 domain)
     float* sm_l = sm_m + 64;                              // [64] running sum
     float* sm_alpha = sm_l + 64;                          // [2][64] correction factors (by tile parity)
     int* sm_any = reinterpret_cast<int*>(sm_alpha + 128); // [2][4]
@@ -271,7 +273,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int i = 0; i < kTcMaxTiles; ++i) tc::mbar_init(tc::smem_u32(&pv_done[i]), 1);
         tc::mbar_init(tc::smem_u32(bt_ready), kTcProdWarps);
         tc::mbar_init(tc::smem_u32(q_full), 1);
-        tc::mbar_init(tc::smem_u32(recv_full), 1);
+        tc::mbar_init(tc::smem_u32(recv_ml), 1);
+        for (int i = 0; i < kEpiParts; ++i) tc::mbar_init(tc::smem_u32(&recv_part[i]), 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -610,8 +613,12 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     uint8_t* recv = smem + kOffRecv;                        // [C] slices from every CTA (own one written here)
     uint8_t* send = smem + kOffSend;                        // [C] slices for the peers
     float* mw = reinterpret_cast<float*>(smem + kOffWeights);   // [8][64] weights, then [64] 1 / L
-    if (threadIdx.x == 0)
-        tc::mbar_arrive_expect_tx(tc::smem_u32(recv_full), static_cast<uint32_t>((C - 1) * slice));
+    const int DP = DS / kEpiParts;                          // dims of one part
+    if (threadIdx.x == 0) {
+        tc::mbar_arrive_expect_tx(tc::smem_u32(recv_ml), static_cast<uint32_t>((C - 1) * 512));
+        for (int i = 0; i < kEpiParts; ++i)
+            tc::mbar_arrive_expect_tx(tc::smem_u32(&recv_part[i]), static_cast<uint32_t>((C - 1) * DP * 128));
+    }
     __syncwarp();
     tc::cluster_arrive_release();
     // 2. stage: O^T dim d (TMEM lane) belongs to CTA d / DS; the unnormalised
@@ -654,73 +661,89 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     tc::fence_proxy_async_smem();
     __syncthreads();
-    // 3. one bulk copy per peer, once every peer is past its main loop
+    // 3. per peer: the running max and sum first, then the parts in order,
+    // once every peer is past its main loop
     tc::cluster_wait_acquire();
     if (threadIdx.x < C && threadIdx.x != rank) {
         const int q = threadIdx.x;
-        tc::bulk_s2s(tc::map_to_rank(tc::smem_u32(recv + rank * slice), q), tc::smem_u32(send + q * slice),
-                     static_cast<uint32_t>(slice), tc::map_to_rank(tc::smem_u32(recv_full), q));
+        const uint32_t dst = tc::map_to_rank(tc::smem_u32(recv + rank * slice), q);
+        const uint32_t src = tc::smem_u32(send + q * slice);
+        tc::bulk_s2s(dst + DS * 128, src + DS * 128, 512u, tc::map_to_rank(tc::smem_u32(recv_ml), q));
+        for (int i = 0; i < kEpiParts; ++i)
+            tc::bulk_s2s(dst + i * DP * 128, src + i * DP * 128, static_cast<uint32_t>(DP * 128),
+                         tc::map_to_rank(tc::smem_u32(&recv_part[i]), q));
     }
-    // 4. combine this CTA's slice (bounded wait, also after an abort)
-    const bool got = tc::mbar_wait_cluster(tc::smem_u32(recv_full), 0, P.status);
-    __syncwarp();
-    tc::cluster_arrive_release();                           // the peers' copies into this CTA have landed
-    if (threadIdx.x < 64) {
-        const int hh = threadIdx.x;
-        float mq[8], lq[8];
-        float M = -INFINITY;
+    // 4. warps 0-7 merge heads 8w .. 8w + 7 of this CTA's slice, part by part as
+    // the parts land (bounded waits, also after an abort); the others only
+    // wait for every part
+    bool got = tc::mbar_wait_cluster(tc::smem_u32(recv_ml), 0, P.status);
+    if (warp < 8) {
+        const int hc = warp;
+        if (got && lane < 8) {
+            const int hh = 8 * hc + lane;
+            float mq[8], lq[8];
+            float M = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            mq[q] = -INFINITY;
-            lq[q] = 0.f;
-            if (q < C) {
-                const float2 ml = *reinterpret_cast<const float2*>(recv + q * slice + DS * 128 + hh * 8);
-                mq[q] = ml.x;
-                lq[q] = ml.y;
+            for (int q = 0; q < 8; ++q) {
+                mq[q] = -INFINITY;
+                lq[q] = 0.f;
+                if (q < C) {
+                    const float2 ml = *reinterpret_cast<const float2*>(recv + q * slice + DS * 128 + hh * 8);
+                    mq[q] = ml.x;
+                    lq[q] = ml.y;
+                }
+                M = fmaxf(M, mq[q]);
             }
-            M = fmaxf(M, mq[q]);
-        }
-        float L = 0.f;
+            float L = 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (q < C) {
-                const float wq = (mq[q] == -INFINITY) ? 0.f : ex2_approx(mq[q] - M);
-                mw[q * 64 + hh] = wq;
-                L += wq * lq[q];
-            }
-        }
-        mw[8 * 64 + hh] = L > 0.f ? 1.0f / L : 0.f;
-        if (rank == 0 && hh < nh && P.lse)
-            P.lse[static_cast<long long>(b) * P.H + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    if (got) {
-        // item = (dim, 8 heads): consecutive threads take consecutive dims
-        for (int it = threadIdx.x; it < DS * 8; it += kTcThreads) {
-            const int dl = it % DS, hc = it / DS;
-            float acc[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-#pragma unroll 1
-            for (int q = 0; q < C; ++q) {
-                const uint4 x = *reinterpret_cast<const uint4*>(recv + q * slice + dl * 128 + ((hc ^ (dl & 7)) << 4));
-                const float4 w0 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc);
-                const float4 w1 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc + 4);
-                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    acc[2 * c] += wv[2 * c] * __uint_as_float(xw[c] << 16);
-                    acc[2 * c + 1] += wv[2 * c + 1] * __uint_as_float(xw[c] & 0xffff0000u);
+            for (int q = 0; q < 8; ++q) {
+                if (q < C) {
+                    const float wq = (mq[q] == -INFINITY) ? 0.f : ex2_approx(mq[q] - M);
+                    mw[q * 64 + hh] = wq;
+                    L += wq * lq[q];
                 }
             }
-            uint16_t* o = P.out + (static_cast<long long>(b) * P.H + h0 + 8 * hc) * kV + rank * DS + dl;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                if (8 * hc + c < nh) o[c * kV] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * mw[8 * 64 + 8 * hc + c]));
+            mw[8 * 64 + hh] = L > 0.f ? 1.0f / L : 0.f;
+            if (rank == 0 && hh < nh && P.lse)
+                P.lse[static_cast<long long>(b) * P.H + h0 + hh] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
         }
+        __syncwarp();
+        float il[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) il[c] = mw[8 * 64 + 8 * hc + c];
+        uint16_t* ob = P.out + (static_cast<long long>(b) * P.H + h0 + 8 * hc) * kV + rank * DS;
+        for (int i = 0; got && i < kEpiParts; ++i) {
+            got = tc::mbar_wait_cluster(tc::smem_u32(&recv_part[i]), 0, P.status);
+            if (!got) break;
+            for (int dl = i * DP + lane; dl < (i + 1) * DP; dl += 32) {
+                float acc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (q < C) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(recv + q * slice + dl * 128 + ((hc ^ (dl & 7)) << 4));
+                        const float4 w0 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc);
+                        const float4 w1 = *reinterpret_cast<const float4*>(mw + q * 64 + 8 * hc + 4);
+                        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            acc[2 * c] += wv[2 * c] * __uint_as_float(xw[c] << 16);
+                            acc[2 * c + 1] += wv[2 * c + 1] * __uint_as_float(xw[c] & 0xffff0000u);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (8 * hc + c < nh) ob[c * kV + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * il[c]));
+            }
+        }
+    } else {
+        for (int i = 0; got && i < kEpiParts; ++i) got = tc::mbar_wait_cluster(tc::smem_u32(&recv_part[i]), 0, P.status);
     }
+    __syncwarp();
+    tc::cluster_arrive_release();                           // the peers' copies into this CTA have landed
     __syncwarp();
     tc::cluster_wait_acquire();                             // every peer has received this CTA's copies
     if (warp == kTcMmaWarp) {
