@@ -620,7 +620,10 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc::mbar_arrive_expect_tx(tc::smem_u32(&recv_part[i]), static_cast<uint32_t>((C - 1) * DP * 128));
     }
     __syncwarp();
-    tc::cluster_arrive_release();
+    // ready to receive: every earlier access to the receive space has
+    // completed (the last MMA reads were observed through pv_done), so the
+    // arrival publishes nothing
+    tc::cluster_arrive_relaxed();
     // 2. stage: O^T dim d (TMEM lane) belongs to CTA d / DS; the unnormalised
     // partial is rounded to bf16 (half the distributed shared memory traffic)
     const bool have = n_tiles > 0 && !*abort_flag;
@@ -676,7 +679,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // 4. warps 0-7 merge heads 8w .. 8w + 7 of this CTA's slice, part by part as
     // the parts land (bounded waits, also after an abort); the others only
     // wait for every part
-    bool got = tc::mbar_wait_cluster(tc::smem_u32(recv_ml), 0, P.status);
+    // (wait results are made warp-uniform: the cluster arrivals are per warp)
+    bool got = __all_sync(0xffffffffu, tc::mbar_wait_cluster(tc::smem_u32(recv_ml), 0, P.status));
     if (warp < 8) {
         const int hc = warp;
         if (got && lane < 8) {
@@ -712,9 +716,15 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
         for (int c = 0; c < 8; ++c) il[c] = mw[8 * 64 + 8 * hc + c];
         uint16_t* ob = P.out + (static_cast<long long>(b) * P.H + h0 + 8 * hc) * kV + rank * DS;
+        bool arrived = false;
         for (int i = 0; got && i < kEpiParts; ++i) {
-            got = tc::mbar_wait_cluster(tc::smem_u32(&recv_part[i]), 0, P.status);
+            got = __all_sync(0xffffffffu, tc::mbar_wait_cluster(tc::smem_u32(&recv_part[i]), 0, P.status));
             if (!got) break;
+            if (i == kEpiParts - 1) {
+                __syncwarp();
+                tc::cluster_arrive_relaxed();               // the peers' copies into this CTA have landed
+                arrived = true;
+            }
             for (int dl = i * DP + lane; dl < (i + 1) * DP; dl += 32) {
                 float acc[8];
 #pragma unroll
@@ -739,11 +749,13 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (8 * hc + c < nh) ob[c * kV + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[c] * il[c]));
             }
         }
+        __syncwarp();
+        if (!arrived) tc::cluster_arrive_relaxed();         // after a failed wait
     } else {
         for (int i = 0; got && i < kEpiParts; ++i) got = tc::mbar_wait_cluster(tc::smem_u32(&recv_part[i]), 0, P.status);
+        __syncwarp();
+        tc::cluster_arrive_relaxed();
     }
-    __syncwarp();
-    tc::cluster_arrive_release();                           // the peers' copies into this CTA have landed
     __syncwarp();
     tc::cluster_wait_acquire();                             // every peer has received this CTA's copies
     if (warp == kTcMmaWarp) {
