@@ -46,21 +46,27 @@ constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * 
 // largest key is taken whole or is one key; keys equal to the threshold taken
 // lowest slot first; slots written in ascending order), here with 8-bit
 // digits and every count summed over the cluster: each CTA pushes its counts
-// into every CTA's shared memory (distributed shared memory stores) before a
-// cluster barrier, after which each CTA reads them locally and takes the same
-// decisions as the others.
+// into every CTA's shared memory (asynchronous distributed shared memory
+// stores that count their bytes on the receiving CTA's mbarrier), so a CTA
+// waits only for the bytes it needs, reads them locally and takes the same
+// decisions as the others -- no cluster-wide barrier.  A buffer that pass p
+// fills is filled again in pass p + 2, which no CTA reaches before every CTA
+// has pushed its pass p + 1 counts, i.e. finished reading pass p.
 // ---------------------------------------------------------------------------
 constexpr int kCtkSlots = 16 * kIdxTileSlots;                        // slots per CTA at most
 constexpr int kCtkPer = (kCtkSlots + kIdxThreads - 1) / kIdxThreads;   // slots per thread (6)
 constexpr int kCtkMaxCluster = 8;
 struct CtkScratch {
+    uint64_t bar_mm;                        // every CTA's (min, max) has landed (bytes)
+    uint64_t bar_h[2];                      // every CTA's histogram of the pass has landed, by pass parity
+    uint64_t bar_cnt;                       // every CTA's compaction counts have landed
     uint32_t mm_in[kCtkMaxCluster][2];      // (min, max) key of CTA q's slots, pushed by q
     int cnt_in[kCtkMaxCluster][2];          // CTA q's keys above / at the threshold, pushed by q
     int hin[2][kCtkMaxCluster][256];        // CTA q's digit histogram, by pass parity, pushed by q
-    int hist[256];                          // this CTA's histogram of the current pass
+    int hist[2][256];                       // this CTA's histogram, by pass parity
     uint32_t mm[2];                         // this CTA's min, max
     uint32_t prefix;                        // the decisions, for the CTA's threads
-    int rem, lo, done;
+    int rem, done, decided, failed;
     int scan[16];
 };
 constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
@@ -92,13 +98,14 @@ __device__ __forceinline__ int ctk_excl_scan(int v, int* scan, int& total)
 
 // Called by every thread of every CTA of the cluster once the CTA's logits
 // are in lg[0, s1 - s0), and after the cluster arrival that the kernel made
-// when it started (this function waits for it before its first push).
-// Writes the row's k slots (or, with at most k slots, all of them and -1
-// past) and its length.
+// when it started, with the scratch barriers initialised (this function waits
+// for it before its first push).  Writes the row's k slots (or, with at most k
+// slots, all of them and -1 past) and its length.  A wait that times out
+// flags `status` and leaves the row unwritten.
 __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, int C, int rank, int* orow,
-                             int* out_len, CtkScratch* S)
+                             int* out_len, CtkScratch* S, int* status)
 {
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     tc::cluster_wait_acquire();                      // every CTA of the cluster has started
     if (n_c <= k) {
         for (int s = s0 + tid; s < s1; s += kIdxThreads) orow[s] = s;
@@ -129,10 +136,22 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
         atomicMin(&S->mm[0], mn);
         atomicMax(&S->mm[1], mx);
     }
+    if (tid < 256) {
+        S->hist[0][tid] = 0;
+        S->hist[1][tid] = 0;
+    }
     __syncthreads();
-    if (tid < C) tc::st_cluster_u32x2(tc::map_to_rank(tc::smem_u32(&S->mm_in[rank][0]), tid), S->mm[0], S->mm[1]);
-    tc::cluster_arrive_release();                    // (a) min / max pushed
-    tc::cluster_wait_acquire();
+    // (a) every CTA's min / max, in every CTA
+    if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&S->bar_mm), static_cast<uint32_t>(C * 8));
+    if (tid < C)
+        tc::st_async_u32x2(tc::map_to_rank(tc::smem_u32(&S->mm_in[rank][0]), tid), S->mm[0], S->mm[1],
+                           tc::map_to_rank(tc::smem_u32(&S->bar_mm), tid));
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_mm), 0, status);
+        if (lane == 0 && !ok) S->failed = 1;
+    }
+    __syncthreads();
+    if (S->failed) return;
     uint32_t base = 0xffffffffu, top = 0u;
     for (int q = 0; q < C; ++q) {
         base = min(base, S->mm_in[q][0]);
@@ -148,33 +167,60 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
     int rem = k;
     for (int pass = 0;; ++pass) {
         const int p = pass & 1;
-        if (tid < 256) S->hist[tid] = 0;
-        __syncthreads();
 #pragma unroll
         for (int j = 0; j < kCtkPer; ++j) {
             const uint32_t o = key[j] - base;
-            if (j < nv && (plo == 32 || (o >> plo) == (prefix >> plo))) atomicAdd(&S->hist[(o >> lo) & 255u], 1);
+            if (j < nv && (plo == 32 || (o >> plo) == (prefix >> plo))) atomicAdd(&S->hist[p][(o >> lo) & 255u], 1);
         }
         __syncthreads();
+        if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&S->bar_h[p]), static_cast<uint32_t>(C * 1024));
         if (tid < 64) {
-            const uint4 h4 = *reinterpret_cast<const uint4*>(&S->hist[4 * tid]);
+            const uint4 h4 = *reinterpret_cast<const uint4*>(&S->hist[p][4 * tid]);
             for (int q = 0; q < C; ++q)
-                tc::st_cluster_u32x4(tc::map_to_rank(tc::smem_u32(&S->hin[p][rank][4 * tid]), q), h4);
+                tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&S->hin[p][rank][4 * tid]), q), h4,
+                                   tc::map_to_rank(tc::smem_u32(&S->bar_h[p]), q));
         }
-        tc::cluster_arrive_release();                // (b) histograms pushed
-        tc::cluster_wait_acquire();
-        // digit 255 - tid, summed over the cluster, scanned from the top
-        int g = 0;
-        if (tid < 256)
-            for (int q = 0; q < C; ++q) g += S->hin[p][q][255 - tid];
-        int tot;
-        const int before = ctk_excl_scan(g, S->scan, tot);
-        if (tid < 256 && before < rem && rem <= before + g) {
-            S->prefix = prefix | (static_cast<uint32_t>(255 - tid) << lo);
-            S->rem = rem - before;
-            S->done = (lo == 0) || (g == rem - before);
+        if (tid < 256) S->hist[p ^ 1][tid] = 0;          // for the next pass (its last reader was the pass before)
+        if (warp == 0) {
+            // lane: digits 8 lane .. 8 lane + 7, summed over the cluster; the bin
+            // of the rem-th largest key among those still in play
+            const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_h[p]), (pass >> 1) & 1, status);
+            int g[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = 0;
+            if (ok) {
+                for (int q = 0; q < C; ++q) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(&S->hin[p][q][8 * lane]);
+                    const uint4 c = *reinterpret_cast<const uint4*>(&S->hin[p][q][8 * lane + 4]);
+                    g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
+                    g[4] += c.x; g[5] += c.y; g[6] += c.z; g[7] += c.w;
+                }
+            }
+            int tl = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tl += g[j];
+            int x = tl;                                      // keys in the digits from 8 lane up
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, x, o);
+                if (lane + o < 32) x += y;
+            }
+            int above = x - tl;                              // keys in the digits above this lane's
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                if (above < rem && rem <= above + g[j]) {
+                    S->prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << lo);
+                    S->rem = rem - above;
+                    S->done = (lo == 0) || (g[j] == rem - above);
+                    S->decided = pass + 1;
+                }
+                above += g[j];
+            }
+            __syncwarp();
+            if (lane == 0 && (!ok || S->decided != pass + 1)) S->failed = 1;
         }
         __syncthreads();
+        if (S->failed) return;
         prefix = S->prefix;
         rem = S->rem;
         plo = lo;
@@ -193,9 +239,17 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
     }
     int tot;
     const int before = ctk_excl_scan((gtn << 16) | eqn, S->scan, tot);   // counts < 2^16
-    if (tid < C) tc::st_cluster_u32x2(tc::map_to_rank(tc::smem_u32(&S->cnt_in[rank][0]), tid), tot >> 16, tot & 0xffff);
-    tc::cluster_arrive_release();                    // (c) counts pushed
-    tc::cluster_wait_acquire();
+    // (c) every CTA's counts, in every CTA
+    if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&S->bar_cnt), static_cast<uint32_t>(C * 8));
+    if (tid < C)
+        tc::st_async_u32x2(tc::map_to_rank(tc::smem_u32(&S->cnt_in[rank][0]), tid), static_cast<uint32_t>(tot >> 16),
+                           static_cast<uint32_t>(tot & 0xffff), tc::map_to_rank(tc::smem_u32(&S->bar_cnt), tid));
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_cnt), 0, status);
+        if (lane == 0 && !ok) S->failed = 1;
+    }
+    __syncthreads();
+    if (S->failed) return;
     int gpos = before >> 16, epos = before & 0xffff;
     for (int q = 0; q < rank; ++q) {
         gpos += S->cnt_in[q][0];
@@ -284,6 +338,13 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
         }
         tc::mbar_init(tc::smem_u32(q_bar), 1);
+        if (kFused) {
+            // the top-k's, which the other CTAs of the cluster complete
+            tc::mbar_init(tc::smem_u32(&ctk->bar_mm), 1);
+            tc::mbar_init(tc::smem_u32(&ctk->bar_h[0]), 1);
+            tc::mbar_init(tc::smem_u32(&ctk->bar_h[1]), 1);
+            tc::mbar_init(tc::smem_u32(&ctk->bar_cnt), 1);
+        }
         *abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -291,6 +352,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (kFused && threadIdx.x == 0) {
         ctk->mm[0] = 0xffffffffu;
         ctk->mm[1] = 0u;
+        ctk->failed = 0;
+        ctk->decided = 0;
     }
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), kIdxTmemCols);
@@ -451,7 +514,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (kFused)
         cluster_topk(lg_s, t_begin * kIdxTileSlots, min(t_end * kIdxTileSlots, n_c), n_c, P.k, static_cast<int>(gridDim.x),
                      static_cast<int>(blockIdx.x), P.out_idx + static_cast<long long>(b) * P.out_stride,
-                     P.out_len + b, ctk);
+                     P.out_len + b, ctk, P.status);
 }
 
 // ---------------------------------------------------------------------------

@@ -354,6 +354,20 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uin
                  : "memory");
 }
 
+__device__ __forceinline__ void st_async_u32x4(uint32_t addr, uint4 v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_u32x2(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr), "r"(a), "r"(b), "r"(bar)
+                 : "memory");
+}
+
 // Bulk copy from this CTA's shared memory into (another) CTA's shared memory
 // of the cluster; completion counted in bytes on the destination's mbarrier.
 __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster)
