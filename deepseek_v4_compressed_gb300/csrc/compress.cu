@@ -261,6 +261,15 @@ template <int RATIO>
 __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the indexer of this layer, launched next, starts by reading the
+    // sequence's indexer block-table row (a caller input): warm it in L2
+    if (static_cast<int>(blockIdx.x) >= Pm.num_tokens && threadIdx.x < 32) {
+        const int t = blockIdx.x - Pm.num_tokens;
+        const int b = t < Pi.num_tokens ? __ldg(Pi.seqs + t) : -1;
+        if (b >= 0 && b < Pi.num_seqs && static_cast<int>(threadIdx.x) * 32 < Pi.bt_stride)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(Pi.bt + static_cast<long long>(b) * Pi.bt_stride +
+                                                          threadIdx.x * 32));
+    }
     // launched behind the previous kernel of the stream (programmatic
     // dependent launch): its outputs may be this kernel's inputs
     asm volatile("griddepcontrol.wait;" ::: "memory");
