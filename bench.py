@@ -73,6 +73,12 @@ def max_over_ranks(x: float, device="cpu") -> float:
     return float(t.item())
 
 
+def job_value(world: int, batch: int, steps: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every rank decodes `batch` sequences per step for
+    `steps` steps (weak scaling), over the slowest rank's time."""
+    return world * batch * steps / (ms_max / 1e3)
+
+
 # ----------------------------------------------------------------------------
 # algorithmic bytes (what the method must move per layer-step)
 # ----------------------------------------------------------------------------
@@ -612,7 +618,7 @@ def main():
     ctx_avg = w["context"] - (bench.P - 1) / 2.0
     ab = algorithmic_bytes(w, int(ctx_avg))
     B = w["batch"]
-    value = world * B * K / (ms / 1e3)
+    value = job_value(world, B, K, ms)
     peak, peak_kind = load_peaks()
     # roofline of the dominant kernel: the sparse MLA decode kernel, the
     # stage with the largest time (each stage is one kernel at this workload:
@@ -643,7 +649,7 @@ def main():
         "achieved_gbs_whole_step": ab["total"] / (ms / K / 1e3) / 1e9,
         "gpu_launches": K * bench.launches_per_step,
         "clocks": clk,
-        "e2e": {"value": world * B * K / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(world, B, K, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
