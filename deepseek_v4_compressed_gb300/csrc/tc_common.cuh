@@ -57,20 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking probe of a phase (no suspension).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // try_wait with acquire at cluster scope: pairs with remote release arrivals.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
@@ -137,24 +123,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
-
-// Plain (non-tensor) bulk copy global -> shared, completing on an mbarrier.
-// Both addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared (L2 only), tracked by commit groups.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
 {
@@ -297,18 +265,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Split cluster barrier: every thread of every CTA arrives (release), and
-// later waits (acquire) for all arrivals of the phase.
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -320,40 +276,9 @@ __device__ __forceinline__ void cluster_arrive_relaxed()
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32x2(uint32_t addr, uint32_t a, uint32_t b)
-{
-    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32x4(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
 // Asynchronous store into (possibly another CTA's) shared memory; completion
 // is counted in bytes on the destination CTA's mbarrier `bar` (both addresses
 // are shared::cluster addresses of the destination CTA).
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-                 ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
-                 ::"r"(addr), "f"(a), "f"(b), "r"(bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ void st_async_u32x4(uint32_t addr, uint4 v, uint32_t bar)
 {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
@@ -377,59 +302,12 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
                  : "memory");
 }
 
-// Plain (weak) stores into another CTA's shared memory.
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v)
-{
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v2(uint32_t addr, float a, float b)
-{
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster()
-{
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank)
 {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
-}
-
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_sync(int id, int count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
