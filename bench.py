@@ -37,12 +37,21 @@ FALLBACK_HBM_GBS = 6800.0
 
 WORKLOAD = dict(name="c4a_32k_b32", batch=32, context=32768, n_heads=64, idx_heads=64, topk=512,
                 window=128, ratio=4)
+# the other workloads of the method's scope table, measured with --workload
+# (the headline line above is the default)
+WORKLOADS = {
+    "c4a_32k_b32": WORKLOAD,
+    "c128a_128k_b64": dict(name="c128a_128k_b64", batch=64, context=131072, n_heads=64, idx_heads=0, topk=512,
+                           window=128, ratio=128),
+    "c4a_1m_b4": dict(name="c4a_1m_b4", batch=4, context=1048576, n_heads=128, idx_heads=64, topk=2048,
+                      window=128, ratio=4),
+}
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture (profiles/mla_decode_tc_c4a_32k_b32_traffic.md), with the sha256 of
 # the sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
-    "sparse_mla": {"bytes_per_launch": 19088896 + 0, "src_sha": "fcae9cd0963efc99"},
+    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19088896 + 0, "src_sha": "fcae9cd0963efc99"},
 }
 
 
@@ -84,12 +93,18 @@ def job_value(world: int, batch: int, steps: int, ms_max: float) -> float:
 # ----------------------------------------------------------------------------
 def algorithmic_bytes(w, ctx):
     B, H, HI, k = w["batch"], w["n_heads"], w["idx_heads"], w["topk"]
+    mla = B * (k * 648 + 128 * 1152 + k * 4 + 4 + H * 576 * 2 + H * 512 * 2 + H * 4
+               + (k + 2) * 4)
+    if w["ratio"] == 128:
+        # main compressor only (ratio 128, no overlap): the token's kv/score row in,
+        # its state row out; at a boundary (1 token in 128) the 128 ring rows and
+        # the entry.  The indices are caller metadata, read by the attention.
+        comp_main = B * (1152 * 2 + 1152 * 4 + (128 * 1152 * 4 + 648) / 128)
+        return dict(compress=comp_main, indexer=0.0, mla=mla, total=comp_main + mla)
     n_c = ctx // 4
     comp_main = B * (2304 * 2 + 2304 * 4 + 0.25 * (7 * 1152 * 4 + 648))
     comp_idx = B * (512 * 2 + 512 * 4 + 0.25 * (7 * 256 * 4 + 132))
     indexer = B * (n_c * 132 + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
-    mla = B * (k * 648 + 128 * 1152 + k * 4 + 4 + H * 576 * 2 + H * 512 * 2 + H * 4
-               + (k + 2) * 4)
     return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla,
                 total=comp_main + comp_idx + indexer + mla)
 
@@ -221,6 +236,45 @@ def build_layers(B, w, n_layers, n_pos, device, seed=1):
     return layers
 
 
+def build_layers_c128a(w, n_layers, n_pos, device, seed=2):
+    """c128a layers: the main compressed cache (ratio 128) and its compressor
+    state, the SWA cache, and per position the caller's index metadata:
+    k sorted slots drawn uniformly without replacement from the n_c visible."""
+    from deepseek_v4_compressed_gb300 import binding as Bd
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    Bsz, H, k = w["batch"], w["n_heads"], w["topk"]
+    ctx_max = w["context"]
+    n_c_max = ctx_max // 128
+    comp_lp = (n_c_max + 63) // 64 + 1
+    swa_lp = (ctx_max + 63) // 64 + 1
+    seqs_all = torch.arange(Bsz, dtype=torch.int32, device=device)
+    layers = []
+    for li in range(n_layers):
+        L = LayerInstance()
+        L.comp_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
+        L.comp = torch.zeros(Bsz * comp_lp * Bd.MLA_PAGE_BYTES, dtype=torch.uint8, device=device)
+        for b in range(Bsz):
+            seq = torch.full((n_c_max,), b, dtype=torch.int32, device=device)
+            slot = torch.arange(n_c_max, dtype=torch.int32, device=device)
+            rows = torch.randn((n_c_max, 576), generator=g, device=device) / math.sqrt(576)
+            Bd.cache_insert_rows(Bd.CACHE_MLA, rows, seq, slot, L.comp, L.comp_bt)
+        phys = torch.randperm(Bsz * 4, generator=g, device=device).to(torch.int32).view(Bsz, 4)
+        L.swa_bt = phys[:, torch.arange(swa_lp, device=device) % 4].contiguous()
+        L.swa = (torch.randn((Bsz * 4 * 64, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+        L.state_main = torch.zeros((Bsz, 128, 1152), dtype=torch.float32, device=device)
+        L.ape_main = torch.randn((128, 576), generator=g, device=device) * 0.1
+        L.rms_main = torch.ones(576, device=device)
+        L.kv_main = [torch.randn((Bsz, 1152), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
+        L.q = [(torch.randn((Bsz, H, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+               for _ in range(n_pos)]
+        L.out = torch.empty((Bsz, H, 512), dtype=torch.bfloat16, device=device)
+        L.lse = torch.empty((Bsz, H), dtype=torch.float32, device=device)
+        L.seqs = seqs_all
+        layers.append(L)
+    return layers
+
+
 class GpuBench:
     def __init__(self, w, n_layers, n_pos, device):
         from deepseek_v4_compressed_gb300 import binding as Bd
@@ -230,10 +284,17 @@ class GpuBench:
         self.R = n_layers
         self.P = n_pos
         Bsz = w["batch"]
-        self.plan = Bd.Plan(Bd.C4A, w["n_heads"], Bsz, w["topk"], w["context"], idx_heads=w["idx_heads"],
-                            window=w["window"])
+        self.c128 = w["ratio"] == 128
+        if self.c128:
+            self.plan = Bd.Plan(Bd.C128A, w["n_heads"], Bsz, w["topk"], w["context"], window=w["window"])
+            self.layers = build_layers_c128a(w, n_layers, n_pos, device)
+            self.stage_names = ["compress", "sparse_mla"]
+        else:
+            self.plan = Bd.Plan(Bd.C4A, w["n_heads"], Bsz, w["topk"], w["context"], idx_heads=w["idx_heads"],
+                                window=w["window"])
+            self.layers = build_layers(Bd, w, n_layers, n_pos, device)
+            self.stage_names = ["compress", "indexer_topk", "sparse_mla"]
         self.ws = self.plan.workspace(device)
-        self.layers = build_layers(Bd, w, n_layers, n_pos, device)
         self.cos_sin = Bd.rope_table(w["context"] + 1).to(device)
         # positions: the last graph position is the context's last token
         p0 = w["context"] - n_pos
@@ -241,6 +302,16 @@ class GpuBench:
         self.ctx = [torch.full((Bsz,), p0 + j + 1, dtype=torch.int32, device=device) for j in range(n_pos)]
         self.topk_idx = torch.empty((Bsz, w["topk"]), dtype=torch.int32, device=device)
         self.topk_len = torch.empty((Bsz,), dtype=torch.int32, device=device)
+        if self.c128:
+            # the caller's metadata per position: k sorted slots of the n_c visible
+            gi = torch.Generator(device=device)
+            gi.manual_seed(3)
+            self.c128_idx = []
+            for j in range(n_pos):
+                n_c = (p0 + j + 1) // 128
+                sel = torch.argsort(torch.rand((Bsz, n_c), generator=gi, device=device), dim=1)[:, :w["topk"]]
+                self.c128_idx.append(torch.sort(sel, dim=1).values.to(torch.int32).contiguous())
+            self.topk_len.fill_(w["topk"])
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.info = self.plan.info()
         self.launches_per_step = 1 + self.info["launches_indexer"] + self.info["launches_mla"]
@@ -249,6 +320,16 @@ class GpuBench:
     def stage_calls(self, r, j):
         Bd, L = self.Bd, self.layers[r]
         Bsz = self.w["batch"]
+        if self.c128:
+            return [
+                lambda: Bd.compress_insert(Bd.CACHE_MLA, 128, L.kv_main[j], self.pos[j], L.seqs, L.ape_main,
+                                           L.rms_main, 1e-6, self.cos_sin, L.state_main, L.comp, L.comp_bt, Bsz,
+                                           status=self.status),
+                lambda: Bd.sparse_mla_decode(self.plan, L.q[j], L.swa, L.swa_bt, self.ctx[j], L.out, self.ws,
+                                             comp_cache=L.comp, comp_block_table=L.comp_bt,
+                                             topk_idx=self.c128_idx[j], topk_len=self.topk_len, lse=L.lse,
+                                             status=self.status),
+            ]
         return [
             lambda: Bd.compress_insert_pair(
                 dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=L.kv_main[j], positions=self.pos[j], seqs=L.seqs,
@@ -410,7 +491,7 @@ def stage_times(bench, n):
     launches over the rotated layer instances in one captured graph, timed
     with CUDA events around the replay (inside the full step, programmatic
     dependent launch overlaps the stages, so their sum exceeds a step)."""
-    names = ["compress", "indexer_topk", "sparse_mla"]
+    names = bench.stage_names
     out = {}
     for s, nm in enumerate(names):
         gr = torch.cuda.CUDAGraph()
@@ -563,9 +644,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sustain-s", type=float, default=1.0,
                     help="seconds of identical untimed load kept running for the clock sampler")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=WORKLOAD["name"],
+                    help="the headline workload (default) or another of the method's configurations; the "
+                         "others report no e2e, cpu_baseline or reference arm")
     args = ap.parse_args()
-    w = dict(WORKLOAD)
+    w = dict(WORKLOADS[args.workload])
+    headline = w["name"] == WORKLOAD["name"]
     if args.impl == "reference":
+        if not headline:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the headline "
+                              "workload only"}), flush=True)
+            return 0
         return reference_arm(args, w)
 
     rank, world, local = dist_env()
@@ -613,21 +702,28 @@ def main():
 
     stages = stage_times(bench, min(G, 64))
     bench.check_status()
-    e2e_ms, h2d, d2h = run_e2e(bench, K, W)
+    e2e = None
+    if w["ratio"] == 4:
+        e2e_ms, h2d, d2h = run_e2e(bench, K, W)
+        e2e = {"value": job_value(world, w["batch"], K, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
 
     ctx_avg = w["context"] - (bench.P - 1) / 2.0
     ab = algorithmic_bytes(w, int(ctx_avg))
     B = w["batch"]
     value = job_value(world, B, K, ms)
     peak, peak_kind = load_peaks()
-    # roofline of the dominant kernel: the sparse MLA decode kernel, the
-    # stage with the largest time (each stage is one kernel at this workload:
-    # the top-k runs inside the logits launch)
+    # roofline of the dominant kernel: the stage with the largest time (each
+    # stage is one kernel at the c4a workloads, where the top-k runs inside the
+    # logits launch when a sequence's CTAs fit one cluster)
     stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
-    dom = "sparse_mla"
+    kernels = {"compress": ("compress_pair_kernel / compress_kernel (dsv4_compress_insert)", "compress.cu"),
+               "indexer_topk": ("indexer_logits_tc (dsv4_indexer_topk)", "indexer.cu"),
+               "sparse_mla": ("mla_decode_tc (dsv4_sparse_mla_decode)", "mla.cu")}
+    dom = max(bench.stage_names, key=lambda nm: stages[nm])
     achieved = stage_bytes[dom] / (stages[dom] / 1e3) / 1e9
-    srcs = ["deepseek_v4_compressed_gb300/csrc/mla.cu"]
-    rec = TRAFFIC_RECORD.get(dom)
+    srcs = ["deepseek_v4_compressed_gb300/csrc/" + kernels[dom][1]]
+    rec = TRAFFIC_RECORD.get((w["name"], dom))
     traffic = rec["bytes_per_launch"] if rec and rec["src_sha"] == src_digest(srcs) else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -640,7 +736,7 @@ def main():
                          "visits of one layer)" % (bench.R, bench.R * ab["total"] / 1e6),
                    "timing": "CUDA graph replay of the K steps, CUDA events on the launch stream",
                    "parallelism": "replicas x%d" % world},
-        "roofline": {"bound": "hbm", "kernel": "mla_decode_tc (dsv4_sparse_mla_decode)", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": kernels[dom][0], "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind,
                      "algorithmic_bytes_per_launch": stage_bytes[dom]},
@@ -649,10 +745,9 @@ def main():
         "achieved_gbs_whole_step": ab["total"] / (ms / K / 1e3) / 1e9,
         "gpu_launches": K * bench.launches_per_step,
         "clocks": clk,
-        "e2e": {"value": job_value(world, B, K, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and headline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)

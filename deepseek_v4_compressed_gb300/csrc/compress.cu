@@ -184,24 +184,42 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
         kv = *reinterpret_cast<const float2*>(src + blk * D + c0);
         sc = *reinterpret_cast<const float2*>(src + COFF * D + blk * D + c0);
     };
+    // Rows are fetched CH at a time (every load of a chunk in flight before
+    // its values are used); the arithmetic and its order are the plain
+    // two-pass ones: max, then sums in ascending s.
+    constexpr int CH = W < 12 ? W : 12;
     const int s0 = (p - W + 1) < 0 ? 0 : p - W + 1;
     float m0 = -INFINITY, m1 = -INFINITY;
-    for (int s = s0; s <= p; ++s) {
-        float2 kv, sc;
-        fetch(s, kv, sc);
-        m0 = fmaxf(m0, sc.x);
-        m1 = fmaxf(m1, sc.y);
+    for (int sb = s0; sb <= p; sb += CH) {
+        float2 kv[CH], sc[CH];
+#pragma unroll
+        for (int u = 0; u < CH; ++u)
+            if (sb + u <= p) fetch(sb + u, kv[u], sc[u]);
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            if (sb + u <= p) {
+                m0 = fmaxf(m0, sc[u].x);
+                m1 = fmaxf(m1, sc[u].y);
+            }
+        }
     }
     float n0 = 0.f, n1 = 0.f, d0 = 0.f, d1 = 0.f;
-    for (int s = s0; s <= p; ++s) {
-        float2 kv, sc;
-        fetch(s, kv, sc);
-        const float e0 = cw_expf(__fsub_rn(sc.x, m0));
-        const float e1 = cw_expf(__fsub_rn(sc.y, m1));
-        n0 = __fadd_rn(n0, __fmul_rn(e0, kv.x));
-        n1 = __fadd_rn(n1, __fmul_rn(e1, kv.y));
-        d0 = __fadd_rn(d0, e0);
-        d1 = __fadd_rn(d1, e1);
+    for (int sb = s0; sb <= p; sb += CH) {
+        float2 kv[CH], sc[CH];
+#pragma unroll
+        for (int u = 0; u < CH; ++u)
+            if (sb + u <= p) fetch(sb + u, kv[u], sc[u]);
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            if (sb + u <= p) {
+                const float e0 = cw_expf(__fsub_rn(sc[u].x, m0));
+                const float e1 = cw_expf(__fsub_rn(sc[u].y, m1));
+                n0 = __fadd_rn(n0, __fmul_rn(e0, kv[u].x));
+                n1 = __fadd_rn(n1, __fmul_rn(e1, kv[u].y));
+                d0 = __fadd_rn(d0, e0);
+                d1 = __fadd_rn(d1, e1);
+            }
+        }
     }
     const float y0 = __fdiv_rn(n0, d0), y1 = __fdiv_rn(n1, d1);
 

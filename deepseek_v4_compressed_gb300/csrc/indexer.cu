@@ -669,28 +669,43 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const uint32_t thr = s_prefix >> lo;   // digit prefix of the threshold bin
     const int take_eq = s_rem;             // keys of the threshold bin to take, lowest slot first
 
-    const int chunk = (n + blockDim.x - 1) / blockDim.x;
-    const int i0 = threadIdx.x * chunk;
-    const int i1 = min(n, i0 + chunk);
-    int gt = 0, eq = 0;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t d = (key_at(i) - base) >> lo;
-        gt += d > thr;
-        eq += d == thr;
+    // ordered compaction: warp w owns slots [w R, (w + 1) R) and walks them 32
+    // consecutive keys at a time (coalesced); one pass counts the keys above /
+    // in the threshold bin per warp, the second writes each selected slot at
+    // (keys above before it) + (keys of the bin taken before it)
+    constexpr int NW = kTopkThreads / 32;
+    __shared__ int wsum[NW][2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = ((n + NW - 1) / NW + 31) & ~31;
+    const int w0 = warp * R, w1 = min(n, w0 + R);
+    int wg = 0, we = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t d = i < w1 ? (key_at(i) - base) >> lo : 0u;
+        wg += __popc(__ballot_sync(0xffffffffu, i < w1 && d > thr));
+        we += __popc(__ballot_sync(0xffffffffu, i < w1 && d == thr));
     }
-    int tot;
-    const int gt_before = block_excl_scan(gt, scratch, tot);
-    const int eq_before = block_excl_scan(eq, scratch, tot);
-    int g = gt_before, e = eq_before;
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t d = (key_at(i) - base) >> lo;
-        if (d > thr) {
-            orow[g + min(e, take_eq)] = i;
-            ++g;
-        } else if (d == thr) {
-            if (e < take_eq) orow[g + e] = i;
-            ++e;
-        }
+    if (lane == 0) {
+        wsum[warp][0] = wg;
+        wsum[warp][1] = we;
+    }
+    __syncthreads();
+    int g = 0, e = 0;
+    for (int q = 0; q < warp; ++q) {
+        g += wsum[q][0];
+        e += wsum[q][1];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t d = i < w1 ? (key_at(i) - base) >> lo : 0u;
+        const uint32_t gb = __ballot_sync(0xffffffffu, i < w1 && d > thr);
+        const uint32_t eb = __ballot_sync(0xffffffffu, i < w1 && d == thr);
+        const int gr = g + __popc(gb & lt), er = e + __popc(eb & lt);
+        if ((gb >> lane) & 1u) orow[gr + min(er, take_eq)] = i;
+        else if (((eb >> lane) & 1u) && er < take_eq) orow[gr + er] = i;
+        g += __popc(gb);
+        e += __popc(eb);
     }
     if (threadIdx.x == 0) out_len[b] = k;
 }
@@ -947,6 +962,244 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
     if (threadIdx.x == 0) out_len[b] = k;
 }
 
+// ---------------------------------------------------------------------------
+// Top-k of long rows (plans whose top-k is not in the logits launch): the row
+// of a query is split over a cluster of C <= 8 CTAs, CTA r holding the keys of
+// slots [r S, (r + 1) S) in shared memory.  The selection is the one of the
+// cluster top-k above -- (min, max) keys, 8-bit digit passes from the top of
+// the row's key range with every count summed over the cluster through
+// st.async pushes on the receivers' mbarriers, keys equal to the threshold
+// taken lowest slot first, slots written in ascending order -- with warp-
+// private histograms (a pass over 32768 keys would otherwise serialise on the
+// shared-memory atomics of its most crowded bins).
+// ---------------------------------------------------------------------------
+constexpr int kTkcSlots = 32768;                 // keys per CTA at most
+constexpr int kTkcWarps = kTopkThreads / 32;     // 16
+struct TkcScratch {
+    uint64_t bar_mm, bar_h[2], bar_cnt;
+    uint32_t mm_in[kCtkMaxCluster][2];
+    int cnt_in[kCtkMaxCluster][2];
+    alignas(16) int hin[2][kCtkMaxCluster][256];
+    alignas(16) int whist[kTkcWarps][256];
+    alignas(16) int hist[256];
+    int wsum[kTkcWarps][2];
+    uint32_t mm[2];
+    uint32_t prefix;
+    int rem, done, decided, failed;
+};
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
+    const float* logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k, int S,
+    int* __restrict__ out_idx, int out_stride, int* __restrict__ out_len, int* status)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ __align__(16) uint32_t tkc_smem[];
+    uint32_t* keys = tkc_smem;                                       // [S]
+    TkcScratch* T = reinterpret_cast<TkcScratch*>(tkc_smem + S);     // S is a multiple of 32
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = static_cast<int>(gridDim.x), rank = static_cast<int>(blockIdx.x), b = blockIdx.y;
+    if (tid == 0) {
+        tc::mbar_init(tc::smem_u32(&T->bar_mm), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_h[0]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_h[1]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_cnt), 1);
+        T->mm[0] = 0xffffffffu;
+        T->mm[1] = 0u;
+        T->failed = 0;
+        T->decided = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    tc::cluster_arrive_relaxed();                    // this CTA's barriers are initialised
+    int n = ctx_len[b] / 4;
+    n = n < 0 ? 0 : (n > max_slots ? max_slots : n);
+    int* orow = out_idx + static_cast<long long>(b) * out_stride;
+    const int s0 = rank * S, s1 = min(n, s0 + S), nl = max(0, s1 - s0);
+    // the logits come from the kernel launched before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    tc::cluster_wait_acquire();                      // every CTA of the cluster has started
+    if (n <= k) {
+        for (int s = s0 + tid; s < s1; s += kTopkThreads) orow[s] = s;
+        if (rank == 0) {
+            for (int i = n + tid; i < k; i += kTopkThreads) orow[i] = -1;
+            if (tid == 0) out_len[b] = n;
+        }
+        return;
+    }
+    // keys of this CTA's slots (s0 and the row stride are multiples of 4)
+    const float* lrow = logits + static_cast<long long>(b) * row_stride + s0;
+    uint32_t mn = 0xffffffffu, mx = 0u;
+    for (int i = 4 * tid; i < nl; i += 4 * kTopkThreads) {
+        if (i + 4 <= nl) {
+            const float4 v = *reinterpret_cast<const float4*>(lrow + i);
+            const uint32_t k0 = f32_order_key(v.x), k1 = f32_order_key(v.y), k2 = f32_order_key(v.z),
+                           k3 = f32_order_key(v.w);
+            *reinterpret_cast<uint4*>(keys + i) = make_uint4(k0, k1, k2, k3);
+            mn = min(min(mn, k0), min(min(k1, k2), k3));
+            mx = max(max(mx, k0), max(max(k1, k2), k3));
+        } else {
+            for (int j = i; j < nl; ++j) {
+                const uint32_t kk = f32_order_key(lrow[j]);
+                keys[j] = kk;
+                mn = min(mn, kk);
+                mx = max(mx, kk);
+            }
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0) {
+        atomicMin(&T->mm[0], mn);
+        atomicMax(&T->mm[1], mx);
+    }
+    __syncthreads();
+    // every CTA's min / max, in every CTA
+    if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_mm), static_cast<uint32_t>(C * 8));
+    if (tid < C)
+        tc::st_async_u32x2(tc::map_to_rank(tc::smem_u32(&T->mm_in[rank][0]), tid), T->mm[0], T->mm[1],
+                           tc::map_to_rank(tc::smem_u32(&T->bar_mm), tid));
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_mm), 0, status);
+        if (lane == 0 && !ok) T->failed = 1;
+    }
+    __syncthreads();
+    if (T->failed) return;
+    uint32_t base = 0xffffffffu, top = 0u;
+    for (int q = 0; q < C; ++q) {
+        base = min(base, T->mm_in[q][0]);
+        top = max(top, T->mm_in[q][1]);
+    }
+    const uint32_t range = top - base;
+    const int shift = range ? 32 - __clz(range) : 0;
+    int lo = shift > 8 ? shift - 8 : 0;
+    int plo = 32;
+    uint32_t prefix = 0;
+    int rem = k;
+    for (int pass = 0;; ++pass) {
+        const int p = pass & 1;
+        for (int i = tid; i < kTkcWarps * 256; i += kTopkThreads) (&T->whist[0][0])[i] = 0;
+        __syncthreads();
+        int* wh = T->whist[warp];
+        for (int i = tid; i < nl; i += kTopkThreads) {
+            const uint32_t o = keys[i] - base;
+            if (plo == 32 || (o >> plo) == (prefix >> plo)) atomicAdd(&wh[(o >> lo) & 255u], 1);
+        }
+        __syncthreads();
+        if (tid < 256) {
+            int acc = 0;
+#pragma unroll
+            for (int w = 0; w < kTkcWarps; ++w) acc += T->whist[w][tid];
+            T->hist[tid] = acc;
+        }
+        __syncthreads();
+        if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_h[p]), static_cast<uint32_t>(C * 1024));
+        if (tid < 64) {
+            const uint4 h4 = *reinterpret_cast<const uint4*>(&T->hist[4 * tid]);
+            for (int q = 0; q < C; ++q)
+                tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&T->hin[p][rank][4 * tid]), q), h4,
+                                   tc::map_to_rank(tc::smem_u32(&T->bar_h[p]), q));
+        }
+        if (warp == 0) {
+            // lane: digits 8 lane .. 8 lane + 7 summed over the cluster; the bin of
+            // the rem-th largest key still in play
+            const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_h[p]), (pass >> 1) & 1, status);
+            int g[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = 0;
+            if (ok) {
+                for (int q = 0; q < C; ++q) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(&T->hin[p][q][8 * lane]);
+                    const uint4 c = *reinterpret_cast<const uint4*>(&T->hin[p][q][8 * lane + 4]);
+                    g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
+                    g[4] += c.x; g[5] += c.y; g[6] += c.z; g[7] += c.w;
+                }
+            }
+            int tl = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tl += g[j];
+            int x = tl;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_down_sync(0xffffffffu, x, o);
+                if (lane + o < 32) x += y;
+            }
+            int above = x - tl;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                if (above < rem && rem <= above + g[j]) {
+                    T->prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << lo);
+                    T->rem = rem - above;
+                    T->done = (lo == 0) || (g[j] == rem - above);
+                    T->decided = pass + 1;
+                }
+                above += g[j];
+            }
+            __syncwarp();
+            if (lane == 0 && (!ok || T->decided != pass + 1)) T->failed = 1;
+        }
+        __syncthreads();
+        if (T->failed) return;
+        prefix = T->prefix;
+        rem = T->rem;
+        plo = lo;
+        if (T->done) break;
+        lo = lo > 8 ? lo - 8 : 0;
+    }
+    // ordered compaction: warp w walks its range of this CTA's slots 32 keys at a
+    // time; counts per warp, per CTA (pushed to every CTA), then the writes
+    const uint32_t thr = prefix >> plo;
+    const int R = ((nl + kTkcWarps - 1) / kTkcWarps + 31) & ~31;
+    const int w0 = warp * R, w1 = min(nl, w0 + R);
+    int wg = 0, we = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t d = i < w1 ? (keys[i] - base) >> plo : 0u;
+        wg += __popc(__ballot_sync(0xffffffffu, i < w1 && d > thr));
+        we += __popc(__ballot_sync(0xffffffffu, i < w1 && d == thr));
+    }
+    if (lane == 0) {
+        T->wsum[warp][0] = wg;
+        T->wsum[warp][1] = we;
+    }
+    __syncthreads();
+    int cg = 0, ce = 0, g = 0, e = 0;
+    for (int q = 0; q < kTkcWarps; ++q) {
+        cg += T->wsum[q][0];
+        ce += T->wsum[q][1];
+        if (q < warp) {
+            g += T->wsum[q][0];
+            e += T->wsum[q][1];
+        }
+    }
+    if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_cnt), static_cast<uint32_t>(C * 8));
+    if (tid < C)
+        tc::st_async_u32x2(tc::map_to_rank(tc::smem_u32(&T->cnt_in[rank][0]), tid), static_cast<uint32_t>(cg),
+                           static_cast<uint32_t>(ce), tc::map_to_rank(tc::smem_u32(&T->bar_cnt), tid));
+    if (warp == 0) {
+        const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_cnt), 0, status);
+        if (lane == 0 && !ok) T->failed = 1;
+    }
+    __syncthreads();
+    if (T->failed) return;
+    for (int q = 0; q < rank; ++q) {
+        g += T->cnt_in[q][0];
+        e += T->cnt_in[q][1];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t d = i < w1 ? (keys[i] - base) >> plo : 0u;
+        const uint32_t gb = __ballot_sync(0xffffffffu, i < w1 && d > thr);
+        const uint32_t eb = __ballot_sync(0xffffffffu, i < w1 && d == thr);
+        const int gr = g + __popc(gb & lt), er = e + __popc(eb & lt);
+        if ((gb >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
+        else if (((eb >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
+        g += __popc(gb);
+        e += __popc(eb);
+    }
+    if (rank == 0 && tid == 0) out_len[b] = k;
+}
+
 }  // namespace dsv4
 
 using namespace dsv4;
@@ -1048,6 +1301,38 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
                                plan->max_slots, a->ctx_len_dev, plan->topk, a->out_idx_dev, a->out_stride,
                                a->out_len_dev);
         return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    }
+    {
+        // long rows: a cluster of C CTAs per query, S keys each
+        const int Cq = min(kCtkMaxCluster, (plan->max_slots + 8191) / 8192);
+        const int S = ((plan->max_slots + Cq - 1) / Cq + 31) & ~31;
+        if (S <= kTkcSlots) {
+            const size_t smem = static_cast<size_t>(S) * 4 + sizeof(TkcScratch);
+            static bool tkc_attr = false;
+            if (!tkc_attr) {
+                cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch)));
+                tkc_attr = true;
+            }
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(Cq, B, 1);
+            cfg.blockDim = dim3(kTopkThreads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = plan->idx_ctas_per_seq > 0 ? 1 : 0;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = Cq;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, static_cast<const float*>(logits), plan->logits_stride,
+                                   plan->max_slots, a->ctx_len_dev, plan->topk, S, a->out_idx_dev, a->out_stride,
+                                   a->out_len_dev, a->status_dev);
+            return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+        }
     }
     const int smem_keys = plan->max_slots <= kTopkSmemKeys ? plan->max_slots : 0;
     const size_t smem = static_cast<size_t>(smem_keys) * 4;

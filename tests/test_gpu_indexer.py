@@ -113,3 +113,16 @@ def test_deterministic_across_runs():
     for _ in range(5):
         again = run_indexer(d)
         assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+
+
+def test_long_rows_cluster_topk_ragged():
+    # plans whose top-k is a separate launch over long rows split across a
+    # cluster of CTAs: 4 sequences with up to 32768 slots (128K context), ragged
+    # lengths (n_c <= k, CTAs with no slots) and an all-equal row
+    ctx = np.array([131072, 70000, 1500, 9000], np.int32)
+    d = _with_zero_weights(make_decode_inputs(4, 4, ctx, 8, 16, 512, seed=34, with_comp=False), [3])
+    plan = B.Plan(B.C4A, d.n_heads, d.batch, d.topk, 131072, idx_heads=d.idx_heads)
+    assert plan.info()["launches_indexer"] == 2
+    idx, ln = run_indexer(d, max_ctx=131072)
+    assert list(ln) == [min(512, int(c) // 4) for c in ctx]
+    check_all(d, idx, ln)
