@@ -718,7 +718,8 @@ def main():
     # logits launch when a sequence's CTAs fit one cluster)
     stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
     kernels = {"compress": ("compress_pair_kernel / compress_kernel (dsv4_compress_insert)", "compress.cu"),
-               "indexer_topk": ("indexer_logits_tc (dsv4_indexer_topk)", "indexer.cu"),
+               "indexer_topk": ("indexer_logits_tc (dsv4_indexer_topk)" if bench.info["launches_indexer"] == 1 else
+                                "indexer_logits_tc + top-k kernel (dsv4_indexer_topk, 2 launches)", "indexer.cu"),
                "sparse_mla": ("mla_decode_tc (dsv4_sparse_mla_decode)", "mla.cu")}
     dom = max(bench.stage_names, key=lambda nm: stages[nm])
     achieved = stage_bytes[dom] / (stages[dom] / 1e3) / 1e9
