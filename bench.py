@@ -45,6 +45,9 @@ WORKLOADS = {
                            window=128, ratio=128),
     "c4a_1m_b4": dict(name="c4a_1m_b4", batch=4, context=1048576, n_heads=128, idx_heads=64, topk=2048,
                       window=128, ratio=4),
+    # 60-layer stack (swaonly / c4a / c128a), IndexCache freq 2 against freq 1
+    "mixed60_b16": dict(name="mixed60_b16", batch=16, context=65536, n_heads=64, idx_heads=64, topk=512,
+                        window=128, ratio=0),
 }
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
@@ -598,6 +601,155 @@ def cpu_baseline(w, budget_s=12.0):
                       (steps, s.n_c, w["topk"], w["n_heads"], dt)}
 
 
+def mixed_stack_bench(args, w):
+    """The 60-layer stack of the scope table: 2 swaonly, 21 c4a and 37 c128a
+    layers (distinct caches per layer), every layer's library calls in order
+    for one decode token per sequence, under the IndexCache schedule with
+    frequency 2 (c4a reuse layers take the previous c4a layer's indices and
+    skip the indexer) and with frequency 1 (every c4a layer runs it).  Prints
+    one JSON line with both step times."""
+    from deepseek_v4_compressed_gb300 import binding as Bd
+    from deepseek_v4_compressed_gb300 import synth
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    Bsz, ctx_max, H, k = w["batch"], w["context"], w["n_heads"], w["topk"]
+    P = 4
+    ratios = [int(r) for r in synth.mixed_stack_ratios()]
+    w4 = dict(w, ratio=4)
+    w128 = dict(w, ratio=128, idx_heads=0, topk=ctx_max // 128)
+    plan4 = Bd.Plan(Bd.C4A, H, Bsz, k, ctx_max, idx_heads=w["idx_heads"], window=w["window"])
+    plan128 = Bd.Plan(Bd.C128A, H, Bsz, w128["topk"], ctx_max, window=w["window"])
+    plan1 = Bd.Plan(Bd.SWAONLY, H, Bsz, 0, ctx_max, window=w["window"])
+    ws4, ws128, ws1 = plan4.workspace(device), plan128.workspace(device), plan1.workspace(device)
+    n4, n128 = ratios.count(4), ratios.count(128)
+    L4 = build_layers(Bd, w4, n4, P, device, seed=5)
+    L128 = build_layers_c128a(w128, n128, P, device, seed=6)
+    L1 = build_layers_c128a(w128, ratios.count(1), P, device, seed=7)   # swaonly layers use the SWA cache and q
+    cos_sin = Bd.rope_table(ctx_max + 1).to(device)
+    p0 = ctx_max - P
+    pos = [torch.full((Bsz,), p0 + j, dtype=torch.int32, device=device) for j in range(P)]
+    ctx = [torch.full((Bsz,), p0 + j + 1, dtype=torch.int32, device=device) for j in range(P)]
+    # c128a metadata: all visible slots (k = every slot of the layer)
+    meta = [torch.arange(w128["topk"], dtype=torch.int32, device=device).repeat(Bsz, 1).contiguous()
+            for _ in range(P)]
+    meta_len = [torch.full((Bsz,), (p0 + j + 1) // 128, dtype=torch.int32, device=device) for j in range(P)]
+    idx_shared = torch.empty((Bsz, k), dtype=torch.int32, device=device)
+    len_shared = torch.empty((Bsz,), dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    launches = {}
+
+    def step(j, skip):
+        i4 = i128 = i1 = 0
+        n_launch = 0
+        for li, r in enumerate(ratios):
+            if r == 1:
+                L = L1[i1]
+                i1 += 1
+                Bd.sparse_mla_decode(plan1, L.q[j], L.swa, L.swa_bt, ctx[j], L.out, ws1, lse=L.lse, status=status)
+                n_launch += plan1.info()["launches_mla"]
+            elif r == 4:
+                L = L4[i4]
+                i4 += 1
+                Bd.compress_insert_pair(
+                    dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=L.kv_main[j], positions=pos[j], seqs=L.seqs,
+                         ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=cos_sin, state=L.state_main,
+                         cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=status),
+                    dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=L.kv_idx[j], positions=pos[j], seqs=L.seqs,
+                         ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=cos_sin, state=L.state_idx,
+                         cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=status))
+                n_launch += 1
+                if not skip[li]:
+                    Bd.indexer_topk(plan4, L.qi[j], L.wts[j], L.idx, L.idx_bt, ctx[j], idx_shared, len_shared, ws4,
+                                    status)
+                    n_launch += plan4.info()["launches_indexer"]
+                Bd.sparse_mla_decode(plan4, L.q[j], L.swa, L.swa_bt, ctx[j], L.out, ws4, comp_cache=L.comp,
+                                     comp_block_table=L.comp_bt, topk_idx=idx_shared, topk_len=len_shared,
+                                     lse=L.lse, status=status)
+                n_launch += plan4.info()["launches_mla"]
+            else:
+                L = L128[i128]
+                i128 += 1
+                Bd.compress_insert(Bd.CACHE_MLA, 128, L.kv_main[j], pos[j], L.seqs, L.ape_main, L.rms_main, 1e-6,
+                                   cos_sin, L.state_main, L.comp, L.comp_bt, Bsz, status=status)
+                Bd.sparse_mla_decode(plan128, L.q[j], L.swa, L.swa_bt, ctx[j], L.out, ws128, comp_cache=L.comp,
+                                     comp_block_table=L.comp_bt, topk_idx=meta[j], topk_len=meta_len[j],
+                                     lse=L.lse, status=status)
+                n_launch += 1 + plan128.info()["launches_mla"]
+        return n_launch
+
+    def measure(skip, K):
+        for j in range(P):
+            step(j, skip)
+        torch.cuda.synchronize()
+        st, bits = Bd.read_device_status(status)
+        if st != Bd.OK:
+            raise RuntimeError("device status %s (bits 0x%x)" % (Bd.status_string(st), bits))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            nl = sum(step(i % P, skip) for i in range(K))
+        g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 4
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), device) / reps
+        return ms / K, nl * reps
+    K = max(4, min(args.steps, 16))
+    skip2 = Bd.index_schedule(ratios, True, 2)
+    skip1 = Bd.index_schedule(ratios, True, 1)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms2, nl2 = measure(skip2, K)
+    ms1, nl1 = measure(skip1, K)
+    clk = clocks.stop()
+    # algorithmic bytes per 60-layer step
+    ctx_avg = ctx_max - (P - 1) / 2.0
+    a4 = algorithmic_bytes(w4, int(ctx_avg))
+    a128 = algorithmic_bytes(w128, int(ctx_avg))
+    swa_b = Bsz * (128 * 1152 + H * 576 * 2 + H * 512 * 2 + H * 4 + 4)
+    n_compute2 = sum(1 for li, r in enumerate(ratios) if r == 4 and not skip2[li])
+    def step_bytes(n_compute):
+        return (n_compute * a4["total"] + (n4 - n_compute) * (a4["compress"] + a4["mla"]) + n128 * a128["total"]
+                + ratios.count(1) * swa_b)
+    b2, b1 = step_bytes(n_compute2), step_bytes(n4)
+    peak, peak_kind = load_peaks()
+    def leg(ms, b, nl):
+        return {"ms_per_step": ms, "tokens_per_s_per_layer": world * Bsz * len(ratios) / (ms / 1e3),
+                "algorithmic_bytes_per_step": b, "achieved_gbs": b / (ms / 1e3) / 1e9,
+                "frac": b / (ms / 1e3) / 1e9 / peak, "gpu_launches": nl}
+    line = {
+        "metric": METRIC.replace("(C4A, 32K ctx, B=32)", "(60-layer mixed stack, 64K ctx, B=16)"),
+        "value": world * Bsz * len(ratios) / (ms2 / 1e3), "unit": UNIT, "n_gpus": world, "steps": K * 4,
+        "warmup": P, "ms_per_step": ms2, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8+bf16", "data": "synthetic",
+        "config": {"workload": w["name"], "batch": Bsz, "context": ctx_max, "heads": H, "idx_heads": w["idx_heads"],
+                   "topk": k, "layers": len(ratios), "swaonly": ratios.count(1), "c4a": n4, "c128a": n128,
+                   "c4a_compute_layers_freq2": n_compute2, "positions": P,
+                   "timing": "CUDA graph replay of K whole-stack steps (every layer's calls), CUDA events",
+                   "parallelism": "replicas x%d" % world},
+        "freq2": leg(ms2, b2, nl2), "freq1": leg(ms1, b1, nl1), "freq1_over_freq2": ms1 / ms2,
+        "roofline": {"bound": "hbm", "kernel": "whole 60-layer step (freq 2)", "achieved": b2 / (ms2 / 1e3) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": b2 / (ms2 / 1e3) / 1e9 / peak, "traffic": None,
+                     "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind},
+        "clocks": clk, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def reference_arm(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -657,6 +809,8 @@ def main():
             return 0
         return reference_arm(args, w)
 
+    if w["name"] == "mixed60_b16":
+        return mixed_stack_bench(args, w)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
