@@ -964,7 +964,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
 
 // ---------------------------------------------------------------------------
 // Top-k of long rows (plans whose top-k is not in the logits launch): the row
-// of a query is split over a cluster of C <= 8 CTAs, CTA r holding the keys of
+// of a query is split over a cluster of C <= 16 CTAs, CTA r holding the keys of
 // slots [r S, (r + 1) S) in shared memory.  The selection is the one of the
 // cluster top-k above -- (min, max) keys, 8-bit digit passes from the top of
 // the row's key range with every count summed over the cluster through
@@ -975,11 +975,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kTkcSlots = 32768;                 // keys per CTA at most
 constexpr int kTkcWarps = kTopkThreads / 32;     // 16
+constexpr int kTkcMaxCluster = 16;               // CTAs per query (above 8: a non-portable cluster size)
 struct TkcScratch {
     uint64_t bar_mm, bar_h[2], bar_cnt;
-    uint32_t mm_in[kCtkMaxCluster][2];
-    int cnt_in[kCtkMaxCluster][2];
-    alignas(16) int hin[2][kCtkMaxCluster][256];
+    uint32_t mm_in[kTkcMaxCluster][2];
+    int cnt_in[kTkcMaxCluster][2];
+    alignas(16) int hin[2][kTkcMaxCluster][256];
     alignas(16) int whist[kTkcWarps][256];
     alignas(16) int hist[256];
     int wsum[kTkcWarps][2];
@@ -1303,21 +1304,24 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
     }
     {
-        // long rows: a cluster of C CTAs per query, S keys each
-        const int Cq = min(kCtkMaxCluster, (plan->max_slots + 8191) / 8192);
-        const int S = ((plan->max_slots + Cq - 1) / Cq + 31) & ~31;
-        if (S <= kTkcSlots) {
-            const size_t smem = static_cast<size_t>(S) * 4 + sizeof(TkcScratch);
-            static bool tkc_attr = false;
-            if (!tkc_attr) {
-                cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch)));
-                tkc_attr = true;
-            }
+        // long rows: a cluster of C CTAs per query (8192 keys or more each), S
+        // keys each; clusters of more than 8 CTAs need the non-portable size,
+        // and a launch the device refuses is retried with 8
+        static bool tkc_attr = false;
+        if (!tkc_attr) {
+            cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch)));
+            cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            tkc_attr = true;
+        }
+        for (int cmax = kTkcMaxCluster; cmax >= kCtkMaxCluster; cmax /= 2) {
+            const int Cq = min(cmax, (plan->max_slots + 8191) / 8192);
+            const int S = ((plan->max_slots + Cq - 1) / Cq + 31) & ~31;
+            if (S > kTkcSlots) break;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(Cq, B, 1);
             cfg.blockDim = dim3(kTopkThreads, 1, 1);
-            cfg.dynamicSmemBytes = smem;
+            cfg.dynamicSmemBytes = static_cast<size_t>(S) * 4 + sizeof(TkcScratch);
             cfg.stream = st;
             cudaLaunchAttribute attr[2];
             attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1331,7 +1335,9 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
             e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, static_cast<const float*>(logits), plan->logits_stride,
                                    plan->max_slots, a->ctx_len_dev, plan->topk, S, a->out_idx_dev, a->out_stride,
                                    a->out_len_dev, a->status_dev);
-            return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+            if (e == cudaSuccess) return DSV4_OK;
+            if (Cq <= kCtkMaxCluster) return DSV4_ERR_CUDA;
+            (void)cudaGetLastError();                   // a refused cluster size: try the portable one
         }
     }
     const int smem_keys = plan->max_slots <= kTopkSmemKeys ? plan->max_slots : 0;
