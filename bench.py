@@ -880,8 +880,9 @@ def main():
     srcs = ["deepseek_v4_compressed_gb300/csrc/" + kernels[dom][1]]
     rec = TRAFFIC_RECORD.get((w["name"], dom))
     traffic = rec["bytes_per_launch"] if rec and rec["src_sha"] == src_digest(srcs) else None
+    metric = METRIC if headline else METRIC.replace("(C4A, 32K ctx, B=32)", "(%s)" % w["name"])
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8+bf16", "data": "synthetic",
         "config": {"workload": w["name"], "batch": B, "context": w["context"], "heads": w["n_heads"],
