@@ -1030,22 +1030,21 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
     // keys of this CTA's slots (s0 and the row stride are multiples of 4)
     const float* lrow = logits + static_cast<long long>(b) * row_stride + s0;
     uint32_t mn = 0xffffffffu, mx = 0u;
-    for (int i = 4 * tid; i < nl; i += 4 * kTopkThreads) {
-        if (i + 4 <= nl) {
-            const float4 v = *reinterpret_cast<const float4*>(lrow + i);
-            const uint32_t k0 = f32_order_key(v.x), k1 = f32_order_key(v.y), k2 = f32_order_key(v.z),
-                           k3 = f32_order_key(v.w);
-            *reinterpret_cast<uint4*>(keys + i) = make_uint4(k0, k1, k2, k3);
-            mn = min(min(mn, k0), min(min(k1, k2), k3));
-            mx = max(max(mx, k0), max(max(k1, k2), k3));
-        } else {
-            for (int j = i; j < nl; ++j) {
-                const uint32_t kk = f32_order_key(lrow[j]);
-                keys[j] = kk;
-                mn = min(mn, kk);
-                mx = max(mx, kk);
-            }
-        }
+    const int n4 = nl >> 2;                          // whole float4 groups, 4 loads in flight per thread
+#pragma unroll 4
+    for (int i = tid; i < n4; i += kTopkThreads) {
+        const float4 v = reinterpret_cast<const float4*>(lrow)[i];
+        const uint32_t k0 = f32_order_key(v.x), k1 = f32_order_key(v.y), k2 = f32_order_key(v.z),
+                       k3 = f32_order_key(v.w);
+        reinterpret_cast<uint4*>(keys)[i] = make_uint4(k0, k1, k2, k3);
+        mn = min(min(mn, k0), min(min(k1, k2), k3));
+        mx = max(max(mx, k0), max(max(k1, k2), k3));
+    }
+    for (int j = 4 * n4 + tid; j < nl; j += kTopkThreads) {
+        const uint32_t kk = f32_order_key(lrow[j]);
+        keys[j] = kk;
+        mn = min(mn, kk);
+        mx = max(mx, kk);
     }
     mn = __reduce_min_sync(0xffffffffu, mn);
     mx = __reduce_max_sync(0xffffffffu, mx);
@@ -1081,6 +1080,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         for (int i = tid; i < kTkcWarps * 256; i += kTopkThreads) (&T->whist[0][0])[i] = 0;
         __syncthreads();
         int* wh = T->whist[warp];
+#pragma unroll 4
         for (int i = tid; i < nl; i += kTopkThreads) {
             const uint32_t o = keys[i] - base;
             if (plo == 32 || (o >> plo) == (prefix >> plo)) atomicAdd(&wh[(o >> lo) & 255u], 1);
@@ -1151,12 +1151,32 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
     const uint32_t thr = prefix >> plo;
     const int R = ((nl + kTkcWarps - 1) / kTkcWarps + 31) & ~31;
     const int w0 = warp * R, w1 = min(nl, w0 + R);
+    // ballots of 4 consecutive 32-key groups of the warp's range (their keys read
+    // at once): gb[u] = lanes whose key lies above the threshold bin, eb[u] = in it
+    auto groups4 = [&](int i0, uint32_t (&gb)[4], uint32_t (&eb)[4]) {
+        uint32_t d[4];
+        bool v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 32 * u + lane;
+            v[u] = i < w1;
+            d[u] = v[u] ? (keys[i] - base) >> plo : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            gb[u] = __ballot_sync(0xffffffffu, v[u] && d[u] > thr);
+            eb[u] = __ballot_sync(0xffffffffu, v[u] && d[u] == thr);
+        }
+    };
     int wg = 0, we = 0;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t d = i < w1 ? (keys[i] - base) >> plo : 0u;
-        wg += __popc(__ballot_sync(0xffffffffu, i < w1 && d > thr));
-        we += __popc(__ballot_sync(0xffffffffu, i < w1 && d == thr));
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        uint32_t gb[4], eb[4];
+        groups4(i0, gb, eb);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            wg += __popc(gb[u]);
+            we += __popc(eb[u]);
+        }
     }
     if (lane == 0) {
         T->wsum[warp][0] = wg;
@@ -1187,16 +1207,18 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         e += T->cnt_in[q][1];
     }
     const uint32_t lt = (1u << lane) - 1u;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t d = i < w1 ? (keys[i] - base) >> plo : 0u;
-        const uint32_t gb = __ballot_sync(0xffffffffu, i < w1 && d > thr);
-        const uint32_t eb = __ballot_sync(0xffffffffu, i < w1 && d == thr);
-        const int gr = g + __popc(gb & lt), er = e + __popc(eb & lt);
-        if ((gb >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
-        else if (((eb >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
-        g += __popc(gb);
-        e += __popc(eb);
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        uint32_t gb[4], eb[4];
+        groups4(i0, gb, eb);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + 32 * u + lane;
+            const int gr = g + __popc(gb[u] & lt), er = e + __popc(eb[u] & lt);
+            if ((gb[u] >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
+            else if (((eb[u] >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
+            g += __popc(gb[u]);
+            e += __popc(eb[u]);
+        }
     }
     if (rank == 0 && tid == 0) out_len[b] = k;
 }
