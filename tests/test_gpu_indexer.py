@@ -126,3 +126,13 @@ def test_long_rows_cluster_topk_ragged():
     idx, ln = run_indexer(d, max_ctx=131072)
     assert list(ln) == [min(512, int(c) // 4) for c in ctx]
     check_all(d, idx, ln)
+
+
+def test_topk_beyond_the_cluster_range():
+    # a plan for rows longer than 16 x 32768 slots (context 2.4M) keeps the
+    # single-CTA top-k with its keys in global memory; actual rows are short
+    ctx = np.array([100000, 3000, 65541], np.int32)
+    d = make_decode_inputs(4, 3, ctx, 8, 16, 512, seed=35, with_comp=False)
+    idx, ln = run_indexer(d, max_ctx=2400000)
+    assert list(ln) == [min(512, int(c) // 4) for c in ctx]
+    check_all(d, idx, ln)
