@@ -1,4 +1,5 @@
-"""The multi-process side of bench.py on CPU (gloo, world size 2).
+"""Host-side logic of bench.py on CPU: the multi-process replica path (gloo,
+world size 2) and the algorithmic byte counts behind its roofline fractions.
 
 The decode path shards by sequence with no exchange between GPUs, so N GPUs
 run N replicas: each rank times its own steps, the job takes the slowest
@@ -87,3 +88,20 @@ def test_reference_arm_runs_on_rank_zero_only():
     line = json.loads(outs[0].splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_algorithmic_bytes_match_the_scope_table():
+    # bench.py's per-layer-step byte count (indexer + attention) against totals
+    # worked out by hand from the entry sizes (132-byte indexer rows, 648-byte
+    # compressed rows, 1152-byte window rows, q, output, indices and tables):
+    # C4A 32K batch 32 54.83 MB, C128A 128K batch 64 39.72 MB (attention only),
+    # C4A 1M batch 4 145.65 MB; they differ only in how table bytes are rounded
+    sys.path.insert(0, ROOT)
+    import bench
+    w = bench.WORKLOADS
+    ab = bench.algorithmic_bytes(w["c4a_32k_b32"], 32768)
+    assert ab["indexer"] + ab["mla"] == pytest.approx(54.83e6, rel=2e-3)
+    ab = bench.algorithmic_bytes(w["c128a_128k_b64"], 131072)
+    assert ab["indexer"] == 0 and ab["mla"] == pytest.approx(39.72e6, rel=5e-3)
+    ab = bench.algorithmic_bytes(w["c4a_1m_b4"], 1048576)
+    assert ab["indexer"] + ab["mla"] == pytest.approx(145.65e6, rel=2e-3)
