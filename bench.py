@@ -183,7 +183,7 @@ class LayerInstance:
     """One c4a layer's caches, compressor state and per-step inputs on the GPU."""
 
 
-def build_layers(B, w, n_layers, n_pos, device, seed=1):
+def build_layers(w, n_layers, n_pos, device, seed=1):
     from deepseek_v4_compressed_gb300 import binding as Bd
     g = torch.Generator(device=device)
     g.manual_seed(seed)
@@ -295,7 +295,7 @@ class GpuBench:
         else:
             self.plan = Bd.Plan(Bd.C4A, w["n_heads"], Bsz, w["topk"], w["context"], idx_heads=w["idx_heads"],
                                 window=w["window"])
-            self.layers = build_layers(Bd, w, n_layers, n_pos, device)
+            self.layers = build_layers(w, n_layers, n_pos, device)
             self.stage_names = ["compress", "indexer_topk", "sparse_mla"]
         self.ws = self.plan.workspace(device)
         self.cos_sin = Bd.rope_table(w["context"] + 1).to(device)
@@ -626,7 +626,7 @@ def mixed_stack_bench(args, w):
     plan1 = Bd.Plan(Bd.SWAONLY, H, Bsz, 0, ctx_max, window=w["window"])
     ws4, ws128, ws1 = plan4.workspace(device), plan128.workspace(device), plan1.workspace(device)
     n4, n128 = ratios.count(4), ratios.count(128)
-    L4 = build_layers(Bd, w4, n4, P, device, seed=5)
+    L4 = build_layers(w4, n4, P, device, seed=5)
     L128 = build_layers_c128a(w128, n128, P, device, seed=6)
     L1 = build_layers_c128a(w128, ratios.count(1), P, device, seed=7)   # swaonly layers use the SWA cache and q
     cos_sin = Bd.rope_table(ctx_max + 1).to(device)
