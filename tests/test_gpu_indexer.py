@@ -136,3 +136,12 @@ def test_topk_beyond_the_cluster_range():
     idx, ln = run_indexer(d, max_ctx=2400000)
     assert list(ln) == [min(512, int(c) // 4) for c in ctx]
     check_all(d, idx, ln)
+
+
+def test_indexer_heads_not_a_multiple_of_16():
+    # 20 indexer heads: the MMA's N is padded to 32 with zero weights past the heads
+    ctx = np.array([9000, 512, 40000], np.int32)
+    d = make_decode_inputs(4, 3, ctx, 8, 20, 256, seed=36, with_comp=False)
+    idx, ln = run_indexer(d)
+    assert list(ln) == [min(256, int(c) // 4) for c in ctx]
+    check_all(d, idx, ln)

@@ -141,3 +141,13 @@ def test_key_dequant_every_code_and_scale():
             g = oracle.bf16_to_f32(got[s][tiny])
             assert np.all(np.abs(g) < 2.0 ** -126)
             assert np.all((np.signbit(g) == np.signbit(v[tiny])) | (g == 0))
+
+
+def test_partial_second_head_group():
+    # 96 heads: a full 64-head group and a 32-head one (rows past the heads
+    # computed but never stored), ragged contexts
+    ctx = np.array([5000, 130, 20000], np.int32)
+    d = make_decode_inputs(4, len(ctx), ctx, 96, 0, 512, seed=8)
+    idx, ln = random_indices(d, 108)
+    out, lse = run_mla(d, idx, ln)
+    check_batch(d, out, lse, idx, ln)
