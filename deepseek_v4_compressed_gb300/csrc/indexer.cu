@@ -56,6 +56,11 @@ constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * 
 constexpr int kCtkSlots = 16 * kIdxTileSlots;                        // slots per CTA at most
 constexpr int kCtkPer = (kCtkSlots + kIdxThreads - 1) / kIdxThreads;   // slots per thread (6)
 constexpr int kCtkMaxCluster = 8;
+// the decisions of a digit pass, shared by the CTA's threads (see ctk_decide)
+struct CtkDecision {
+    uint32_t prefix;
+    int rem, done, decided, failed;
+};
 struct CtkScratch {
     uint64_t bar_mm;                        // every CTA's (min, max) has landed (bytes)
     uint64_t bar_h[2];                      // every CTA's histogram of the pass has landed, by pass parity
@@ -65,11 +70,57 @@ struct CtkScratch {
     int hin[2][kCtkMaxCluster][256];        // CTA q's digit histogram, by pass parity, pushed by q
     int hist[2][256];                       // this CTA's histogram, by pass parity
     uint32_t mm[2];                         // this CTA's min, max
-    uint32_t prefix;                        // the decisions, for the CTA's threads
-    int rem, done, decided, failed;
+    CtkDecision dec;                        // the decisions, for the CTA's threads
     int scan[16];
 };
 constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
+
+// The decision of a digit pass of the cluster top-k, taken alike by one warp
+// of every CTA once the pass's histograms of all C CTAs are in hin[q][256]:
+// lane l sums digits 8l .. 8l + 7 over the cluster, a shuffle scan from the
+// top gives the keys above each lane's digits, and the lane holding the digit
+// of the rem-th largest key still in play writes the new prefix (that digit at
+// bit lo), the keys of that bin still to take, whether the selection is
+// complete (lo == 0, or the bin is taken whole) and decided = pass + 1.  After
+// a failed wait (ok false) nothing is decided and `failed` is set.
+__device__ __forceinline__ void ctk_decide(const int (*hin)[256], int C, bool ok, uint32_t prefix, int lo, int rem,
+                                           int pass, CtkDecision* D)
+{
+    const int lane = threadIdx.x & 31;
+    int g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) g[j] = 0;
+    if (ok) {
+        for (int q = 0; q < C; ++q) {
+            const uint4 a = *reinterpret_cast<const uint4*>(&hin[q][8 * lane]);
+            const uint4 c = *reinterpret_cast<const uint4*>(&hin[q][8 * lane + 4]);
+            g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
+            g[4] += c.x; g[5] += c.y; g[6] += c.z; g[7] += c.w;
+        }
+    }
+    int tl = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tl += g[j];
+    int x = tl;                                      // keys in the digits from 8 lane up
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+    }
+    int above = x - tl;                              // keys in the digits above this lane's
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+        if (above < rem && rem <= above + g[j]) {
+            D->prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << lo);
+            D->rem = rem - above;
+            D->done = (lo == 0) || (g[j] == rem - above);
+            D->decided = pass + 1;
+        }
+        above += g[j];
+    }
+    __syncwarp();
+    if (lane == 0 && (!ok || D->decided != pass + 1)) D->failed = 1;
+}
 
 // Exclusive scan of one int per thread over the CTA (kIdxThreads threads).
 __device__ __forceinline__ int ctk_excl_scan(int v, int* scan, int& total)
@@ -148,10 +199,10 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
                            tc::map_to_rank(tc::smem_u32(&S->bar_mm), tid));
     if (warp == 0) {
         const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_mm), 0, status);
-        if (lane == 0 && !ok) S->failed = 1;
+        if (lane == 0 && !ok) S->dec.failed = 1;
     }
     __syncthreads();
-    if (S->failed) return;
+    if (S->dec.failed) return;
     uint32_t base = 0xffffffffu, top = 0u;
     for (int q = 0; q < C; ++q) {
         base = min(base, S->mm_in[q][0]);
@@ -182,49 +233,15 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
         }
         if (tid < 256) S->hist[p ^ 1][tid] = 0;          // for the next pass (its last reader was the pass before)
         if (warp == 0) {
-            // lane: digits 8 lane .. 8 lane + 7, summed over the cluster; the bin
-            // of the rem-th largest key among those still in play
             const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_h[p]), (pass >> 1) & 1, status);
-            int g[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = 0;
-            if (ok) {
-                for (int q = 0; q < C; ++q) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(&S->hin[p][q][8 * lane]);
-                    const uint4 c = *reinterpret_cast<const uint4*>(&S->hin[p][q][8 * lane + 4]);
-                    g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
-                    g[4] += c.x; g[5] += c.y; g[6] += c.z; g[7] += c.w;
-                }
-            }
-            int tl = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) tl += g[j];
-            int x = tl;                                      // keys in the digits from 8 lane up
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_down_sync(0xffffffffu, x, o);
-                if (lane + o < 32) x += y;
-            }
-            int above = x - tl;                              // keys in the digits above this lane's
-#pragma unroll
-            for (int j = 7; j >= 0; --j) {
-                if (above < rem && rem <= above + g[j]) {
-                    S->prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << lo);
-                    S->rem = rem - above;
-                    S->done = (lo == 0) || (g[j] == rem - above);
-                    S->decided = pass + 1;
-                }
-                above += g[j];
-            }
-            __syncwarp();
-            if (lane == 0 && (!ok || S->decided != pass + 1)) S->failed = 1;
+            ctk_decide(S->hin[p], C, ok, prefix, lo, rem, pass, &S->dec);
         }
         __syncthreads();
-        if (S->failed) return;
-        prefix = S->prefix;
-        rem = S->rem;
+        if (S->dec.failed) return;
+        prefix = S->dec.prefix;
+        rem = S->dec.rem;
         plo = lo;
-        if (S->done) break;
+        if (S->dec.done) break;
         lo = lo > 8 ? lo - 8 : 0;
     }
     // ordered compaction: keys above the threshold bin, and the first `rem`
@@ -246,10 +263,10 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
                            static_cast<uint32_t>(tot & 0xffff), tc::map_to_rank(tc::smem_u32(&S->bar_cnt), tid));
     if (warp == 0) {
         const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_cnt), 0, status);
-        if (lane == 0 && !ok) S->failed = 1;
+        if (lane == 0 && !ok) S->dec.failed = 1;
     }
     __syncthreads();
-    if (S->failed) return;
+    if (S->dec.failed) return;
     int gpos = before >> 16, epos = before & 0xffff;
     for (int q = 0; q < rank; ++q) {
         gpos += S->cnt_in[q][0];
@@ -352,8 +369,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (kFused && threadIdx.x == 0) {
         ctk->mm[0] = 0xffffffffu;
         ctk->mm[1] = 0u;
-        ctk->failed = 0;
-        ctk->decided = 0;
+        ctk->dec.failed = 0;
+        ctk->dec.decided = 0;
     }
     if (warp == 0) {
         tc::tmem_alloc(tc::smem_u32(tmem_slot), kIdxTmemCols);
@@ -985,8 +1002,7 @@ struct TkcScratch {
     alignas(16) int hist[256];
     int wsum[kTkcWarps][2];
     uint32_t mm[2];
-    uint32_t prefix;
-    int rem, done, decided, failed;
+    CtkDecision dec;
 };
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
@@ -1006,8 +1022,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         tc::mbar_init(tc::smem_u32(&T->bar_cnt), 1);
         T->mm[0] = 0xffffffffu;
         T->mm[1] = 0u;
-        T->failed = 0;
-        T->decided = 0;
+        T->dec.failed = 0;
+        T->dec.decided = 0;
         tc::fence_barrier_init();
     }
     __syncthreads();
@@ -1060,10 +1076,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
                            tc::map_to_rank(tc::smem_u32(&T->bar_mm), tid));
     if (warp == 0) {
         const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_mm), 0, status);
-        if (lane == 0 && !ok) T->failed = 1;
+        if (lane == 0 && !ok) T->dec.failed = 1;
     }
     __syncthreads();
-    if (T->failed) return;
+    if (T->dec.failed) return;
     uint32_t base = 0xffffffffu, top = 0u;
     for (int q = 0; q < C; ++q) {
         base = min(base, T->mm_in[q][0]);
@@ -1101,49 +1117,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
                                    tc::map_to_rank(tc::smem_u32(&T->bar_h[p]), q));
         }
         if (warp == 0) {
-            // lane: digits 8 lane .. 8 lane + 7 summed over the cluster; the bin of
-            // the rem-th largest key still in play
             const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_h[p]), (pass >> 1) & 1, status);
-            int g[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = 0;
-            if (ok) {
-                for (int q = 0; q < C; ++q) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(&T->hin[p][q][8 * lane]);
-                    const uint4 c = *reinterpret_cast<const uint4*>(&T->hin[p][q][8 * lane + 4]);
-                    g[0] += a.x; g[1] += a.y; g[2] += a.z; g[3] += a.w;
-                    g[4] += c.x; g[5] += c.y; g[6] += c.z; g[7] += c.w;
-                }
-            }
-            int tl = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) tl += g[j];
-            int x = tl;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_down_sync(0xffffffffu, x, o);
-                if (lane + o < 32) x += y;
-            }
-            int above = x - tl;
-#pragma unroll
-            for (int j = 7; j >= 0; --j) {
-                if (above < rem && rem <= above + g[j]) {
-                    T->prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << lo);
-                    T->rem = rem - above;
-                    T->done = (lo == 0) || (g[j] == rem - above);
-                    T->decided = pass + 1;
-                }
-                above += g[j];
-            }
-            __syncwarp();
-            if (lane == 0 && (!ok || T->decided != pass + 1)) T->failed = 1;
+            ctk_decide(T->hin[p], C, ok, prefix, lo, rem, pass, &T->dec);
         }
         __syncthreads();
-        if (T->failed) return;
-        prefix = T->prefix;
-        rem = T->rem;
+        if (T->dec.failed) return;
+        prefix = T->dec.prefix;
+        rem = T->dec.rem;
         plo = lo;
-        if (T->done) break;
+        if (T->dec.done) break;
         lo = lo > 8 ? lo - 8 : 0;
     }
     // ordered compaction: warp w walks its range of this CTA's slots 32 keys at a
@@ -1198,10 +1180,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
                            static_cast<uint32_t>(ce), tc::map_to_rank(tc::smem_u32(&T->bar_cnt), tid));
     if (warp == 0) {
         const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_cnt), 0, status);
-        if (lane == 0 && !ok) T->failed = 1;
+        if (lane == 0 && !ok) T->dec.failed = 1;
     }
     __syncthreads();
-    if (T->failed) return;
+    if (T->dec.failed) return;
     for (int q = 0; q < rank; ++q) {
         g += T->cnt_in[q][0];
         e += T->cnt_in[q][1];
