@@ -105,3 +105,13 @@ def test_algorithmic_bytes_match_the_scope_table():
     assert ab["indexer"] == 0 and ab["mla"] == pytest.approx(39.72e6, rel=5e-3)
     ab = bench.algorithmic_bytes(w["c4a_1m_b4"], 1048576)
     assert ab["indexer"] + ab["mla"] == pytest.approx(145.65e6, rel=2e-3)
+
+
+def test_reference_arm_names_what_it_cannot_time():
+    # the reference arm times the headline workload only; for the others it
+    # prints one line saying so and exits 0
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "c128a_128k_b64"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "headline" in line["unavailable"]
