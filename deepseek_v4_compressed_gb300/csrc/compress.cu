@@ -36,8 +36,13 @@ struct CompressParams {
     int* status;
 };
 
-// Per-block double reduction of the RMSNorm sum of squares (any order: the
-// double sum is rounded once to fp32 afterwards).
+// Per-block double reduction of the RMSNorm sum of squares, in the fixed
+// association that defines the mean square: each thread's pair (channels 2i,
+// 2i + 1) summed first, a butterfly over the 32 lanes of each warp (= one
+// 64-channel group; at distance 16, 8, 4, 2, 1 lane l adds lane l ^ distance),
+// then the warps' totals added to 0 in ascending warp order.  Double addition
+// is commutative, so every lane of a warp holds the same total, and the
+// result is the same bits wherever the order is followed.
 template <int NT>
 __device__ __forceinline__ double block_sum_d(double v, double* red)
 {
@@ -223,7 +228,7 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
     }
     const float y0 = __fdiv_rn(n0, d0), y1 = __fdiv_rn(n1, d1);
 
-    // RMSNorm: mean square accumulated in double, rounded once.
+    // RMSNorm: mean square accumulated in double in the fixed order, rounded once.
     const double ss = block_sum_d<NT>(static_cast<double>(y0) * y0 + static_cast<double>(y1) * y1, red_d);
     const float ms = __double2float_rn(ss / static_cast<double>(D));
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, P.eps)));

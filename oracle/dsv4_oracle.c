@@ -322,14 +322,38 @@ int or_compress_pool(int ratio, int d, const uint16_t* kv_score, long long row_s
 
 /* RMSNorm over the d channels, weight w ([vLLM-classes] DeepseekCompressor:
  * self.norm = RMSNorm(head_dim, eps); "compress -> RMSNorm -> RoPE").
- * Reading (precision): the mean square is accumulated in double and rounded
- * once to fp32; then inv = 1 / sqrt(ms + eps) and z = (y * inv) * w, each an
- * IEEE-rounded fp32 operation. */
+ * Reading (precision and summation order): the pages give the mean of the
+ * squares but not how the sum is formed.  It is formed here in double in one
+ * fixed association, so that every implementation following it gets the same
+ * bits:
+ *  - the squares of channels 2i and 2i+1 are added first (pair i);
+ *  - the 32 pair sums of each group of 64 channels are combined by a
+ *    butterfly of five levels: at distance 16, 8, 4, 2 and 1, element l
+ *    becomes element l plus element (l xor distance); element 0 is then the
+ *    group's total;
+ *  - the group totals are added to 0 in ascending group order.
+ * Every square of an fp32 value is exact in double, so this order alone
+ * decides the rounding.  The sum is divided by d in double and rounded once
+ * to fp32; then inv = 1 / sqrt(ms + eps) and z = (y * inv) * w, each an
+ * IEEE-rounded fp32 operation.  d must be a multiple of 64. */
 void or_rmsnorm(const float* y, int d, const float* w, float eps, float* z)
 {
     double ss = 0.0;
-    for (int c = 0; c < d; ++c)
-        ss += (double)y[c] * (double)y[c];
+    for (int g = 0; g < d / 64; ++g) {
+        double v[32], nv[32];
+        for (int l = 0; l < 32; ++l) {
+            double a = (double)y[64 * g + 2 * l];
+            double b = (double)y[64 * g + 2 * l + 1];
+            double aa = a * a, bb = b * b;
+            v[l] = aa + bb;
+        }
+        for (int dist = 16; dist >= 1; dist /= 2) {
+            for (int l = 0; l < 32; ++l)
+                nv[l] = v[l] + v[l ^ dist];
+            memcpy(v, nv, sizeof v);
+        }
+        ss += v[0];
+    }
     float ms = (float)(ss / (double)d);
     float root = sqrtf(ms + eps);
     float inv = 1.0f / root;

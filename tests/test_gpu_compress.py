@@ -212,3 +212,25 @@ def test_pair_launch_bit_exact(ratio):
             got = entries_from_pages(st["kind"], host, st["bt"][b], n)
             want = oracle_entries(st["kind"], st["ratio"], st["streams"][b], st["ape"], st["w"], cs)
             assert_bytes_equal(got, want, "%s seq %d" % (name, b))
+
+
+@pytest.mark.parametrize("kind,d", [(B.CACHE_IDX, 128), (B.CACHE_MLA, 576)])
+def test_rmsnorm_order_sensitive_vector_bytes_equal(kind, d):
+    """A stream whose RMSNorm sum of squares rounds differently in ascending
+    channel order than in the fixed butterfly-then-groups order (the fp32 mean
+    squares differ, asserted here): the kernel's cache bytes still equal the
+    oracle's, token by token and in one multi-token call."""
+    from _rms_case import ascending_sum, butterfly_sum, mean_square_pair, pooled_vector, token_rows
+    y = pooled_vector(d)
+    assert ascending_sum(y) != butterfly_sum(y)
+    ms_asc, ms_tree = mean_square_pair(d)
+    assert ms_asc != ms_tree
+    ks = token_rows(d)
+    ape = np.zeros((4, 2 * d), np.float32)
+    w = np.ones(d, np.float32)
+    cs = oracle.rope_table(8, 64)
+    want = oracle_entries(kind, 4, ks, ape, w, cs)
+    assert want[0].shape[0] == 1
+    for chunks in (None, [[4]]):
+        got = run_gpu_streams(kind, 4, [(ks, ape, w)], chunks, cs)
+        assert_bytes_equal(got[0], want, "order-sensitive d=%d chunks=%s" % (d, chunks))

@@ -274,3 +274,31 @@ def test_page_write_follows_block_table():
         r = j % 64
         assert np.array_equal(pg[r * 640:(r + 1) * 640], data[j])
         assert np.array_equal(pg[64 * 640 + r * 8: 64 * 640 + (r + 1) * 8], sc[j])
+
+
+def test_rmsnorm_sum_order_is_the_fixed_one():
+    """The RMSNorm mean square is summed in one fixed association (channel
+    pairs, a 32-way butterfly per 64-channel group, groups in ascending order).
+    The crafted stream makes that order matter: summed in ascending channel
+    order the mean square rounds to the other fp32 neighbour, and the indexer
+    entry's stored fp32 scale (amax / 448) would differ."""
+    from _rms_case import ascending_sum, butterfly_sum, mean_square_pair, pooled_vector, token_rows
+    d = 128
+    y = pooled_vector(d)
+    assert ascending_sum(y) != butterfly_sum(y)
+    ms_asc, ms_tree = mean_square_pair(d)
+    assert ms_asc != ms_tree
+    ks = token_rows(d)
+    ape = np.zeros((4, 2 * d), np.float32)
+    # the compressor pools exactly the constructed vector
+    assert np.array_equal(oracle.compress_pool(4, ks, ape, 3), y)
+
+    def scale_for(ms):
+        inv = np.float32(1) / np.sqrt(ms + np.float32(1e-6))
+        return np.max(np.abs(y * inv)) / np.float32(448)
+
+    cs = oracle.rope_table(4, 64)
+    data, sc = oracle.compress_stream(1, 4, ks, ape, np.ones(d, np.float32), 1e-6, cs, nope_dim=64)
+    stored = sc.view(np.float32).ravel()[0]
+    assert scale_for(ms_tree) != scale_for(ms_asc)
+    assert stored == scale_for(ms_tree)
