@@ -9,6 +9,7 @@
 #include "plan.h"
 #include "tc_common.cuh"
 #include "tmap.h"
+#include "host_once.h"
 
 namespace dsv4 {
 
@@ -1257,17 +1258,19 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         P.out_stride = a->out_stride;
         P.out_len = a->out_len_dev;
         const bool fused = plan->idx_fused_topk != 0;
-        static bool tc_attr = false;
-        if (!tc_attr) {
-            cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmem);
-            cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kIdxSmemFused);
+        static PerDeviceOnce tc_attr;
+        const bool attr_ok = tc_attr.run([] {
             // the whole unified L1 as shared memory
-            cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-            cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-            tc_attr = true;
-        }
+            return cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kIdxSmem) == cudaSuccess &&
+                   cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kIdxSmemFused) == cudaSuccess &&
+                   cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared) == cudaSuccess &&
+                   cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+        });
+        if (!attr_ok) return DSV4_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(plan->idx_ctas_per_seq, B, 1);
         cfg.blockDim = dim3(kIdxThreads, 1, 1);
@@ -1311,13 +1314,14 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         // long rows: a cluster of C CTAs per query (8192 keys or more each), S
         // keys each; clusters of more than 8 CTAs need the non-portable size,
         // and a launch the device refuses is retried with 8
-        static bool tkc_attr = false;
-        if (!tkc_attr) {
-            cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch)));
-            cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            tkc_attr = true;
-        }
+        static PerDeviceOnce tkc_attr;
+        if (!tkc_attr.run([] {
+                return cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch))) == cudaSuccess &&
+                       cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                            1) == cudaSuccess;
+            }))
+            return DSV4_ERR_CUDA;
         for (int cmax = kTkcMaxCluster; cmax >= kCtkMaxCluster; cmax /= 2) {
             const int Cq = min(cmax, (plan->max_slots + 8191) / 8192);
             const int S = ((plan->max_slots + Cq - 1) / Cq + 31) & ~31;
@@ -1346,11 +1350,12 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
     }
     const int smem_keys = plan->max_slots <= kTopkSmemKeys ? plan->max_slots : 0;
     const size_t smem = static_cast<size_t>(smem_keys) * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemKeys * 4);
-        attr_set = true;
-    }
+    static PerDeviceOnce topk_attr;
+    if (!topk_attr.run([] {
+            return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kTopkSmemKeys * 4) == cudaSuccess;
+        }))
+        return DSV4_ERR_CUDA;
     topk_kernel<<<B, kTopkThreads, smem, st>>>(logits, plan->logits_stride, plan->max_slots, a->ctx_len_dev,
                                                plan->topk, a->out_idx_dev, a->out_stride, a->out_len_dev,
                                                smem_keys);

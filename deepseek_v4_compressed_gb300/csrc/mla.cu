@@ -10,6 +10,7 @@
 #include "plan.h"
 #include "tc_common.cuh"
 #include "tmap.h"
+#include "host_once.h"
 
 namespace dsv4 {
 
@@ -847,11 +848,12 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     if (!encode_tmap(&tm_swa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->swa_cache_dev, sdims, sstr, sbox,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return DSV4_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(mla_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        attr_set = true;
-    }
+    static PerDeviceOnce attr_once;
+    if (!attr_once.run([] {
+            return cudaFuncSetAttribute(mla_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) ==
+                   cudaSuccess;
+        }))
+        return DSV4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T.cluster, plan->batch * T.head_groups, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);

@@ -332,6 +332,9 @@ dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_indexer_args* ar
  *   - All calls share the one array: calls whose executions overlap on the
  *     GPU (other streams, other host threads) race on it.  Nothing in it has
  *     to start at zero; each call writes every logit it reads.
+ *   - The looked-up address belongs to the device's current context.  After
+ *     cudaDeviceReset (or any other end of that context) it is stale: do not
+ *     call this entry point on that device again in the same process.
  * Arguments and errors otherwise as dsv4_indexer_topk. */
 dsv4_status dsv4_indexer_topk_noalloc(const dsv4_plan* plan, const dsv4_indexer_args* args,
                                       dsv4_stream_t stream);

@@ -1,0 +1,254 @@
+"""A decode loop of one c4a layer exactly as the benchmark runs it: per step
+dsv4_compress_insert_pair (both compressor streams, one token per sequence),
+dsv4_indexer_topk and dsv4_sparse_mla_decode, back to back on one stream
+(programmatic dependent launch between them), captured in a CUDA graph and
+replayed.  Steps include ratio-4 boundaries: the slot emitted by the
+compressor in a step must be visible to that step's indexer and attention.
+
+Expected values come from the oracle: cache entries (pool -> RMSNorm -> RoPE
+-> quantise), indexer logits, top-k and attention.  Inputs come from the
+seeded generators; at boundary steps the queries are built from the oracle's
+entry for the new slot so that the indexer must select it and the attention
+must be dominated by it.
+"""
+import concurrent.futures
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from deepseek_v4_compressed_gb300 import binding as B
+from deepseek_v4_compressed_gb300 import synth
+
+from _util import SCALE, bf16_bits, bits_tensor, check_attention, check_topk, dev
+
+EPS = 1e-6
+D_MAIN, D_IDX = 576, 128
+
+
+def _pool():
+    return concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4))
+
+
+def oracle_entry(kind, ks, ape, w, cs, p):
+    """The compressed entry emitted at boundary p (oracle steps, one entry)."""
+    nope = 512 if kind == B.CACHE_MLA else 64
+    y = oracle.compress_pool(4, ks, ape, p)
+    z = oracle.rmsnorm(y, w, EPS)
+    z[nope:] = oracle.rope_gptj(z[nope:], cs[(p // 4) * 4])
+    if kind == B.CACHE_MLA:
+        d, s = oracle.quant_mla_rows(z[None])
+    else:
+        d, s = oracle.quant_idx_rows(z[None])
+    return d[0], s[0]
+
+
+def dequant_nope(data, sc):
+    return oracle.e4m3_to_f64(data[:512]) * np.repeat(2.0 ** (sc[:8].astype(np.int64) - 127), 64)
+
+
+def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
+    """prefill: 'stream' runs tokens 0..L0-1 through the library's multi-token
+    compressor (caches and ring built by the library, checked against the
+    oracle's whole-stream entries); 'direct' writes oracle-quantised random
+    rows into the slots below L0 // 4 and the ring rows of tokens L0-8..L0-1
+    (the compressor state layout of dsv4.h) so that long contexts stay cheap."""
+    g = synth.rng(seed)
+    L0 = np.broadcast_to(np.asarray(L0, np.int64), (batch,)).astype(np.int64).copy()
+    T = L0 + n_steps
+    Tmax = int(T.max())
+    cs = oracle.rope_table(Tmax + 1, 64)
+    ape_m = synth.normal(g, (4, 2 * D_MAIN), 0.1)
+    ape_i = synth.normal(g, (4, 2 * D_IDX), 0.1)
+    w_m = synth.uniform(g, D_MAIN, 0.5, 1.5)
+    w_i = synth.uniform(g, D_IDX, 0.5, 1.5)
+    lo = np.zeros(batch, np.int64) if prefill == "stream" else np.maximum(L0 - 8, 0)
+    ks_m, ks_i = [], []
+    for b in range(batch):
+        km = np.zeros((int(T[b]), 4 * D_MAIN), np.uint16)
+        ki = np.zeros((int(T[b]), 4 * D_IDX), np.uint16)
+        km[lo[b]:] = bf16_bits(synth.normal(g, (int(T[b] - lo[b]), 4 * D_MAIN)))
+        ki[lo[b]:] = bf16_bits(synth.normal(g, (int(T[b] - lo[b]), 4 * D_IDX)))
+        ks_m.append(km)
+        ks_i.append(ki)
+
+    # entries of every slot below T // 4, in the oracle
+    n_ent = T // 4
+    pps = int(max(1, (n_ent.max() + 63) // 64))
+    comp_bt = synth.page_tables(g, batch, pps, extra_pages=1)
+    idx_bt = synth.page_tables(g, batch, pps, extra_pages=1)
+    ent_m, ent_i = [], []
+
+    def entries(b):
+        if prefill == "stream":
+            dm, sm = oracle.compress_stream(0, 4, ks_m[b], ape_m, w_m, EPS, cs, nope_dim=512)
+            di, si = oracle.compress_stream(1, 4, ks_i[b], ape_i, w_i, EPS, cs, nope_dim=64)
+            return (dm, sm), (di, si)
+        return None
+
+    if prefill == "stream":
+        with _pool() as ex:
+            res = list(ex.map(entries, range(batch)))
+        ent_m = [r[0] for r in res]
+        ent_i = [r[1] for r in res]
+    else:
+        pool_n = 4096
+        pm, psm = oracle.quant_mla_rows(synth.normal(g, (pool_n, D_MAIN), 1.0))
+        for b in range(batch):
+            n0 = int(L0[b] // 4)
+            pick = g.integers(0, pool_n, size=int(n_ent[b]))
+            dm, sm = pm[pick].copy(), psm[pick].copy()
+            di, si = oracle.quant_idx_rows(synth.normal(g, (int(n_ent[b]), D_IDX), 1.0))
+            for p in range(int(L0[b]), int(T[b])):
+                if (p + 1) % 4 == 0:
+                    j = p // 4
+                    dm[j], sm[j] = oracle_entry(B.CACHE_MLA, ks_m[b], ape_m, w_m, cs, p)
+                    di[j], si[j] = oracle_entry(B.CACHE_IDX, ks_i[b], ape_i, w_i, cs, p)
+            assert n0 <= n_ent[b]
+            ent_m.append((dm, sm))
+            ent_i.append((di, si))
+    comp_o = np.zeros((batch * pps + 1) * oracle.page_bytes(0), np.uint8)
+    idx_o = np.zeros((batch * pps + 1) * oracle.page_bytes(1), np.uint8)
+    for b in range(batch):
+        oracle.page_write(0, comp_o, comp_bt[b], *ent_m[b])
+        oracle.page_write(1, idx_o, idx_bt[b], *ent_i[b], nope_dim=64)
+
+    # SWA cache: rows of tokens max(0, L0 - 128) .. T - 1 (the windows of every step)
+    swa_lp = (Tmax + 63) // 64
+    swa_bt = np.full((batch, swa_lp), -1, np.int32)
+    npg = 0
+    for b in range(batch):
+        for lp in range(max(0, int(L0[b]) - 128) // 64, (int(T[b]) - 1) // 64 + 1):
+            swa_bt[b, lp] = npg
+            npg += 1
+    swa = bf16_bits(synth.normal(g, (npg * 64, 576), SCALE))
+
+    # per-step queries; at a boundary step the new slot's own codes / latent
+    steps = []
+    for s in range(n_steps):
+        st = dict(p=(L0 + s).astype(np.int32))
+        qi = oracle.f32_to_e4m3(synth.normal(g, (batch, HI, 128)))
+        wq = synth.uniform(g, (batch, HI))
+        q = synth.normal(g, (batch, H, 576), SCALE)
+        st["boundary"] = [(int(st["p"][b]) + 1) % 4 == 0 for b in range(batch)]
+        for b in range(batch):
+            if st["boundary"][b]:
+                j = int(st["p"][b]) // 4
+                qi[b, :, :] = ent_i[b][0][j]
+                q[b, :, :512] = dequant_nope(ent_m[b][0][j], ent_m[b][1][j]).astype(np.float32)
+        st["qi"], st["w"], st["q"] = qi, wq, bf16_bits(q)
+        steps.append(st)
+
+    # ---- GPU
+    plan = B.Plan(B.C4A, H, batch, k, Tmax, idx_heads=HI)
+    ws = plan.workspace()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    comp = torch.zeros(comp_o.size, dtype=torch.uint8, device="cuda")
+    idxc = torch.zeros(idx_o.size, dtype=torch.uint8, device="cuda")
+    t_comp_bt, t_idx_bt = dev(comp_bt), dev(idx_bt)
+    st_m = torch.zeros((batch, 8, 4 * D_MAIN), dtype=torch.float32, device="cuda")
+    st_i = torch.zeros((batch, 8, 4 * D_IDX), dtype=torch.float32, device="cuda")
+    t_ape_m, t_ape_i, t_w_m, t_w_i, t_cs = dev(ape_m), dev(ape_i), dev(w_m), dev(w_i), dev(cs)
+    seqs = dev(np.arange(batch, dtype=np.int32))
+    if prefill == "stream":
+        for kind, ks, ape, w, st, cache, bt in ((B.CACHE_MLA, ks_m, t_ape_m, t_w_m, st_m, comp, t_comp_bt),
+                                                (B.CACHE_IDX, ks_i, t_ape_i, t_w_i, st_i, idxc, t_idx_bt)):
+            rows, ps, sq = [], [], []
+            for b in range(batch):
+                rows.append(ks[b][:L0[b]])
+                ps += list(range(int(L0[b])))
+                sq += [b] * int(L0[b])
+            B.compress_insert(kind, 4, bits_tensor(np.concatenate(rows)), dev(np.array(ps, np.int32)),
+                              dev(np.array(sq, np.int32)), ape, w, EPS, t_cs, st, cache, bt, batch,
+                              one_token_per_seq=False, status=status)
+    else:
+        # slots below L0 // 4 hold their entries already; the ring holds tokens L0-8 .. L0-1
+        n0 = [int(L0[b] // 4) for b in range(batch)]
+        part_c = np.zeros_like(comp_o)
+        part_i = np.zeros_like(idx_o)
+        for b in range(batch):
+            oracle.page_write(0, part_c, comp_bt[b], ent_m[b][0][:n0[b]], ent_m[b][1][:n0[b]])
+            oracle.page_write(1, part_i, idx_bt[b], ent_i[b][0][:n0[b]], ent_i[b][1][:n0[b]], nope_dim=64)
+        comp.copy_(dev(part_c))
+        idxc.copy_(dev(part_i))
+        ring_m = np.zeros((batch, 8, 4 * D_MAIN), np.float32)
+        ring_i = np.zeros((batch, 8, 4 * D_IDX), np.float32)
+        for b in range(batch):
+            for t in range(int(lo[b]), int(L0[b])):
+                for ring, ks, ape, d in ((ring_m, ks_m, ape_m, D_MAIN), (ring_i, ks_i, ape_i, D_IDX)):
+                    row = oracle.bf16_to_f32(ks[b][t])
+                    ring[b, t % 8, :2 * d] = row[:2 * d]
+                    ring[b, t % 8, 2 * d:] = (row[2 * d:] + ape[t % 4]).astype(np.float32)
+        st_m.copy_(dev(ring_m))
+        st_i.copy_(dev(ring_i))
+    t_swa, t_swa_bt = bits_tensor(swa), dev(swa_bt)
+    gin = []
+    for s, st in enumerate(steps):
+        kvm = bits_tensor(np.stack([ks_m[b][st["p"][b]] for b in range(batch)]))
+        kvi = bits_tensor(np.stack([ks_i[b][st["p"][b]] for b in range(batch)]))
+        gin.append(dict(kvm=kvm, kvi=kvi, pos=dev(st["p"]), ctx=dev(st["p"] + 1), qi=dev(st["qi"]),
+                        w=dev(st["w"]), q=bits_tensor(st["q"]),
+                        idx=torch.full((batch, k), -9, dtype=torch.int32, device="cuda"),
+                        len=torch.full((batch,), -9, dtype=torch.int32, device="cuda"),
+                        out=torch.zeros((batch, H, 512), dtype=torch.bfloat16, device="cuda"),
+                        lse=torch.zeros((batch, H), dtype=torch.float32, device="cuda")))
+    torch.cuda.synchronize()
+
+    def decode_steps():
+        for x in gin:
+            B.compress_insert_pair(
+                dict(kind=B.CACHE_MLA, ratio=4, kv_score=x["kvm"], positions=x["pos"], seqs=seqs, ape=t_ape_m,
+                     rms_weight=t_w_m, rms_eps=EPS, cos_sin=t_cs, state=st_m, cache=comp, block_table=t_comp_bt,
+                     num_seqs=batch, status=status),
+                dict(kind=B.CACHE_IDX, ratio=4, kv_score=x["kvi"], positions=x["pos"], seqs=seqs, ape=t_ape_i,
+                     rms_weight=t_w_i, rms_eps=EPS, cos_sin=t_cs, state=st_i, cache=idxc, block_table=t_idx_bt,
+                     num_seqs=batch, status=status))
+            B.indexer_topk(plan, x["qi"], x["w"], idxc, t_idx_bt, x["ctx"], x["idx"], x["len"], ws, status)
+            B.sparse_mla_decode(plan, x["q"], t_swa, t_swa_bt, x["ctx"], x["out"], ws, comp_cache=comp,
+                                comp_block_table=t_comp_bt, topk_idx=x["idx"], topk_len=x["len"], lse=x["lse"],
+                                status=status)
+
+    if graph:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            decode_steps()
+        gr.replay()
+    else:
+        decode_steps()
+    torch.cuda.synchronize()
+    st_code, bits = B.read_device_status(status)
+    assert st_code == B.OK, bits
+
+    # ---- checks
+    assert np.array_equal(comp.cpu().numpy(), comp_o), "compressed cache bytes differ from the oracle"
+    assert np.array_equal(idxc.cpu().numpy(), idx_o), "indexer cache bytes differ from the oracle"
+    tolerated = 0
+    n_boundary = 0
+    for s, (st, x) in enumerate(zip(steps, gin)):
+        gidx, glen = x["idx"].cpu().numpy(), x["len"].cpu().numpy()
+        gout, glse = x["out"].float().cpu().numpy(), x["lse"].cpu().numpy()
+
+        def check(b):
+            p = int(st["p"][b])
+            n_c = (p + 1) // 4
+            logits = oracle.indexer_logits(st["qi"][b], st["w"][b], idx_o, idx_bt[b], n_c)
+            tol = check_topk(gidx[b], int(glen[b]), logits, k)
+            if st["boundary"][b]:
+                assert p // 4 in set(gidx[b][:glen[b]].tolist()), "step %d seq %d: new slot not selected" % (s, b)
+            sel = gidx[b][:glen[b]].copy()
+            ref, ref_lse, _ = oracle.sparse_mla(st["q"][b], comp_o, comp_bt[b], sel, int(glen[b]), swa, swa_bt[b],
+                                                p, SCALE)
+            check_attention(gout[b], ref, "step %d seq %d" % (s, b))
+            np.testing.assert_allclose(glse[b], ref_lse, rtol=1e-3, atol=1e-3)
+            if st["boundary"][b]:
+                # the new slot dominates: the output is close to its latent
+                lat = dequant_nope(ent_m[b][0][p // 4], ent_m[b][1][p // 4])
+                assert np.linalg.norm(gout[b] - lat[None, :]) / np.linalg.norm(np.broadcast_to(lat, gout[b].shape)) < 0.1
+            return tol
+
+        with _pool() as ex:
+            tolerated += sum(ex.map(check, range(batch)))
+        n_boundary += sum(st["boundary"])
+    return tolerated, n_boundary

@@ -23,6 +23,11 @@ ATT_MEAN_ABS = 2e-3
 ATT_REL_L2 = 1e-2
 TOPK_REL = 1e-3
 
+# Top-k parity record of the session: rows compared, slots that differ from
+# the oracle's set (all within TOPK_REL of the k-th score, else the check
+# fails) and oracle slots inside that band; conftest prints the totals.
+TOPK_STATS = {"rows": 0, "differ": 0, "in_band": 0}
+
 
 def bf16_bits(x):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16) \
@@ -151,6 +156,7 @@ def check_topk(gpu_idx, gpu_len, logits, k):
     """Top-k set rule: exact, except slots whose oracle score is within 1e-3
     relative of the k-th score.  Returns the number of such tolerated slots."""
     n = logits.size
+    TOPK_STATS["rows"] += 1
     o_idx, o_len = oracle.topk(logits, k)
     assert gpu_len == o_len, (gpu_len, o_len)
     g = gpu_idx[:gpu_len]
@@ -164,6 +170,8 @@ def check_topk(gpu_idx, gpu_len, logits, k):
     diff = np.setxor1d(g, o_idx[:o_len])
     near = np.abs(logits[diff] - kth) <= TOPK_REL * abs(kth)
     assert np.all(near), "slots %s differ and are not near the k-th score" % diff[~near][:10]
+    TOPK_STATS["differ"] += int(diff.size)
+    TOPK_STATS["in_band"] += int(np.count_nonzero(np.abs(logits - kth) <= TOPK_REL * abs(kth)))
     return int(diff.size)
 
 

@@ -24,3 +24,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Top-k parity totals: rows compared against the oracle, slots that
+    differ from its set (each within 1e-3 relative of the k-th score), and
+    oracle slots inside that near-tie band."""
+    mod = sys.modules.get("_util")
+    st = getattr(mod, "TOPK_STATS", None) if mod else None
+    if st and st["rows"]:
+        terminalreporter.write_line(
+            "top-k parity: %d rows compared with the oracle; %d slots differ from its set, all within 1e-3 "
+            "relative of the k-th score; %d oracle slots lie in that near-tie band" %
+            (st["rows"], st["differ"], st["in_band"]))

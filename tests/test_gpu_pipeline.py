@@ -79,10 +79,14 @@ def test_tiny_c4a_end_to_end():
     torch.cuda.synchronize()
     assert np.array_equal(cache_main.cpu().numpy(), comp)
     assert np.array_equal(cache_idx.cpu().numpy(), idxc)
-    tol = check_topk(out_idx.cpu().numpy()[0], int(out_len.cpu()[0]), logits, K)
-    if tol == 0:
-        check_attention(out.float().cpu().numpy()[0], ref)
-        np.testing.assert_allclose(lse.cpu().numpy()[0], ref_lse, rtol=1e-3, atol=1e-3)
+    g_idx, g_len = out_idx.cpu().numpy()[0], int(out_len.cpu()[0])
+    tol = check_topk(g_idx, g_len, logits, K)
+    if tol:
+        # near-ties: the GPU's set is a valid top-k; attend over it in the oracle
+        ref, ref_lse, _ = oracle.sparse_mla(q[0], comp, bt[0], g_idx[:g_len].copy(), g_len, swa, swa_bt[0],
+                                            L - 1, SCALE)
+    check_attention(out.float().cpu().numpy()[0], ref)
+    np.testing.assert_allclose(lse.cpu().numpy()[0], ref_lse, rtol=1e-3, atol=1e-3)
 
 
 def test_indexcache_reuse_layer_reads_its_own_kv():
@@ -153,3 +157,99 @@ def test_bad_block_table_is_flagged_not_faulted():
                         topk_len=torch.full((2,), 32, dtype=torch.int32, device="cuda"), status=status)
     st, bits = B.read_device_status(status)
     assert st == B.ERR_DEVICE_CHECK and bits & B.DEV_BAD_INDEX
+
+
+@pytest.mark.parametrize("case", ["b4_streamed_prefill", "c4a_32k_b32"])
+def test_bench_call_chain_under_dependent_launch(case):
+    """The benchmark's decode loop (compress pair -> indexer + top-k -> sparse
+    MLA under programmatic dependent launch, captured in a CUDA graph) over
+    steps that include ratio-4 boundaries: the slot a step's compressor emits
+    is selected by that step's indexer and dominates its attention, and every
+    cache byte, top-k set and output matches the oracle."""
+    from _chain import run_chain
+    if case == "b4_streamed_prefill":
+        tol, nb = run_chain(4, [1021, 2046, 517, 3072], 6, 64, 64, 64, seed=51, prefill="stream")
+    else:
+        tol, nb = run_chain(32, 32763, 5, 64, 64, 512, seed=52, prefill="direct")
+    assert nb > 0
+    print("boundary steps checked:", nb, "near-tie slots tolerated:", tol)
+
+
+def test_mixed_stack_plans_b16_64k():
+    """The 60-layer stack's per-type plans at its full size (batch 16, context
+    65536, 64 heads, top-k 512): a swaonly layer, a c4a layer that runs the
+    indexer (16384 slots per sequence: on 152 SMs the logits take 9 CTAs per
+    sequence and the top-k a separate cluster launch), a c4a reuse layer under
+    IndexCache frequency 2 (the previous c4a layer's indices over its own
+    caches and query) and a c128a layer whose metadata selects all 512
+    visible slots.  All calls in order on one stream; every output against
+    the oracle."""
+    import concurrent.futures
+    from _util import make_decode_inputs
+    ratios = [1, 4, 4, 128]
+    skip = B.index_schedule(ratios, True, 2)
+    assert skip == [0, 0, 1, 0]
+    Bsz, L, H, K = 16, 65536, 64, 512
+    d_sw = make_decode_inputs(1, Bsz, L, H, 0, 0, seed=61)
+    d_c1 = make_decode_inputs(4, Bsz, L, H, 64, K, seed=62)
+    d_c2 = make_decode_inputs(4, Bsz, L, H, 64, K, seed=63)
+    d_128 = make_decode_inputs(128, Bsz, L, H, 0, K, seed=64)
+    assert np.all(d_128.meta_len == 512) and np.array_equal(d_128.meta_idx[0], np.arange(512))
+    p_sw = B.Plan(B.SWAONLY, H, Bsz, 0, L)
+    p_c4 = B.Plan(B.C4A, H, Bsz, K, L, idx_heads=64)
+    p_128 = B.Plan(B.C128A, H, Bsz, K, L)
+    info = p_c4.info()
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert info["idx_ctas_per_seq"] == 9 and info["launches_indexer"] == 2
+    ws = torch.zeros(max(p_sw.workspace_bytes, p_c4.workspace_bytes, p_128.workspace_bytes),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    shared_idx = torch.full((Bsz, K), -9, dtype=torch.int32, device="cuda")
+    shared_len = torch.full((Bsz,), -9, dtype=torch.int32, device="cuda")
+
+    def out_buf():
+        return (torch.zeros((Bsz, H, 512), dtype=torch.bfloat16, device="cuda"),
+                torch.zeros((Bsz, H), dtype=torch.float32, device="cuda"))
+
+    outs = []
+    o, l = out_buf()
+    B.sparse_mla_decode(p_sw, d_sw.t["q"], d_sw.t["swa"], d_sw.t["swa_bt"], d_sw.t["ctx"], o, ws, lse=l, status=status)
+    outs.append((o, l))
+    for layer, d in ((1, d_c1), (2, d_c2)):
+        if not skip[layer]:
+            B.indexer_topk(p_c4, d.t["qi"], d.t["w"], d.t["idx"], d.t["idx_bt"], d.t["ctx"], shared_idx, shared_len,
+                           ws, status)
+        o, l = out_buf()
+        B.sparse_mla_decode(p_c4, d.t["q"], d.t["swa"], d.t["swa_bt"], d.t["ctx"], o, ws, comp_cache=d.t["comp"],
+                            comp_block_table=d.t["comp_bt"], topk_idx=shared_idx, topk_len=shared_len, lse=l,
+                            status=status)
+        outs.append((o, l))
+    o, l = out_buf()
+    B.sparse_mla_decode(p_128, d_128.t["q"], d_128.t["swa"], d_128.t["swa_bt"], d_128.t["ctx"], o, ws,
+                        comp_cache=d_128.t["comp"], comp_block_table=d_128.t["comp_bt"], topk_idx=d_128.t["meta_idx"],
+                        topk_len=d_128.t["meta_len"], lse=l, status=status)
+    outs.append((o, l))
+    torch.cuda.synchronize()
+    st, bits = B.read_device_status(status)
+    assert st == B.OK, bits
+    gidx, glen = shared_idx.cpu().numpy(), shared_len.cpu().numpy()
+    res = [(x.float().cpu().numpy(), y.cpu().numpy()) for x, y in outs]
+
+    def check(b):
+        logits = oracle.indexer_logits(d_c1.qi[b], d_c1.w[b], d_c1.idx, d_c1.idx_bt[b], int(d_c1.n_c[b]))
+        tol = check_topk(gidx[b], int(glen[b]), logits, K)
+        sel = gidx[b][:glen[b]].copy()
+        refs = [oracle.sparse_mla(d_sw.q[b], None, None, None, 0, d_sw.swa, d_sw.swa_bt[b], int(d_sw.p[b]), SCALE)]
+        for d in (d_c1, d_c2):
+            refs.append(oracle.sparse_mla(d.q[b], d.comp, d.comp_bt[b], sel, int(glen[b]), d.swa, d.swa_bt[b],
+                                          int(d.p[b]), SCALE))
+        refs.append(oracle.sparse_mla(d_128.q[b], d_128.comp, d_128.comp_bt[b], d_128.meta_idx[b],
+                                      int(d_128.meta_len[b]), d_128.swa, d_128.swa_bt[b], int(d_128.p[b]), SCALE))
+        for li, ((got, got_lse), (ref, ref_lse, _)) in enumerate(zip(res, refs)):
+            check_attention(got[b], ref, "layer %d seq %d" % (li, b))
+            np.testing.assert_allclose(got_lse[b], ref_lse, rtol=1e-3, atol=1e-3)
+        return tol
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=16) as ex:
+        tol = sum(ex.map(check, range(Bsz)))
+    print("near-tie slots tolerated:", tol)
