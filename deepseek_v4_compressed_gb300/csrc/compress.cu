@@ -283,7 +283,6 @@ __global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
 template <int RATIO>
 __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
 {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the indexer of this layer, launched next, starts by reading the
     // sequence's indexer block-table row (a caller input): warm it in L2
     if (static_cast<int>(blockIdx.x) >= Pm.num_tokens && threadIdx.x < 32) {
@@ -294,8 +293,12 @@ __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams
                                                           threadIdx.x * 32));
     }
     // launched behind the previous kernel of the stream (programmatic
-    // dependent launch): its outputs may be this kernel's inputs
+    // dependent launch): its outputs may be this kernel's inputs.  The
+    // indexer launched next may start once every CTA is past this wait: by
+    // then every earlier kernel is complete, and this one writes at most the
+    // newest entry of each sequence (the indexer reads the other slots early).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
         compress_token<kHead, RATIO, false, true>(Pm, blockIdx.x);
     else if (threadIdx.x < kIdx / 2)

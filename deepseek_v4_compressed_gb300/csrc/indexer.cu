@@ -408,10 +408,21 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             return pg;
         };
         int pgl = page_group(0);
-        // the cache may have been written by the kernel before this one, which
-        // this kernel may overlap (programmatic dependent launch)
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // This kernel may overlap the one before it (programmatic dependent
+        // launch).  When that is the library's decode compressor, it writes at
+        // most the newest entry of each sequence (slot n_c - 1, in the last
+        // tile), and every kernel before it is complete (the library's
+        // compressors let their dependents start only once those are); a
+        // caller kernel in between does not let this one start early.  So
+        // the tiles before the last are read at once, and the wait for the
+        // previous grid comes right before the last tile's loads -- and in
+        // every CTA, so that this grid completes only after it.
+        bool waited = false;
         for (int i = pgrp; i < n_my; i += 2) {
+            if (!waited && t_begin + i == n_tiles - 1) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                waited = true;
+            }
             if (i >= 16 && (i & 15) < 2) pgl = page_group(i & ~15);
             const int v = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15) + (lane & 1));   // this lane's page
             const int st = i % kIdxStages;
@@ -435,6 +446,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                                 0, 0, v < 0 ? P.num_pages : v);          // unreadable page: outside the map, zeros
             if (lane == 0) issued = i + 1;
         }
+        if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
     } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t idesc = tc::idesc(128, P.n_pad, tc::kFmtE4M3, tc::kFmtE4M3);
@@ -461,12 +473,13 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         }
     } else {
         // epilogue group (warps 0-3 or 4-7) takes every other tile; the scales it
-        // reads may come from the kernel before this one
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        // reads come straight from the pages, and the last tile's may be written
+        // by the kernel before this one (see the producers)
         const int grp = warp >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
         for (int i = grp; i < n_my; i += 2) {
+            if (t_begin + i == n_tiles - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
             const int ab = i % kIdxAcc;
             const uint32_t aph = (i / kIdxAcc) & 1;
             const int st = i % kIdxStages;
