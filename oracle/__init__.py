@@ -90,8 +90,66 @@ _lib.or_sparse_mla.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, 
                                _u8p, _i32p, _i32p, ctypes.c_int, _u16p, _i32p, ctypes.c_int,
                                ctypes.c_int, ctypes.c_double, _f64p, _f64p]
 
+_lib.or_e2m1_to_f64.restype = ctypes.c_double
+_lib.or_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+_lib.or_f32_to_e2m1.restype = ctypes.c_uint8
+_lib.or_f32_to_e2m1.argtypes = [ctypes.c_float]
+_lib.or_mxfp4_exponent.restype = ctypes.c_int
+_lib.or_mxfp4_exponent.argtypes = [ctypes.c_float]
+_lib.or_quant_idx_fp4_rows.restype = None
+_lib.or_quant_idx_fp4_rows.argtypes = [ctypes.c_longlong, _f32p, ctypes.c_int, _u8p, _u8p]
+_lib.or_idx_fp4_entry_bytes.restype = ctypes.c_int
+_lib.or_idx_fp4_entry_bytes.argtypes = [ctypes.c_int]
+_lib.or_indexer_logits_fp4.restype = None
+_lib.or_indexer_logits_fp4.argtypes = [_u8p, _f32p, ctypes.c_int, ctypes.c_int, _u8p, _i32p,
+                                       ctypes.c_int, ctypes.c_int, _f64p]
+
 MLA_KIND = 0
 IDX_KIND = 1
+IDX_FP4_KIND = 2
+
+
+def e2m1_to_f64(code):
+    """E2M1 code(s) (low 4 bits) -> value(s), same shape."""
+    code = np.asarray(code, np.uint8)
+    table = np.array([_lib.or_e2m1_to_f64(c) for c in range(16)], np.float64)
+    return table[code & 15]
+
+
+def f32_to_e2m1(x):
+    x = _c(x, np.float32)
+    return np.array([_lib.or_f32_to_e2m1(float(v)) for v in x.ravel()], np.uint8).reshape(x.shape)
+
+
+def mxfp4_exponent(amax: float) -> int:
+    return int(_lib.or_mxfp4_exponent(float(np.float32(amax))))
+
+
+def idx_fp4_entry_bytes(head_dim=128) -> int:
+    return int(_lib.or_idx_fp4_entry_bytes(head_dim))
+
+
+def quant_idx_fp4_rows(z):
+    """Rows [n, d] fp32 -> (codes [n, d/2] u8 (two per byte, low nibble first),
+    exponent bytes [n, d/32] u8)."""
+    z = _c(z, np.float32)
+    n, d = z.shape
+    data = np.empty((n, d // 2), np.uint8)
+    sc = np.empty((n, d // 32), np.uint8)
+    _lib.or_quant_idx_fp4_rows(n, _p(z, _f32p), d, _p(data, _u8p), _p(sc, _u8p))
+    return data, sc
+
+
+def indexer_logits_fp4(q_fp8, w, cache, block_table_row, n_c, page=64):
+    q = _c(q_fp8, np.uint8)
+    n_heads, d = q.shape
+    w = _c(w, np.float32)
+    cache = _c(cache, np.uint8)
+    bt = _c(block_table_row, np.int32)
+    out = np.empty(max(n_c, 1), np.float64)
+    _lib.or_indexer_logits_fp4(_p(q, _u8p), _p(w, _f32p), n_heads, d, _p(cache, _u8p),
+                               _p(bt, _i32p), page, int(n_c), _p(out, _f64p))
+    return out[:n_c]
 
 
 def _p(a, t):
@@ -235,14 +293,16 @@ def quant_idx_rows(z):
 def compress_stream(kind, ratio, kv_score_bf16, ape, rms_w, eps, cos_sin, nope_dim, rope_dim=64):
     """All compressed entries of one sequence's token stream, in slot order.
 
-    Returns (data [n, data_bytes] uint8, scale [n, 8] uint8 or [n] float32)."""
+    Returns (data [n, data_bytes] uint8, scale [n, 8] uint8 (main), [n] float32
+    (FP8 indexer) or [n, d/32] uint8 exponent bytes (FP4 indexer))."""
     ks = _c(kv_score_bf16, np.uint16)
     n_tok = ks.shape[0]
     n_out = n_tok // ratio
     d = nope_dim + rope_dim
-    data_b = nope_dim + 2 * rope_dim if kind == MLA_KIND else d
+    data_b = nope_dim + 2 * rope_dim if kind == MLA_KIND else (d if kind == IDX_KIND else d // 2)
+    scale_b = 8 if kind == MLA_KIND else (4 if kind == IDX_KIND else d // 32)
     data = np.zeros((max(n_out, 1), data_b), np.uint8)
-    scale = np.zeros((max(n_out, 1), 8 if kind == MLA_KIND else 4), np.uint8)
+    scale = np.zeros((max(n_out, 1), scale_b), np.uint8)
     ape = _c(ape, np.float32)
     w = _c(rms_w, np.float32)
     cs = _c(cos_sin, np.float32)
@@ -264,6 +324,9 @@ def page_bytes(kind, page=64, nope_dim=None, rope_dim=64):
     nope_dim = _nope(kind, nope_dim)
     if kind == MLA_KIND:
         return page * (nope_dim + 2 * rope_dim + 8)
+    if kind == IDX_FP4_KIND:
+        d = nope_dim + rope_dim
+        return page * (d // 2 + d // 32)
     return page * (nope_dim + rope_dim + 4)
 
 

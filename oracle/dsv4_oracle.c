@@ -425,6 +425,96 @@ void or_quant_idx(const float* z, int d, uint8_t* data, float* scale)
     *scale = s;
 }
 
+/* ---- FP4 (MXFP4) indexer cache ------------------------------------------ */
+
+/* OCP MX FP4 "E2M1": 1 sign, 2 exponent bits (bias 1), 1 mantissa bit, no
+ * infinities or NaN.  Exponent field e > 0 gives (1 + m/2) * 2^(e-1);
+ * e = 0 gives the subnormals m * 0.5.  The non-negative values are 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6.  [V4-attn] eval note use_fp4_indexer_cache (the
+ * indexer's K cache in MXFP4); [MLA-to-CSA] 6.1 (lightning-indexer K cache
+ * FP4 / MXFP4). */
+double or_e2m1_to_f64(uint8_t code)
+{
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return s ? -v : v;
+}
+
+/* Encode to E2M1: the nearest of the 8 magnitudes, ties to the even code
+ * (mantissa bit 0), magnitudes past 6 saturate to 6.  Same bisection as the
+ * E4M3 encoder: the codes 0..7 increase in value. */
+uint8_t or_f32_to_e2m1(float x)
+{
+    uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    double a = fabs((double)x);
+    if (isnan(x) || a >= 6.0)
+        return (uint8_t)(sign | 0x7);
+    int lo = 0, hi = 7;                  /* value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (or_e2m1_to_f64((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double dlo = a - or_e2m1_to_f64((uint8_t)lo);
+    double dhi = or_e2m1_to_f64((uint8_t)hi) - a;
+    int best = (dlo < dhi) ? lo : (dhi < dlo) ? hi : ((lo & 1) == 0 ? lo : hi);
+    return (uint8_t)(sign | best);
+}
+
+/* MX block exponent for FP4.
+ * Reading: the pages name MXFP4 but not how its shared scale is chosen.  We
+ * take the rule of the FP8 UE8M0 scales (or_ue8m0_exponent) with E2M1's
+ * largest magnitude 6 in place of 448: the smallest e with amax <= 6 * 2^e,
+ * so no value saturates; clamped to [-127, 127]; an all-zero block takes
+ * e = 0.  Stored as the byte e + 127. */
+int or_mxfp4_exponent(float amax)
+{
+    if (!(amax > 0.0f))
+        return 0;
+    int e = -127;
+    while (e < 127 && (double)amax > 6.0 * ldexp(1.0, e))
+        ++e;
+    return e;
+}
+
+/* FP4 indexer entry of d (= 128) dims: E2M1 codes of blocks of 32 dims, each
+ * block with its own UE8M0 exponent: code = E2M1(z * 2^-e), the scaling
+ * exact.  data holds d/2 bytes, element 2i in the low nibble of byte i and
+ * element 2i+1 in the high nibble; scales holds d/32 bytes e + 127.
+ * Reading: 64 + 4 = 68 bytes per entry, the C4 indexer's 64 x 68 B FP4 block
+ * of the V4 internals talk (the class walkthrough keeps the FP8 allocation of
+ * 132 B and uses only part of it). */
+void or_quant_idx_fp4(const float* z, int d, uint8_t* data, uint8_t* scales)
+{
+    memset(data, 0, (size_t)d / 2);
+    for (int b = 0; b < d / 32; ++b) {
+        float amax = 0.0f;
+        for (int c = 0; c < 32; ++c) {
+            float a = fabsf(z[b * 32 + c]);
+            if (a > amax)
+                amax = a;
+        }
+        int e = or_mxfp4_exponent(amax);
+        float mult = (float)ldexp(1.0, -e);
+        for (int c = 0; c < 32; ++c) {
+            int i = b * 32 + c;
+            uint8_t code = or_f32_to_e2m1(z[i] * mult);
+            data[i / 2] |= (uint8_t)((i & 1) ? (code << 4) : code);
+        }
+        scales[b] = (uint8_t)(e + 127);
+    }
+}
+
+void or_quant_idx_fp4_rows(long long n, const float* z, int d, uint8_t* data, uint8_t* scales)
+{
+    for (long long i = 0; i < n; ++i)
+        or_quant_idx_fp4(z + i * d, d, data + i * (d / 2), scales + i * (d / 32));
+}
+
+int or_idx_fp4_entry_bytes(int head_dim) { return head_dim / 2 + head_dim / 32; }
+
 /* Row-batched forms of or_quant_mla / or_quant_idx (n rows of d floats). */
 void or_quant_mla_rows(long long n, const float* z, int nope_dim, int rope_dim, uint8_t* data,
                        uint8_t* scales)
@@ -449,7 +539,9 @@ void or_quant_idx_rows(long long n, const float* z, int d, uint8_t* data, float*
  * quantised.
  * kind 0 = main cache (d = nope + rope; out_data rows of nope + 2*rope bytes,
  * out_scale rows of 8 bytes); kind 1 = indexer cache (d = nope + rope, usually
- * 64 + 64; out_data rows of d bytes, out_scale rows of one fp32).
+ * 64 + 64; out_data rows of d bytes, out_scale rows of one fp32); kind 2 =
+ * FP4 indexer cache (out_data rows of d/2 bytes, out_scale rows of d/32
+ * exponent bytes, or_quant_idx_fp4).
  * Returns the number of entries written, or -1. */
 int or_compress_stream(int kind, int ratio, int n_tokens, const uint16_t* kv_score,
                        long long row_stride, const float* ape, const float* rms_w, float eps,
@@ -474,10 +566,13 @@ int or_compress_stream(int kind, int ratio, int n_tokens, const uint16_t* kv_sco
             int eb = nope_dim + 2 * rope_dim;
             or_quant_mla(z, nope_dim, rope_dim, out_data + (long long)n_out * eb,
                          out_scale + (long long)n_out * 8);
-        } else {
+        } else if (kind == 1) {
             float s;
             or_quant_idx(z, d, out_data + (long long)n_out * d, &s);
             memcpy(out_scale + (long long)n_out * 4, &s, 4);
+        } else {
+            or_quant_idx_fp4(z, d, out_data + (long long)n_out * (d / 2),
+                             out_scale + (long long)n_out * (d / 32));
         }
         ++n_out;
     }
@@ -491,12 +586,15 @@ int or_compress_stream(int kind, int ratio, int n_tokens, const uint16_t* kv_sco
  * ([MLA-to-CSA] 6.3 slot mapping).  Page layout ([vLLM-classes] "CSA layer
  * Compressor": data plane of page*entry bytes, then the scale plane):
  *   kind 0: [page][nope + 2*rope] data, then [page][8] UE8M0 scale bytes;
- *   kind 1: [page][d] fp8 data, then [page] fp32 scales (d = nope + rope). */
+ *   kind 1: [page][d] fp8 data, then [page] fp32 scales (d = nope + rope);
+ *   kind 2: [page][d/2] E2M1 codes, then [page][d/32] exponent bytes (the
+ *           FP4 indexer cache: 64 x (64 + 4) bytes for d = 128). */
 void or_page_write(int kind, int nope_dim, int rope_dim, int page, const int* block_table,
                    int n_entries, const uint8_t* data, const uint8_t* scale, uint8_t* cache)
 {
-    int data_b = (kind == 0) ? nope_dim + 2 * rope_dim : nope_dim + rope_dim;
-    int scale_b = (kind == 0) ? 8 : 4;
+    int d = nope_dim + rope_dim;
+    int data_b = (kind == 0) ? nope_dim + 2 * rope_dim : (kind == 1 ? d : d / 2);
+    int scale_b = (kind == 0) ? 8 : (kind == 1 ? 4 : d / 32);
     long long page_b = (long long)page * (data_b + scale_b);
     for (int j = 0; j < n_entries; ++j) {
         uint8_t* base = cache + (long long)block_table[j / page] * page_b;
@@ -543,6 +641,41 @@ void or_indexer_logits(const uint8_t* q_fp8, const float* w, int n_heads, int d,
             acc += (double)w[j] * (dot > 0.0 ? dot : 0.0);
         }
         out[s] = (double)scale * acc;
+    }
+    free(qd);
+}
+
+/* Indexer logits over an FP4 indexer cache (kind 2 pages): the same
+ * formula as or_indexer_logits with k[s][c] = E2M1(code) * 2^(byte_b - 127)
+ * for the 32-dim block b of c, and no per-row fp32 scale.  The query stays
+ * FP8 E4M3 ([V4-attn]: the FP4 option changes only the indexer's K cache).
+ * Every product is exact in double, so are the 128-term dots. */
+void or_indexer_logits_fp4(const uint8_t* q_fp8, const float* w, int n_heads, int d,
+                           const uint8_t* cache, const int* block_table, int page, int n_c,
+                           double* out)
+{
+    long long page_b = (long long)page * (d / 2 + d / 32);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)n_heads * (size_t)d);
+    for (int i = 0; i < n_heads * d; ++i)
+        qd[i] = or_e4m3_to_f64(q_fp8[i]);
+    double kd[512];
+    for (int s = 0; s < n_c; ++s) {
+        const uint8_t* base = cache + (long long)block_table[s / page] * page_b;
+        int r = s % page;
+        const uint8_t* k = base + (long long)r * (d / 2);
+        const uint8_t* sc = base + (long long)page * (d / 2) + (long long)r * (d / 32);
+        for (int c = 0; c < d; ++c) {
+            uint8_t code = (c & 1) ? (uint8_t)(k[c / 2] >> 4) : (uint8_t)(k[c / 2] & 15);
+            kd[c] = or_e2m1_to_f64(code) * ldexp(1.0, (int)sc[c / 32] - 127);
+        }
+        double acc = 0.0;
+        for (int j = 0; j < n_heads; ++j) {
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c)
+                dot += qd[(long long)j * d + c] * kd[c];
+            acc += (double)w[j] * (dot > 0.0 ? dot : 0.0);
+        }
+        out[s] = acc;
     }
     free(qd);
 }

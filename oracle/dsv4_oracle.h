@@ -68,6 +68,14 @@ void or_quant_idx(const float* z, int d, uint8_t* data, float* scale);
 void or_quant_mla_rows(long long n, const float* z, int nope_dim, int rope_dim, uint8_t* data,
                        uint8_t* scales);
 void or_quant_idx_rows(long long n, const float* z, int d, uint8_t* data, float* scale);
+/* ---- FP4 (MXFP4) indexer cache ------------------------------------------ */
+double  or_e2m1_to_f64(uint8_t code);
+uint8_t or_f32_to_e2m1(float x);
+int     or_mxfp4_exponent(float amax);
+void    or_quant_idx_fp4(const float* z, int d, uint8_t* data, uint8_t* scales);
+void    or_quant_idx_fp4_rows(long long n, const float* z, int d, uint8_t* data, uint8_t* scales);
+int     or_idx_fp4_entry_bytes(int head_dim);
+
 int  or_compress_stream(int kind, int ratio, int n_tokens, const uint16_t* kv_score,
                         long long row_stride, const float* ape, const float* rms_w, float eps,
                         const float* cos_sin, int rope_dim, int nope_dim,
@@ -79,6 +87,9 @@ void or_page_write(int kind, int nope_dim, int rope_dim, int page, const int* bl
 void or_indexer_logits(const uint8_t* q_fp8, const float* w, int n_heads, int d,
                        const uint8_t* cache, const int* block_table, int page, int n_c,
                        double* out);
+void or_indexer_logits_fp4(const uint8_t* q_fp8, const float* w, int n_heads, int d,
+                           const uint8_t* cache, const int* block_table, int page, int n_c,
+                           double* out);
 int  or_topk(const double* logits, int n, int k, int* out_idx, int* out_len);
 
 /* ---- attention ----------------------------------------------------------- */
