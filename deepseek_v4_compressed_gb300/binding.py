@@ -13,7 +13,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsv4.so")
 
 SWAONLY, C4A, C128A = 1, 4, 128
-CACHE_MLA, CACHE_IDX = 0, 1
+CACHE_MLA, CACHE_IDX, CACHE_IDX_FP4 = 0, 1, 2
+IDX_FP8, IDX_FP4 = 0, 1
 
 OK, ERR_INVALID, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
@@ -21,6 +22,8 @@ DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 NOPE_DIM, ROPE_DIM, HEAD_DIM, V_DIM, IDX_DIM, PAGE, WINDOW = 512, 64, 576, 512, 128, 64, 128
 MLA_PAGE_BYTES = 64 * 648
 IDX_PAGE_BYTES = 64 * 132
+IDX_FP4_PAGE_BYTES = 64 * 68
+PAGE_BYTES = {CACHE_MLA: MLA_PAGE_BYTES, CACHE_IDX: IDX_PAGE_BYTES, CACHE_IDX_FP4: IDX_FP4_PAGE_BYTES}
 SWA_PAGE_BYTES = 64 * 576 * 2
 
 EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
@@ -28,7 +31,7 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_plan_create", "dsv4_plan_destroy", "dsv4_plan_workspace_bytes",
             "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
             "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
-            "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair"]
+            "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair", "dsv4_plan_set_indexer_format"]
 
 
 class Dsv4Error(RuntimeError):
@@ -141,6 +144,8 @@ def lib():
     L.dsv4_compress_insert_pair.argtypes = [ctypes.POINTER(CompressArgs), ctypes.POINTER(CompressArgs), vp]
     L.dsv4_selftest_key_dequant.restype = st
     L.dsv4_selftest_key_dequant.argtypes = [vp, vp]
+    L.dsv4_plan_set_indexer_format.restype = st
+    L.dsv4_plan_set_indexer_format.argtypes = [vp, ctypes.c_int]
     _lib = L
     return L
 
@@ -227,13 +232,21 @@ class Plan:
     """One plan per layer type, reused by every layer of that type in a step."""
 
     def __init__(self, layer_type, n_heads, batch, topk, max_ctx, idx_heads=64, window=WINDOW,
-                 softmax_scale=HEAD_DIM ** -0.5):
+                 softmax_scale=HEAD_DIM ** -0.5, idx_format=IDX_FP8):
         self.geom = Geom(int(n_heads), int(idx_heads), int(window), float(softmax_scale))
         h = ctypes.c_void_p()
         _check(lib().dsv4_plan_create(int(layer_type), ctypes.byref(self.geom), int(batch), int(topk),
                                       int(max_ctx), ctypes.byref(h)), "plan_create")
         self.handle = h
         self.layer_type = int(layer_type)
+        self.idx_format = IDX_FP8
+        if idx_format != IDX_FP8:
+            _check(lib().dsv4_plan_set_indexer_format(self.handle, int(idx_format)), "plan_set_indexer_format")
+            self.idx_format = int(idx_format)
+
+    @property
+    def idx_page_bytes(self):
+        return IDX_FP4_PAGE_BYTES if self.idx_format == IDX_FP4 else IDX_PAGE_BYTES
 
     @property
     def workspace_bytes(self):
@@ -262,7 +275,7 @@ def compress_insert(kind, ratio, kv_score, positions, seqs, ape, rms_weight, rms
                      int(bool(one_token_per_seq)), _ptr(kv_score), int(kv_score.stride(0)),
                      _ptr(positions), _ptr(seqs), _ptr(ape), _ptr(rms_weight), float(rms_eps),
                      _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(state), _ptr(cache),
-                     int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                     int(_nbytes(cache) // PAGE_BYTES[kind]),
                      _ptr(block_table), int(block_table.shape[1]), _ptr(status))
     _check(lib().dsv4_compress_insert(ctypes.byref(a), _stream(stream)), "compress_insert")
 
@@ -273,7 +286,7 @@ def _compress_args(kind, ratio, kv_score, positions, seqs, ape, rms_weight, rms_
                         int(bool(one_token_per_seq)), _ptr(kv_score), int(kv_score.stride(0)),
                         _ptr(positions), _ptr(seqs), _ptr(ape), _ptr(rms_weight), float(rms_eps),
                         _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(state), _ptr(cache),
-                        int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                        int(_nbytes(cache) // PAGE_BYTES[kind]),
                         _ptr(block_table), int(block_table.shape[1]), _ptr(status))
 
 
@@ -291,7 +304,7 @@ def compress_insert_pair(main, idx, stream=None):
 def cache_insert_rows(kind, rows, seqs, slots, cache, block_table, status=None, stream=None):
     a = InsertRowsArgs(int(kind), int(rows.shape[0]), _ptr(rows), _ptr(seqs), _ptr(slots),
                        _ptr(cache),
-                       int(_nbytes(cache) // (MLA_PAGE_BYTES if kind == CACHE_MLA else IDX_PAGE_BYTES)),
+                       int(_nbytes(cache) // PAGE_BYTES[kind]),
                        _ptr(block_table), int(block_table.shape[1]), int(block_table.shape[0]),
                        _ptr(status))
     _check(lib().dsv4_cache_insert_rows(ctypes.byref(a), _stream(stream)), "cache_insert_rows")
@@ -299,7 +312,7 @@ def cache_insert_rows(kind, rows, seqs, slots, cache, block_table, status=None, 
 
 def indexer_topk(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx, out_len, workspace,
                  status=None, stream=None):
-    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // IDX_PAGE_BYTES),
+    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // plan.idx_page_bytes),
                     _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
                     int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
     _check(lib().dsv4_indexer_topk(plan.handle, ctypes.byref(a), _ptr(workspace), _nbytes(workspace),
@@ -327,7 +340,7 @@ def indexer_topk_noalloc(plan, q_fp8, weights, idx_cache, block_table, ctx_len, 
     f = lib().dsv4_indexer_topk_noalloc
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p, ctypes.POINTER(IndexerArgs), ctypes.c_void_p]
-    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // IDX_PAGE_BYTES),
+    a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // plan.idx_page_bytes),
                     _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
                     int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
     _check(f(plan.handle, ctypes.byref(a), _stream(stream)), "indexer_topk_noalloc")

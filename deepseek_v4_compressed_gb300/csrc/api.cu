@@ -206,6 +206,17 @@ extern "C" dsv4_status dsv4_plan_create(dsv4_layer_type type, const dsv4_geom* g
     return DSV4_OK;
 }
 
+// The indexer cache format of a c4a plan: FP8 (the default) or MXFP4
+// ([V4-attn] use_fp4_indexer_cache; [V4-internals] section 4).
+extern "C" dsv4_status dsv4_plan_set_indexer_format(dsv4_plan* plan, dsv4_idx_format format)
+{
+    if (plan == nullptr) return DSV4_ERR_INVALID;
+    if (format != DSV4_IDX_FP8 && format != DSV4_IDX_FP4) return DSV4_ERR_INVALID;
+    if (plan->type != DSV4_C4A) return DSV4_ERR_UNSUPPORTED;
+    plan->idx_fp4 = format == DSV4_IDX_FP4;
+    return DSV4_OK;
+}
+
 extern "C" void dsv4_plan_destroy(dsv4_plan* plan) { free(plan); }
 
 extern "C" size_t dsv4_plan_workspace_bytes(const dsv4_plan* plan) { return plan ? plan->ws_bytes : 0; }

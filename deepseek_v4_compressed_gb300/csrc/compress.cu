@@ -94,9 +94,52 @@ __device__ __forceinline__ void store_idx_entry(float z0, float z1, int c0, uint
     if (threadIdx.x == 0) *scale_ptr = s;
 }
 
+// E2M1 code of v (FP4: 1 sign, 2 exponent, 1 mantissa bit): the nearest of
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6, ties to the even code, saturating at 6 (NaN
+// gives the largest code).  Written out as the comparisons that rule implies.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float v)
+{
+    const float a = fabsf(v);
+    uint32_t c;
+    if (a <= 0.25f) c = 0;
+    else if (a < 0.75f) c = 1;
+    else if (a <= 1.25f) c = 2;
+    else if (a < 1.75f) c = 3;
+    else if (a <= 2.5f) c = 4;
+    else if (a < 3.5f) c = 5;
+    else if (a <= 5.0f) c = 6;
+    else c = 7;
+    return c | ((__float_as_uint(v) >> 31) << 3);
+}
+
+// FP4 indexer entry (MXFP4): blocks of 32 dims, each with a UE8M0 exponent e
+// = the smallest with amax <= 6 * 2^e (6 = 0.75 * 2^3: with amax = m * 2^k,
+// m in [0.5, 1), e = k - 3 if m <= 0.75, else k - 2), clamped to [-127, 127],
+// 0 for an all-zero block; codes E2M1(z * 2^-e), two per byte (the low nibble
+// the even dim).  Called by all 64 threads (16 threads per block).
+__device__ __forceinline__ void store_idx_fp4_entry(float z0, float z1, int c0, uint8_t* data_row,
+                                                    uint8_t* scale_row)
+{
+    float amax = fmaxf(fabsf(z0), fabsf(z1));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = 0;
+    if (amax > 0.0f) {
+        int k;
+        const float m = frexpf(amax, &k);
+        e = (m <= 0.75f) ? k - 3 : k - 2;
+        e = e < -127 ? -127 : (e > 127 ? 127 : e);
+    }
+    // -e lies in [-126, 127] for every finite amax, so 2^-e is a normal fp32
+    const float mult = exp2i(-e);
+    const uint32_t lo = f32_to_e2m1(__fmul_rn(z0, mult)), hi = f32_to_e2m1(__fmul_rn(z1, mult));
+    data_row[c0 >> 1] = static_cast<uint8_t>(lo | (hi << 4));
+    if ((threadIdx.x & 15) == 0) scale_row[c0 >> 5] = static_cast<uint8_t>(e + 127);
+}
+
 // Resolve the page of logical slot j of sequence seq; nullptr (and a status
 // bit) when the table entry is out of range.
-template <bool IDX>
+template <int KIND>
 __device__ __forceinline__ uint8_t* entry_page(const CompressParams& P, int seq, int j)
 {
     const int pi = j / kPage;
@@ -109,7 +152,8 @@ __device__ __forceinline__ uint8_t* entry_page(const CompressParams& P, int seq,
         flag(P.status, DSV4_DEV_BAD_PAGE);
         return nullptr;
     }
-    return P.cache + static_cast<long long>(pg) * (IDX ? kIdxPage : kMlaPage);
+    return P.cache + static_cast<long long>(pg) * (KIND == DSV4_CACHE_MLA ? kMlaPage
+                                                   : (KIND == DSV4_CACHE_IDX ? kIdxPage : kIdxFp4Page));
 }
 
 // The state values (kv, score + ape) of one token for this thread's two
@@ -130,9 +174,10 @@ __device__ __forceinline__ void token_values(const CompressParams& P, int t, int
 // the token's state row is written here too.  Otherwise (multi-token calls)
 // window rows inside the call come from the inputs and the ring is written
 // by state_write_kernel afterwards.
-template <int D, int RATIO, bool IDX, bool FUSED>
+template <int D, int RATIO, int KIND, bool FUSED>
 __device__ __forceinline__ void compress_token(const CompressParams& P, const int t)
 {
+    constexpr bool IDX = KIND != DSV4_CACHE_MLA;
     constexpr int COFF = (RATIO == 4) ? 2 : 1;
     constexpr int W = COFF * RATIO;
     constexpr int ROW = 2 * COFF * D;
@@ -253,9 +298,12 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
     }
 
     const int j = p / RATIO;
-    uint8_t* page = entry_page<IDX>(P, seq, j);
+    uint8_t* page = entry_page<KIND>(P, seq, j);
     const int r = j % kPage;
-    if (IDX) {
+    if (KIND == DSV4_CACHE_IDX_FP4) {
+        if (page == nullptr) return;   // uniform across the CTA
+        store_idx_fp4_entry(z0, z1, c0, page + r * (kIdx / 2), page + kPage * (kIdx / 2) + r * (kIdx / 32));
+    } else if (IDX) {
         if (page == nullptr) return;   // uniform across the CTA
         store_idx_entry(z0, z1, c0, page + r * kIdx,
                         reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
@@ -270,17 +318,17 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
 // A dependent kernel launched behind this one (programmatic dependent
 // launch) may be scheduled at once; it waits for this grid before reading
 // what it writes.
-template <int D, int RATIO, bool IDX, bool FUSED>
+template <int D, int RATIO, int KIND, bool FUSED>
 __global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    compress_token<D, RATIO, IDX, FUSED>(P, blockIdx.x);
+    compress_token<D, RATIO, KIND, FUSED>(P, blockIdx.x);
 }
 
 // The main (d = 576) and indexer (d = 128) streams of a layer in one launch,
 // one token per sequence: blocks [0, main tokens) take the main entries,
 // the rest the indexer entries with their first 64 threads.
-template <int RATIO>
+template <int RATIO, int IDX_KIND>
 __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
 {
     // the indexer of this layer, launched next, starts by reading the
@@ -300,9 +348,9 @@ __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
-        compress_token<kHead, RATIO, false, true>(Pm, blockIdx.x);
+        compress_token<kHead, RATIO, DSV4_CACHE_MLA, true>(Pm, blockIdx.x);
     else if (threadIdx.x < kIdx / 2)
-        compress_token<kIdx, 4, true, true>(Pi, blockIdx.x - Pm.num_tokens);
+        compress_token<kIdx, 4, IDX_KIND, true>(Pi, blockIdx.x - Pm.num_tokens);
 }
 
 template <int D, int RATIO>
@@ -328,7 +376,7 @@ __global__ void __launch_bounds__(D / 2) state_write_kernel(CompressParams P)
 }
 
 // Quantise-and-insert of given fp32 rows (no pooling / norm / rope).
-template <int D, bool IDX>
+template <int D, int KIND>
 __global__ void __launch_bounds__(D / 2) insert_rows_kernel(const float* rows, const int* seqs,
                                                             const int* slots, CompressParams P)
 {
@@ -341,25 +389,27 @@ __global__ void __launch_bounds__(D / 2) insert_rows_kernel(const float* rows, c
         return;
     }
     const float2 z = *reinterpret_cast<const float2*>(rows + static_cast<long long>(i) * D + c0);
-    uint8_t* page = entry_page<IDX>(P, seq, j);
+    uint8_t* page = entry_page<KIND>(P, seq, j);
     if (page == nullptr) return;
     const int r = j % kPage;
-    if (IDX)
+    if (KIND == DSV4_CACHE_IDX_FP4)
+        store_idx_fp4_entry(z.x, z.y, c0, page + r * (kIdx / 2), page + kPage * (kIdx / 2) + r * (kIdx / 32));
+    else if (KIND == DSV4_CACHE_IDX)
         store_idx_entry(z.x, z.y, c0, page + r * kIdx,
                         reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
     else
         store_mla_entry(z.x, z.y, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
 }
 
-template <int D, int RATIO, bool IDX>
+template <int D, int RATIO, int KIND>
 static cudaError_t launch_compress(const CompressParams& P, bool fused, cudaStream_t st)
 {
     if (P.num_tokens == 0) return cudaSuccess;
     if (fused) {
-        compress_kernel<D, RATIO, IDX, true><<<P.num_tokens, D / 2, 0, st>>>(P);
+        compress_kernel<D, RATIO, KIND, true><<<P.num_tokens, D / 2, 0, st>>>(P);
         return cudaGetLastError();
     }
-    compress_kernel<D, RATIO, IDX, false><<<P.num_tokens, D / 2, 0, st>>>(P);
+    compress_kernel<D, RATIO, KIND, false><<<P.num_tokens, D / 2, 0, st>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state_write_kernel<D, RATIO><<<P.num_tokens, D / 2, 0, st>>>(P);
@@ -376,9 +426,10 @@ static dsv4_status compress_params(const dsv4_compress_args* a, CompressParams& 
     if (a == nullptr) return DSV4_ERR_INVALID;
     if (a->num_tokens < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
         return DSV4_ERR_INVALID;
-    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4)
+        return DSV4_ERR_INVALID;
     if (a->ratio != 4 && a->ratio != 128) return DSV4_ERR_UNSUPPORTED;
-    if (a->kind == DSV4_CACHE_IDX && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
+    if (a->kind != DSV4_CACHE_MLA && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
     if (a->num_tokens > 0 &&
         (!a->kv_score_dev || !a->positions_dev || !a->seq_dev || !a->ape_dev || !a->rms_weight_dev ||
          !a->cos_sin_dev || !a->state_dev || !a->cache_dev || !a->block_table_dev))
@@ -419,11 +470,13 @@ extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_st
     const bool fused = a->one_token_per_seq != 0;
     cudaError_t e;
     if (a->kind == DSV4_CACHE_IDX)
-        e = launch_compress<kIdx, 4, true>(P, fused, st);
+        e = launch_compress<kIdx, 4, DSV4_CACHE_IDX>(P, fused, st);
+    else if (a->kind == DSV4_CACHE_IDX_FP4)
+        e = launch_compress<kIdx, 4, DSV4_CACHE_IDX_FP4>(P, fused, st);
     else if (a->ratio == 4)
-        e = launch_compress<kHead, 4, false>(P, fused, st);
+        e = launch_compress<kHead, 4, DSV4_CACHE_MLA>(P, fused, st);
     else
-        e = launch_compress<kHead, 128, false>(P, fused, st);
+        e = launch_compress<kHead, 128, DSV4_CACHE_MLA>(P, fused, st);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -435,7 +488,9 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     if (s != DSV4_OK) return s;
     s = compress_params(idx_args, Pi);
     if (s != DSV4_OK) return s;
-    if (main_args->kind != DSV4_CACHE_MLA || idx_args->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (main_args->kind != DSV4_CACHE_MLA ||
+        (idx_args->kind != DSV4_CACHE_IDX && idx_args->kind != DSV4_CACHE_IDX_FP4))
+        return DSV4_ERR_INVALID;
     if (!main_args->one_token_per_seq || !idx_args->one_token_per_seq) return DSV4_ERR_INVALID;
     const int n = Pm.num_tokens + Pi.num_tokens;
     if (n == 0) return DSV4_OK;
@@ -451,8 +506,13 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = main_args->ratio == 4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4>, Pm, Pi)
-                                                : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128>, Pm, Pi);
+    const bool fp4 = idx_args->kind == DSV4_CACHE_IDX_FP4;
+    const cudaError_t e =
+        main_args->ratio == 4
+            ? (fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX_FP4>, Pm, Pi)
+                   : cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX>, Pm, Pi))
+            : (fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX_FP4>, Pm, Pi)
+                   : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX>, Pm, Pi));
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -461,7 +521,8 @@ extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, ds
     if (a == nullptr) return DSV4_ERR_INVALID;
     if (a->num_rows < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
         return DSV4_ERR_INVALID;
-    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX) return DSV4_ERR_INVALID;
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4)
+        return DSV4_ERR_INVALID;
     if (a->num_rows == 0) return DSV4_OK;
     if (!a->rows_dev || !a->seq_dev || !a->slot_dev || !a->cache_dev || !a->block_table_dev)
         return DSV4_ERR_INVALID;
@@ -476,8 +537,13 @@ extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, ds
     P.status = a->status_dev;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (a->kind == DSV4_CACHE_IDX)
-        insert_rows_kernel<kIdx, true><<<a->num_rows, kIdx / 2, 0, st>>>(a->rows_dev, a->seq_dev, a->slot_dev, P);
+        insert_rows_kernel<kIdx, DSV4_CACHE_IDX><<<a->num_rows, kIdx / 2, 0, st>>>(a->rows_dev, a->seq_dev,
+                                                                                 a->slot_dev, P);
+    else if (a->kind == DSV4_CACHE_IDX_FP4)
+        insert_rows_kernel<kIdx, DSV4_CACHE_IDX_FP4><<<a->num_rows, kIdx / 2, 0, st>>>(a->rows_dev, a->seq_dev,
+                                                                                     a->slot_dev, P);
     else
-        insert_rows_kernel<kHead, false><<<a->num_rows, kHead / 2, 0, st>>>(a->rows_dev, a->seq_dev, a->slot_dev, P);
+        insert_rows_kernel<kHead, DSV4_CACHE_MLA><<<a->num_rows, kHead / 2, 0, st>>>(a->rows_dev, a->seq_dev,
+                                                                                   a->slot_dev, P);
     return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

@@ -19,6 +19,7 @@ constexpr int kPage = DSV4_PAGE;         // 64
 constexpr int kMlaData = kNope + 2 * kRope;   // 640 data bytes per compressed entry
 constexpr int kMlaPage = DSV4_MLA_PAGE_BYTES;
 constexpr int kIdxPage = DSV4_IDX_PAGE_BYTES;
+constexpr int kIdxFp4Page = DSV4_IDX_FP4_PAGE_BYTES;
 constexpr int kSwaPage = DSV4_SWA_PAGE_BYTES;
 
 __device__ __forceinline__ void flag(int* status, int bits)

@@ -38,6 +38,15 @@ constexpr int kIdxTmemCols = kIdxAcc * 64;                // 4 accumulators x 64
 constexpr int kIdxScaleBytes = 16;                           // the tile's two page ids (+ padding)
 constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
                          2048 /* barriers etc */ + 1024 /* align */;
+// FP4 (MXFP4) indexer cache: each tile arrives as the two pages' code planes
+// (2 x 4 KB of E2M1 codes) in a ring of its own after the FP8 layout; the
+// epilogue warps expand it into the E4M3 tile ring (every E2M1 value is an
+// E4M3 value), and each 32-dim block is one MMA into its own accumulator, so
+// the blocks' exponents are applied in the epilogue.
+constexpr int kIdxFp4TileBytes = kIdxTileSlots * kIdx / 2;                // 8 KB
+constexpr int kIdxRawOff4 = (kIdxSmem - 1024 + 127) / 128 * 128;
+constexpr int kIdxSmem4 = kIdxRawOff4 + kIdxStages * kIdxFp4TileBytes + 1024;
+constexpr int kIdxAcc4 = 2;                                                // tiles in flight, 4 x 64 columns each
 
 // ---------------------------------------------------------------------------
 // Top-k inside the logits launch: the CTAs of a sequence form a cluster, CTA
@@ -75,6 +84,22 @@ struct CtkScratch {
     int scan[16];
 };
 constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
+constexpr int kIdxSmem4Fused = kIdxSmem4 + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
+static_assert(kIdxSmem4Fused <= 232448, "shared memory budget");
+
+// Four E2M1 codes (the nibbles of the low 16 bits, the first in bits 0-3) as
+// four E4M3 bytes (the first in byte 0): a byte permute picks each magnitude
+// from the table of the eight E2M1 magnitudes' E4M3 encodings (0, 0.5, 1,
+// 1.5, 2, 3, 4, 6 -> 0x00, 0x30, 0x38, 0x3c, 0x40, 0x44, 0x48, 0x4c), a
+// second one in sign-replicate mode spreads each code's sign bit over its
+// byte.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t n16)
+{
+    uint32_t mag, sgn;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(0x3c383000u), "r"(0x4c484440u), "r"(n16 & 0x7777u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sgn) : "r"(n16 << 4), "r"(n16), "r"(0xd9c8u));
+    return mag | (sgn & 0x80808080u);
+}
 
 // The decision of a digit pass of the cluster top-k, taken alike by one warp
 // of every CTA once the pass's histograms of all C CTAs are in hin[q][256]:
@@ -308,11 +333,16 @@ struct IdxTcParams {
     int* out_len;
 };
 
-template <bool kFused>
+template <bool kFused, bool kFp4>
 __global__ void __launch_bounds__(kIdxThreads, 1)
 indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_q,
                   IdxTcParams P)
 {
+    constexpr int kAcc = kFp4 ? kIdxAcc4 : kIdxAcc;           // accumulator sets in flight
+    constexpr int kAccCols = kFp4 ? 4 * 64 : 64;               // TMEM columns per set
+    constexpr int kTmemCols = kFp4 ? 512 : kIdxTmemCols;
+    constexpr int kTileIn = kFp4 ? kIdxFp4TileBytes : kIdxTileBytes;   // bytes a tile's TMA brings in
+    constexpr int kPageBytes = kFp4 ? kIdxFp4Page : kIdxPage;
     // the top-k kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading the logits
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -327,11 +357,13 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     uint64_t* acc_full = bars + 2 * kIdxStages;   // [kIdxAcc]
     uint64_t* acc_empty = acc_full + kIdxAcc;     // [kIdxAcc]
     uint64_t* q_bar = acc_empty + kIdxAcc;
+    uint64_t* conv = q_bar + 1;                   // [kIdxStages] FP4: the tile's E4M3 expansion written
     float* w_s = reinterpret_cast<float*>(bars + 32);            // [64], 16-byte aligned, zero past H
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_s + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint8_t* raw_tiles = smem + kIdxRawOff4;      // FP4: [kIdxStages] the tiles' code planes
     // with the top-k in the launch: this CTA's logits, then the top-k scratch
-    float* lg_s = reinterpret_cast<float*>(smem + kIdxSmem - 1024);
+    float* lg_s = reinterpret_cast<float*>(smem + (kFp4 ? kIdxSmem4 : kIdxSmem) - 1024);
     CtkScratch* ctk = reinterpret_cast<CtkScratch*>(lg_s + kCtkSlots);
 
     const int b = blockIdx.y;
@@ -350,8 +382,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         for (int i = 0; i < kIdxStages; ++i) {
             tc::mbar_init(tc::smem_u32(&full[i]), 1);
             tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (page ids read)
+            if (kFp4) tc::mbar_init(tc::smem_u32(&conv[i]), 4);   // the 4 warps of the tile's epilogue group
         }
-        for (int i = 0; i < kIdxAcc; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
             tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
         }
@@ -374,7 +407,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         ctk->dec.decided = 0;
     }
     if (warp == 0) {
-        tc::tmem_alloc(tc::smem_u32(tmem_slot), kIdxTmemCols);
+        tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
@@ -438,11 +471,13 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             // scales straight from those pages) before the phase is armed
             if (lane < 2) stage_pages[st * 2 + lane] = v < 0 ? 0 : v;   // scales from a valid page
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive_expect_tx(fb, kIdxTileBytes);
+            if (lane == 0) tc::mbar_arrive_expect_tx(fb, kTileIn);
             __syncwarp();
-            // lanes 0-1: the two pages' rows (TMA tensor loads)
+            // lanes 0-1: the two pages' rows (TMA tensor loads; FP4: the code
+            // planes into the raw ring)
+            uint8_t* dst = kFp4 ? raw_tiles + st * kIdxFp4TileBytes : a_tiles + st * kIdxTileBytes;
             if (lane < 2)
-                tc::tma_load_3d(tc::smem_u32(a_tiles + st * kIdxTileBytes + lane * (kIdxTileBytes / 2)), &tm_cache, fb,
+                tc::tma_load_3d(tc::smem_u32(dst + lane * (kTileIn / 2)), &tm_cache, fb,
                                 0, 0, v < 0 ? P.num_pages : v);          // unreadable page: outside the map, zeros
             if (lane == 0) issued = i + 1;
         }
@@ -455,16 +490,20 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                 for (int i = 0; i < n_my; ++i) {
                     const int st = i % kIdxStages;
                     const uint32_t ph = (i / kIdxStages) & 1;
-                    const int ab = i % kIdxAcc;
-                    const uint32_t aph = (i / kIdxAcc) & 1;
-                    if (!tc::mbar_wait(tc::smem_u32(&full[st]), ph, abort_flag, P.status)) break;
-                    if (i >= kIdxAcc && !tc::mbar_wait(tc::smem_u32(&acc_empty[ab]), aph ^ 1, abort_flag, P.status)) break;
+                    const int ab = i % kAcc;
+                    const uint32_t aph = (i / kAcc) & 1;
+                    if (!tc::mbar_wait(tc::smem_u32(kFp4 ? &conv[st] : &full[st]), ph, abort_flag, P.status)) break;
+                    if (i >= kAcc && !tc::mbar_wait(tc::smem_u32(&acc_empty[ab]), aph ^ 1, abort_flag, P.status)) break;
                     tc::tc_fence_after();
                     const uint64_t a_desc = tc::desc_kmajor_sw128(tc::smem_u32(a_tiles + st * kIdxTileBytes));
-                    const uint32_t d = tmem + ab * 64;
+                    const uint32_t d = tmem + ab * kAccCols;
+                    // K = 32 FP8 (32 bytes) per instruction; FP4: one 32-dim block
+                    // per accumulator (its exponent applied in the epilogue)
 #pragma unroll
-                    for (int k = 0; k < kIdx / 32; ++k)   // K = 32 FP8 (32 bytes) per instruction
-                        tc::mma_f8f6f4(d, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < kIdx / 32; ++k) {
+                        if (kFp4) tc::mma_f8f6f4(d + 64 * k, a_desc + 2 * k, b_desc + 2 * k, idesc, 0u);
+                        else tc::mma_f8f6f4(d, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    }
                     tc::mma_commit(tc::smem_u32(&empty[st]));
                     tc::mma_commit(tc::smem_u32(&acc_full[ab]));
                     consumed = i + 1;
@@ -478,22 +517,93 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         const int grp = warp >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
-        for (int i = grp; i < n_my; i += 2) {
+        // FP4: this group expands its tiles' code planes into the E4M3 tile
+        // ring two of its tiles ahead of the epilogue (thread = tile row; the
+        // four 16-byte units of a row, one 32-dim block each, are read in a
+        // lane-rotated order, which spreads them over the banks)
+        auto convert4 = [&](int i) {
+            const int st = i % kIdxStages;
+            if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) return false;
+            const uint8_t* src = raw_tiles + st * kIdxFp4TileBytes + (row >> 6) * (kIdxFp4TileBytes / 2) +
+                                 (row & (kPage - 1)) * (kIdx / 2);
+            uint8_t* dst = a_tiles + st * kIdxTileBytes + row * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int u = (lane + k) & 3;
+                const uint4 w = *reinterpret_cast<const uint4*>(src + u * 16);
+                const uint4 lo = make_uint4(e2m1x4_to_e4m3x4(w.x & 0xffffu), e2m1x4_to_e4m3x4(w.x >> 16),
+                                            e2m1x4_to_e4m3x4(w.y & 0xffffu), e2m1x4_to_e4m3x4(w.y >> 16));
+                const uint4 hi = make_uint4(e2m1x4_to_e4m3x4(w.z & 0xffffu), e2m1x4_to_e4m3x4(w.z >> 16),
+                                            e2m1x4_to_e4m3x4(w.w & 0xffffu), e2m1x4_to_e4m3x4(w.w >> 16));
+                // 128-byte swizzle of the tile: unit v of row r at ((v ^ (r & 7)) << 4)
+                *reinterpret_cast<uint4*>(dst + (((2 * u) ^ (row & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4*>(dst + (((2 * u + 1) ^ (row & 7)) << 4)) = hi;
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&conv[st]));
+            return true;
+        };
+        bool conv_ok = true;
+        if (kFp4) {
+            for (int i = grp; conv_ok && i < n_my && i < grp + 4; i += 2) conv_ok = convert4(i);
+        }
+        for (int i = grp; conv_ok && i < n_my; i += 2) {
             if (t_begin + i == n_tiles - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
-            const int ab = i % kIdxAcc;
-            const uint32_t aph = (i / kIdxAcc) & 1;
+            if (kFp4 && i + 4 < n_my && !convert4(i + 4)) break;
+            const int ab = i % kAcc;
+            const uint32_t aph = (i / kAcc) & 1;
             const int st = i % kIdxStages;
             // the tile's rows have landed: its page ids are known; this row's
-            // scale comes straight from its page (in flight during the MMA)
+            // scale (FP4: its four block exponents) comes straight from its
+            // page (in flight during the MMA)
             if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) break;
-            const float scale = *reinterpret_cast<const float*>(
-                P.cache + static_cast<long long>(stage_pages[st * 2 + (row >> 6)]) * kIdxPage + kPage * kIdx +
-                (row & (kPage - 1)) * 4);
+            const uint8_t* pg_base = P.cache + static_cast<long long>(stage_pages[st * 2 + (row >> 6)]) * kPageBytes;
+            float scale = 1.0f;
+            uint32_t exps = 0;
+            if (kFp4)
+                exps = *reinterpret_cast<const uint32_t*>(pg_base + kPage * (kIdx / 2) + (row & (kPage - 1)) * 4);
+            else
+                scale = *reinterpret_cast<const float*>(pg_base + kPage * kIdx + (row & (kPage - 1)) * 4);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
             if (!tc::mbar_wait(tc::smem_u32(&acc_full[ab]), aph, abort_flag, P.status)) break;
             tc::tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + ab * 64;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + ab * kAccCols;
+            if (kFp4) {
+                // dot_j = sum over the 4 blocks of 2^(e_b - 127) * acc_b[j]
+                float sb[4];
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int eb = static_cast<int>((exps >> (8 * bb)) & 0xffu);
+                    sb[bb] = eb == 0 ? __int_as_float(0x00400000) : exp2i(eb - 127);   // 2^-127 is subnormal
+                }
+                float acc = 0.f;
+#pragma unroll 1
+                for (int hf = 0; hf * 32 < P.n_pad; ++hf) {
+                    float dot[32], va[32], vb[32];
+                    tc::tmem_ld32(taddr + hf * 32, va);
+                    tc::tmem_ld32(taddr + 64 + hf * 32, vb);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dot[j] = fmaf(vb[j], sb[1], va[j] * sb[0]);
+                    tc::tmem_ld32(taddr + 128 + hf * 32, va);
+                    tc::tmem_ld32(taddr + 192 + hf * 32, vb);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        dot[j] = fmaf(vb[j], sb[3], fmaf(va[j], sb[2], dot[j]));
+                        acc += (hf * 32 + j < P.H) ? w_s[hf * 32 + j] * fmaxf(dot[j], 0.f) : 0.f;
+                    }
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acc_empty[ab]));
+                const int s = (t_begin + i) * kIdxTileSlots + row;
+                if (kFused) lg_s[i * kIdxTileSlots + row] = acc;
+                else if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc;
+                continue;
+            }
             float v0[32], v1[32];
             tc::tmem_ld32(taddr, v0);
             if (P.n_pad > 32) tc::tmem_ld32(taddr + 32, v1);
@@ -540,7 +650,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, kIdxTmemCols);
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
     if (kFused)
         cluster_topk(lg_s, t_begin * kIdxTileSlots, min(t_end * kIdxTileSlots, n_c), n_c, P.k, static_cast<int>(gridDim.x),
@@ -1239,16 +1349,19 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
     const int B = plan->batch, H = plan->geom.idx_heads;
     if (plan->idx_ctas_per_seq > 0) {
         CUtensorMap tm_cache, tm_q;
-        const uint64_t cdims[3] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(kPage),
-                                   static_cast<uint64_t>(a->num_pages)};
-        const uint64_t cstr[2] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(kIdxPage)};
-        const uint32_t cbox[3] = {static_cast<uint32_t>(kIdx), static_cast<uint32_t>(kPage), 1};
+        // the pages' data planes: FP8 rows of 128 bytes (128-byte swizzle,
+        // the MMA's layout) or FP4 code rows of 64 bytes (expanded in the kernel)
+        const bool fp4 = plan->idx_fp4 != 0;
+        const uint32_t row_b = fp4 ? kIdx / 2 : kIdx;
+        const uint64_t cdims[3] = {row_b, static_cast<uint64_t>(kPage), static_cast<uint64_t>(a->num_pages)};
+        const uint64_t cstr[2] = {row_b, static_cast<uint64_t>(fp4 ? kIdxFp4Page : kIdxPage)};
+        const uint32_t cbox[3] = {row_b, static_cast<uint32_t>(kPage), 1};
         const int n_pad = H <= 16 ? 16 : (H + 15) / 16 * 16;
         const uint64_t qdims[2] = {static_cast<uint64_t>(kIdx), static_cast<uint64_t>(B) * H};
         const uint64_t qstr[1] = {static_cast<uint64_t>(kIdx)};
         const uint32_t qbox[2] = {static_cast<uint32_t>(kIdx), static_cast<uint32_t>(n_pad)};
         if (!encode_tmap(&tm_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a->idx_cache_dev, cdims, cstr, cbox,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+                         fp4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a->q_fp8_dev, qdims, qstr, qbox,
                          CU_TENSOR_MAP_SWIZZLE_128B))
             return DSV4_ERR_CUDA;
@@ -1274,20 +1387,21 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         static PerDeviceOnce tc_attr;
         const bool attr_ok = tc_attr.run([] {
             // the whole unified L1 as shared memory
-            return cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kIdxSmem) == cudaSuccess &&
-                   cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kIdxSmemFused) == cudaSuccess &&
-                   cudaFuncSetAttribute(indexer_logits_tc<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                        cudaSharedmemCarveoutMaxShared) == cudaSuccess &&
-                   cudaFuncSetAttribute(indexer_logits_tc<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                        cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+            const auto set = [](const void* f, int smem) {
+                return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess &&
+                       cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                            cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+            };
+            return set(reinterpret_cast<const void*>(indexer_logits_tc<false, false>), kIdxSmem) &&
+                   set(reinterpret_cast<const void*>(indexer_logits_tc<true, false>), kIdxSmemFused) &&
+                   set(reinterpret_cast<const void*>(indexer_logits_tc<false, true>), kIdxSmem4) &&
+                   set(reinterpret_cast<const void*>(indexer_logits_tc<true, true>), kIdxSmem4Fused);
         });
         if (!attr_ok) return DSV4_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(plan->idx_ctas_per_seq, B, 1);
         cfg.blockDim = dim3(kIdxThreads, 1, 1);
-        cfg.dynamicSmemBytes = fused ? kIdxSmemFused : kIdxSmem;
+        cfg.dynamicSmemBytes = fp4 ? (fused ? kIdxSmem4Fused : kIdxSmem4) : (fused ? kIdxSmemFused : kIdxSmem);
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1299,8 +1413,11 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = fused ? 2 : 1;
-        cudaError_t e = fused ? cudaLaunchKernelEx(&cfg, indexer_logits_tc<true>, tm_cache, tm_q, P)
-                              : cudaLaunchKernelEx(&cfg, indexer_logits_tc<false>, tm_cache, tm_q, P);
+        cudaError_t e =
+            fp4 ? (fused ? cudaLaunchKernelEx(&cfg, indexer_logits_tc<true, true>, tm_cache, tm_q, P)
+                         : cudaLaunchKernelEx(&cfg, indexer_logits_tc<false, true>, tm_cache, tm_q, P))
+                : (fused ? cudaLaunchKernelEx(&cfg, indexer_logits_tc<true, false>, tm_cache, tm_q, P)
+                         : cudaLaunchKernelEx(&cfg, indexer_logits_tc<false, false>, tm_cache, tm_q, P));
         if (e != cudaSuccess) return DSV4_ERR_CUDA;
         if (fused) return DSV4_OK;
     }

@@ -75,6 +75,8 @@ extern "C" {
 #define DSV4_MLA_PAGE_BYTES (64 * 648)
 #define DSV4_IDX_ENTRY_BYTES 132
 #define DSV4_IDX_PAGE_BYTES (64 * 132)
+#define DSV4_IDX_FP4_ENTRY_BYTES 68
+#define DSV4_IDX_FP4_PAGE_BYTES (64 * 68)
 #define DSV4_SWA_PAGE_BYTES (64 * 576 * 2)
 #define DSV4_MAX_HEADS 128
 #define DSV4_MAX_IDX_HEADS 64
@@ -105,8 +107,13 @@ typedef enum dsv4_layer_type {
 } dsv4_layer_type;
 
 typedef enum dsv4_cache_kind {
-    DSV4_CACHE_MLA = 0,   /* main compressed cache, d = 576, 648-byte entries */
-    DSV4_CACHE_IDX = 1    /* indexer cache, d = 128, 132-byte entries */
+    DSV4_CACHE_MLA = 0,     /* main compressed cache, d = 576, 648-byte entries */
+    DSV4_CACHE_IDX = 1,     /* indexer cache, d = 128, 132-byte entries (FP8 + fp32 scale) */
+    DSV4_CACHE_IDX_FP4 = 2  /* indexer cache in MXFP4, d = 128, 68-byte entries: 64 bytes of
+                               E2M1 codes (two per byte, the low nibble the even dim) and one
+                               UE8M0 exponent byte per 32 dims; page = 64 x 64 code bytes, then
+                               64 x 4 exponent bytes.  [V4-attn] use_fp4_indexer_cache;
+                               [V4-internals] section 4 (64 x 68 B); [MLA-to-CSA] 6.1 */
 } dsv4_cache_kind;
 
 /* ---- host utilities ------------------------------------------------------ */
@@ -182,6 +189,21 @@ void dsv4_plan_destroy(dsv4_plan* plan);
 /* Device workspace the plan's calls need (bytes, 256-byte aligned base). */
 size_t dsv4_plan_workspace_bytes(const dsv4_plan* plan);
 dsv4_status dsv4_plan_get_info(const dsv4_plan* plan, dsv4_plan_info* info);
+
+/* Indexer cache format of a c4a plan ([V4-attn] eval note
+ * use_fp4_indexer_cache: only the indexer's K cache changes format;
+ * [V4-internals] section 4: the C4 indexer block as 64 x 68 B;
+ * [MLA-to-CSA] 6.1: lightning-indexer K cache in FP4 / MXFP4).
+ *   DSV4_IDX_FP8 (the default): 132-byte entries (DSV4_CACHE_IDX pages);
+ *   DSV4_IDX_FP4: 68-byte MXFP4 entries (DSV4_CACHE_IDX_FP4 pages).
+ * With FP4, dsv4_indexer_topk scores k[s][c] = E2M1(code) * 2^(exponent
+ * byte of c's 32-dim block - 127) with the same FP8 query and the same top-k
+ * rule; idx_cache_dev then holds DSV4_IDX_FP4_PAGE_BYTES pages and
+ * num_pages counts those.  Set it after dsv4_plan_create, before the plan's
+ * first call.  Errors: DSV4_ERR_INVALID (NULL plan or unknown format),
+ * DSV4_ERR_UNSUPPORTED (not a c4a plan). */
+typedef enum dsv4_idx_format { DSV4_IDX_FP8 = 0, DSV4_IDX_FP4 = 1 } dsv4_idx_format;
+dsv4_status dsv4_plan_set_indexer_format(dsv4_plan* plan, dsv4_idx_format format);
 
 /* ---- (1) compressor insert ----------------------------------------------- */
 

@@ -52,7 +52,7 @@ class DecodeInputs:
 
 
 def make_decode_inputs(layer_type, batch, ctx, n_heads, idx_heads, topk, seed, comp_pool=8192,
-                       peaky=False, with_comp=True, device="cuda"):
+                       peaky=False, with_comp=True, idx_fp4=False, device="cuda"):
     """ctx: int or per-sequence array of contexts L (query position L - 1).
 
     c4a: indexer cache with L // 4 oracle-quantised rows per sequence, q_fp8
@@ -99,11 +99,13 @@ def make_decode_inputs(layer_type, batch, ctx, n_heads, idx_heads, topk, seed, c
     if layer_type == 4 and idx_heads > 0:
         ip = int(max(1, (n_c.max() + 63) // 64))
         d.idx_bt = synth.page_tables(g, batch, ip, extra_pages=1)
-        d.idx = np.zeros((batch * ip + 1) * oracle.page_bytes(oracle.IDX_KIND), np.uint8)
+        kind = oracle.IDX_FP4_KIND if idx_fp4 else oracle.IDX_KIND
+        d.idx_fp4 = idx_fp4
+        d.idx = np.zeros((batch * ip + 1) * oracle.page_bytes(kind), np.uint8)
         for b in range(batch):
             rows = synth.normal(g, (int(n_c[b]), 128), 1.0 / math.sqrt(128))
-            data, sc = oracle.quant_idx_rows(rows)
-            oracle.page_write(oracle.IDX_KIND, d.idx, d.idx_bt[b], data, sc, nope_dim=64)
+            data, sc = oracle.quant_idx_fp4_rows(rows) if idx_fp4 else oracle.quant_idx_rows(rows)
+            oracle.page_write(kind, d.idx, d.idx_bt[b], data, sc, nope_dim=64)
         d.qi = oracle.f32_to_e4m3(synth.normal(g, (batch, idx_heads, 128)))
         d.w = synth.uniform(g, (batch, idx_heads))
     if layer_type == 128:
@@ -149,7 +151,8 @@ def make_decode_inputs(layer_type, batch, ctx, n_heads, idx_heads, topk, seed, c
 
 
 def oracle_indexer(d, b):
-    return oracle.indexer_logits(d.qi[b], d.w[b], d.idx, d.idx_bt[b], int(d.n_c[b]))
+    f = oracle.indexer_logits_fp4 if getattr(d, "idx_fp4", False) else oracle.indexer_logits
+    return f(d.qi[b], d.w[b], d.idx, d.idx_bt[b], int(d.n_c[b]))
 
 
 def check_topk(gpu_idx, gpu_len, logits, k):
