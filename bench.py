@@ -45,6 +45,11 @@ WORKLOADS = {
                            window=128, ratio=128),
     "c4a_1m_b4": dict(name="c4a_1m_b4", batch=4, context=1048576, n_heads=128, idx_heads=64, topk=2048,
                       window=128, ratio=4),
+    # the same two c4a workloads with the indexer cache in MXFP4 (68-byte entries)
+    "c4a_32k_b32_fp4": dict(name="c4a_32k_b32_fp4", batch=32, context=32768, n_heads=64, idx_heads=64, topk=512,
+                            window=128, ratio=4, idx_fp4=True),
+    "c4a_1m_b4_fp4": dict(name="c4a_1m_b4_fp4", batch=4, context=1048576, n_heads=128, idx_heads=64, topk=2048,
+                          window=128, ratio=4, idx_fp4=True),
     # 60-layer stack (swaonly / c4a / c128a), IndexCache freq 2 against freq 1
     "mixed60_b16": dict(name="mixed60_b16", batch=16, context=65536, n_heads=64, idx_heads=64, topk=512,
                         window=128, ratio=0),
@@ -105,9 +110,10 @@ def algorithmic_bytes(w, ctx):
         comp_main = B * (1152 * 2 + 1152 * 4 + (128 * 1152 * 4 + 648) / 128)
         return dict(compress=comp_main, indexer=0.0, mla=mla, total=comp_main + mla)
     n_c = ctx // 4
+    idx_entry = 68 if w.get("idx_fp4") else 132      # MXFP4 or FP8 indexer entries
     comp_main = B * (2304 * 2 + 2304 * 4 + 0.25 * (7 * 1152 * 4 + 648))
-    comp_idx = B * (512 * 2 + 512 * 4 + 0.25 * (7 * 256 * 4 + 132))
-    indexer = B * (n_c * 132 + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
+    comp_idx = B * (512 * 2 + 512 * 4 + 0.25 * (7 * 256 * 4 + idx_entry))
+    indexer = B * (n_c * idx_entry + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
     return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla,
                 total=comp_main + comp_idx + indexer + mla)
 
@@ -201,7 +207,8 @@ def build_layers(w, n_layers, n_pos, device, seed=1):
         L.comp_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
         L.idx_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
         L.comp = torch.zeros(Bsz * comp_lp * Bd.MLA_PAGE_BYTES, dtype=torch.uint8, device=device)
-        L.idx = torch.zeros(Bsz * comp_lp * Bd.IDX_PAGE_BYTES, dtype=torch.uint8, device=device)
+        idx_kind = Bd.CACHE_IDX_FP4 if w.get("idx_fp4") else Bd.CACHE_IDX
+        L.idx = torch.zeros(Bsz * comp_lp * Bd.PAGE_BYTES[idx_kind], dtype=torch.uint8, device=device)
         chunk = 8192
         for b in range(Bsz):
             for s0 in range(0, n_c_max, chunk):
@@ -211,7 +218,7 @@ def build_layers(w, n_layers, n_pos, device, seed=1):
                 rows = torch.randn((n, 576), generator=g, device=device) / math.sqrt(576)
                 Bd.cache_insert_rows(Bd.CACHE_MLA, rows, seq, slot, L.comp, L.comp_bt)
                 rows = torch.randn((n, 128), generator=g, device=device) / math.sqrt(128)
-                Bd.cache_insert_rows(Bd.CACHE_IDX, rows, seq, slot, L.idx, L.idx_bt)
+                Bd.cache_insert_rows(idx_kind, rows, seq, slot, L.idx, L.idx_bt)
         # SWA cache: 4 physical pages per sequence used as a ring of logical pages
         phys = torch.randperm(Bsz * 4, generator=g, device=device).to(torch.int32).view(Bsz, 4)
         lp = torch.arange(swa_lp, device=device) % 4
@@ -294,9 +301,11 @@ class GpuBench:
             self.stage_names = ["compress", "sparse_mla"]
         else:
             self.plan = Bd.Plan(Bd.C4A, w["n_heads"], Bsz, w["topk"], w["context"], idx_heads=w["idx_heads"],
+                                idx_format=Bd.IDX_FP4 if w.get("idx_fp4") else Bd.IDX_FP8,
                                 window=w["window"])
             self.layers = build_layers(w, n_layers, n_pos, device)
             self.stage_names = ["compress", "indexer_topk", "sparse_mla"]
+        self.idx_kind = Bd.CACHE_IDX_FP4 if w.get("idx_fp4") else Bd.CACHE_IDX
         self.ws = self.plan.workspace(device)
         self.cos_sin = Bd.rope_table(w["context"] + 1).to(device)
         # positions: the last graph position is the context's last token
@@ -338,7 +347,7 @@ class GpuBench:
                 dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=L.kv_main[j], positions=self.pos[j], seqs=L.seqs,
                      ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=self.cos_sin,
                      state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=self.status),
-                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=L.kv_idx[j], positions=self.pos[j], seqs=L.seqs,
+                dict(kind=self.idx_kind, ratio=4, kv_score=L.kv_idx[j], positions=self.pos[j], seqs=L.seqs,
                      ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=self.cos_sin,
                      state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=self.status)),
             lambda: Bd.indexer_topk(self.plan, L.qi[j], L.wts[j], L.idx, L.idx_bt, self.ctx[j], self.topk_idx,
@@ -449,7 +458,7 @@ def run_e2e(bench, steps, warmup):
                 dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=d["kv_main"], positions=d["pos"], seqs=L.seqs,
                      ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=bench.cos_sin,
                      state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=bench.status),
-                dict(kind=Bd.CACHE_IDX, ratio=4, kv_score=d["kv_idx"], positions=d["pos"], seqs=L.seqs,
+                dict(kind=bench.idx_kind, ratio=4, kv_score=d["kv_idx"], positions=d["pos"], seqs=L.seqs,
                      ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=bench.cos_sin,
                      state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=bench.status))
             Bd.indexer_topk(bench.plan, d["qi"], d["wts"], L.idx, L.idx_bt, d["ctx"], bench.topk_idx,

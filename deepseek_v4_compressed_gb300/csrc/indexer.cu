@@ -38,15 +38,23 @@ constexpr int kIdxTmemCols = kIdxAcc * 64;                // 4 accumulators x 64
 constexpr int kIdxScaleBytes = 16;                           // the tile's two page ids (+ padding)
 constexpr int kIdxSmem = kIdxStages * kIdxTileBytes + kIdxQBytes + kIdxStages * kIdxScaleBytes +
                          2048 /* barriers etc */ + 1024 /* align */;
-// FP4 (MXFP4) indexer cache: each tile arrives as the two pages' code planes
-// (2 x 4 KB of E2M1 codes) in a ring of its own after the FP8 layout; the
-// epilogue warps expand it into the E4M3 tile ring (every E2M1 value is an
-// E4M3 value), and each 32-dim block is one MMA into its own accumulator, so
-// the blocks' exponents are applied in the epilogue.
-constexpr int kIdxFp4TileBytes = kIdxTileSlots * kIdx / 2;                // 8 KB
+// FP4 (MXFP4) indexer cache: each tile arrives as its two whole pages
+// (4352 B each: 64 x 64 code bytes, then 64 x 4 exponent bytes; 1-D bulk
+// copies) in a ring of its own after the FP8 layout.  The epilogue warps
+// expand a tile into the E4M3 tile ring: a slot's 32-dim block b is stored as
+// E2M1 value x 2^-(E - e_b), E the largest of the slot's four exponents,
+// which E4M3 holds exactly while E - e_b <= 8; the epilogue then scales the
+// one accumulator by 2^(E - 127), as the FP8 path scales by its fp32 scale.
+// A slot with a wider exponent spread is scored exactly by the converter
+// from the page bytes instead.  The converter, not the epilogue, releases a
+// FP4 stage (with the MMA): the epilogue needs only the per-slot scale (or
+// exact score) the converter leaves beside the tile.
+constexpr int kIdxFp4PageB = DSV4_IDX_FP4_PAGE_BYTES;                       // 4352
+constexpr int kIdxFp4Stage = 2 * kIdxFp4PageB;                              // 8704
 constexpr int kIdxRawOff4 = (kIdxSmem - 1024 + 127) / 128 * 128;
-constexpr int kIdxSmem4 = kIdxRawOff4 + kIdxStages * kIdxFp4TileBytes + 1024;
-constexpr int kIdxAcc4 = 2;                                                // tiles in flight, 4 x 64 columns each
+constexpr int kIdxRowScaleOff4 = kIdxRawOff4 + kIdxStages * kIdxFp4Stage;  // [stage][128] 2^(E-127), < 0: exact path
+constexpr int kIdxExactOff4 = kIdxRowScaleOff4 + kIdxStages * kIdxTileSlots * 4;    // [stage][128] exact logits
+constexpr int kIdxSmem4 = kIdxExactOff4 + kIdxStages * kIdxTileSlots * 4 + 1024;
 
 // ---------------------------------------------------------------------------
 // Top-k inside the logits launch: the CTAs of a sequence form a cluster, CTA
@@ -87,16 +95,46 @@ constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof
 constexpr int kIdxSmem4Fused = kIdxSmem4 + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
 static_assert(kIdxSmem4Fused <= 232448, "shared memory budget");
 
+// E4M3 byte of the E2M1 magnitude with index c (0, 0.5, 1, 1.5, 2, 3, 4, 6)
+// times 2^-k, k = 0..8: every such value is an E4M3 value (normal when its
+// exponent is at least -6, else a multiple of 2^-9).
+__host__ __device__ constexpr uint32_t e4m3_of_e2m1_shifted(int c, int k)
+{
+    constexpr int twice[8] = {0, 1, 2, 3, 4, 6, 8, 12};   // 2 x magnitude
+    const int n = twice[c];                                // value = n * 2^(-1-k)
+    if (n == 0) return 0;
+    const int e = -1 - k;
+    int p = 0;
+    while ((2 << p) <= n) ++p;                             // 2^p <= n < 2^(p+1)
+    const int ex = e + p;                                  // value = (n / 2^p) * 2^ex
+    if (ex >= -6) return static_cast<uint32_t>(((ex + 7) << 3) | (((n * 8) >> p) - 8));
+    return static_cast<uint32_t>(n << (9 + e));           // subnormal: m * 2^-9
+}
+
+__host__ __device__ constexpr uint32_t e2m1_lut_word(int k, int half)
+{
+    return e4m3_of_e2m1_shifted(4 * half, k) | (e4m3_of_e2m1_shifted(4 * half + 1, k) << 8) |
+           (e4m3_of_e2m1_shifted(4 * half + 2, k) << 16) | (e4m3_of_e2m1_shifted(4 * half + 3, k) << 24);
+}
+
+// [k][2]: the byte-permute tables of shift k
+__constant__ uint32_t c_e2m1_lut[9][2] = {
+    {e2m1_lut_word(0, 0), e2m1_lut_word(0, 1)}, {e2m1_lut_word(1, 0), e2m1_lut_word(1, 1)},
+    {e2m1_lut_word(2, 0), e2m1_lut_word(2, 1)}, {e2m1_lut_word(3, 0), e2m1_lut_word(3, 1)},
+    {e2m1_lut_word(4, 0), e2m1_lut_word(4, 1)}, {e2m1_lut_word(5, 0), e2m1_lut_word(5, 1)},
+    {e2m1_lut_word(6, 0), e2m1_lut_word(6, 1)}, {e2m1_lut_word(7, 0), e2m1_lut_word(7, 1)},
+    {e2m1_lut_word(8, 0), e2m1_lut_word(8, 1)}};
+static_assert(e2m1_lut_word(0, 0) == 0x3c383000u && e2m1_lut_word(0, 1) == 0x4c484440u, "E4M3 of the E2M1 values");
+
 // Four E2M1 codes (the nibbles of the low 16 bits, the first in bits 0-3) as
-// four E4M3 bytes (the first in byte 0): a byte permute picks each magnitude
-// from the table of the eight E2M1 magnitudes' E4M3 encodings (0, 0.5, 1,
-// 1.5, 2, 3, 4, 6 -> 0x00, 0x30, 0x38, 0x3c, 0x40, 0x44, 0x48, 0x4c), a
+// four E4M3 bytes (the first in byte 0), each magnitude scaled by the table's
+// power of two: a byte permute picks the magnitude from the table (lo, hi), a
 // second one in sign-replicate mode spreads each code's sign bit over its
 // byte.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t n16)
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t n16, uint32_t lut_lo, uint32_t lut_hi)
 {
     uint32_t mag, sgn;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(0x3c383000u), "r"(0x4c484440u), "r"(n16 & 0x7777u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(mag) : "r"(lut_lo), "r"(lut_hi), "r"(n16 & 0x7777u));
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sgn) : "r"(n16 << 4), "r"(n16), "r"(0xd9c8u));
     return mag | (sgn & 0x80808080u);
 }
@@ -338,10 +376,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_q,
                   IdxTcParams P)
 {
-    constexpr int kAcc = kFp4 ? kIdxAcc4 : kIdxAcc;           // accumulator sets in flight
-    constexpr int kAccCols = kFp4 ? 4 * 64 : 64;               // TMEM columns per set
-    constexpr int kTmemCols = kFp4 ? 512 : kIdxTmemCols;
-    constexpr int kTileIn = kFp4 ? kIdxFp4TileBytes : kIdxTileBytes;   // bytes a tile's TMA brings in
+    constexpr int kAcc = kIdxAcc;                              // accumulators in flight
+    constexpr int kAccCols = 64;                               // TMEM columns per accumulator
+    constexpr int kTmemCols = kIdxTmemCols;
+    constexpr int kTileIn = kFp4 ? kIdxFp4Stage : kIdxTileBytes;   // bytes a tile's copies bring in
     constexpr int kPageBytes = kFp4 ? kIdxFp4Page : kIdxPage;
     // the top-k kernel that follows may be scheduled now; it waits for this
     // grid's completion before reading the logits
@@ -361,7 +399,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     float* w_s = reinterpret_cast<float*>(bars + 32);            // [64], 16-byte aligned, zero past H
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_s + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    uint8_t* raw_tiles = smem + kIdxRawOff4;      // FP4: [kIdxStages] the tiles' code planes
+    uint32_t* lut_s = tmem_slot + 4;              // FP4: [9][2] byte-permute tables by exponent shift
+    uint8_t* raw_tiles = smem + kIdxRawOff4;      // FP4: [kIdxStages] the tiles' two pages
+    float* row_scale = reinterpret_cast<float*>(smem + kIdxRowScaleOff4);   // FP4: [kIdxStages][128]
+    float* exact_s = reinterpret_cast<float*>(smem + kIdxExactOff4);         // FP4: [kIdxStages][128]
     // with the top-k in the launch: this CTA's logits, then the top-k scratch
     float* lg_s = reinterpret_cast<float*>(smem + (kFp4 ? kIdxSmem4 : kIdxSmem) - 1024);
     CtkScratch* ctk = reinterpret_cast<CtkScratch*>(lg_s + kCtkSlots);
@@ -381,7 +422,8 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < kIdxStages; ++i) {
             tc::mbar_init(tc::smem_u32(&full[i]), 1);
-            tc::mbar_init(tc::smem_u32(&empty[i]), 5);   // MMA commit + 4 epilogue warps (page ids read)
+            // MMA commit + 4 warps: the epilogue's (page ids read), FP4: the converter's (tile read)
+            tc::mbar_init(tc::smem_u32(&empty[i]), 5);
             if (kFp4) tc::mbar_init(tc::smem_u32(&conv[i]), 4);   // the 4 warps of the tile's epilogue group
         }
         for (int i = 0; i < kAcc; ++i) {
@@ -400,6 +442,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         tc::fence_barrier_init();
     }
     if (threadIdx.x < 64) w_s[threadIdx.x] = (threadIdx.x < P.H) ? P.w[static_cast<long long>(b) * P.H + threadIdx.x] : 0.f;
+    if (kFp4 && threadIdx.x >= 64 && threadIdx.x < 64 + 18) lut_s[threadIdx.x - 64] = (&c_e2m1_lut[0][0])[threadIdx.x - 64];
     if (kFused && threadIdx.x == 0) {
         ctk->mm[0] = 0xffffffffu;
         ctk->mm[1] = 0u;
@@ -473,12 +516,18 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_expect_tx(fb, kTileIn);
             __syncwarp();
-            // lanes 0-1: the two pages' rows (TMA tensor loads; FP4: the code
-            // planes into the raw ring)
-            uint8_t* dst = kFp4 ? raw_tiles + st * kIdxFp4TileBytes : a_tiles + st * kIdxTileBytes;
-            if (lane < 2)
-                tc::tma_load_3d(tc::smem_u32(dst + lane * (kTileIn / 2)), &tm_cache, fb,
-                                0, 0, v < 0 ? P.num_pages : v);          // unreadable page: outside the map, zeros
+            // lanes 0-1: the two pages' rows (TMA tensor loads; an unreadable
+            // page is outside the map and reads zeros).  FP4: the two whole
+            // pages by 1-D bulk copies (an unreadable page, already flagged,
+            // is read as page 0)
+            if (kFp4) {
+                if (lane < 2)
+                    tc::bulk_g2s(tc::smem_u32(raw_tiles + st * kIdxFp4Stage + lane * kIdxFp4PageB),
+                                 P.cache + static_cast<long long>(v < 0 ? 0 : v) * kIdxFp4PageB, kIdxFp4PageB, fb);
+            } else if (lane < 2) {
+                tc::tma_load_3d(tc::smem_u32(a_tiles + st * kIdxTileBytes + lane * (kIdxTileBytes / 2)), &tm_cache,
+                                fb, 0, 0, v < 0 ? P.num_pages : v);
+            }
             if (lane == 0) issued = i + 1;
         }
         if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -497,13 +546,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                     tc::tc_fence_after();
                     const uint64_t a_desc = tc::desc_kmajor_sw128(tc::smem_u32(a_tiles + st * kIdxTileBytes));
                     const uint32_t d = tmem + ab * kAccCols;
-                    // K = 32 FP8 (32 bytes) per instruction; FP4: one 32-dim block
-                    // per accumulator (its exponent applied in the epilogue)
 #pragma unroll
-                    for (int k = 0; k < kIdx / 32; ++k) {
-                        if (kFp4) tc::mma_f8f6f4(d + 64 * k, a_desc + 2 * k, b_desc + 2 * k, idesc, 0u);
-                        else tc::mma_f8f6f4(d, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kIdx / 32; ++k)   // K = 32 FP8 (32 bytes) per instruction
+                        tc::mma_f8f6f4(d, a_desc + 2 * k, b_desc + 2 * k, idesc, k > 0 ? 1u : 0u);
                     tc::mma_commit(tc::smem_u32(&empty[st]));
                     tc::mma_commit(tc::smem_u32(&acc_full[ab]));
                     consumed = i + 1;
@@ -517,24 +562,63 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         const int grp = warp >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;
-        // FP4: this group expands its tiles' code planes into the E4M3 tile
-        // ring two of its tiles ahead of the epilogue (thread = tile row; the
-        // four 16-byte units of a row, one 32-dim block each, are read in a
-        // lane-rotated order, which spreads them over the banks)
+        // FP4 slot scored exactly from its page bytes (codes, exponent bytes)
+        // and the FP8 query tile: sum over heads of w_j ReLU(sum_c q_jc k_c),
+        // k_c = E2M1 x 2^(e_b - 127)
+        auto exact_fp4 = [&](const uint8_t* codes, const uint8_t* exb) {
+            constexpr float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+            float acc = 0.f;
+            for (int j = 0; j < P.H; ++j) {
+                float dot = 0.f;
+                for (int c = 0; c < kIdx; ++c) {
+                    const uint32_t code = (codes[c >> 1] >> (4 * (c & 1))) & 15u;
+                    const float kv = ldexpf((code & 8u) ? -mags[code & 7u] : mags[code & 7u],
+                                            static_cast<int>(exb[c >> 5]) - 127);
+                    const uint8_t qb = q_tile[j * 128 + ((((c >> 4) ^ (j & 7))) << 4) + (c & 15)];
+                    dot = fmaf(e4m3_to_f32(qb), kv, dot);
+                }
+                acc += w_s[j] * fmaxf(dot, 0.f);
+            }
+            return acc;
+        };
+        // FP4: this group expands its tiles into the E4M3 tile ring two of its
+        // tiles ahead of the epilogue (thread = tile row = slot).  Block b of a
+        // slot becomes E2M1 x 2^-(E - e_b), E the slot's largest exponent; the
+        // slot's 2^(E - 127) goes to row_scale, or -1 when a block lies more
+        // than 8 binades below E (the epilogue then scores it exactly).  The
+        // four 16-byte units of a row are read in a lane-rotated order, which
+        // spreads them over the banks.
         auto convert4 = [&](int i) {
             const int st = i % kIdxStages;
             if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) return false;
-            const uint8_t* src = raw_tiles + st * kIdxFp4TileBytes + (row >> 6) * (kIdxFp4TileBytes / 2) +
-                                 (row & (kPage - 1)) * (kIdx / 2);
+            const uint8_t* pg = raw_tiles + st * kIdxFp4Stage + (row >> 6) * kIdxFp4PageB;
+            const uint8_t* src = pg + (row & (kPage - 1)) * (kIdx / 2);
+            const uint32_t ex = *reinterpret_cast<const uint32_t*>(pg + kPage * (kIdx / 2) + (row & (kPage - 1)) * 4);
+            int eb[4], E = 0;
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+                eb[bb] = static_cast<int>((ex >> (8 * bb)) & 0xffu);
+                E = max(E, eb[bb]);
+            }
+            bool exact = true;
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) exact = exact && E - eb[bb] <= 8;
+            row_scale[st * kIdxTileSlots + row] = !exact ? -1.0f : (E == 0 ? __int_as_float(0x00400000) : exp2i(E - 127));
             uint8_t* dst = a_tiles + st * kIdxTileBytes + row * 128;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int u = (lane + k) & 3;
+                const int sh = min(E - (u == 0 ? eb[0] : (u == 1 ? eb[1] : (u == 2 ? eb[2] : eb[3]))), 8);
+                const uint32_t lo_t = lut_s[2 * sh], hi_t = lut_s[2 * sh + 1];
                 const uint4 w = *reinterpret_cast<const uint4*>(src + u * 16);
-                const uint4 lo = make_uint4(e2m1x4_to_e4m3x4(w.x & 0xffffu), e2m1x4_to_e4m3x4(w.x >> 16),
-                                            e2m1x4_to_e4m3x4(w.y & 0xffffu), e2m1x4_to_e4m3x4(w.y >> 16));
-                const uint4 hi = make_uint4(e2m1x4_to_e4m3x4(w.z & 0xffffu), e2m1x4_to_e4m3x4(w.z >> 16),
-                                            e2m1x4_to_e4m3x4(w.w & 0xffffu), e2m1x4_to_e4m3x4(w.w >> 16));
+                const uint4 lo = make_uint4(e2m1x4_to_e4m3x4(w.x & 0xffffu, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.x >> 16, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.y & 0xffffu, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.y >> 16, lo_t, hi_t));
+                const uint4 hi = make_uint4(e2m1x4_to_e4m3x4(w.z & 0xffffu, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.z >> 16, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.w & 0xffffu, lo_t, hi_t),
+                                            e2m1x4_to_e4m3x4(w.w >> 16, lo_t, hi_t));
                 // 128-byte swizzle of the tile: unit v of row r at ((v ^ (r & 7)) << 4)
                 *reinterpret_cast<uint4*>(dst + (((2 * u) ^ (row & 7)) << 4)) = lo;
                 *reinterpret_cast<uint4*>(dst + (((2 * u + 1) ^ (row & 7)) << 4)) = hi;
@@ -542,6 +626,9 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&conv[st]));
+            if (!exact) exact_s[st * kIdxTileSlots + row] = exact_fp4(src, pg + kPage * (kIdx / 2) + (row & (kPage - 1)) * 4);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));   // the pages are read
             return true;
         };
         bool conv_ok = true;
@@ -557,53 +644,24 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             // the tile's rows have landed: its page ids are known; this row's
             // scale (FP4: its four block exponents) comes straight from its
             // page (in flight during the MMA)
-            if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) break;
-            const uint8_t* pg_base = P.cache + static_cast<long long>(stage_pages[st * 2 + (row >> 6)]) * kPageBytes;
-            float scale = 1.0f;
-            uint32_t exps = 0;
-            if (kFp4)
-                exps = *reinterpret_cast<const uint32_t*>(pg_base + kPage * (kIdx / 2) + (row & (kPage - 1)) * 4);
-            else
-                scale = *reinterpret_cast<const float*>(pg_base + kPage * kIdx + (row & (kPage - 1)) * 4);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
+            float scale, exact_logit = 0.f;
+            if (kFp4) {
+                // the converter's per-slot scale (or exact score), beside the
+                // tile until the converter of the stage's next tile
+                scale = row_scale[st * kIdxTileSlots + row];
+                if (scale < 0.f) exact_logit = exact_s[st * kIdxTileSlots + row];
+            } else {
+                if (!tc::mbar_wait(tc::smem_u32(&full[st]), (i / kIdxStages) & 1, abort_flag, P.status)) break;
+                scale = *reinterpret_cast<const float*>(P.cache +
+                                                        static_cast<long long>(stage_pages[st * 2 + (row >> 6)]) *
+                                                            kPageBytes +
+                                                        kPage * kIdx + (row & (kPage - 1)) * 4);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty[st]));
+            }
             if (!tc::mbar_wait(tc::smem_u32(&acc_full[ab]), aph, abort_flag, P.status)) break;
             tc::tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + ab * kAccCols;
-            if (kFp4) {
-                // dot_j = sum over the 4 blocks of 2^(e_b - 127) * acc_b[j]
-                float sb[4];
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    const int eb = static_cast<int>((exps >> (8 * bb)) & 0xffu);
-                    sb[bb] = eb == 0 ? __int_as_float(0x00400000) : exp2i(eb - 127);   // 2^-127 is subnormal
-                }
-                float acc = 0.f;
-#pragma unroll 1
-                for (int hf = 0; hf * 32 < P.n_pad; ++hf) {
-                    float dot[32], va[32], vb[32];
-                    tc::tmem_ld32(taddr + hf * 32, va);
-                    tc::tmem_ld32(taddr + 64 + hf * 32, vb);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) dot[j] = fmaf(vb[j], sb[1], va[j] * sb[0]);
-                    tc::tmem_ld32(taddr + 128 + hf * 32, va);
-                    tc::tmem_ld32(taddr + 192 + hf * 32, vb);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        dot[j] = fmaf(vb[j], sb[3], fmaf(va[j], sb[2], dot[j]));
-                        acc += (hf * 32 + j < P.H) ? w_s[hf * 32 + j] * fmaxf(dot[j], 0.f) : 0.f;
-                    }
-                }
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acc_empty[ab]));
-                const int s = (t_begin + i) * kIdxTileSlots + row;
-                if (kFused) lg_s[i * kIdxTileSlots + row] = acc;
-                else if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc;
-                continue;
-            }
             float v0[32], v1[32];
             tc::tmem_ld32(taddr, v0);
             if (P.n_pad > 32) tc::tmem_ld32(taddr + 32, v1);
@@ -631,9 +689,10 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                     for (int j = 0; j < 32; ++j) acc += (j + 32 < P.H) ? w_s[j + 32] * fmaxf(v1[j], 0.f) : 0.f;
                 }
             }
+            const float lg = (kFp4 && scale < 0.f) ? exact_logit : acc * scale;
             const int s = (t_begin + i) * kIdxTileSlots + row;
-            if (kFused) lg_s[i * kIdxTileSlots + row] = acc * scale;
-            else if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = acc * scale;
+            if (kFused) lg_s[i * kIdxTileSlots + row] = lg;
+            else if (s < n_c) P.logits[static_cast<long long>(b) * P.logits_stride + s] = lg;
         }
     }
 

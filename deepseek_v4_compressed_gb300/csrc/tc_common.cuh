@@ -302,6 +302,16 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
                  : "memory");
 }
 
+// 1-D bulk copy from global memory into this CTA's shared memory (both
+// addresses 16-byte aligned, size a multiple of 16); completion counted in
+// bytes on this CTA's mbarrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank)
 {

@@ -151,3 +151,35 @@ def test_fp4_indexer_1m_batch4_full_size():
     assert plan.info()["launches_indexer"] == 2          # logits, then the long-row top-k
     assert np.all(ln == 2048)
     print("near-tie slots tolerated:", check_rows(d, idx, ln))
+
+
+def test_fp4_indexer_wide_exponent_spread_slots():
+    """Slots whose four 32-dim blocks lie more than 8 binades apart take the
+    kernel's exact per-slot path; their scores (and every other slot's) still
+    give the oracle's top-k."""
+    g = synth.rng(77)
+    B_, n_c, HI, K = 3, 1500, 16, 96
+    ctx = np.full(B_, 4 * n_c, np.int32)
+    pages = (n_c + 63) // 64
+    bt = synth.page_tables(g, B_, pages, extra_pages=1)
+    cache = np.zeros((B_ * pages + 1) * oracle.page_bytes(oracle.IDX_FP4_KIND), np.uint8)
+    for b in range(B_):
+        rows = synth.normal(g, (n_c, 128), 1.0)
+        spread = g.random(n_c) < 0.2                     # a fifth of the slots
+        shift = g.integers(9, 30, size=n_c)
+        rows[spread, :32] *= 2.0 ** shift[spread, None]  # block 0 far above the others
+        rows[spread, 96:] *= 2.0 ** -shift[spread, None]
+        oracle.page_write(oracle.IDX_FP4_KIND, cache, bt[b], *oracle.quant_idx_fp4_rows(rows), nope_dim=64)
+    qi = oracle.f32_to_e4m3(synth.normal(g, (B_, HI, 128)))
+    wq = synth.uniform(g, (B_, HI))
+    plan = B.Plan(B.C4A, 8, B_, K, int(ctx.max()), idx_heads=HI, idx_format=B.IDX_FP4)
+    ws = plan.workspace()
+    out_idx = torch.full((B_, K), -7, dtype=torch.int32, device="cuda")
+    out_len = torch.full((B_,), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.indexer_topk(plan, dev(qi), dev(wq), dev(cache), dev(bt), dev(ctx), out_idx, out_len, ws, status=status)
+    torch.cuda.synchronize()
+    assert B.read_device_status(status)[0] == B.OK
+    idx, ln = out_idx.cpu().numpy(), out_len.cpu().numpy()
+    for b in range(B_):
+        check_topk(idx[b], int(ln[b]), oracle.indexer_logits_fp4(qi[b], wq[b], cache, bt[b], n_c), K)
