@@ -104,9 +104,35 @@ _lib.or_indexer_logits_fp4.restype = None
 _lib.or_indexer_logits_fp4.argtypes = [_u8p, _f32p, ctypes.c_int, ctypes.c_int, _u8p, _i32p,
                                        ctypes.c_int, ctypes.c_int, _f64p]
 
+_lib.or_dequant_gather.restype = None
+_lib.or_dequant_gather.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u8p, _i32p,
+                                   ctypes.c_int, ctypes.c_int, _u16p]
+_lib.or_combine_topk_swa_indices.restype = ctypes.c_int
+_lib.or_combine_topk_swa_indices.argtypes = [_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, _i32p]
+
 MLA_KIND = 0
 IDX_KIND = 1
 IDX_FP4_KIND = 2
+
+
+def dequant_gather(kind, cache, block_table_row, s0, n, nope_dim=512, rope_dim=64, page=64):
+    """bf16 bits [n][nope + rope] of compressed slots (kind 0) or SWA tokens
+    (kind 1) s0 .. s0 + n - 1 of one sequence."""
+    cache = _c(cache, np.uint8) if kind == 0 else _c(cache, np.uint16).view(np.uint8)
+    bt = _c(block_table_row, np.int32)
+    out = np.zeros((max(n, 1), nope_dim + rope_dim), np.uint16)
+    _lib.or_dequant_gather(kind, nope_dim, rope_dim, page, _p(cache, _u8p), _p(bt, _i32p), int(s0), int(n),
+                           _p(out, _u16p))
+    return out[:n]
+
+
+def combine_topk_swa_indices(topk, topk_len, pos, seq_len, gather_len, window, n_comp):
+    topk = _c(topk, np.int32)
+    out = np.zeros(max(1, topk.size + window), np.int32)
+    n = _lib.or_combine_topk_swa_indices(_p(topk, _i32p), int(topk_len), int(pos), int(seq_len),
+                                         int(gather_len), int(window), int(n_comp), _p(out, _i32p))
+    return None if n < 0 else out[:n]
 
 
 def e2m1_to_f64(code):

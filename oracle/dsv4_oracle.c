@@ -811,6 +811,66 @@ int or_gather_keys(int nope_dim, int rope_dim, int page,
     return n;
 }
 
+/* ---- prefill helpers ----------------------------------------------------- */
+
+/* Dequantise-and-gather of cache rows into a dense bf16 buffer ([vLLM-classes]
+ * _forward_prefill, dequantize_and_gather_k_cache: the compressed cache into
+ * kv[:, 0:N], the SWA cache into kv[:, N : N + gather_len]).
+ * kind 0: compressed entries of logical slots s0 .. s0 + n - 1 of a sequence
+ * (block table bt, 64-entry pages of nope + 2*rope data bytes then 8 scale
+ * bytes): row = FP8 * 2^(scale - 127) for the nope dims, the bf16 rope dims;
+ * kind 1: SWA rows of tokens s0 .. s0 + n - 1 (bf16, nope + rope per token).
+ * out: bf16 [n][nope + rope], each value rounded to bf16 (exact for the
+ * dequantised FP8 values in bf16's normal range). */
+void or_dequant_gather(int kind, int nope_dim, int rope_dim, int page, const uint8_t* cache,
+                       const int* bt, int s0, int n, uint16_t* out)
+{
+    int d = nope_dim + rope_dim;
+    int data_b = nope_dim + 2 * rope_dim;
+    long long cpage_b = (long long)page * (data_b + 8);
+    for (int i = 0; i < n; ++i) {
+        int s = s0 + i;
+        uint16_t* o = out + (long long)i * d;
+        if (kind == 0) {
+            const uint8_t* base = cache + (long long)bt[s / page] * cpage_b;
+            const uint8_t* row = base + (long long)(s % page) * data_b;
+            const uint8_t* sc = base + (long long)page * data_b + (long long)(s % page) * 8;
+            for (int c = 0; c < nope_dim; ++c)
+                o[c] = or_f32_to_bf16((float)(or_e4m3_to_f64(row[c]) * ldexp(1.0, (int)sc[c / 64] - 127)));
+            for (int c = 0; c < rope_dim; ++c)
+                o[nope_dim + c] = (uint16_t)(row[nope_dim + 2 * c] | (row[nope_dim + 2 * c + 1] << 8));
+        } else {
+            const uint16_t* row = (const uint16_t*)cache + ((long long)bt[s / page] * page + s % page) * d;
+            memcpy(o, row, sizeof(uint16_t) * (size_t)d);
+        }
+    }
+}
+
+/* Key index list of one prefill query token over the gathered buffer
+ * ([vLLM-classes] _forward_prefill, combine_topk_swa_indices): its top-k
+ * compressed slots (indices 0..N-1 of the buffer: slot j at j) followed by its
+ * causal window, the raw tokens max(0, pos - window + 1) .. pos, which the
+ * buffer holds from index N on for tokens seq_len - gather_len .. seq_len - 1.
+ * Reading: the top-k entries past topk_len (or -1) are dropped; the window
+ * follows the compressed entries in token order; a window token outside the
+ * gathered range is an error (returns -1).  Returns the list's length. */
+int or_combine_topk_swa_indices(const int* topk, int topk_len, int pos, int seq_len, int gather_len,
+                                int window, int n_comp, int* out)
+{
+    int n = 0;
+    for (int i = 0; i < topk_len; ++i)
+        if (topk[i] >= 0)
+            out[n++] = topk[i];
+    int first = seq_len - gather_len;
+    int t0 = pos - window + 1 < 0 ? 0 : pos - window + 1;
+    for (int t = t0; t <= pos; ++t) {
+        if (t < first || t >= seq_len)
+            return -1;
+        out[n++] = n_comp + (t - first);
+    }
+    return n;
+}
+
 /* Sparse absorbed-MQA decode for one query token at position p: gather the
  * key set (or_gather_keys) and attend densely over it with the 576-dim key,
  * the value being its first nope_dim dims (the latent)
