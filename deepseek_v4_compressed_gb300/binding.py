@@ -31,7 +31,9 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_plan_create", "dsv4_plan_destroy", "dsv4_plan_workspace_bytes",
             "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
             "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
-            "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair", "dsv4_plan_set_indexer_format"]
+            "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair", "dsv4_plan_set_indexer_format",
+            "dsv4_sparse_mla_prefill", "dsv4_dequant_gather", "dsv4_combine_topk_swa_indices"]
+GATHER_COMP, GATHER_SWA = 0, 1
 
 
 class Dsv4Error(RuntimeError):
@@ -81,7 +83,7 @@ class IndexerArgs(ctypes.Structure):
                 ("block_table_dev", ctypes.c_void_p), ("bt_stride", ctypes.c_int),
                 ("ctx_len_dev", ctypes.c_void_p), ("out_idx_dev", ctypes.c_void_p),
                 ("out_stride", ctypes.c_int), ("out_len_dev", ctypes.c_void_p),
-                ("status_dev", ctypes.c_void_p)]
+                ("status_dev", ctypes.c_void_p), ("row_seq_dev", ctypes.c_void_p), ("bt_rows", ctypes.c_int)]
 
 
 class MlaArgs(ctypes.Structure):
@@ -92,7 +94,24 @@ class MlaArgs(ctypes.Structure):
                 ("comp_bt_stride", ctypes.c_int), ("topk_idx_dev", ctypes.c_void_p),
                 ("topk_stride", ctypes.c_int), ("topk_len_dev", ctypes.c_void_p),
                 ("ctx_len_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
-                ("lse_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
+                ("lse_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p),
+                ("row_seq_dev", ctypes.c_void_p), ("bt_rows", ctypes.c_int)]
+
+
+class GatherArgs(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("cache_dev", ctypes.c_void_p), ("num_pages", ctypes.c_int),
+                ("block_table_dev", ctypes.c_void_p), ("bt_stride", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("first_dev", ctypes.c_void_p), ("count_dev", ctypes.c_void_p), ("max_count", ctypes.c_int),
+                ("out_dev", ctypes.c_void_p), ("out_rows", ctypes.c_int), ("out_offset", ctypes.c_int),
+                ("status_dev", ctypes.c_void_p)]
+
+
+class CombineArgs(ctypes.Structure):
+    _fields_ = [("topk_dev", ctypes.c_void_p), ("topk_stride", ctypes.c_int), ("topk_len_dev", ctypes.c_void_p),
+                ("pos_dev", ctypes.c_void_p), ("row_seq_dev", ctypes.c_void_p), ("seq_len_dev", ctypes.c_void_p),
+                ("gather_len_dev", ctypes.c_void_p), ("num_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("window", ctypes.c_int), ("n_comp", ctypes.c_int), ("out_dev", ctypes.c_void_p),
+                ("out_stride", ctypes.c_int), ("out_len_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
 
 
 _lib = None
@@ -146,6 +165,12 @@ def lib():
     L.dsv4_selftest_key_dequant.argtypes = [vp, vp]
     L.dsv4_plan_set_indexer_format.restype = st
     L.dsv4_plan_set_indexer_format.argtypes = [vp, ctypes.c_int]
+    L.dsv4_sparse_mla_prefill.restype = st
+    L.dsv4_sparse_mla_prefill.argtypes = [vp, ctypes.POINTER(MlaArgs), vp, ctypes.c_size_t, vp]
+    L.dsv4_dequant_gather.restype = st
+    L.dsv4_dequant_gather.argtypes = [ctypes.POINTER(GatherArgs), vp]
+    L.dsv4_combine_topk_swa_indices.restype = st
+    L.dsv4_combine_topk_swa_indices.argtypes = [ctypes.POINTER(CombineArgs), vp]
     _lib = L
     return L
 
@@ -311,24 +336,28 @@ def cache_insert_rows(kind, rows, seqs, slots, cache, block_table, status=None, 
 
 
 def indexer_topk(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx, out_len, workspace,
-                 status=None, stream=None):
+                 status=None, stream=None, row_seq=None):
+    """dsv4_indexer_topk; row_seq (int32 [rows]) maps each query row to its
+    block-table row (prefill: one row per query token)."""
     a = IndexerArgs(_ptr(q_fp8), _ptr(weights), _ptr(idx_cache), int(_nbytes(idx_cache) // plan.idx_page_bytes),
                     _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
-                    int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
+                    int(out_idx.shape[1]), _ptr(out_len), _ptr(status), _ptr(row_seq),
+                    int(block_table.shape[0]))
     _check(lib().dsv4_indexer_topk(plan.handle, ctypes.byref(a), _ptr(workspace), _nbytes(workspace),
                                    _stream(stream)), "indexer_topk")
 
 
 def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspace, comp_cache=None,
                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None,
-                      stream=None):
+                      stream=None, row_seq=None):
     a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // SWA_PAGE_BYTES),
                 _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
                 int(_nbytes(comp_cache) // MLA_PAGE_BYTES) if comp_cache is not None else 0,
                 _ptr(comp_block_table),
                 int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
                 _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
-                _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status))
+                _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status), _ptr(row_seq),
+                int(swa_block_table.shape[0]))
     _check(lib().dsv4_sparse_mla_decode(plan.handle, ctypes.byref(a), _ptr(workspace),
                                         workspace.numel(), _stream(stream)), "sparse_mla_decode")
 
@@ -344,3 +373,37 @@ def indexer_topk_noalloc(plan, q_fp8, weights, idx_cache, block_table, ctx_len, 
                     _ptr(block_table), int(block_table.shape[1]), _ptr(ctx_len), _ptr(out_idx),
                     int(out_idx.shape[1]), _ptr(out_len), _ptr(status))
     _check(f(plan.handle, ctypes.byref(a), _stream(stream)), "indexer_topk_noalloc")
+
+
+def sparse_mla_prefill(plan, q, swa_cache, swa_block_table, ctx_len, row_seq, out, workspace, comp_cache=None,
+                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None, stream=None):
+    """dsv4_sparse_mla_prefill: one query row per prefill token (position
+    ctx_len - 1), row_seq mapping each row to its block-table row."""
+    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // SWA_PAGE_BYTES),
+                _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
+                int(_nbytes(comp_cache) // MLA_PAGE_BYTES) if comp_cache is not None else 0,
+                _ptr(comp_block_table),
+                int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
+                _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
+                _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status), _ptr(row_seq),
+                int(swa_block_table.shape[0]))
+    _check(lib().dsv4_sparse_mla_prefill(plan.handle, ctypes.byref(a), _ptr(workspace), workspace.numel(),
+                                         _stream(stream)), "sparse_mla_prefill")
+
+
+def dequant_gather(kind, cache, block_table, first, count, max_count, out, out_offset=0, status=None, stream=None):
+    """dsv4_dequant_gather: out[s][out_offset + i] = dequantised row first[s] + i, i < count[s]."""
+    page_b = MLA_PAGE_BYTES if kind == GATHER_COMP else SWA_PAGE_BYTES
+    a = GatherArgs(int(kind), _ptr(cache), int(_nbytes(cache) // page_b), _ptr(block_table),
+                   int(block_table.shape[1]), int(block_table.shape[0]), _ptr(first), _ptr(count), int(max_count),
+                   _ptr(out), int(out.shape[1]), int(out_offset), _ptr(status))
+    _check(lib().dsv4_dequant_gather(ctypes.byref(a), _stream(stream)), "dequant_gather")
+
+
+def combine_topk_swa_indices(topk, topk_len, pos, row_seq, seq_len, gather_len, window, n_comp, out, out_len,
+                             status=None, stream=None):
+    """dsv4_combine_topk_swa_indices: each prefill token's top-k slots, then its window rows."""
+    a = CombineArgs(_ptr(topk), int(topk.shape[1]), _ptr(topk_len), _ptr(pos), _ptr(row_seq), _ptr(seq_len),
+                    _ptr(gather_len), int(topk.shape[0]), int(seq_len.shape[0]), int(window), int(n_comp),
+                    _ptr(out), int(out.shape[1]), _ptr(out_len), _ptr(status))
+    _check(lib().dsv4_combine_topk_swa_indices(ctypes.byref(a), _stream(stream)), "combine_topk_swa_indices")

@@ -369,6 +369,9 @@ struct IdxTcParams {
     int* out_idx;
     int out_stride;
     int* out_len;
+    // prefill rows: block-table row of query row b (NULL: b), bt_rows rows
+    const int* row_seq;
+    int bt_rows;
 };
 
 template <bool kFused, bool kFp4>
@@ -469,13 +472,22 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
             tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
             tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
         }
+        // the query row's block-table row (prefill rows map to their sequence's)
+        int seq = b;
+        if (P.row_seq) {
+            seq = P.row_seq[b];
+            if (seq < 0 || seq >= P.bt_rows) {
+                if (lane == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+                seq = 0;
+            }
+        }
         // lane l: page id of page l of the group of 16 tiles starting at tile i,
         // loaded by the lanes at once
         auto page_group = [&](int i) {
             int pg = -1;
             if (2 * i + lane < 2 * n_my) {
                 const int pi = min(2 * (t_begin + i) + lane, n_pages - 1);
-                pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(b) * P.bt_stride + pi] : -1;
+                pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(seq) * P.bt_stride + pi] : -1;
                 if (pg < 0 || pg >= P.num_pages) {
                     flag(P.status, DSV4_DEV_BAD_PAGE);
                     pg = -1;
@@ -1403,6 +1415,7 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         return DSV4_ERR_INVALID;
     if (a->out_stride < plan->topk || a->bt_stride < 1 || a->num_pages < 1) return DSV4_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(a->idx_cache_dev) & 15) return DSV4_ERR_SHAPE;
+    if (a->row_seq_dev && a->bt_rows < 1) return DSV4_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_logits_off);
     const int B = plan->batch, H = plan->geom.idx_heads;
@@ -1442,6 +1455,8 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         P.out_idx = a->out_idx_dev;
         P.out_stride = a->out_stride;
         P.out_len = a->out_len_dev;
+        P.row_seq = a->row_seq_dev;
+        P.bt_rows = a->bt_rows;
         const bool fused = plan->idx_fused_topk != 0;
         static PerDeviceOnce tc_attr;
         const bool attr_ok = tc_attr.run([] {

@@ -34,6 +34,9 @@ struct MlaParams {
     int window;
     float scale;
     int* status;
+    // prefill rows: block-table row of query row b (NULL: b), bt_rows rows
+    const int* row_seq;
+    int bt_rows;
 };
 
 // ---------------------------------------------------------------------------
@@ -233,6 +236,15 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     const int rank = blockIdx.x;                          // the cluster spans gridDim.x
     const int b = blockIdx.y / T.head_groups, g_head = blockIdx.y % T.head_groups;
+    // the query row's block-table row (prefill rows map to their sequence's)
+    int seq = b;
+    if (P.row_seq) {
+        seq = P.row_seq[b];
+        if (seq < 0 || seq >= P.bt_rows) {
+            if (threadIdx.x == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+            seq = 0;
+        }
+    }
     const int h0 = g_head * 64;
     const int nh = min(64, P.H - h0);
     const int p = P.ctx_len[b] - 1;
@@ -358,7 +370,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const bool bt_smem = P.comp_bt != nullptr && P.comp_bt_stride <= kBtSmem;
             if (bt_smem)
                 for (int i = threadIdx.x - 128; i < P.comp_bt_stride; i += 32 * kTcProdWarps)
-                    bt_s[i] = P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + i];
+                    bt_s[i] = P.comp_bt[static_cast<long long>(seq) * P.comp_bt_stride + i];
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(bt_ready));
             // Row table, spread over the lanes: lane l holds row pw + 8 (l % 8) of
@@ -392,7 +404,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     pg[q] = -2;
                     if (slot[q] >= 0 && (slot[q] >> 6) < P.comp_bt_stride)
                         pg[q] = bt_smem ? bt_s[slot[q] >> 6]
-                                        : P.comp_bt[static_cast<long long>(b) * P.comp_bt_stride + (slot[q] >> 6)];
+                                        : P.comp_bt[static_cast<long long>(seq) * P.comp_bt_stride + (slot[q] >> 6)];
                     else if (slot[q] != -1)
                         flag(P.status, DSV4_DEV_BAD_INDEX);
                 }
@@ -470,7 +482,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (pw == 0) {
                     if (lane == 0) {
                         const int lp = pg0 + rank + i * C;
-                        int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(b) * P.swa_bt_stride + lp] : -1;
+                        int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(seq) * P.swa_bt_stride + lp] : -1;
                         if (pg < 0 || pg >= P.swa_pages) {
                             flag(P.status, DSV4_DEV_BAD_PAGE);
                             pg = -1;
@@ -787,9 +799,166 @@ __global__ void key_dequant_selftest_kernel(uint16_t* out)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill helpers (_forward_prefill of the "DeepseekV4Attention" class
+// walkthrough): dequantise-and-gather of cache rows into a dense bf16 buffer,
+// and each prefill token's combined index list over that buffer.
+// ---------------------------------------------------------------------------
+struct GatherParams {
+    int kind;
+    const uint8_t* cache;
+    int num_pages;
+    const int* bt;
+    int bt_stride;
+    const int* first;
+    const int* count;
+    int max_count;
+    uint8_t* out;
+    int out_rows;
+    int out_offset;
+    int* status;
+};
+
+// One warp per gathered row: (row i of run s) -> out[s][out_offset + i].
+// Compressed entries: lane l dequantises nope codes 16l .. 16l + 15 (as the
+// decode kernel does), lanes 0-7 copy the bf16 rope dims; SWA rows are copied.
+__global__ void __launch_bounds__(32) dequant_gather_kernel(GatherParams G)
+{
+    const int s = blockIdx.y, i = blockIdx.x, lane = threadIdx.x;
+    int cnt = G.count[s];
+    if (cnt > G.max_count || cnt < 0) {
+        if (i == 0 && lane == 0) flag(G.status, DSV4_DEV_BAD_INDEX);
+        cnt = min(max(cnt, 0), G.max_count);
+    }
+    if (i >= cnt) return;
+    const int slot = G.first[s] + i;
+    uint8_t* orow = G.out + (static_cast<long long>(s) * G.out_rows + G.out_offset + i) * (kHead * 2);
+    int pg = -1;
+    if (slot >= 0 && (slot >> 6) < G.bt_stride) {
+        pg = G.bt[static_cast<long long>(s) * G.bt_stride + (slot >> 6)];
+        if (pg < 0 || pg >= G.num_pages) pg = -1;
+    }
+    if (pg < 0) {
+        if (lane == 0) flag(G.status, DSV4_DEV_BAD_PAGE);
+        for (int u = lane; u < kHead * 2 / 16; u += 32) reinterpret_cast<uint4*>(orow)[u] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    if (G.kind == DSV4_GATHER_COMP) {
+        const uint8_t* page = G.cache + static_cast<long long>(pg) * kMlaPage;
+        const uint8_t* row = page + (slot & 63) * kMlaData;
+        const uint4 w = *reinterpret_cast<const uint4*>(row + lane * 16);
+        const uint32_t sb = page[kPage * kMlaData + (slot & 63) * 8 + (lane >> 2)];
+        uint4 lo, hi;
+        dequant16(w, sb, lo, hi);
+        reinterpret_cast<uint4*>(orow)[2 * lane] = lo;
+        reinterpret_cast<uint4*>(orow)[2 * lane + 1] = hi;
+        if (lane < 8)
+            reinterpret_cast<uint4*>(orow + kNope * 2)[lane] = *reinterpret_cast<const uint4*>(row + kNope + lane * 16);
+    } else {
+        const uint4* row = reinterpret_cast<const uint4*>(G.cache + static_cast<long long>(pg) * kSwaPage +
+                                                          (slot & 63) * (kHead * 2));
+        for (int u = lane; u < kHead * 2 / 16; u += 32) reinterpret_cast<uint4*>(orow)[u] = row[u];
+    }
+}
+
+struct CombineParams {
+    const int* topk;
+    int topk_stride;
+    const int* topk_len;
+    const int* pos;
+    const int* row_seq;
+    const int* seq_len;
+    const int* gather_len;
+    int num_seqs;
+    int window;
+    int n_comp;
+    int* out;
+    int out_stride;
+    int* out_len;
+    int* status;
+};
+
+// One warp per prefill token: the valid top-k entries in order (ballot
+// compaction), then the window tokens as rows n_comp + (t - first gathered).
+// A window token outside the gathered run, a bad sequence or too short an
+// output row sets DSV4_DEV_BAD_INDEX and length -1.
+__global__ void __launch_bounds__(32) combine_indices_kernel(CombineParams C)
+{
+    const int t = blockIdx.x, lane = threadIdx.x;
+    int* orow = C.out + static_cast<long long>(t) * C.out_stride;
+    const int s = C.row_seq[t];
+    const int len = C.topk_len[t];
+    const int pos = C.pos[t];
+    bool bad = s < 0 || s >= C.num_seqs || len < 0 || len > C.topk_stride || pos < 0;
+    int first = 0, seq_len = 0;
+    if (!bad) {
+        seq_len = C.seq_len[s];
+        first = seq_len - C.gather_len[s];
+        const int w0 = max(0, pos - C.window + 1);
+        bad = pos >= seq_len || w0 < first || len + (pos - w0 + 1) > C.out_stride;
+    }
+    if (bad) {
+        if (lane == 0) {
+            flag(C.status, DSV4_DEV_BAD_INDEX);
+            C.out_len[t] = -1;
+        }
+        return;
+    }
+    const int* krow = C.topk + static_cast<long long>(t) * C.topk_stride;
+    int n = 0;
+    for (int i0 = 0; i0 < len; i0 += 32) {
+        const int v = i0 + lane < len ? krow[i0 + lane] : -1;
+        const uint32_t m = __ballot_sync(0xffffffffu, v >= 0);
+        if (v >= 0) orow[n + __popc(m & ((1u << lane) - 1u))] = v;
+        n += __popc(m);
+    }
+    const int w0 = max(0, pos - C.window + 1);
+    for (int tok = w0 + lane; tok <= pos; tok += 32) orow[n + tok - w0] = C.n_comp + (tok - first);
+    n += pos - w0 + 1;
+    for (int i = n + lane; i < C.out_stride; i += 32) orow[i] = -1;
+    if (lane == 0) C.out_len[t] = n;
+}
+
 }  // namespace dsv4
 
 using namespace dsv4;
+
+extern "C" dsv4_status dsv4_dequant_gather(const dsv4_gather_args* a, dsv4_stream_t stream)
+{
+    if (a == nullptr) return DSV4_ERR_INVALID;
+    if (a->kind != DSV4_GATHER_COMP && a->kind != DSV4_GATHER_SWA) return DSV4_ERR_INVALID;
+    if (a->num_seqs < 0 || a->max_count < 0 || a->bt_stride < 1 || a->num_pages < 1 || a->out_offset < 0 ||
+        a->out_rows < a->out_offset + a->max_count)
+        return DSV4_ERR_SHAPE;
+    if (a->num_seqs == 0 || a->max_count == 0) return DSV4_OK;
+    if (!a->cache_dev || !a->block_table_dev || !a->first_dev || !a->count_dev || !a->out_dev)
+        return DSV4_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(a->cache_dev) & 15) || (reinterpret_cast<uintptr_t>(a->out_dev) & 15))
+        return DSV4_ERR_SHAPE;
+    if (a->max_count > 65535 || a->num_seqs > 65535) return DSV4_ERR_UNSUPPORTED;
+    GatherParams G{a->kind, static_cast<const uint8_t*>(a->cache_dev), a->num_pages, a->block_table_dev,
+                   a->bt_stride, a->first_dev, a->count_dev, a->max_count, static_cast<uint8_t*>(a->out_dev),
+                   a->out_rows, a->out_offset, a->status_dev};
+    dequant_gather_kernel<<<dim3(a->max_count, a->num_seqs), 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(G);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+extern "C" dsv4_status dsv4_combine_topk_swa_indices(const dsv4_combine_args* a, dsv4_stream_t stream)
+{
+    if (a == nullptr) return DSV4_ERR_INVALID;
+    if (a->num_tokens < 0 || a->num_seqs < 1 || a->window < 1 || a->n_comp < 0 || a->topk_stride < 0 ||
+        a->out_stride < 1)
+        return DSV4_ERR_SHAPE;
+    if (a->num_tokens == 0) return DSV4_OK;
+    if ((a->topk_stride > 0 && !a->topk_dev) || !a->topk_len_dev || !a->pos_dev || !a->row_seq_dev ||
+        !a->seq_len_dev || !a->gather_len_dev || !a->out_dev || !a->out_len_dev)
+        return DSV4_ERR_INVALID;
+    CombineParams C{a->topk_dev, a->topk_stride, a->topk_len_dev, a->pos_dev, a->row_seq_dev, a->seq_len_dev,
+                    a->gather_len_dev, a->num_seqs, a->window, a->n_comp, a->out_dev, a->out_stride,
+                    a->out_len_dev, a->status_dev};
+    combine_indices_kernel<<<a->num_tokens, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(C);
+    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
 
 extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_mla_args* a,
                                               void* workspace, size_t workspace_bytes,
@@ -823,6 +992,9 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     P.window = plan->geom.window;
     P.scale = plan->geom.softmax_scale;
     P.status = a->status_dev;
+    P.row_seq = a->row_seq_dev;
+    P.bt_rows = a->bt_rows;
+    if (P.row_seq && P.bt_rows < 1) return DSV4_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     MlaTcParams T;
     T.base = P;
@@ -873,6 +1045,16 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_tc, tm_q, tm_swa, T);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+}
+
+// Sparse prefill attention: one query row per prefill token, each over its
+// own top-k compressed slots and its own causal window, straight from the
+// paged caches (the decode kernel with the rows mapped to their sequences).
+extern "C" dsv4_status dsv4_sparse_mla_prefill(const dsv4_plan* plan, const dsv4_mla_args* a,
+                                               void* workspace, size_t workspace_bytes, dsv4_stream_t stream)
+{
+    if (a == nullptr || a->row_seq_dev == nullptr) return DSV4_ERR_INVALID;
+    return dsv4_sparse_mla_decode(plan, a, workspace, workspace_bytes, stream);
 }
 
 extern "C" dsv4_status dsv4_selftest_key_dequant(void* out_dev, dsv4_stream_t stream)

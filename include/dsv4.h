@@ -331,6 +331,14 @@ typedef struct dsv4_indexer_args {
     int out_stride;
     int* out_len_dev;
     int* status_dev;
+    /* Prefill (and any caller whose rows are not sequences): NULL for decode,
+     * where row b is sequence b; else int32 [batch], the block-table row of
+     * each query row (a prefill query token of position ctx_len[b] - 1 takes
+     * its sequence's row).  bt_rows: the block table's row count, which every
+     * row_seq value must stay below (checked: DSV4_DEV_BAD_INDEX, the row
+     * then reads row 0). */
+    const int* row_seq_dev;
+    int bt_rows;
 } dsv4_indexer_args;
 
 dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_indexer_args* args,
@@ -400,11 +408,87 @@ typedef struct dsv4_mla_args {
     void* out_dev;
     float* lse_dev;
     int* status_dev;
+    /* As in dsv4_indexer_args: NULL for decode; else the block-table row
+     * (of both tables, bt_rows rows each) of each query row. */
+    const int* row_seq_dev;
+    int bt_rows;
 } dsv4_mla_args;
 
 dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_mla_args* args,
                                    void* workspace_dev, size_t workspace_bytes,
                                    dsv4_stream_t stream);
+
+/* ---- (4) sparse prefill -------------------------------------------------------- */
+
+/* Sparse prefill attention ([vLLM-classes] _forward_prefill: each prefill
+ * token attends over its top-k compressed slots and its causal SWA window,
+ * flash_mla_sparse_fwd).  Computes, for each query row b (a prefill token at
+ * position ctx_len[b] - 1 of sequence row_seq_dev[b]), exactly what
+ * dsv4_sparse_mla_decode computes for a decode row, reading the paged caches
+ * through the sequence's block-table rows: a plan whose batch is the number
+ * of query rows serves a prefill chunk.  The top-k of each row comes from
+ * dsv4_indexer_topk with the same row_seq_dev (c4a) or from caller metadata
+ * (c128a); the SWA cache must hold every token of the windows.
+ * Errors: as dsv4_sparse_mla_decode; DSV4_ERR_INVALID if row_seq_dev is NULL. */
+dsv4_status dsv4_sparse_mla_prefill(const dsv4_plan* plan, const dsv4_mla_args* args, void* workspace_dev,
+                                    size_t workspace_bytes, dsv4_stream_t stream);
+
+/* Dequantise-and-gather of cache rows into a dense bf16 buffer
+ * ([vLLM-classes] _forward_prefill, dequantize_and_gather_k_cache: the
+ * compressed cache into kv[:, 0:N], the SWA cache into kv[:, N:N+gather_len]).
+ * For each sequence s < num_seqs and i < count_dev[s] (<= max_count):
+ *   out[s][out_offset + i][0:576] = row of slot / token first_dev[s] + i,
+ * through block_table_dev[s][...].  DSV4_GATHER_COMP: a compressed entry
+ * dequantised (FP8 * 2^(scale - 127) for dims 0..511, the bf16 rope dims);
+ * DSV4_GATHER_SWA: the bf16 SWA row.  out_dev: bf16 [num_seqs][out_rows][576]
+ * (16-byte aligned, out_rows >= out_offset + max_count).  A bad page sets
+ * DSV4_DEV_BAD_PAGE and writes a zero row; a count past max_count sets
+ * DSV4_DEV_BAD_INDEX and is clamped.  Errors: DSV4_ERR_INVALID, _SHAPE,
+ * _UNSUPPORTED (max_count or num_seqs above 65535). */
+typedef enum dsv4_gather_kind { DSV4_GATHER_COMP = 0, DSV4_GATHER_SWA = 1 } dsv4_gather_kind;
+typedef struct dsv4_gather_args {
+    int kind;                      /* dsv4_gather_kind */
+    const void* cache_dev;         /* compressed pages (DSV4_MLA_PAGE_BYTES) or SWA pages */
+    int num_pages;
+    const int* block_table_dev;    /* int32 [num_seqs][bt_stride] */
+    int bt_stride;
+    int num_seqs;
+    const int* first_dev;          /* int32 [num_seqs] */
+    const int* count_dev;          /* int32 [num_seqs] */
+    int max_count;
+    void* out_dev;
+    int out_rows;
+    int out_offset;
+    int* status_dev;
+} dsv4_gather_args;
+dsv4_status dsv4_dequant_gather(const dsv4_gather_args* args, dsv4_stream_t stream);
+
+/* Each prefill token's key list over the gathered buffer ([vLLM-classes]
+ * _forward_prefill, combine_topk_swa_indices): the valid (>= 0) entries of
+ * topk_dev[t][0:topk_len_dev[t]] in order, then the window tokens
+ * max(0, pos - window + 1) .. pos as rows n_comp + (token - (seq_len -
+ * gather_len)) of its sequence row_seq_dev[t]; out_len_dev[t] is the count
+ * and the rest of the row is -1.  A window token outside the gathered run, a
+ * sequence out of range or an output row too short sets DSV4_DEV_BAD_INDEX
+ * and out_len -1. */
+typedef struct dsv4_combine_args {
+    const int* topk_dev;           /* int32 [num_tokens][topk_stride] (logical slots, -1 padding) */
+    int topk_stride;
+    const int* topk_len_dev;       /* int32 [num_tokens] */
+    const int* pos_dev;            /* int32 [num_tokens] query positions */
+    const int* row_seq_dev;        /* int32 [num_tokens] sequence of each token */
+    const int* seq_len_dev;        /* int32 [num_seqs] */
+    const int* gather_len_dev;     /* int32 [num_seqs] SWA tokens gathered (the last of the sequence) */
+    int num_tokens;
+    int num_seqs;
+    int window;
+    int n_comp;                    /* N: buffer row of the first gathered SWA token */
+    int* out_dev;                  /* int32 [num_tokens][out_stride] */
+    int out_stride;
+    int* out_len_dev;              /* int32 [num_tokens] */
+    int* status_dev;
+} dsv4_combine_args;
+dsv4_status dsv4_combine_topk_swa_indices(const dsv4_combine_args* args, dsv4_stream_t stream);
 
 /* ---- diagnostics ------------------------------------------------------------- */
 

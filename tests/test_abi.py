@@ -122,3 +122,25 @@ def test_plan_choices_on_152_sms(args, expect):
     info = B.Plan(t, h, b, k, ctx, idx_heads=hi).info()
     for key, v in expect.items():
         assert info[key] == v, (key, info)
+
+
+def test_fp4_format_and_prefill_entry_points_validate_on_the_host():
+    lib = B.lib()
+    p4 = B.Plan(B.C4A, 8, 2, 32, 4096, idx_heads=8)
+    assert lib.dsv4_plan_set_indexer_format(p4.handle, B.IDX_FP4) == B.OK
+    assert lib.dsv4_plan_set_indexer_format(p4.handle, 7) == B.ERR_INVALID
+    pswa = B.Plan(B.SWAONLY, 8, 2, 0, 4096)
+    assert lib.dsv4_plan_set_indexer_format(pswa.handle, B.IDX_FP4) == B.ERR_UNSUPPORTED
+    # prefill attention needs the row -> sequence map
+    a = B.MlaArgs()
+    assert lib.dsv4_sparse_mla_prefill(p4.handle, ctypes.byref(a), None, 0, None) == B.ERR_INVALID
+    # gather: unknown kind, output rows too few for offset + count
+    g = B.GatherArgs(5, None, 1, None, 1, 1, None, None, 1, None, 1, 0, None)
+    assert lib.dsv4_dequant_gather(ctypes.byref(g), None) == B.ERR_INVALID
+    g = B.GatherArgs(B.GATHER_COMP, None, 1, None, 1, 1, None, None, 4, None, 3, 0, None)
+    assert lib.dsv4_dequant_gather(ctypes.byref(g), None) == B.ERR_SHAPE
+    # combine: a window of 0 is rejected; no tokens is a no-op
+    c = B.CombineArgs(None, 0, None, None, None, None, None, 3, 1, 0, 0, None, 1, None, None)
+    assert lib.dsv4_combine_topk_swa_indices(ctypes.byref(c), None) == B.ERR_SHAPE
+    c = B.CombineArgs(None, 0, None, None, None, None, None, 0, 1, 128, 0, None, 1, None, None)
+    assert lib.dsv4_combine_topk_swa_indices(ctypes.byref(c), None) == B.OK
