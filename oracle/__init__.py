@@ -111,9 +111,43 @@ _lib.or_combine_topk_swa_indices.restype = ctypes.c_int
 _lib.or_combine_topk_swa_indices.argtypes = [_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, _i32p]
 
+_lib.or_sparse_mla_v4.restype = ctypes.c_int
+_lib.or_sparse_mla_v4.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, _u8p, _i32p, _i32p, ctypes.c_int, _u8p,
+                                  _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_double, _f64p, _f64p]
+_lib.or_inv_rope_fp8_quant.restype = None
+_lib.or_inv_rope_fp8_quant.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, _f32p, ctypes.c_int, _u8p, _f32p]
+
 MLA_KIND = 0
 IDX_KIND = 1
 IDX_FP4_KIND = 2
+
+
+def sparse_mla_v4(q_bf16, comp_cache, comp_bt_row, idx, length, swa_cache, swa_bt_row, p, scale, window=128,
+                  page=64):
+    """V4-native sparse decode attention (K = V over 512 dims, FP8 caches of
+    584-byte rows): (out [H][512] double, lse [H])."""
+    q = _c(q_bf16, np.uint16)
+    n_heads = q.shape[0]
+    out = np.empty((n_heads, 512), np.float64)
+    lse = np.empty(n_heads, np.float64)
+    cc = _c(comp_cache if comp_cache is not None else _EMPTY_U8, np.uint8)
+    cbt = _c(comp_bt_row if comp_bt_row is not None else _EMPTY_I32, np.int32)
+    ix = _c(idx if idx is not None and length else _EMPTY_I32, np.int32)
+    _lib.or_sparse_mla_v4(_p(q, _u16p), n_heads, page, _p(cc, _u8p), _p(cbt, _i32p), _p(ix, _i32p), int(length),
+                          _p(_c(swa_cache, np.uint8), _u8p), _p(_c(swa_bt_row, np.int32), _i32p), int(p), window,
+                          float(scale), _p(out, _f64p), _p(lse, _f64p))
+    return out, lse
+
+
+def inv_rope_fp8_quant(o_bf16, pos, cos_sin, rope_dim=64):
+    """o bf16 bits [H][512] -> (E4M3 codes [H][512], fp32 scales [H][4])."""
+    o = _c(o_bf16, np.uint16)
+    n_heads = o.shape[0]
+    codes = np.empty((n_heads, 512), np.uint8)
+    sc = np.empty((n_heads, 4), np.float32)
+    _lib.or_inv_rope_fp8_quant(_p(o, _u16p), n_heads, int(pos), _p(_c(cos_sin, np.float32), _f32p), rope_dim,
+                               _p(codes, _u8p), _p(sc, _f32p))
+    return codes, sc
 
 
 def dequant_gather(kind, cache, block_table_row, s0, n, nope_dim=512, rope_dim=64, page=64):

@@ -811,6 +811,92 @@ int or_gather_keys(int nope_dim, int rope_dim, int page,
     return n;
 }
 
+/* ---- V4-native geometry: K = V over 512 dims, FP8 SWA, inverse RoPE ------ */
+
+/* One V4 cache row of 584 bytes ([MLA-to-CSA] 5.5: 448 NoPE fp8 + 128 RoPE
+ * bf16 + 7 UE8M0 scales + 1 pad; pages of 64: data plane then scale plane),
+ * dequantised to double: dims 0..447 = fp8 * 2^(scale_b - 127) (64-dim blocks),
+ * dims 448..511 = the bf16 RoPE values. */
+static void or_v4_row(const uint8_t* cache, const int* bt, int page, int s, double* k)
+{
+    const int nope = 448, rope = 64, data_b = 576;
+    long long page_b = (long long)page * (data_b + 8);
+    const uint8_t* base = cache + (long long)bt[s / page] * page_b;
+    const uint8_t* row = base + (long long)(s % page) * data_b;
+    const uint8_t* sc = base + (long long)page * data_b + (long long)(s % page) * 8;
+    for (int c = 0; c < nope; ++c)
+        k[c] = or_e4m3_to_f64(row[c]) * ldexp(1.0, (int)sc[c / 64] - 127);
+    for (int i = 0; i < rope; ++i) {
+        uint16_t h = (uint16_t)(row[nope + 2 * i] | (row[nope + 2 * i + 1] << 8));
+        k[nope + i] = (double)or_bf16_to_f32(h);
+    }
+}
+
+/* Sparse decode attention in the V4-native geometry ([MLA-to-CSA] 5.5 and 6.4:
+ * K and V share one 512-dim vector; the SWA cache is FP8 like the compressed
+ * one): keys = the compressed slots idx[0..len) (logical ids through comp_bt)
+ * followed by the window tokens max(0, p - window + 1) .. p (through swa_bt),
+ * both caches of 584-byte rows; s = scale * q.k over the 512 dims; the value
+ * is the same 512-dim row.  q bf16 [n_heads][512]; out double [n_heads][512]
+ * (the output still carries the keys' rotation: see or_inv_rope_fp8_quant). */
+int or_sparse_mla_v4(const uint16_t* q, int n_heads, int page, const uint8_t* comp_cache,
+                     const int* comp_bt, const int* idx, int len, const uint8_t* swa_cache,
+                     const int* swa_bt, int p, int window, double scale, double* out, double* lse)
+{
+    const int d = 512;
+    int t0 = p - window + 1 < 0 ? 0 : p - window + 1;
+    int n = len + (p - t0 + 1);
+    double* keys = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * d);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)n_heads * d);
+    for (int i = 0; i < n_heads * d; ++i)
+        qd[i] = (double)or_bf16_to_f32(q[i]);
+    int m = 0;
+    for (int i = 0; i < len; ++i)
+        or_v4_row(comp_cache, comp_bt, page, idx[i], keys + (long long)(m++) * d);
+    for (int t = t0; t <= p; ++t)
+        or_v4_row(swa_cache, swa_bt, page, t, keys + (long long)(m++) * d);
+    or_dense_attention(qd, n_heads, keys, m, d, d, scale, out, lse);
+    free(keys);
+    free(qd);
+    return m;
+}
+
+/* Inverse RoPE and FP8 quantisation of the attention output
+ * ([MLA-to-CSA] 6.4, fused_inv_rope_fp8_quant; [V4-internals] section 6:
+ * Inverse RoPE + FP8 Quant after Flash MLA).  Per head: the 64 RoPE dims
+ * (448..511) rotated by R(-pos) -- GPT-J pairs, cos / sin of the query
+ * position from the table: x0' = x0 c + x1 s, x1' = x1 c - x0 s, each
+ * product and sum rounded to fp32 -- so that R(-i) R(j) k = R(j - i) k; then
+ * every 128-dim block quantised as the indexer cache is: scale = amax / 448
+ * (fp32; 1 for an all-zero block), code = E4M3(x / scale).
+ * Reading: the pages name the fused operator and its inputs (o, positions,
+ * cos_sin_cache, groups, nope / rope dims) but not the quantisation grain;
+ * 128-dim blocks with fp32 scales (the indexer cache's rule) are taken.
+ * o: bf16 bits [n_heads][512]; codes [n_heads][512]; scales [n_heads][4]. */
+void or_inv_rope_fp8_quant(const uint16_t* o, int n_heads, int pos, const float* cos_sin, int rope_dim,
+                           uint8_t* codes, float* scales)
+{
+    const int d = 512, nope = 448;
+    float x[512];
+    for (int h = 0; h < n_heads; ++h) {
+        for (int c = 0; c < d; ++c)
+            x[c] = or_bf16_to_f32(o[(long long)h * d + c]);
+        const float* row = cos_sin + (long long)pos * rope_dim;
+        for (int i = 0; i < rope_dim / 2; ++i) {
+            float x0 = x[nope + 2 * i], x1 = x[nope + 2 * i + 1];
+            float c = row[i], sn = row[rope_dim / 2 + i];
+            float a = x0 * c, b = x1 * sn, e = x1 * c, f = x0 * sn;
+            x[nope + 2 * i] = a + b;
+            x[nope + 2 * i + 1] = e - f;
+        }
+        for (int blk = 0; blk < d / 128; ++blk) {
+            float sc;
+            or_quant_idx(x + blk * 128, 128, codes + (long long)h * d + blk * 128, &sc);
+            scales[h * (d / 128) + blk] = sc;
+        }
+    }
+}
+
 /* ---- prefill helpers ----------------------------------------------------- */
 
 /* Dequantise-and-gather of cache rows into a dense bf16 buffer ([vLLM-classes]

@@ -99,6 +99,11 @@ int  or_gather_keys(int nope_dim, int rope_dim, int page,
                     const uint8_t* comp_cache, const int* comp_bt, const int* idx, int len,
                     const uint16_t* swa_cache, const int* swa_bt, int p, int window,
                     double* keys);
+int  or_sparse_mla_v4(const uint16_t* q, int n_heads, int page, const uint8_t* comp_cache,
+                      const int* comp_bt, const int* idx, int len, const uint8_t* swa_cache,
+                      const int* swa_bt, int p, int window, double scale, double* out, double* lse);
+void or_inv_rope_fp8_quant(const uint16_t* o, int n_heads, int pos, const float* cos_sin, int rope_dim,
+                           uint8_t* codes, float* scales);
 void or_dequant_gather(int kind, int nope_dim, int rope_dim, int page, const uint8_t* cache,
                        const int* bt, int s0, int n, uint16_t* out);
 int  or_combine_topk_swa_indices(const int* topk, int topk_len, int pos, int seq_len, int gather_len,
