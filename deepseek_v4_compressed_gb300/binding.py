@@ -13,8 +13,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsv4.so")
 
 SWAONLY, C4A, C128A = 1, 4, 128
-CACHE_MLA, CACHE_IDX, CACHE_IDX_FP4 = 0, 1, 2
+CACHE_MLA, CACHE_IDX, CACHE_IDX_FP4, CACHE_V4 = 0, 1, 2, 3
 IDX_FP8, IDX_FP4 = 0, 1
+KV_576, KV_V4 = 0, 1
 
 OK, ERR_INVALID, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_CHECK, ERR_TIMEOUT = range(7)
 DEV_BAD_INDEX, DEV_BAD_PAGE, DEV_BAD_POSITION, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
@@ -23,7 +24,10 @@ NOPE_DIM, ROPE_DIM, HEAD_DIM, V_DIM, IDX_DIM, PAGE, WINDOW = 512, 64, 576, 512, 
 MLA_PAGE_BYTES = 64 * 648
 IDX_PAGE_BYTES = 64 * 132
 IDX_FP4_PAGE_BYTES = 64 * 68
-PAGE_BYTES = {CACHE_MLA: MLA_PAGE_BYTES, CACHE_IDX: IDX_PAGE_BYTES, CACHE_IDX_FP4: IDX_FP4_PAGE_BYTES}
+V4_NOPE_DIM, V4_HEAD_DIM = 448, 512
+V4_PAGE_BYTES = 64 * 584
+PAGE_BYTES = {CACHE_MLA: MLA_PAGE_BYTES, CACHE_IDX: IDX_PAGE_BYTES, CACHE_IDX_FP4: IDX_FP4_PAGE_BYTES,
+              CACHE_V4: V4_PAGE_BYTES}
 SWA_PAGE_BYTES = 64 * 576 * 2
 
 EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
@@ -32,7 +36,8 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_plan_get_info", "dsv4_compress_insert", "dsv4_cache_insert_rows",
             "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
             "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair", "dsv4_plan_set_indexer_format",
-            "dsv4_sparse_mla_prefill", "dsv4_dequant_gather", "dsv4_combine_topk_swa_indices"]
+            "dsv4_sparse_mla_prefill", "dsv4_dequant_gather", "dsv4_combine_topk_swa_indices",
+            "dsv4_plan_set_kv_layout", "dsv4_inv_rope_fp8_quant"]
 GATHER_COMP, GATHER_SWA = 0, 1
 
 
@@ -114,6 +119,12 @@ class CombineArgs(ctypes.Structure):
                 ("out_stride", ctypes.c_int), ("out_len_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
 
 
+class InvRopeQuantArgs(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int), ("n_heads", ctypes.c_int), ("o_dev", ctypes.c_void_p),
+                ("positions_dev", ctypes.c_void_p), ("cos_sin_dev", ctypes.c_void_p), ("max_pos", ctypes.c_int),
+                ("codes_dev", ctypes.c_void_p), ("scales_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -171,6 +182,10 @@ def lib():
     L.dsv4_dequant_gather.argtypes = [ctypes.POINTER(GatherArgs), vp]
     L.dsv4_combine_topk_swa_indices.restype = st
     L.dsv4_combine_topk_swa_indices.argtypes = [ctypes.POINTER(CombineArgs), vp]
+    L.dsv4_plan_set_kv_layout.restype = st
+    L.dsv4_plan_set_kv_layout.argtypes = [vp, ctypes.c_int]
+    L.dsv4_inv_rope_fp8_quant.restype = st
+    L.dsv4_inv_rope_fp8_quant.argtypes = [ctypes.POINTER(InvRopeQuantArgs), vp]
     _lib = L
     return L
 
@@ -257,7 +272,9 @@ class Plan:
     """One plan per layer type, reused by every layer of that type in a step."""
 
     def __init__(self, layer_type, n_heads, batch, topk, max_ctx, idx_heads=64, window=WINDOW,
-                 softmax_scale=HEAD_DIM ** -0.5, idx_format=IDX_FP8):
+                 softmax_scale=None, idx_format=IDX_FP8, kv_layout=KV_576):
+        if softmax_scale is None:
+            softmax_scale = (V4_HEAD_DIM if kv_layout == KV_V4 else HEAD_DIM) ** -0.5
         self.geom = Geom(int(n_heads), int(idx_heads), int(window), float(softmax_scale))
         h = ctypes.c_void_p()
         _check(lib().dsv4_plan_create(int(layer_type), ctypes.byref(self.geom), int(batch), int(topk),
@@ -268,6 +285,18 @@ class Plan:
         if idx_format != IDX_FP8:
             _check(lib().dsv4_plan_set_indexer_format(self.handle, int(idx_format)), "plan_set_indexer_format")
             self.idx_format = int(idx_format)
+        self.kv_layout = KV_576
+        if kv_layout != KV_576:
+            _check(lib().dsv4_plan_set_kv_layout(self.handle, int(kv_layout)), "plan_set_kv_layout")
+            self.kv_layout = int(kv_layout)
+
+    @property
+    def comp_page_bytes(self):
+        return V4_PAGE_BYTES if self.kv_layout == KV_V4 else MLA_PAGE_BYTES
+
+    @property
+    def swa_page_bytes(self):
+        return V4_PAGE_BYTES if self.kv_layout == KV_V4 else SWA_PAGE_BYTES
 
     @property
     def idx_page_bytes(self):
@@ -350,9 +379,9 @@ def indexer_topk(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx,
 def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspace, comp_cache=None,
                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None,
                       stream=None, row_seq=None):
-    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // SWA_PAGE_BYTES),
+    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // plan.swa_page_bytes),
                 _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
-                int(_nbytes(comp_cache) // MLA_PAGE_BYTES) if comp_cache is not None else 0,
+                int(_nbytes(comp_cache) // plan.comp_page_bytes) if comp_cache is not None else 0,
                 _ptr(comp_block_table),
                 int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
                 _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
@@ -379,9 +408,9 @@ def sparse_mla_prefill(plan, q, swa_cache, swa_block_table, ctx_len, row_seq, ou
                        comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None, stream=None):
     """dsv4_sparse_mla_prefill: one query row per prefill token (position
     ctx_len - 1), row_seq mapping each row to its block-table row."""
-    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // SWA_PAGE_BYTES),
+    a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // plan.swa_page_bytes),
                 _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
-                int(_nbytes(comp_cache) // MLA_PAGE_BYTES) if comp_cache is not None else 0,
+                int(_nbytes(comp_cache) // plan.comp_page_bytes) if comp_cache is not None else 0,
                 _ptr(comp_block_table),
                 int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
                 _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
@@ -407,3 +436,11 @@ def combine_topk_swa_indices(topk, topk_len, pos, row_seq, seq_len, gather_len, 
                     _ptr(gather_len), int(topk.shape[0]), int(seq_len.shape[0]), int(window), int(n_comp),
                     _ptr(out), int(out.shape[1]), _ptr(out_len), _ptr(status))
     _check(lib().dsv4_combine_topk_swa_indices(ctypes.byref(a), _stream(stream)), "combine_topk_swa_indices")
+
+
+def inv_rope_fp8_quant(o, positions, cos_sin, codes, scales, status=None, stream=None):
+    """dsv4_inv_rope_fp8_quant: o bf16 [T, H, 512] -> codes uint8 [T, H, 512]
+    (E4M3) and scales fp32 [T, H, 4], R(-position) applied to dims 448..511."""
+    a = InvRopeQuantArgs(int(o.shape[0]), int(o.shape[1]), _ptr(o), _ptr(positions), _ptr(cos_sin),
+                         int(cos_sin.shape[0]), _ptr(codes), _ptr(scales), _ptr(status))
+    _check(lib().dsv4_inv_rope_fp8_quant(ctypes.byref(a), _stream(stream)), "inv_rope_fp8_quant")

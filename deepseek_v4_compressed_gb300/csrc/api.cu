@@ -217,6 +217,14 @@ extern "C" dsv4_status dsv4_plan_set_indexer_format(dsv4_plan* plan, dsv4_idx_fo
     return DSV4_OK;
 }
 
+extern "C" dsv4_status dsv4_plan_set_kv_layout(dsv4_plan* plan, dsv4_kv_layout layout)
+{
+    if (plan == nullptr) return DSV4_ERR_INVALID;
+    if (layout != DSV4_KV_576 && layout != DSV4_KV_V4) return DSV4_ERR_INVALID;
+    plan->kv_v4 = layout == DSV4_KV_V4;
+    return DSV4_OK;
+}
+
 extern "C" void dsv4_plan_destroy(dsv4_plan* plan) { free(plan); }
 
 extern "C" size_t dsv4_plan_workspace_bytes(const dsv4_plan* plan) { return plan ? plan->ws_bytes : 0; }

@@ -7,7 +7,8 @@
 //
 // One CTA per token, d/2 threads, thread i owns channels 2i and 2i+1
 // (main cache d = 576: 288 threads = 9 warps, warp w < 8 owns nope block w of
-// 64 dims, warp 8 the rope dims; indexer d = 128: 64 threads).  The per-token
+// 64 dims, warp 8 the rope dims; V4-native main cache d = 512: 8 warps, warps
+// 0-6 the 448 nope dims, warp 7 the rope dims; indexer d = 128: 64 threads).  The per-token
 // state row is [kv block 0..coff-1 | score block 0..coff-1] in fp32; the
 // window of a boundary token is read from the per-sequence ring (and, in a
 // multi-token call, from this call's own inputs).  Work per entry is tiny and
@@ -59,12 +60,15 @@ __device__ __forceinline__ double block_sum_d(double v, double* red)
 
 // Quantise the normalised, rotated vector (this thread's channels c0, c0+1)
 // into a main-cache entry: E4M3 nope with one UE8M0 byte per 64 dims, bf16
-// rope.  Called by all 288 threads.
+// rope; with 448 nope dims the eighth scale byte is a zero pad.  Called by
+// all (NOPE + 64) / 2 threads.
+template <int NOPE>
 __device__ __forceinline__ void store_mla_entry(float z0, float z1, int c0, uint8_t* data_row,
                                                 uint8_t* scale_row)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < kNope / 64) {
+    if (NOPE < 512 && warp == NOPE / 64 && lane == 0) scale_row[7] = 0;
+    if (warp < NOPE / 64) {
         const float amax = warp_max(fmaxf(fabsf(z0), fabsf(z1)));
         const int e = ue8m0_exponent(amax);
         const float mult = exp2i(-e);
@@ -74,8 +78,18 @@ __device__ __forceinline__ void store_mla_entry(float z0, float z1, int c0, uint
     } else {
         const uint32_t pk = static_cast<uint32_t>(f32_to_bf16_bits(z0)) |
                             (static_cast<uint32_t>(f32_to_bf16_bits(z1)) << 16);
-        *reinterpret_cast<uint32_t*>(data_row + kNope + 2 * (c0 - kNope)) = pk;
+        *reinterpret_cast<uint32_t*>(data_row + NOPE + 2 * (c0 - NOPE)) = pk;
     }
+}
+
+constexpr int kV4Nope = DSV4_V4_NOPE_DIM;                 // 448
+constexpr int kV4Data = kV4Nope + 2 * kRope;              // 576 data bytes per V4 row
+
+// Model dimension of a cache kind's stream.
+template <int KIND>
+constexpr int kind_dim()
+{
+    return KIND == DSV4_CACHE_MLA ? kHead : (KIND == DSV4_CACHE_V4 ? DSV4_V4_HEAD_DIM : kIdx);
 }
 
 // Indexer entry: E4M3 of all 128 dims, one fp32 scale = amax / 448.
@@ -152,8 +166,10 @@ __device__ __forceinline__ uint8_t* entry_page(const CompressParams& P, int seq,
         flag(P.status, DSV4_DEV_BAD_PAGE);
         return nullptr;
     }
-    return P.cache + static_cast<long long>(pg) * (KIND == DSV4_CACHE_MLA ? kMlaPage
-                                                   : (KIND == DSV4_CACHE_IDX ? kIdxPage : kIdxFp4Page));
+    return P.cache + static_cast<long long>(pg) *
+                         (KIND == DSV4_CACHE_MLA ? kMlaPage
+                          : (KIND == DSV4_CACHE_V4 ? DSV4_V4_PAGE_BYTES
+                             : (KIND == DSV4_CACHE_IDX ? kIdxPage : kIdxFp4Page)));
 }
 
 // The state values (kv, score + ape) of one token for this thread's two
@@ -177,12 +193,13 @@ __device__ __forceinline__ void token_values(const CompressParams& P, int t, int
 template <int D, int RATIO, int KIND, bool FUSED>
 __device__ __forceinline__ void compress_token(const CompressParams& P, const int t)
 {
-    constexpr bool IDX = KIND != DSV4_CACHE_MLA;
+    constexpr bool IDX = KIND == DSV4_CACHE_IDX || KIND == DSV4_CACHE_IDX_FP4;
     constexpr int COFF = (RATIO == 4) ? 2 : 1;
     constexpr int W = COFF * RATIO;
     constexpr int ROW = 2 * COFF * D;
     constexpr int NT = D / 2;
-    constexpr int NOPE = IDX ? kIdx - kRope : kNope;
+    constexpr int NOPE = D - kRope;
+    static_assert(D == kind_dim<KIND>(), "stream dimension of the cache kind");
     __shared__ double red_d[NT / 32];
     __shared__ float red_f[2];
 
@@ -307,9 +324,12 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
         if (page == nullptr) return;   // uniform across the CTA
         store_idx_entry(z0, z1, c0, page + r * kIdx,
                         reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
+    } else if (KIND == DSV4_CACHE_V4) {
+        if (page == nullptr) return;
+        store_mla_entry<kV4Nope>(z0, z1, c0, page + r * kV4Data, page + kPage * kV4Data + r * 8);
     } else {
         if (page == nullptr) return;
-        store_mla_entry(z0, z1, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
+        store_mla_entry<kNope>(z0, z1, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
     }
 }
 
@@ -325,11 +345,12 @@ __global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
     compress_token<D, RATIO, KIND, FUSED>(P, blockIdx.x);
 }
 
-// The main (d = 576) and indexer (d = 128) streams of a layer in one launch,
-// one token per sequence: blocks [0, main tokens) take the main entries,
-// the rest the indexer entries with their first 64 threads.
-template <int RATIO, int IDX_KIND>
-__global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams Pm, CompressParams Pi)
+// The main (d = 576, or 512 for the V4 row) and indexer (d = 128) streams of
+// a layer in one launch, one token per sequence: blocks [0, main tokens) take
+// the main entries, the rest the indexer entries with their first 64 threads.
+template <int RATIO, int IDX_KIND, int MAIN_KIND>
+__global__ void __launch_bounds__(kind_dim<MAIN_KIND>() / 2) compress_pair_kernel(CompressParams Pm,
+                                                                                 CompressParams Pi)
 {
     // the indexer of this layer, launched next, starts by reading the
     // sequence's indexer block-table row (a caller input): warm it in L2
@@ -348,7 +369,7 @@ __global__ void __launch_bounds__(kHead / 2) compress_pair_kernel(CompressParams
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
-        compress_token<kHead, RATIO, DSV4_CACHE_MLA, true>(Pm, blockIdx.x);
+        compress_token<kind_dim<MAIN_KIND>(), RATIO, MAIN_KIND, true>(Pm, blockIdx.x);
     else if (threadIdx.x < kIdx / 2)
         compress_token<kIdx, 4, IDX_KIND, true>(Pi, blockIdx.x - Pm.num_tokens);
 }
@@ -397,8 +418,10 @@ __global__ void __launch_bounds__(D / 2) insert_rows_kernel(const float* rows, c
     else if (KIND == DSV4_CACHE_IDX)
         store_idx_entry(z.x, z.y, c0, page + r * kIdx,
                         reinterpret_cast<float*>(page + kPage * kIdx) + r, red_f);
+    else if (KIND == DSV4_CACHE_V4)
+        store_mla_entry<kV4Nope>(z.x, z.y, c0, page + r * kV4Data, page + kPage * kV4Data + r * 8);
     else
-        store_mla_entry(z.x, z.y, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
+        store_mla_entry<kNope>(z.x, z.y, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
 }
 
 template <int D, int RATIO, int KIND>
@@ -426,15 +449,17 @@ static dsv4_status compress_params(const dsv4_compress_args* a, CompressParams& 
     if (a == nullptr) return DSV4_ERR_INVALID;
     if (a->num_tokens < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
         return DSV4_ERR_INVALID;
-    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4)
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4 &&
+        a->kind != DSV4_CACHE_V4)
         return DSV4_ERR_INVALID;
+    const bool main_kind = a->kind == DSV4_CACHE_MLA || a->kind == DSV4_CACHE_V4;
     if (a->ratio != 4 && a->ratio != 128) return DSV4_ERR_UNSUPPORTED;
-    if (a->kind != DSV4_CACHE_MLA && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
+    if (!main_kind && a->ratio != 4) return DSV4_ERR_UNSUPPORTED;
     if (a->num_tokens > 0 &&
         (!a->kv_score_dev || !a->positions_dev || !a->seq_dev || !a->ape_dev || !a->rms_weight_dev ||
          !a->cos_sin_dev || !a->state_dev || !a->cache_dev || !a->block_table_dev))
         return DSV4_ERR_INVALID;
-    const int d = (a->kind == DSV4_CACHE_MLA) ? kHead : kIdx;
+    const int d = a->kind == DSV4_CACHE_MLA ? kHead : (a->kind == DSV4_CACHE_V4 ? DSV4_V4_HEAD_DIM : kIdx);
     const int coff = (a->ratio == 4) ? 2 : 1;
     if (a->num_tokens > 0 && (a->kv_score_stride < 2LL * coff * d || (a->kv_score_stride & 1)))
         return DSV4_ERR_SHAPE;
@@ -473,6 +498,9 @@ extern "C" dsv4_status dsv4_compress_insert(const dsv4_compress_args* a, dsv4_st
         e = launch_compress<kIdx, 4, DSV4_CACHE_IDX>(P, fused, st);
     else if (a->kind == DSV4_CACHE_IDX_FP4)
         e = launch_compress<kIdx, 4, DSV4_CACHE_IDX_FP4>(P, fused, st);
+    else if (a->kind == DSV4_CACHE_V4)
+        e = a->ratio == 4 ? launch_compress<DSV4_V4_HEAD_DIM, 4, DSV4_CACHE_V4>(P, fused, st)
+                          : launch_compress<DSV4_V4_HEAD_DIM, 128, DSV4_CACHE_V4>(P, fused, st);
     else if (a->ratio == 4)
         e = launch_compress<kHead, 4, DSV4_CACHE_MLA>(P, fused, st);
     else
@@ -488,7 +516,7 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     if (s != DSV4_OK) return s;
     s = compress_params(idx_args, Pi);
     if (s != DSV4_OK) return s;
-    if (main_args->kind != DSV4_CACHE_MLA ||
+    if ((main_args->kind != DSV4_CACHE_MLA && main_args->kind != DSV4_CACHE_V4) ||
         (idx_args->kind != DSV4_CACHE_IDX && idx_args->kind != DSV4_CACHE_IDX_FP4))
         return DSV4_ERR_INVALID;
     if (!main_args->one_token_per_seq || !idx_args->one_token_per_seq) return DSV4_ERR_INVALID;
@@ -498,7 +526,8 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     // previous kernel drains; they wait for it before reading anything
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n, 1, 1);
-    cfg.blockDim = dim3(kHead / 2, 1, 1);
+    const bool v4 = main_args->kind == DSV4_CACHE_V4;
+    cfg.blockDim = dim3((v4 ? DSV4_V4_HEAD_DIM : kHead) / 2, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -507,12 +536,23 @@ extern "C" dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool fp4 = idx_args->kind == DSV4_CACHE_IDX_FP4;
-    const cudaError_t e =
-        main_args->ratio == 4
-            ? (fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX_FP4>, Pm, Pi)
-                   : cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX>, Pm, Pi))
-            : (fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX_FP4>, Pm, Pi)
-                   : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX>, Pm, Pi));
+    const bool r4 = main_args->ratio == 4;
+    cudaError_t e;
+    if (v4) {
+        if (r4)
+            e = fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX_FP4, DSV4_CACHE_V4>, Pm, Pi)
+                    : cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX, DSV4_CACHE_V4>, Pm, Pi);
+        else
+            e = fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX_FP4, DSV4_CACHE_V4>, Pm, Pi)
+                    : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX, DSV4_CACHE_V4>, Pm, Pi);
+    } else {
+        if (r4)
+            e = fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX_FP4, DSV4_CACHE_MLA>, Pm, Pi)
+                    : cudaLaunchKernelEx(&cfg, compress_pair_kernel<4, DSV4_CACHE_IDX, DSV4_CACHE_MLA>, Pm, Pi);
+        else
+            e = fp4 ? cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX_FP4, DSV4_CACHE_MLA>, Pm, Pi)
+                    : cudaLaunchKernelEx(&cfg, compress_pair_kernel<128, DSV4_CACHE_IDX, DSV4_CACHE_MLA>, Pm, Pi);
+    }
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 
@@ -521,7 +561,8 @@ extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, ds
     if (a == nullptr) return DSV4_ERR_INVALID;
     if (a->num_rows < 0 || a->num_seqs < 0 || a->bt_stride < 0 || a->num_pages < 0)
         return DSV4_ERR_INVALID;
-    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4)
+    if (a->kind != DSV4_CACHE_MLA && a->kind != DSV4_CACHE_IDX && a->kind != DSV4_CACHE_IDX_FP4 &&
+        a->kind != DSV4_CACHE_V4)
         return DSV4_ERR_INVALID;
     if (a->num_rows == 0) return DSV4_OK;
     if (!a->rows_dev || !a->seq_dev || !a->slot_dev || !a->cache_dev || !a->block_table_dev)
@@ -542,6 +583,9 @@ extern "C" dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* a, ds
     else if (a->kind == DSV4_CACHE_IDX_FP4)
         insert_rows_kernel<kIdx, DSV4_CACHE_IDX_FP4><<<a->num_rows, kIdx / 2, 0, st>>>(a->rows_dev, a->seq_dev,
                                                                                      a->slot_dev, P);
+    else if (a->kind == DSV4_CACHE_V4)
+        insert_rows_kernel<DSV4_V4_HEAD_DIM, DSV4_CACHE_V4><<<a->num_rows, DSV4_V4_HEAD_DIM / 2, 0, st>>>(
+            a->rows_dev, a->seq_dev, a->slot_dev, P);
     else
         insert_rows_kernel<kHead, DSV4_CACHE_MLA><<<a->num_rows, kHead / 2, 0, st>>>(a->rows_dev, a->seq_dev,
                                                                                    a->slot_dev, P);

@@ -1,5 +1,7 @@
 // mla.cu -- sparse absorbed-MQA decode over (selected compressed slots) ||
-// (SWA window), one 576-dim latent KV head, value = the 512 latent dims.
+// (SWA window), one 576-dim latent KV head, value = the 512 latent dims; and
+// the V4-native variant: one 512-dim head (448 FP8 nope + 64 bf16 rope) that
+// is both key and value, with the SWA window in the same FP8 row format.
 //
 // _forward_decode of the "DeepseekV4Attention" class walkthrough
 // (flash_mla_with_kvcache over the SWA cache plus the compressed cache with
@@ -67,6 +69,12 @@ struct MlaParams {
 // 4-11: producers (window pages by TMA; compressed rows loaded into registers
 // one tile ahead and dequantised into the swizzled tile); warp 12: Q load and
 // QK issue; warp 13: PV issue (two issuers keep PV(t) off QK(t+1)'s path).
+//
+// V4-native rows ([MLA-to-CSA] 5.5: K = V, FP8 SWA at 584 bytes): Q and K
+// are 8 chunks of 64 dims (448 nope + 64 rope), the value is the whole key
+// tile, so P(t) gets a buffer of its own (double-buffered, reused once PV(t-2)
+// is complete); window tiles are FP8 rows too and go through the producers'
+// register gather like the compressed ones.
 // ---------------------------------------------------------------------------
 constexpr int kTcKeys = 64;
 constexpr int kTcStages = 2;
@@ -98,6 +106,26 @@ constexpr int kOffSend = 64 * kV * 2 + 8 * 512;
 constexpr int kOffWeights = 2 * kOffSend;
 static_assert(kOffWeights + 9 * 64 * 4 <= kOffMisc, "epilogue buffers fit in the Q / K space");
 static_assert(kTcSmem <= 232448, "shared memory budget");
+
+// Shared-memory plan and cache-row geometry of the two variants.
+template <bool V4>
+struct AttnGeom {
+    static constexpr int kChunks = V4 ? 8 : 9;                  // 64-dim chunks of Q and K
+    static constexpr int kQBytes = kChunks * kTcQChunk;
+    static constexpr int kKBytes = kChunks * kTcKChunk;         // per stage
+    static constexpr int kOffK = kQBytes;
+    static constexpr int kOffP = kOffK + kTcStages * kKBytes;   // V4: P(t) double buffer
+    static constexpr int kPBytes = V4 ? 2 * kTcKChunk : 0;
+    static constexpr int kOffMisc = kOffP + kPBytes;
+    static constexpr int kSmem = kOffMisc + kMiscBytes + 1024;
+    static constexpr int kRowBytes = V4 ? DSV4_V4_NOPE_DIM + 2 * kRope : kMlaData;   // data bytes of a row
+    static constexpr int kNopeBytes = V4 ? DSV4_V4_NOPE_DIM : kNope;
+    static constexpr int kPageBytes = V4 ? DSV4_V4_PAGE_BYTES : kMlaPage;
+    static constexpr int kNopeLanes = kNopeBytes / 16;          // lanes holding a 16-code unit of a row
+};
+static_assert(AttnGeom<false>::kOffMisc == kOffMisc && AttnGeom<false>::kSmem == kTcSmem, "576 plan");
+static_assert(AttnGeom<true>::kSmem <= 232448, "shared memory budget (V4)");
+static_assert(kOffWeights + 9 * 64 * 4 <= AttnGeom<true>::kOffMisc, "epilogue buffers fit (V4)");
 
 struct MlaTcParams {
     MlaParams base;
@@ -207,15 +235,18 @@ __device__ __forceinline__ int ldcg_s32_if(const int* p, bool pred, int dflt)
     return v;
 }
 
+template <bool V4>
 __global__ void __launch_bounds__(kTcThreads, 1)
 mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_swa, MlaTcParams T)
 {
+    using G = AttnGeom<V4>;
     const MlaParams& P = T.base;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = tc::align1024_shared(smem_raw);
     uint8_t* q_s = smem + kOffQ;
-    uint8_t* k_s = smem + kOffK;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffMisc);
+    uint8_t* k_s = smem + G::kOffK;
+    uint8_t* p_s = smem + G::kOffP;    // V4 only
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::kOffMisc);
     uint64_t* kv_full = bars;          // [2] producers (8 warps; window tiles: + TMA bytes) -> MMA
     uint64_t* kv_empty = bars + 2;     // [2] MMA -> producers (stage read by QK and PV)
     uint64_t* s_full = bars + 4;       // [2] MMA -> softmax
@@ -231,7 +262,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     int* sm_any = reinterpret_cast<int*>(sm_alpha + 128); // [2][4]
     volatile int* abort_flag = sm_any + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm_any + 9);
-    int* bt_s = reinterpret_cast<int*>(smem + kOffMisc + 2048);  // [kBtSmem] this sequence's block-table row
+    int* bt_s = reinterpret_cast<int*>(smem + G::kOffMisc + 2048);  // [kBtSmem] this sequence's block-table row
     uint64_t* bt_ready = bars + 12 + kTcMaxTiles;                 // producers: bt_s loaded
 
     const int rank = blockIdx.x;                          // the cluster spans gridDim.x
@@ -312,8 +343,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (lane == 0) {
                 tc::prefetch_tensormap(&tm_q);
                 tc::prefetch_tensormap(&tm_swa);
-                tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), kTcQBytes);
-                for (int c = 0; c < 9; ++c)
+                tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), G::kQBytes);
+                for (int c = 0; c < G::kChunks; ++c)
                     tc::tma_load_2d(tc::smem_u32(q_s + c * kTcQChunk), &tm_q, tc::smem_u32(q_full), c * 64,
                                     b * P.H + h0);
                 constexpr uint32_t id_qk = tc::idesc(64, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
@@ -328,9 +359,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!ok) break;
                     tc::tc_fence_after();
                     const uint32_t d = tmem + (t & 1) * kTcKeys;
-                    const uint64_t kd = tc::desc_kmajor_sw128(tc::smem_u32(k_s + (t & 1) * kTcKBytes));
+                    const uint64_t kd = tc::desc_kmajor_sw128(tc::smem_u32(k_s + (t & 1) * G::kKBytes));
 #pragma unroll
-                    for (int c = 0; c < 9; ++c)
+                    for (int c = 0; c < G::kChunks; ++c)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             tc::mma_f16(d, qd + (c * kTcQChunk >> 4) + 2 * k, kd + (c * kTcKChunk >> 4) + 2 * k,
@@ -340,7 +371,8 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
         } else if (warp == kTcPvWarp) {
             // ------------------------------------------------------- PV issue
-            // O^T += V^T P^T once P(u) is written (in the RoPE chunk of tile u).
+            // O^T += V^T P^T once P(u) is written (in the RoPE chunk of tile u;
+            // V4: in P buffer u % 2).
             if (lane == 0) {
                 constexpr uint32_t id_pv = tc::idesc(128, 64, tc::kFmtBF16, tc::kFmtBF16, true, false);
                 for (int u = 0;; ++u) {
@@ -348,8 +380,9 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (u >= n_tiles) break;
                     if (!tc::mbar_wait(tc::smem_u32(&p_full[u & 1]), (u >> 1) & 1, abort_flag, P.status)) break;
                     tc::tc_fence_after();
-                    const uint32_t kb = tc::smem_u32(k_s + (u & 1) * kTcKBytes);
-                    const uint64_t pd = tc::desc_kmajor_sw128(kb + 8 * kTcKChunk);
+                    const uint32_t kb = tc::smem_u32(k_s + (u & 1) * G::kKBytes);
+                    const uint64_t pd = tc::desc_kmajor_sw128(V4 ? tc::smem_u32(p_s + (u & 1) * kTcKChunk)
+                                                                 : kb + 8 * kTcKChunk);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -417,30 +450,37 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
             };
-            // raw data of one compressed tile, loaded one tile ahead of its use:
-            // nope unit `lane` (16 codes) of rows pw + 8k with its scale byte,
-            // rope unit lane % 8 of rows pw + 8 (lane / 8) and pw + 8 (lane / 8 + 4)
+            // raw data of one tile, loaded one tile ahead of its use: nope unit
+            // `lane` (16 codes; V4: lanes below 28) of rows pw + 8k with its
+            // scale byte, rope unit lane % 8 of rows pw + 8 (lane / 8) and
+            // pw + 8 (lane / 8 + 4).  ent_of(k): cache entry (page * 64 + row)
+            // of row pw + 8k, -1 for none (the row then reads as zeros).
             uint4 rn[8];
             uint32_t rs[8];
             uint4 rr[2];
+            auto fetch_rows = [&](const uint8_t* cache, auto&& ent_of) {
+                const bool nope_lane = lane < G::kNopeLanes;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int e = ent_of(k);
+                    const uint8_t* page = cache + static_cast<long long>(e >> 6) * G::kPageBytes;
+                    rn[k] = ldg_stream_v4_if(page + (e & 63) * G::kRowBytes + lane * 16, e >= 0 && nope_lane);
+                    rs[k] = ldg_stream_u8_if(page + kPage * G::kRowBytes + (e & 63) * 8 + (lane >> 2),
+                                             e >= 0 && nope_lane, 127);
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int e = ent_of((lane >> 3) + 4 * hh);
+                    rr[hh] = ldg_stream_v4_if(cache + static_cast<long long>(e >> 6) * G::kPageBytes +
+                                                  (e & 63) * G::kRowBytes + G::kNopeBytes + (lane & 7) * 16,
+                                              e >= 0);
+                }
+            };
             auto fetch = [&](int jc) {
                 const int q = jc >> 2;
                 const int e_src = q == 0 ? ent[0] : (q == 1 ? ent[1] : (q == 2 ? ent[2] : ent[3]));
                 const int base = (jc & 3) * 8;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int e = __shfl_sync(0xffffffffu, e_src, base + k);
-                    const uint8_t* page = P.comp + static_cast<long long>(e >> 6) * kMlaPage;
-                    rn[k] = ldg_stream_v4_if(page + (e & 63) * kMlaData + lane * 16, e >= 0);
-                    rs[k] = ldg_stream_u8_if(page + kPage * kMlaData + (e & 63) * 8 + (lane >> 2), e >= 0, 127);
-                }
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int e = __shfl_sync(0xffffffffu, e_src, base + (lane >> 3) + 4 * hh);
-                    rr[hh] = ldg_stream_v4_if(P.comp + static_cast<long long>(e >> 6) * kMlaPage + (e & 63) * kMlaData +
-                                                  kNope + (lane & 7) * 16,
-                                              e >= 0);
-                }
+                fetch_rows(P.comp, [&](int k) { return __shfl_sync(0xffffffffu, e_src, base + k); });
             };
             // dequantise into the 128-byte-swizzled tile (row r, 16-byte unit u
             // of 64-dim chunk c at c * kTcKChunk + r * 128 + ((u ^ (r & 7)) << 4);
@@ -449,29 +489,63 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             auto convert = [&](uint8_t* kp) {
                 const int w0 = 2 * (lane & 3);
                 const int flip = (lane >> 2) & 1;
+                if (lane < G::kNopeLanes) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int r = pw + 8 * k;
-                    uint4 lo, hi;
-                    dequant16(rn[k], rs[k], lo, hi);
-                    uint8_t* row = kp + (lane >> 2) * kTcKChunk + r * 128;
-                    const uint4 first = flip ? hi : lo;
-                    const uint4 second = flip ? lo : hi;
-                    *reinterpret_cast<uint4*>(row + (((w0 + flip) ^ pw) << 4)) = first;
-                    *reinterpret_cast<uint4*>(row + (((w0 + 1 - flip) ^ pw) << 4)) = second;
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = pw + 8 * k;
+                        uint4 lo, hi;
+                        dequant16(rn[k], rs[k], lo, hi);
+                        uint8_t* row = kp + (lane >> 2) * kTcKChunk + r * 128;
+                        const uint4 first = flip ? hi : lo;
+                        const uint4 second = flip ? lo : hi;
+                        *reinterpret_cast<uint4*>(row + (((w0 + flip) ^ pw) << 4)) = first;
+                        *reinterpret_cast<uint4*>(row + (((w0 + 1 - flip) ^ pw) << 4)) = second;
+                    }
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = pw + 8 * ((lane >> 3) + 4 * hh);
-                    *reinterpret_cast<uint4*>(kp + 8 * kTcKChunk + r * 128 + (((lane & 7) ^ pw) << 4)) = rr[hh];
+                    *reinterpret_cast<uint4*>(kp + (G::kChunks - 1) * kTcKChunk + r * 128 +
+                                              (((lane & 7) ^ pw) << 4)) = rr[hh];
                 }
             };
             // window pages first: they need nothing from the kernel before
             int i = 0;
             bool ok = true;
-            for (; i < n_swa_mine; ++i) {
+            if constexpr (V4) {
+                // FP8 window rows through the register gather, one tile ahead;
+                // rows outside [t0, p] read as zeros
+                auto fetch_win = [&](int wi) {
+                    const int lp = pg0 + rank + wi * C;
+                    int pg = lp < P.swa_bt_stride ? P.swa_bt[static_cast<long long>(seq) * P.swa_bt_stride + lp] : -1;
+                    if (pg < 0 || pg >= P.swa_pages) {
+                        if (lane == 0) flag(P.status, DSV4_DEV_BAD_PAGE);
+                        pg = -1;
+                    }
+                    fetch_rows(P.swa, [&](int k) {
+                        const int tok = lp * kPage + pw + 8 * k;
+                        return (pg >= 0 && tok >= t0 && tok <= p) ? pg * kPage + pw + 8 * k : -1;
+                    });
+                };
+                if (n_swa_mine > 0) fetch_win(0);
+                for (; i < n_swa_mine; ++i) {
+                    const int kst = i & 1;
+                    uint8_t* kp = k_s + kst * G::kKBytes;
+                    if (i >= kTcStages &&
+                        !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    convert(kp);
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
+                    if (i + 1 < n_swa_mine) fetch_win(i + 1);
+                }
+            }
+            for (; !V4 && i < n_swa_mine; ++i) {
                 const int kst = i & 1;
-                uint8_t* kp = k_s + kst * kTcKBytes;
+                uint8_t* kp = k_s + kst * G::kKBytes;
                 if (i >= kTcStages &&
                     !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status)) {
                     ok = false;
@@ -507,7 +581,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             for (; ok && i < n_tiles; ++i) {
                 const int kst = i & 1;
-                uint8_t* kp = k_s + kst * kTcKBytes;
+                uint8_t* kp = k_s + kst * G::kKBytes;
                 if (i >= kTcStages &&
                     !tc::mbar_wait(tc::smem_u32(&kv_empty[kst]), ((i >> 1) & 1) ^ 1, abort_flag, P.status))
                     break;
@@ -597,7 +671,12 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 l = l * alpha + rowsum;
                 m = m_use;
-                uint8_t* prow = k_s + sb * kTcKBytes + 8 * kTcKChunk + h * 128;
+                // V4: P buffer t % 2 was last read by PV(t - 2)
+                if (V4 && t >= 2) {
+                    if (!tc::mbar_wait(tc::smem_u32(&pv_done[t - 2]), 0, abort_flag, P.status)) break;
+                    tc::tc_fence_after();
+                }
+                uint8_t* prow = V4 ? p_s + sb * kTcKChunk + h * 128 : k_s + sb * G::kKBytes + 8 * kTcKChunk + h * 128;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     *reinterpret_cast<uint4*>(prow + (((4 * half + u) ^ (h & 7)) << 4)) =
@@ -1001,9 +1080,11 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     T.head_groups = plan->mla_head_groups;
     T.cluster = plan->mla_splits;
     T.topk = plan->topk;
+    const bool v4 = plan->kv_v4 != 0;
+    const int qdim = v4 ? DSV4_V4_HEAD_DIM : kHead;
     CUtensorMap tm_q;
-    const uint64_t qdims[2] = {static_cast<uint64_t>(kHead), static_cast<uint64_t>(plan->batch) * P.H};
-    const uint64_t qstr[1] = {static_cast<uint64_t>(kHead) * 2};
+    const uint64_t qdims[2] = {static_cast<uint64_t>(qdim), static_cast<uint64_t>(plan->batch) * P.H};
+    const uint64_t qstr[1] = {static_cast<uint64_t>(qdim) * 2};
     const uint32_t qbox[2] = {64, 64};
     if ((reinterpret_cast<uintptr_t>(a->q_dev) & 15) || (reinterpret_cast<uintptr_t>(a->swa_cache_dev) & 15) ||
         (reinterpret_cast<uintptr_t>(a->out_dev) & 15) ||
@@ -1012,24 +1093,33 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     if (!encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a->q_dev, qdims, qstr, qbox,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return DSV4_ERR_CUDA;
-    CUtensorMap tm_swa;
-    const uint64_t sdims[3] = {static_cast<uint64_t>(kHead), static_cast<uint64_t>(kPage),
-                               static_cast<uint64_t>(a->swa_num_pages > 0 ? a->swa_num_pages : 1)};
-    const uint64_t sstr[2] = {static_cast<uint64_t>(kHead) * 2, static_cast<uint64_t>(kSwaPage)};
-    const uint32_t sbox[3] = {64, static_cast<uint32_t>(kTcKeys), 1};
-    if (!encode_tmap(&tm_swa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->swa_cache_dev, sdims, sstr, sbox,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
-        return DSV4_ERR_CUDA;
-    static PerDeviceOnce attr_once;
-    if (!attr_once.run([] {
-            return cudaFuncSetAttribute(mla_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) ==
-                   cudaSuccess;
-        }))
-        return DSV4_ERR_CUDA;
+    // the bf16 SWA pages by TMA (the V4 window rows are FP8 and gathered by
+    // the producers: the Q map stands in for the unused parameter)
+    CUtensorMap tm_swa = tm_q;
+    if (!v4) {
+        const uint64_t sdims[3] = {static_cast<uint64_t>(kHead), static_cast<uint64_t>(kPage),
+                                   static_cast<uint64_t>(a->swa_num_pages > 0 ? a->swa_num_pages : 1)};
+        const uint64_t sstr[2] = {static_cast<uint64_t>(kHead) * 2, static_cast<uint64_t>(kSwaPage)};
+        const uint32_t sbox[3] = {64, static_cast<uint32_t>(kTcKeys), 1};
+        if (!encode_tmap(&tm_swa, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a->swa_cache_dev, sdims, sstr, sbox,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+            return DSV4_ERR_CUDA;
+    }
+    static PerDeviceOnce attr_once, attr_once_v4;
+    const bool attr_ok =
+        v4 ? attr_once_v4.run([] {
+                 return cudaFuncSetAttribute(mla_decode_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             AttnGeom<true>::kSmem) == cudaSuccess;
+             })
+           : attr_once.run([] {
+                 return cudaFuncSetAttribute(mla_decode_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             AttnGeom<false>::kSmem) == cudaSuccess;
+             });
+    if (!attr_ok) return DSV4_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T.cluster, plan->batch * T.head_groups, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
-    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.dynamicSmemBytes = v4 ? AttnGeom<true>::kSmem : AttnGeom<false>::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1043,7 +1133,8 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, mla_decode_tc, tm_q, tm_swa, T);
+    const cudaError_t e = v4 ? cudaLaunchKernelEx(&cfg, mla_decode_tc<true>, tm_q, tm_swa, T)
+                             : cudaLaunchKernelEx(&cfg, mla_decode_tc<false>, tm_q, tm_swa, T);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

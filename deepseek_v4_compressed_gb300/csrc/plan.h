@@ -17,6 +17,7 @@ struct dsv4_plan {
     int idx_tiles_per_cta;   // 128-slot tiles per indexer CTA
     int idx_fused_topk;      // the top-k runs inside the logits launch (one cluster per sequence)
     int idx_fp4;             // the indexer cache is MXFP4 (68-byte entries), not FP8 (132-byte)
+    int kv_v4;               // V4-native attention rows (512 dims, K = V, FP8 SWA)
     int mla_head_groups;     // ceil(n_heads / 64)
     int mla_splits;          // key splits per (sequence, head group)
     int mla_keys_per_split;

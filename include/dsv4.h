@@ -51,6 +51,18 @@
  *   SWA cache page, 64 * 1152 = 73728 bytes: [64 tokens x 576 bf16].
  *   Logical compressed slot j of a sequence lives in page bt[j / 64], row
  *   j % 64; SWA token t in page bt[t / 64], row t % 64.
+ *
+ * V4-native geometry (plans set to DSV4_KV_V4, cache kind DSV4_CACHE_V4;
+ * [MLA-to-CSA] 5.5 and 6.4, [V4-internals] section 6): head 512 = 448 nope
+ * + 64 rope dims, one vector serving as key and value (K = V, the value
+ * includes the rope dims), and both the compressed and the SWA cache in one
+ * FP8 row format of 584 bytes:
+ *   page, 64 * 584 = 37376 bytes:
+ *     [64 rows x 576 B: 448 FP8 E4M3 nope codes, 64 bf16 rope values]
+ *     [64 rows x 8 B: UE8M0 byte per 64 nope dims (7), one zero pad byte]
+ * The attention output then carries the keys' rotation on dims 448..511;
+ * dsv4_inv_rope_fp8_quant applies R(-position) and quantises it for the
+ * output projection.
  */
 #ifndef DSV4_H
 #define DSV4_H
@@ -78,6 +90,10 @@ extern "C" {
 #define DSV4_IDX_FP4_ENTRY_BYTES 68
 #define DSV4_IDX_FP4_PAGE_BYTES (64 * 68)
 #define DSV4_SWA_PAGE_BYTES (64 * 576 * 2)
+#define DSV4_V4_NOPE_DIM 448
+#define DSV4_V4_HEAD_DIM 512
+#define DSV4_V4_ENTRY_BYTES 584
+#define DSV4_V4_PAGE_BYTES (64 * 584)
 #define DSV4_MAX_HEADS 128
 #define DSV4_MAX_IDX_HEADS 64
 
@@ -109,11 +125,14 @@ typedef enum dsv4_layer_type {
 typedef enum dsv4_cache_kind {
     DSV4_CACHE_MLA = 0,     /* main compressed cache, d = 576, 648-byte entries */
     DSV4_CACHE_IDX = 1,     /* indexer cache, d = 128, 132-byte entries (FP8 + fp32 scale) */
-    DSV4_CACHE_IDX_FP4 = 2  /* indexer cache in MXFP4, d = 128, 68-byte entries: 64 bytes of
+    DSV4_CACHE_IDX_FP4 = 2, /* indexer cache in MXFP4, d = 128, 68-byte entries: 64 bytes of
                                E2M1 codes (two per byte, the low nibble the even dim) and one
                                UE8M0 exponent byte per 32 dims; page = 64 x 64 code bytes, then
                                64 x 4 exponent bytes.  [V4-attn] use_fp4_indexer_cache;
                                [V4-internals] section 4 (64 x 68 B); [MLA-to-CSA] 6.1 */
+    DSV4_CACHE_V4 = 3       /* V4-native row, d = 512 (448 nope + 64 rope), 584-byte entries
+                               (DSV4_V4_PAGE_BYTES pages): the main compressed cache of a
+                               DSV4_KV_V4 plan, and its FP8 SWA cache ([MLA-to-CSA] 5.5) */
 } dsv4_cache_kind;
 
 /* ---- host utilities ------------------------------------------------------ */
@@ -205,6 +224,22 @@ dsv4_status dsv4_plan_get_info(const dsv4_plan* plan, dsv4_plan_info* info);
 typedef enum dsv4_idx_format { DSV4_IDX_FP8 = 0, DSV4_IDX_FP4 = 1 } dsv4_idx_format;
 dsv4_status dsv4_plan_set_indexer_format(dsv4_plan* plan, dsv4_idx_format format);
 
+/* KV geometry of a plan's attention ([MLA-to-CSA] 5.5: the V4 layout with
+ * K = V sharing and the FP8 SWA cache; 6.4: the output keeps the keys'
+ * rotation until the inverse RoPE).
+ *   DSV4_KV_576 (the default): q 576 dims, value = the 512 latent dims,
+ *     compressed cache DSV4_CACHE_MLA, SWA cache bf16 [576].
+ *   DSV4_KV_V4: q_dev bf16 [batch][n_heads][512]; keys are 512-dim rows of
+ *     DSV4_CACHE_V4 pages in BOTH caches (compressed slots and SWA tokens,
+ *     swa_cache_dev / swa_num_pages then count DSV4_V4_PAGE_BYTES pages);
+ *     key = FP8 * 2^(scale byte - 127) on dims 0..447, bf16 on 448..511;
+ *     s = softmax_scale * q . key (512 dims), out[b][h] = sum P * key (all 512
+ *     dims, bf16).  Everything else as for DSV4_KV_576.
+ * Set it after dsv4_plan_create, before the plan's first call.  Errors:
+ * DSV4_ERR_INVALID (NULL plan or unknown layout). */
+typedef enum dsv4_kv_layout { DSV4_KV_576 = 0, DSV4_KV_V4 = 1 } dsv4_kv_layout;
+dsv4_status dsv4_plan_set_kv_layout(dsv4_plan* plan, dsv4_kv_layout layout);
+
 /* ---- (1) compressor insert ----------------------------------------------- */
 
 /* [vLLM-classes] DeepseekCompressor.forward, save_partial_states and "CSA
@@ -226,7 +261,9 @@ dsv4_status dsv4_plan_set_indexer_format(dsv4_plan* plan, dsv4_idx_format format
  *
  * kv_score_dev: bf16 [num_tokens][2*coff*d] (row stride kv_score_stride
  *   elements): [kv block 0 | kv block 1 | score block 0 | score block 1],
- *   coff = 2 for r = 4, 1 for r = 128; d = 576 (main) or 128 (indexer).
+ *   coff = 2 for r = 4, 1 for r = 128; d = 576 (main), 512 (DSV4_CACHE_V4:
+ *   RMSNorm over 512 dims, RoPE on 448..511, FP8 on 0..447 with 7 UE8M0
+ *   bytes and a zero pad byte) or 128 (indexer).
  * positions_dev, seq_dev: int32 [num_tokens].  The tokens of one sequence in
  *   one call are adjacent in the token array with contiguous increasing
  *   positions (checked: DSV4_DEV_BAD_POSITION).
@@ -268,8 +305,8 @@ typedef struct dsv4_compress_args {
 dsv4_status dsv4_compress_insert(const dsv4_compress_args* args, dsv4_stream_t stream);
 
 /* Both compressor streams of a layer in one launch, for decode steps:
- * main_args (DSV4_CACHE_MLA, ratio 4 or 128) and idx_args (DSV4_CACHE_IDX,
- * ratio 4), each with one_token_per_seq set.  Same effect, arguments and
+ * main_args (DSV4_CACHE_MLA or DSV4_CACHE_V4, ratio 4 or 128) and idx_args
+ * (DSV4_CACHE_IDX or DSV4_CACHE_IDX_FP4, ratio 4), each with one_token_per_seq set.  Same effect, arguments and
  * errors as the two dsv4_compress_insert calls (DSV4_ERR_INVALID also for a
  * wrong kind or a call without one_token_per_seq); the two streams touch
  * disjoint state and caches, so their entries are computed side by side. */
@@ -279,7 +316,9 @@ dsv4_status dsv4_compress_insert_pair(const dsv4_compress_args* main_args, const
 /* Quantise already-final rows into the cache format and insert them: the
  * quantise-and-insert tail of dsv4_compress_insert on its own (no pooling,
  * normalisation or rotation), for filling caches with given entries.
- * rows_dev: fp32 [num_rows][d] (d = 576 or 128 by kind); seq_dev, slot_dev:
+ * rows_dev: fp32 [num_rows][d] (d = 576, 128 or 512 by kind; DSV4_CACHE_V4
+ * rows also serve as the FP8 SWA tokens of a DSV4_KV_V4 plan, slot = token
+ * position); seq_dev, slot_dev:
  * int32 [num_rows] (sequence and logical slot of each row). */
 typedef struct dsv4_insert_rows_args {
     int kind;
@@ -417,6 +456,38 @@ typedef struct dsv4_mla_args {
 dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_mla_args* args,
                                    void* workspace_dev, size_t workspace_bytes,
                                    dsv4_stream_t stream);
+
+/* Inverse RoPE and FP8 quantisation of the attention output of a DSV4_KV_V4
+ * plan ([MLA-to-CSA] 6.4, fused_inv_rope_fp8_quant ahead of the FP8 output
+ * projection; [V4-internals] section 6, "Inverse RoPE + FP8 Quant" fused so
+ * the rotated output never reaches HBM).  For token t (position
+ * positions_dev[t]) and head h, with x = fp32 of o[t][h][0:512]:
+ *   dims 448..511, GPT-J pairs i: (x0, x1) -> (x0 c + x1 s, x1 c - x0 s),
+ *     c = cos_sin[pos][i], s = cos_sin[pos][32 + i] (the rotation R(-pos);
+ *     each product and the sum rounded to fp32), so that the value rotated
+ *     by R(j) at key position j carries R(j - pos);
+ *   then each 128-dim block k: scale = amax / 448 (fp32, 1 for an all-zero
+ *     block), codes = E4M3(x / scale) (round to nearest even, saturating).
+ * Reading: the pages name the operator and its inputs but not the scale
+ * grain; 128-dim blocks with fp32 scales (the indexer cache's rule) are used.
+ * o_dev: bf16 [num_tokens][n_heads][512]; positions_dev: int32 [num_tokens];
+ * cos_sin_dev: fp32 [max_pos][64]; codes_dev: E4M3 [num_tokens][n_heads][512];
+ * scales_dev: fp32 [num_tokens][n_heads][4].  A position outside
+ * [0, max_pos) sets DSV4_DEV_BAD_POSITION and leaves that token's rows
+ * unwritten.  Errors: DSV4_ERR_INVALID (NULL pointers, negative sizes),
+ * DSV4_ERR_SHAPE (o_dev or codes_dev not 16-byte aligned). */
+typedef struct dsv4_inv_rope_quant_args {
+    int num_tokens;
+    int n_heads;
+    const void* o_dev;
+    const int* positions_dev;
+    const float* cos_sin_dev;
+    int max_pos;
+    void* codes_dev;
+    float* scales_dev;
+    int* status_dev;
+} dsv4_inv_rope_quant_args;
+dsv4_status dsv4_inv_rope_fp8_quant(const dsv4_inv_rope_quant_args* args, dsv4_stream_t stream);
 
 /* ---- (4) sparse prefill -------------------------------------------------------- */
 

@@ -186,3 +186,79 @@ def check_attention(out_gpu, out_ref, what=""):
     assert err.mean() <= ATT_MEAN_ABS, "%s mean abs %g" % (what, err.mean())
     assert rel <= ATT_REL_L2, "%s rel L2 %g" % (what, rel)
     return float(err.max()), float(err.mean()), float(rel)
+
+
+SCALE_V4 = 1.0 / math.sqrt(512)
+V4_PAGE_BYTES = 64 * 584
+
+
+def make_v4_decode_inputs(layer_type, batch, ctx, n_heads, topk, seed, comp_pool=8192, peaky=False,
+                          device="cuda"):
+    """One layer's decode inputs in the V4-native geometry: compressed and SWA
+    caches both of 584-byte rows (oracle-quantised N(0,1)/sqrt(512) rows, nope
+    448), bf16 queries [batch][n_heads][512], and per sequence either random
+    top-k slots (c4a), sorted metadata slots (c128a) or none (swaonly)."""
+    g = synth.rng(seed)
+    ctx = np.broadcast_to(np.asarray(ctx, np.int64), (batch,)).astype(np.int32).copy()
+    ratio = {4: 4, 128: 128, 1: 0}[layer_type]
+    d = DecodeInputs()
+    d.layer_type, d.batch, d.ctx, d.n_heads, d.topk = layer_type, batch, ctx, n_heads, topk
+    d.n_c = ((ctx // ratio) if ratio else np.zeros(batch, np.int64)).astype(np.int32)
+    d.p = (ctx - 1).astype(np.int32)
+    # SWA: the window's pages only, each page filled with 64 quantised rows
+    swa_lp = int(ctx.max() + 63) // 64
+    d.swa_bt = np.full((batch, swa_lp), -1, np.int32)
+    n_pages = 0
+    for b in range(batch):
+        for lp in range(max(0, int(d.p[b]) - 127) // 64, int(d.p[b]) // 64 + 1):
+            d.swa_bt[b, lp] = n_pages
+            n_pages += 1
+    perm = g.permutation(n_pages).astype(np.int32)
+    d.swa_bt = np.where(d.swa_bt >= 0, perm[np.maximum(d.swa_bt, 0)], -1).astype(np.int32)
+    d.swa = np.zeros(n_pages * V4_PAGE_BYTES, np.uint8)
+    for pg in range(n_pages):
+        data, sc = oracle.quant_mla_rows(synth.normal(g, (64, 512), SCALE_V4), nope_dim=448)
+        oracle.page_write(oracle.MLA_KIND, d.swa, np.array([pg], np.int32), data, sc, nope_dim=448)
+    d.comp = None
+    if ratio:
+        cp = int(max(1, (d.n_c.max() + 63) // 64))
+        d.comp_bt = synth.page_tables(g, batch, cp, extra_pages=1)
+        pool_n = int(min(comp_pool, max(1, d.n_c.sum())))
+        pool_z = synth.normal(g, (pool_n, 512), SCALE_V4)
+        pool_data, pool_sc = oracle.quant_mla_rows(pool_z, nope_dim=448)
+        d.comp = np.zeros((batch * cp + 1) * V4_PAGE_BYTES, np.uint8)
+        picks = []
+        for b in range(batch):
+            pick = g.integers(0, pool_n, size=int(d.n_c[b]))
+            oracle.page_write(oracle.MLA_KIND, d.comp, d.comp_bt[b], pool_data[pick], pool_sc[pick], nope_dim=448)
+            picks.append(pick)
+        d.idx = np.full((batch, topk), -1, np.int32)
+        d.idx_len = np.zeros(batch, np.int32)
+        for b in range(batch):
+            s = synth.sorted_sample(g, int(d.n_c[b]), topk)
+            if layer_type == 4:
+                s = g.permutation(s)               # c4a: any order
+            d.idx[b, :len(s)] = s
+            d.idx_len[b] = len(s)
+    q = synth.normal(g, (batch, n_heads, 512), SCALE_V4)
+    if peaky and ratio:
+        for b in range(batch):
+            if d.n_c[b] == 0:
+                continue
+            for h in range(n_heads):
+                sel = d.idx[b, g.integers(0, max(1, int(d.idx_len[b])), size=4)]
+                q[b, h] = (150.0 * pool_z[picks[b][sel]].sum(axis=0)).astype(np.float32)
+    d.q = bf16_bits(q)
+    d.t = {"q": bits_tensor(d.q, device), "swa": dev(d.swa, device), "swa_bt": dev(d.swa_bt, device),
+           "ctx": dev(d.ctx, device)}
+    if ratio:
+        d.t.update(comp=dev(d.comp, device), comp_bt=dev(d.comp_bt, device), idx=dev(d.idx, device),
+                   idx_len=dev(d.idx_len, device))
+    return d
+
+
+def oracle_v4(d, b):
+    if d.comp is None:
+        return oracle.sparse_mla_v4(d.q[b], None, None, None, 0, d.swa, d.swa_bt[b], int(d.p[b]), SCALE_V4)
+    return oracle.sparse_mla_v4(d.q[b], d.comp, d.comp_bt[b], d.idx[b], int(d.idx_len[b]), d.swa, d.swa_bt[b],
+                                int(d.p[b]), SCALE_V4)

@@ -144,3 +144,38 @@ def test_fp4_format_and_prefill_entry_points_validate_on_the_host():
     assert lib.dsv4_combine_topk_swa_indices(ctypes.byref(c), None) == B.ERR_SHAPE
     c = B.CombineArgs(None, 0, None, None, None, None, None, 0, 1, 128, 0, None, 1, None, None)
     assert lib.dsv4_combine_topk_swa_indices(ctypes.byref(c), None) == B.OK
+
+
+def test_v4_layout_and_output_quant_validate_on_the_host():
+    lib = B.lib()
+    p = B.Plan(B.C4A, 8, 2, 32, 4096, idx_heads=8)
+    assert lib.dsv4_plan_set_kv_layout(None, B.KV_V4) == B.ERR_INVALID
+    assert lib.dsv4_plan_set_kv_layout(p.handle, 9) == B.ERR_INVALID
+    assert lib.dsv4_plan_set_kv_layout(p.handle, B.KV_V4) == B.OK
+    pv = B.Plan(B.SWAONLY, 8, 2, 0, 4096, kv_layout=B.KV_V4)
+    assert pv.swa_page_bytes == B.V4_PAGE_BYTES == 37376 and abs(pv.geom.softmax_scale - 512 ** -0.5) < 1e-9
+    # the V4 kind takes both ratios on the main stream; kind 4 does not exist
+    a = B.CompressArgs()
+    a.kind, a.ratio, a.num_tokens, a.num_seqs = B.CACHE_V4, 128, 0, 1
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.OK
+    a.ratio = 8
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_UNSUPPORTED
+    a.kind, a.ratio = 4, 4
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_INVALID
+    m = B.CompressArgs()
+    m.kind, m.ratio, m.num_tokens, m.num_seqs, m.one_token_per_seq = B.CACHE_V4, 4, 0, 1, 1
+    i = B.CompressArgs()
+    i.kind, i.ratio, i.num_tokens, i.num_seqs, i.one_token_per_seq = B.CACHE_IDX, 4, 0, 1, 1
+    assert lib.dsv4_compress_insert_pair(ctypes.byref(m), ctypes.byref(i), None) == B.OK
+    r = B.InsertRowsArgs(4, 1, None, None, None, None, 1, None, 1, 1, None)
+    assert lib.dsv4_cache_insert_rows(ctypes.byref(r), None) == B.ERR_INVALID
+    # output quant: NULL args, nothing to do, NULL buffers, misaligned codes
+    assert lib.dsv4_inv_rope_fp8_quant(None, None) == B.ERR_INVALID
+    q = B.InvRopeQuantArgs(0, 8, None, None, None, 16, None, None, None)
+    assert lib.dsv4_inv_rope_fp8_quant(ctypes.byref(q), None) == B.OK
+    q = B.InvRopeQuantArgs(2, 8, None, None, None, 16, None, None, None)
+    assert lib.dsv4_inv_rope_fp8_quant(ctypes.byref(q), None) == B.ERR_INVALID
+    q = B.InvRopeQuantArgs(2, 8, 4096, 4096, 4096, 16, 4100, 4096, None)
+    assert lib.dsv4_inv_rope_fp8_quant(ctypes.byref(q), None) == B.ERR_SHAPE
+    q = B.InvRopeQuantArgs(-1, 8, 4096, 4096, 4096, 16, 4096, 4096, None)
+    assert lib.dsv4_inv_rope_fp8_quant(ctypes.byref(q), None) == B.ERR_INVALID

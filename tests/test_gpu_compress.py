@@ -16,10 +16,16 @@ pytestmark = pytest.mark.gpu
 
 EPS = 1e-6
 
+# per cache kind: stream dimension, (data, scale) bytes of an entry, page bytes,
+# the oracle's kind and nope dims
+DIM = {B.CACHE_MLA: 576, B.CACHE_IDX: 128, B.CACHE_V4: 512}
+ENTRY = {B.CACHE_MLA: (640, 8), B.CACHE_IDX: (128, 4), B.CACHE_V4: (576, 8)}
+ORACLE = {B.CACHE_MLA: (oracle.MLA_KIND, 512), B.CACHE_IDX: (oracle.IDX_KIND, 64), B.CACHE_V4: (oracle.MLA_KIND, 448)}
+
 
 def make_stream(kind, ratio, n_tok, seed, w_ones=False):
     g = synth.rng(seed)
-    d = 576 if kind == B.CACHE_MLA else 128
+    d = DIM[kind]
     coff = 2 if ratio == 4 else 1
     ks = bf16_bits(synth.normal(g, (n_tok, 2 * coff * d)))
     ape = synth.normal(g, (ratio, coff * d), 0.1)
@@ -29,7 +35,7 @@ def make_stream(kind, ratio, n_tok, seed, w_ones=False):
 
 def entries_from_pages(kind, cache, bt_row, n):
     """Read entries 0..n-1 (slot order) back out of the paged bytes."""
-    data_b, sc_b = (640, 8) if kind == B.CACHE_MLA else (128, 4)
+    data_b, sc_b = ENTRY[kind]
     if n == 0:
         return np.zeros((0, data_b), np.uint8), np.zeros((0, sc_b), np.uint8)
     pages = cache.reshape(-1, 64 * (data_b + sc_b))
@@ -44,14 +50,14 @@ def run_gpu_streams(kind, ratio, streams, chunks, cos_sin):
     share ape / w (one layer).  chunks: per-step token counts per sequence (list of
     lists) or None for one token per step.  Returns per-sequence cache entries."""
     nseq = len(streams)
-    d = 576 if kind == B.CACHE_MLA else 128
+    d = DIM[kind]
     coff = 2 if ratio == 4 else 1
     ape, w = streams[0][1], streams[0][2]
     n_ent = [s[0].shape[0] // ratio for s in streams]
     pps = max(1, (max(n_ent) + 63) // 64)
     g = synth.rng(99)
     bt = synth.page_tables(g, nseq, pps, extra_pages=2)
-    page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
+    page_b = B.PAGE_BYTES[kind]
     cache = torch.zeros((nseq * pps + 2) * page_b, dtype=torch.uint8, device="cuda")
     state = torch.zeros((nseq, coff * ratio, 2 * coff * d), dtype=torch.float32, device="cuda")
     t_ape, t_w, t_cs, t_bt = dev(ape), dev(w), dev(cos_sin), dev(bt)
@@ -85,8 +91,8 @@ def run_gpu_streams(kind, ratio, streams, chunks, cos_sin):
 
 
 def oracle_entries(kind, ratio, ks, ape, w, cos_sin):
-    nope = 512 if kind == B.CACHE_MLA else 64
-    data, sc = oracle.compress_stream(kind, ratio, ks, ape, w, EPS, cos_sin, nope_dim=nope)
+    okind, nope = ORACLE[kind]
+    data, sc = oracle.compress_stream(okind, ratio, ks, ape, w, EPS, cos_sin, nope_dim=nope)
     if kind == B.CACHE_IDX:
         sc = sc.view(np.uint8).reshape(-1, 4)
     return data, sc
@@ -101,7 +107,8 @@ def assert_bytes_equal(got, want, what):
 
 
 @pytest.mark.parametrize("kind,ratio,n_tok", [(B.CACHE_MLA, 4, 512), (B.CACHE_IDX, 4, 512),
-                                              (B.CACHE_MLA, 128, 384)])
+                                              (B.CACHE_MLA, 128, 384), (B.CACHE_V4, 4, 512),
+                                              (B.CACHE_V4, 128, 384)])
 def test_decode_stream_bit_exact(kind, ratio, n_tok):
     ks, ape, w = make_stream(kind, ratio, n_tok, seed=kind * 10 + ratio, w_ones=(ratio == 4))
     cs = oracle.rope_table(n_tok, 64)
@@ -109,7 +116,8 @@ def test_decode_stream_bit_exact(kind, ratio, n_tok):
     assert_bytes_equal(got, oracle_entries(kind, ratio, ks, ape, w, cs), "decode stream")
 
 
-@pytest.mark.parametrize("kind,ratio", [(B.CACHE_MLA, 4), (B.CACHE_IDX, 4), (B.CACHE_MLA, 128)])
+@pytest.mark.parametrize("kind,ratio", [(B.CACHE_MLA, 4), (B.CACHE_IDX, 4), (B.CACHE_MLA, 128),
+                                        (B.CACHE_V4, 4), (B.CACHE_V4, 128)])
 def test_chunked_stream_bit_exact(kind, ratio):
     n_tok = 700 if ratio == 4 else 600
     ks, ape, w = make_stream(kind, ratio, n_tok, seed=77 + ratio)
@@ -136,10 +144,10 @@ def test_batched_sequences_bit_exact(ratio):
                                    "seq %d" % b)
 
 
-@pytest.mark.parametrize("kind", [B.CACHE_MLA, B.CACHE_IDX])
+@pytest.mark.parametrize("kind", [B.CACHE_MLA, B.CACHE_IDX, B.CACHE_V4])
 def test_insert_rows_bit_exact(kind):
     g = synth.rng(31 + kind)
-    d = 576 if kind == B.CACHE_MLA else 128
+    d = DIM[kind]
     n = 300
     rows = synth.normal(g, (n, d), 1.0)
     rows *= (10.0 ** g.uniform(-6, 3, size=(n, 1))).astype(np.float32)
@@ -151,12 +159,13 @@ def test_insert_rows_bit_exact(kind):
     bt = synth.page_tables(g, nseq, pps)
     seqs = np.array([i % nseq for i in range(n)], np.int32)
     slots = np.array([i // nseq for i in range(n)], np.int32)
-    page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
-    cache = torch.zeros(nseq * pps * page_b, dtype=torch.uint8, device="cuda")
+    page_b = B.PAGE_BYTES[kind]
+    # pre-filled with 0xff: every byte of an entry (the V4 pad byte too) is written
+    cache = torch.full((nseq * pps * page_b,), 255, dtype=torch.uint8, device="cuda")
     B.cache_insert_rows(kind, dev(rows), dev(seqs), dev(slots), cache, dev(bt))
     host = cache.cpu().numpy()
-    if kind == B.CACHE_MLA:
-        wd, ws = oracle.quant_mla_rows(rows)
+    if kind != B.CACHE_IDX:
+        wd, ws = oracle.quant_mla_rows(rows, nope_dim=ORACLE[kind][1])
     else:
         wd, wsf = oracle.quant_idx_rows(rows)
         ws = wsf.view(np.uint8).reshape(-1, 4)
@@ -166,15 +175,16 @@ def test_insert_rows_bit_exact(kind):
         assert_bytes_equal(got, (wd[sel], ws[sel]), "insert rows seq %d" % b)
 
 
-@pytest.mark.parametrize("ratio", [4, 128])
-def test_pair_launch_bit_exact(ratio):
+@pytest.mark.parametrize("ratio,main_kind", [(4, B.CACHE_MLA), (128, B.CACHE_MLA), (4, B.CACHE_V4),
+                                             (128, B.CACHE_V4)])
+def test_pair_launch_bit_exact(ratio, main_kind):
     """dsv4_compress_insert_pair (main + indexer streams in one launch, one token
     per sequence per step) writes the same bytes as the oracle for both caches."""
     lens = [300, 129, 517] if ratio == 4 else [300, 256, 384]
     nseq = len(lens)
     cs = oracle.rope_table(max(lens), 64)
     t_cs = dev(cs)
-    kinds = {"main": (B.CACHE_MLA, ratio, 576), "idx": (B.CACHE_IDX, 4, 128)}
+    kinds = {"main": (main_kind, ratio, DIM[main_kind]), "idx": (B.CACHE_IDX, 4, 128)}
     setup = {}
     for name, (kind, r, d) in kinds.items():
         coff = 2 if r == 4 else 1
@@ -183,7 +193,7 @@ def test_pair_launch_bit_exact(ratio):
         n_ent = max(L // r for L in lens)
         pps = max(1, (n_ent + 63) // 64)
         bt = synth.page_tables(synth.rng(40 + kind), nseq, pps, extra_pages=1)
-        page_b = B.MLA_PAGE_BYTES if kind == B.CACHE_MLA else B.IDX_PAGE_BYTES
+        page_b = B.PAGE_BYTES[kind]
         setup[name] = dict(kind=kind, ratio=r, ape=ape, w=w, streams=streams, bt=bt,
                            t_ks=[bits_tensor(s) for s in streams],
                            cache=torch.zeros((nseq * pps + 1) * page_b, dtype=torch.uint8, device="cuda"),
