@@ -50,6 +50,12 @@ WORKLOADS = {
                             window=128, ratio=4, idx_fp4=True),
     "c4a_1m_b4_fp4": dict(name="c4a_1m_b4_fp4", batch=4, context=1048576, n_heads=128, idx_heads=64, topk=2048,
                           window=128, ratio=4, idx_fp4=True),
+    # the V4-native geometry: 512-dim rows (448 FP8 nope + 64 bf16 rope) as key
+    # and value, FP8 SWA cache, inverse RoPE + FP8 output quant in the step
+    "c4a_32k_b32_v4": dict(name="c4a_32k_b32_v4", batch=32, context=32768, n_heads=64, idx_heads=64, topk=512,
+                           window=128, ratio=4, v4=True),
+    "c128a_128k_b64_v4": dict(name="c128a_128k_b64_v4", batch=64, context=131072, n_heads=64, idx_heads=0,
+                              topk=512, window=128, ratio=128, v4=True),
     # 60-layer stack (swaonly / c4a / c128a), IndexCache freq 2 against freq 1
     "mixed60_b16": dict(name="mixed60_b16", batch=16, context=65536, n_heads=64, idx_heads=64, topk=512,
                         window=128, ratio=0),
@@ -101,21 +107,27 @@ def job_value(world: int, batch: int, steps: int, ms_max: float) -> float:
 # ----------------------------------------------------------------------------
 def algorithmic_bytes(w, ctx):
     B, H, HI, k = w["batch"], w["n_heads"], w["idx_heads"], w["topk"]
-    mla = B * (k * 648 + 128 * 1152 + k * 4 + 4 + H * 576 * 2 + H * 512 * 2 + H * 4
-               + (k + 2) * 4)
+    v4 = bool(w.get("v4"))
+    d = 512 if v4 else 576                   # main stream dimension (= q dims)
+    entry = 584 if v4 else 648               # compressed entry bytes
+    swa_row = 584 if v4 else 1152            # SWA token bytes (FP8 row or bf16 [576])
+    mla = B * (k * entry + 128 * swa_row + k * 4 + 4 + H * d * 2 + H * 512 * 2 + H * 4 + (k + 2) * 4)
+    # V4: the output read back, codes + scales written, position and its cos/sin row
+    out_quant = B * (H * 512 * 2 + H * (512 + 16) + 4 + 256) if v4 else 0.0
     if w["ratio"] == 128:
         # main compressor only (ratio 128, no overlap): the token's kv/score row in,
         # its state row out; at a boundary (1 token in 128) the 128 ring rows and
         # the entry.  The indices are caller metadata, read by the attention.
-        comp_main = B * (1152 * 2 + 1152 * 4 + (128 * 1152 * 4 + 648) / 128)
-        return dict(compress=comp_main, indexer=0.0, mla=mla, total=comp_main + mla)
+        comp_main = B * (2 * d * 2 + 2 * d * 4 + (128 * 2 * d * 4 + entry) / 128)
+        return dict(compress=comp_main, indexer=0.0, mla=mla, out_quant=out_quant,
+                    total=comp_main + mla + out_quant)
     n_c = ctx // 4
     idx_entry = 68 if w.get("idx_fp4") else 132      # MXFP4 or FP8 indexer entries
-    comp_main = B * (2304 * 2 + 2304 * 4 + 0.25 * (7 * 1152 * 4 + 648))
+    comp_main = B * (4 * d * 2 + 4 * d * 4 + 0.25 * (7 * 2 * d * 4 + entry))
     comp_idx = B * (512 * 2 + 512 * 4 + 0.25 * (7 * 256 * 4 + idx_entry))
     indexer = B * (n_c * idx_entry + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
-    return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla,
-                total=comp_main + comp_idx + indexer + mla)
+    return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla, out_quant=out_quant,
+                total=comp_main + comp_idx + indexer + mla + out_quant)
 
 
 def src_digest(paths):
@@ -198,6 +210,7 @@ def build_layers(w, n_layers, n_pos, device, seed=1):
     n_c_max = ctx_max // 4
     comp_lp = (n_c_max + 63) // 64 + 1
     swa_lp = (ctx_max + 63) // 64 + 1
+    main_kind, d = main_geometry(w)
     layers = []
     seqs_all = torch.arange(Bsz, dtype=torch.int32, device=device)
     for li in range(n_layers):
@@ -206,7 +219,7 @@ def build_layers(w, n_layers, n_pos, device, seed=1):
         # the library's own quantise-and-insert kernel
         L.comp_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
         L.idx_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
-        L.comp = torch.zeros(Bsz * comp_lp * Bd.MLA_PAGE_BYTES, dtype=torch.uint8, device=device)
+        L.comp = torch.zeros(Bsz * comp_lp * Bd.PAGE_BYTES[main_kind], dtype=torch.uint8, device=device)
         idx_kind = Bd.CACHE_IDX_FP4 if w.get("idx_fp4") else Bd.CACHE_IDX
         L.idx = torch.zeros(Bsz * comp_lp * Bd.PAGE_BYTES[idx_kind], dtype=torch.uint8, device=device)
         chunk = 8192
@@ -215,35 +228,62 @@ def build_layers(w, n_layers, n_pos, device, seed=1):
                 n = min(chunk, n_c_max - s0)
                 seq = torch.full((n,), b, dtype=torch.int32, device=device)
                 slot = torch.arange(s0, s0 + n, dtype=torch.int32, device=device)
-                rows = torch.randn((n, 576), generator=g, device=device) / math.sqrt(576)
-                Bd.cache_insert_rows(Bd.CACHE_MLA, rows, seq, slot, L.comp, L.comp_bt)
+                rows = torch.randn((n, d), generator=g, device=device) / math.sqrt(d)
+                Bd.cache_insert_rows(main_kind, rows, seq, slot, L.comp, L.comp_bt)
                 rows = torch.randn((n, 128), generator=g, device=device) / math.sqrt(128)
                 Bd.cache_insert_rows(idx_kind, rows, seq, slot, L.idx, L.idx_bt)
-        # SWA cache: 4 physical pages per sequence used as a ring of logical pages
-        phys = torch.randperm(Bsz * 4, generator=g, device=device).to(torch.int32).view(Bsz, 4)
-        lp = torch.arange(swa_lp, device=device) % 4
-        L.swa_bt = phys[:, lp].contiguous()
-        L.swa = (torch.randn((Bsz * 4 * 64, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+        L.swa_bt, L.swa = build_swa(w, Bsz, swa_lp, g, device)
         # compressor states (rings) and parameters
-        L.state_main = torch.zeros((Bsz, 8, 4 * 576), dtype=torch.float32, device=device)
+        L.state_main = torch.zeros((Bsz, 8, 4 * d), dtype=torch.float32, device=device)
         L.state_idx = torch.zeros((Bsz, 8, 4 * 128), dtype=torch.float32, device=device)
-        L.ape_main = torch.randn((4, 2 * 576), generator=g, device=device) * 0.1
+        L.ape_main = torch.randn((4, 2 * d), generator=g, device=device) * 0.1
         L.ape_idx = torch.randn((4, 2 * 128), generator=g, device=device) * 0.1
-        L.rms_main = torch.ones(576, device=device)
+        L.rms_main = torch.ones(d, device=device)
         L.rms_idx = torch.ones(128, device=device)
         # per-position inputs (one decode token per sequence)
-        L.kv_main = [torch.randn((Bsz, 4 * 576), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
+        L.kv_main = [torch.randn((Bsz, 4 * d), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
         L.kv_idx = [torch.randn((Bsz, 4 * 128), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
-        L.q = [(torch.randn((Bsz, H, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+        L.q = [(torch.randn((Bsz, H, d), generator=g, device=device) / math.sqrt(d)).to(torch.bfloat16)
                for _ in range(n_pos)]
         L.qi = [torch.randn((Bsz, HI, 128), generator=g, device=device).to(torch.float8_e4m3fn).view(torch.uint8)
                 for _ in range(n_pos)]
         L.wts = [torch.rand((Bsz, HI), generator=g, device=device) for _ in range(n_pos)]
-        L.out = torch.empty((Bsz, H, 512), dtype=torch.bfloat16, device=device)
-        L.lse = torch.empty((Bsz, H), dtype=torch.float32, device=device)
+        add_outputs(L, w, device)
         L.seqs = seqs_all
         layers.append(L)
     return layers
+
+
+def main_geometry(w):
+    """(main cache kind, main stream dimension) of a workload."""
+    from deepseek_v4_compressed_gb300 import binding as Bd
+    return (Bd.CACHE_V4, 512) if w.get("v4") else (Bd.CACHE_MLA, 576)
+
+
+def build_swa(w, Bsz, swa_lp, g, device):
+    """SWA cache: 4 physical pages per sequence used as a ring of logical
+    pages; bf16 [576] rows, or (V4) FP8 584-byte rows written by the
+    library's row insert."""
+    from deepseek_v4_compressed_gb300 import binding as Bd
+    phys = torch.randperm(Bsz * 4, generator=g, device=device).to(torch.int32).view(Bsz, 4)
+    bt = phys[:, torch.arange(swa_lp, device=device) % 4].contiguous()
+    if not w.get("v4"):
+        return bt, (torch.randn((Bsz * 4 * 64, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+    swa = torch.zeros(Bsz * 4 * Bd.V4_PAGE_BYTES, dtype=torch.uint8, device=device)
+    seq = torch.arange(Bsz, dtype=torch.int32, device=device).repeat_interleave(256)
+    tok = torch.arange(256, dtype=torch.int32, device=device).repeat(Bsz)
+    rows = torch.randn((Bsz * 256, 512), generator=g, device=device) / math.sqrt(512)
+    Bd.cache_insert_rows(Bd.CACHE_V4, rows, seq, tok, swa, bt)
+    return bt, swa
+
+
+def add_outputs(L, w, device):
+    Bsz, H = w["batch"], w["n_heads"]
+    L.out = torch.empty((Bsz, H, 512), dtype=torch.bfloat16, device=device)
+    L.lse = torch.empty((Bsz, H), dtype=torch.float32, device=device)
+    if w.get("v4"):
+        L.codes = torch.empty((Bsz, H, 512), dtype=torch.uint8, device=device)
+        L.scales = torch.empty((Bsz, H, 4), dtype=torch.float32, device=device)
 
 
 def build_layers_c128a(w, n_layers, n_pos, device, seed=2):
@@ -258,28 +298,26 @@ def build_layers_c128a(w, n_layers, n_pos, device, seed=2):
     n_c_max = ctx_max // 128
     comp_lp = (n_c_max + 63) // 64 + 1
     swa_lp = (ctx_max + 63) // 64 + 1
+    main_kind, d = main_geometry(w)
     seqs_all = torch.arange(Bsz, dtype=torch.int32, device=device)
     layers = []
     for li in range(n_layers):
         L = LayerInstance()
         L.comp_bt = torch.randperm(Bsz * comp_lp, generator=g, device=device).to(torch.int32).view(Bsz, comp_lp)
-        L.comp = torch.zeros(Bsz * comp_lp * Bd.MLA_PAGE_BYTES, dtype=torch.uint8, device=device)
+        L.comp = torch.zeros(Bsz * comp_lp * Bd.PAGE_BYTES[main_kind], dtype=torch.uint8, device=device)
         for b in range(Bsz):
             seq = torch.full((n_c_max,), b, dtype=torch.int32, device=device)
             slot = torch.arange(n_c_max, dtype=torch.int32, device=device)
-            rows = torch.randn((n_c_max, 576), generator=g, device=device) / math.sqrt(576)
-            Bd.cache_insert_rows(Bd.CACHE_MLA, rows, seq, slot, L.comp, L.comp_bt)
-        phys = torch.randperm(Bsz * 4, generator=g, device=device).to(torch.int32).view(Bsz, 4)
-        L.swa_bt = phys[:, torch.arange(swa_lp, device=device) % 4].contiguous()
-        L.swa = (torch.randn((Bsz * 4 * 64, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
-        L.state_main = torch.zeros((Bsz, 128, 1152), dtype=torch.float32, device=device)
-        L.ape_main = torch.randn((128, 576), generator=g, device=device) * 0.1
-        L.rms_main = torch.ones(576, device=device)
-        L.kv_main = [torch.randn((Bsz, 1152), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
-        L.q = [(torch.randn((Bsz, H, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+            rows = torch.randn((n_c_max, d), generator=g, device=device) / math.sqrt(d)
+            Bd.cache_insert_rows(main_kind, rows, seq, slot, L.comp, L.comp_bt)
+        L.swa_bt, L.swa = build_swa(w, Bsz, swa_lp, g, device)
+        L.state_main = torch.zeros((Bsz, 128, 2 * d), dtype=torch.float32, device=device)
+        L.ape_main = torch.randn((128, d), generator=g, device=device) * 0.1
+        L.rms_main = torch.ones(d, device=device)
+        L.kv_main = [torch.randn((Bsz, 2 * d), generator=g, device=device).to(torch.bfloat16) for _ in range(n_pos)]
+        L.q = [(torch.randn((Bsz, H, d), generator=g, device=device) / math.sqrt(d)).to(torch.bfloat16)
                for _ in range(n_pos)]
-        L.out = torch.empty((Bsz, H, 512), dtype=torch.bfloat16, device=device)
-        L.lse = torch.empty((Bsz, H), dtype=torch.float32, device=device)
+        add_outputs(L, w, device)
         L.seqs = seqs_all
         layers.append(L)
     return layers
@@ -295,16 +333,22 @@ class GpuBench:
         self.P = n_pos
         Bsz = w["batch"]
         self.c128 = w["ratio"] == 128
+        self.v4 = bool(w.get("v4"))
+        self.main_kind, _ = main_geometry(w)
+        kv_layout = Bd.KV_V4 if self.v4 else Bd.KV_576
         if self.c128:
-            self.plan = Bd.Plan(Bd.C128A, w["n_heads"], Bsz, w["topk"], w["context"], window=w["window"])
+            self.plan = Bd.Plan(Bd.C128A, w["n_heads"], Bsz, w["topk"], w["context"], window=w["window"],
+                                kv_layout=kv_layout)
             self.layers = build_layers_c128a(w, n_layers, n_pos, device)
             self.stage_names = ["compress", "sparse_mla"]
         else:
             self.plan = Bd.Plan(Bd.C4A, w["n_heads"], Bsz, w["topk"], w["context"], idx_heads=w["idx_heads"],
                                 idx_format=Bd.IDX_FP4 if w.get("idx_fp4") else Bd.IDX_FP8,
-                                window=w["window"])
+                                window=w["window"], kv_layout=kv_layout)
             self.layers = build_layers(w, n_layers, n_pos, device)
             self.stage_names = ["compress", "indexer_topk", "sparse_mla"]
+        if self.v4:
+            self.stage_names.append("out_quant")
         self.idx_kind = Bd.CACHE_IDX_FP4 if w.get("idx_fp4") else Bd.CACHE_IDX
         self.ws = self.plan.workspace(device)
         self.cos_sin = Bd.rope_table(w["context"] + 1).to(device)
@@ -326,36 +370,55 @@ class GpuBench:
             self.topk_len.fill_(w["topk"])
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.info = self.plan.info()
-        self.launches_per_step = 1 + self.info["launches_indexer"] + self.info["launches_mla"]
+        self.launches_per_step = 1 + self.info["launches_indexer"] + self.info["launches_mla"] + int(self.v4)
 
-    # one layer-step: the three library calls (both compressor streams in one launch)
-    def stage_calls(self, r, j):
-        Bd, L = self.Bd, self.layers[r]
+    def step_inputs(self, r, j):
+        """The per-step inputs of layer instance r at graph position j."""
+        L = self.layers[r]
+        x = dict(kv_main=L.kv_main[j], q=L.q[j], pos=self.pos[j], ctx=self.ctx[j])
+        if not self.c128:
+            x.update(kv_idx=L.kv_idx[j], qi=L.qi[j], wts=L.wts[j])
+        return x
+
+    def result_tensors(self, L):
+        """What a step hands to the next stage of the model: the attention output
+        and its log-sum-exp, or (V4) the FP8 codes and scales of the inverse-rotated
+        output."""
+        return [L.codes, L.scales] if self.v4 else [L.out, L.lse]
+
+    # one layer-step: the library calls (both compressor streams in one launch)
+    def calls_for(self, L, x, j=0):
+        Bd = self.Bd
         Bsz = self.w["batch"]
+        quant = [lambda: Bd.inv_rope_fp8_quant(L.out, x["pos"], self.cos_sin, L.codes, L.scales,
+                                               status=self.status)] if self.v4 else []
         if self.c128:
             return [
-                lambda: Bd.compress_insert(Bd.CACHE_MLA, 128, L.kv_main[j], self.pos[j], L.seqs, L.ape_main,
+                lambda: Bd.compress_insert(self.main_kind, 128, x["kv_main"], x["pos"], L.seqs, L.ape_main,
                                            L.rms_main, 1e-6, self.cos_sin, L.state_main, L.comp, L.comp_bt, Bsz,
                                            status=self.status),
-                lambda: Bd.sparse_mla_decode(self.plan, L.q[j], L.swa, L.swa_bt, self.ctx[j], L.out, self.ws,
+                lambda: Bd.sparse_mla_decode(self.plan, x["q"], L.swa, L.swa_bt, x["ctx"], L.out, self.ws,
                                              comp_cache=L.comp, comp_block_table=L.comp_bt,
                                              topk_idx=self.c128_idx[j], topk_len=self.topk_len, lse=L.lse,
                                              status=self.status),
-            ]
+            ] + quant
         return [
             lambda: Bd.compress_insert_pair(
-                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=L.kv_main[j], positions=self.pos[j], seqs=L.seqs,
+                dict(kind=self.main_kind, ratio=4, kv_score=x["kv_main"], positions=x["pos"], seqs=L.seqs,
                      ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=self.cos_sin,
                      state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=self.status),
-                dict(kind=self.idx_kind, ratio=4, kv_score=L.kv_idx[j], positions=self.pos[j], seqs=L.seqs,
+                dict(kind=self.idx_kind, ratio=4, kv_score=x["kv_idx"], positions=x["pos"], seqs=L.seqs,
                      ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=self.cos_sin,
                      state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=self.status)),
-            lambda: Bd.indexer_topk(self.plan, L.qi[j], L.wts[j], L.idx, L.idx_bt, self.ctx[j], self.topk_idx,
+            lambda: Bd.indexer_topk(self.plan, x["qi"], x["wts"], L.idx, L.idx_bt, x["ctx"], self.topk_idx,
                                     self.topk_len, self.ws, self.status),
-            lambda: Bd.sparse_mla_decode(self.plan, L.q[j], L.swa, L.swa_bt, self.ctx[j], L.out, self.ws,
+            lambda: Bd.sparse_mla_decode(self.plan, x["q"], L.swa, L.swa_bt, x["ctx"], L.out, self.ws,
                                          comp_cache=L.comp, comp_block_table=L.comp_bt, topk_idx=self.topk_idx,
                                          topk_len=self.topk_len, lse=L.lse, status=self.status),
-        ]
+        ] + quant
+
+    def stage_calls(self, r, j):
+        return self.calls_for(self.layers[r], self.step_inputs(r, j), j)
 
     def step_order(self, n):
         """(layer, position) of steps 0..n-1: each position visits all R layers."""
@@ -386,11 +449,8 @@ class GpuBench:
 def make_pinned_inputs(bench):
     """Host (pinned) inputs of every (layer, position) step, each step's seven
     tensors packed in one block (one copy per step), with the byte offsets."""
-    names = ["kv_main", "kv_idx", "q", "qi", "wts", "pos", "ctx"]
-    def step_tensors(L, j):
-        return dict(kv_main=L.kv_main[j], kv_idx=L.kv_idx[j], q=L.q[j], qi=L.qi[j], wts=L.wts[j],
-                    pos=bench.pos[j], ctx=bench.ctx[j])
-    t0 = step_tensors(bench.layers[0], 0)
+    t0 = bench.step_inputs(0, 0)
+    names = list(t0)
     layout, off = {}, 0
     for n in names:
         nbytes = t0[n].numel() * t0[n].element_size()
@@ -402,16 +462,15 @@ def make_pinned_inputs(bench):
         per = []
         for j in range(bench.P):
             blk = torch.empty(total, dtype=torch.uint8).pin_memory()
-            for n, t in step_tensors(bench.layers[r], j).items():
+            for n, t in bench.step_inputs(r, j).items():
                 o, _, _ = layout[n]
                 raw = t.contiguous().view(torch.uint8).reshape(-1).cpu()
                 blk[o:o + raw.numel()].copy_(raw)
             per.append(blk)
         host.append(per)
     h2d = sum(t0[n].numel() * t0[n].element_size() for n in names)
-    out_host = torch.empty((bench.w["batch"], bench.w["n_heads"], 512), dtype=torch.bfloat16).pin_memory()
-    lse_host = torch.empty((bench.w["batch"], bench.w["n_heads"]), dtype=torch.float32).pin_memory()
-    return host, layout, total, h2d, out_host, lse_host
+    res_host = [torch.empty_like(t, device="cpu").pin_memory() for t in bench.result_tensors(bench.layers[0])]
+    return host, layout, total, h2d, res_host
 
 
 def run_e2e(bench, steps, warmup):
@@ -421,8 +480,7 @@ def run_e2e(bench, steps, warmup):
     previous step's kernels: a step's inputs go to one of two device blocks, its
     kernels wait for them, and its output is read back once its kernels end."""
     Bd = bench.Bd
-    host, layout, total, h2d, out_host, lse_host = make_pinned_inputs(bench)
-    Bsz = bench.w["batch"]
+    host, layout, total, h2d, res_host = make_pinned_inputs(bench)
     dblk = [torch.empty(total, dtype=torch.uint8, device=bench.device) for _ in range(2)]
 
     def views(blk):
@@ -432,7 +490,7 @@ def run_e2e(bench, steps, warmup):
             v[n] = blk[o:o + nbytes].view(dt).view(shp)
         return v
     dv = [views(b) for b in dblk]
-    d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in res_host)
     s_in = torch.cuda.Stream(bench.device)
     s_out = torch.cuda.Stream(bench.device)
 
@@ -453,26 +511,15 @@ def run_e2e(bench, steps, warmup):
             s_c.wait_event(ev_in)
             if r in out_read:
                 s_c.wait_event(out_read[r])
-            d = dv[b]
-            Bd.compress_insert_pair(
-                dict(kind=Bd.CACHE_MLA, ratio=4, kv_score=d["kv_main"], positions=d["pos"], seqs=L.seqs,
-                     ape=L.ape_main, rms_weight=L.rms_main, rms_eps=1e-6, cos_sin=bench.cos_sin,
-                     state=L.state_main, cache=L.comp, block_table=L.comp_bt, num_seqs=Bsz, status=bench.status),
-                dict(kind=bench.idx_kind, ratio=4, kv_score=d["kv_idx"], positions=d["pos"], seqs=L.seqs,
-                     ape=L.ape_idx, rms_weight=L.rms_idx, rms_eps=1e-6, cos_sin=bench.cos_sin,
-                     state=L.state_idx, cache=L.idx, block_table=L.idx_bt, num_seqs=Bsz, status=bench.status))
-            Bd.indexer_topk(bench.plan, d["qi"], d["wts"], L.idx, L.idx_bt, d["ctx"], bench.topk_idx,
-                            bench.topk_len, bench.ws, bench.status)
-            Bd.sparse_mla_decode(bench.plan, d["q"], L.swa, L.swa_bt, d["ctx"], L.out, bench.ws, comp_cache=L.comp,
-                                 comp_block_table=L.comp_bt, topk_idx=bench.topk_idx, topk_len=bench.topk_len,
-                                 lse=L.lse, status=bench.status)
+            for c in bench.calls_for(L, dv[b], j):
+                c()
             ev_c = torch.cuda.Event()
             ev_c.record(s_c)
             read_done[b] = ev_c
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_c)
-                out_host.copy_(L.out, non_blocking=True)
-                lse_host.copy_(L.lse, non_blocking=True)
+                for hst, t in zip(res_host, bench.result_tensors(L)):
+                    hst.copy_(t, non_blocking=True)
                 ev_o = torch.cuda.Event()
                 ev_o.record(s_out)
             out_read[r] = ev_o
@@ -962,11 +1009,13 @@ def main():
     # roofline of the dominant kernel: the stage with the largest time (each
     # stage is one kernel at the c4a workloads, where the top-k runs inside the
     # logits launch when a sequence's CTAs fit one cluster)
-    stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
+    stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"],
+                   "out_quant": ab["out_quant"]}
     kernels = {"compress": ("compress_pair_kernel / compress_kernel (dsv4_compress_insert)", "compress.cu"),
                "indexer_topk": ("indexer_logits_tc (dsv4_indexer_topk)" if bench.info["launches_indexer"] == 1 else
                                 "indexer_logits_tc + top-k kernel (dsv4_indexer_topk, 2 launches)", "indexer.cu"),
-               "sparse_mla": ("mla_decode_tc (dsv4_sparse_mla_decode)", "mla.cu")}
+               "sparse_mla": ("mla_decode_tc%s (dsv4_sparse_mla_decode)" % ("<V4>" if bench.v4 else ""), "mla.cu"),
+               "out_quant": ("inv_rope_fp8_quant_kernel (dsv4_inv_rope_fp8_quant)", "out_quant.cu")}
     dom = max(bench.stage_names, key=lambda nm: stages[nm])
     achieved = stage_bytes[dom] / (stages[dom] / 1e3) / 1e9
     srcs = ["deepseek_v4_compressed_gb300/csrc/" + kernels[dom][1]]

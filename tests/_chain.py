@@ -5,8 +5,12 @@ dsv4_indexer_topk and dsv4_sparse_mla_decode, back to back on one stream
 replayed.  Steps include ratio-4 boundaries: the slot emitted by the
 compressor in a step must be visible to that step's indexer and attention.
 
+With v4=True the layer is in the V4-native geometry: 512-dim main stream
+(448 FP8 nope + 64 bf16 rope, 584-byte rows), FP8 SWA rows, K = V attention,
+and each step ends with dsv4_inv_rope_fp8_quant of the attention output.
+
 Expected values come from the oracle: cache entries (pool -> RMSNorm -> RoPE
--> quantise), indexer logits, top-k and attention.  Inputs come from the
+-> quantise), indexer logits, top-k, attention and the output quantisation.  Inputs come from the
 seeded generators; at boundary steps the queries are built from the oracle's
 entry for the new slot so that the indexer must select it and the attention
 must be dominated by it.
@@ -22,40 +26,53 @@ import oracle
 from deepseek_v4_compressed_gb300 import binding as B
 from deepseek_v4_compressed_gb300 import synth
 
-from _util import SCALE, bf16_bits, bits_tensor, check_attention, check_topk, dev
+from _util import SCALE, SCALE_V4, bf16_bits, bits_tensor, check_attention, check_topk, dev
 
 EPS = 1e-6
-D_MAIN, D_IDX = 576, 128
+D_IDX = 128
 
 
 def _pool():
     return concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4))
 
 
+NOPE = {B.CACHE_MLA: 512, B.CACHE_V4: 448, B.CACHE_IDX: 64}
+
+
 def oracle_entry(kind, ks, ape, w, cs, p):
     """The compressed entry emitted at boundary p (oracle steps, one entry)."""
-    nope = 512 if kind == B.CACHE_MLA else 64
+    nope = NOPE[kind]
     y = oracle.compress_pool(4, ks, ape, p)
     z = oracle.rmsnorm(y, w, EPS)
     z[nope:] = oracle.rope_gptj(z[nope:], cs[(p // 4) * 4])
-    if kind == B.CACHE_MLA:
-        d, s = oracle.quant_mla_rows(z[None])
+    if kind != B.CACHE_IDX:
+        d, s = oracle.quant_mla_rows(z[None], nope_dim=nope)
     else:
         d, s = oracle.quant_idx_rows(z[None])
     return d[0], s[0]
 
 
-def dequant_nope(data, sc):
-    return oracle.e4m3_to_f64(data[:512]) * np.repeat(2.0 ** (sc[:8].astype(np.int64) - 127), 64)
+def dequant_nope(data, sc, nope=512):
+    return oracle.e4m3_to_f64(data[:nope]) * np.repeat(2.0 ** (sc[:nope // 64].astype(np.int64) - 127), 64)
 
 
-def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
+def dequant_row(data, sc, nope):
+    """The whole dequantised key (nope dims, then the bf16 rope dims)."""
+    rope = oracle.bf16_to_f32(np.ascontiguousarray(data[nope:]).view(np.uint16)).astype(np.float64)
+    return np.concatenate([dequant_nope(data, sc, nope), rope])
+
+
+def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False):
     """prefill: 'stream' runs tokens 0..L0-1 through the library's multi-token
     compressor (caches and ring built by the library, checked against the
     oracle's whole-stream entries); 'direct' writes oracle-quantised random
     rows into the slots below L0 // 4 and the ring rows of tokens L0-8..L0-1
     (the compressor state layout of dsv4.h) so that long contexts stay cheap."""
     g = synth.rng(seed)
+    kind_m = B.CACHE_V4 if v4 else B.CACHE_MLA
+    D_MAIN = 512 if v4 else 576
+    nope_m = NOPE[kind_m]
+    scale = SCALE_V4 if v4 else SCALE
     L0 = np.broadcast_to(np.asarray(L0, np.int64), (batch,)).astype(np.int64).copy()
     T = L0 + n_steps
     Tmax = int(T.max())
@@ -83,7 +100,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
 
     def entries(b):
         if prefill == "stream":
-            dm, sm = oracle.compress_stream(0, 4, ks_m[b], ape_m, w_m, EPS, cs, nope_dim=512)
+            dm, sm = oracle.compress_stream(0, 4, ks_m[b], ape_m, w_m, EPS, cs, nope_dim=nope_m)
             di, si = oracle.compress_stream(1, 4, ks_i[b], ape_i, w_i, EPS, cs, nope_dim=64)
             return (dm, sm), (di, si)
         return None
@@ -95,7 +112,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
         ent_i = [r[1] for r in res]
     else:
         pool_n = 4096
-        pm, psm = oracle.quant_mla_rows(synth.normal(g, (pool_n, D_MAIN), 1.0))
+        pm, psm = oracle.quant_mla_rows(synth.normal(g, (pool_n, D_MAIN), 1.0), nope_dim=nope_m)
         for b in range(batch):
             n0 = int(L0[b] // 4)
             pick = g.integers(0, pool_n, size=int(n_ent[b]))
@@ -104,15 +121,15 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
             for p in range(int(L0[b]), int(T[b])):
                 if (p + 1) % 4 == 0:
                     j = p // 4
-                    dm[j], sm[j] = oracle_entry(B.CACHE_MLA, ks_m[b], ape_m, w_m, cs, p)
+                    dm[j], sm[j] = oracle_entry(kind_m, ks_m[b], ape_m, w_m, cs, p)
                     di[j], si[j] = oracle_entry(B.CACHE_IDX, ks_i[b], ape_i, w_i, cs, p)
             assert n0 <= n_ent[b]
             ent_m.append((dm, sm))
             ent_i.append((di, si))
-    comp_o = np.zeros((batch * pps + 1) * oracle.page_bytes(0), np.uint8)
+    comp_o = np.zeros((batch * pps + 1) * oracle.page_bytes(0, nope_dim=nope_m), np.uint8)
     idx_o = np.zeros((batch * pps + 1) * oracle.page_bytes(1), np.uint8)
     for b in range(batch):
-        oracle.page_write(0, comp_o, comp_bt[b], *ent_m[b])
+        oracle.page_write(0, comp_o, comp_bt[b], *ent_m[b], nope_dim=nope_m)
         oracle.page_write(1, idx_o, idx_bt[b], *ent_i[b], nope_dim=64)
 
     # SWA cache: rows of tokens max(0, L0 - 128) .. T - 1 (the windows of every step)
@@ -123,7 +140,13 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
         for lp in range(max(0, int(L0[b]) - 128) // 64, (int(T[b]) - 1) // 64 + 1):
             swa_bt[b, lp] = npg
             npg += 1
-    swa = bf16_bits(synth.normal(g, (npg * 64, 576), SCALE))
+    if v4:
+        swa = np.zeros(npg * oracle.page_bytes(0, nope_dim=448), np.uint8)
+        for pg in range(npg):
+            data, sc = oracle.quant_mla_rows(synth.normal(g, (64, 512), SCALE_V4), nope_dim=448)
+            oracle.page_write(0, swa, np.array([pg], np.int32), data, sc, nope_dim=448)
+    else:
+        swa = bf16_bits(synth.normal(g, (npg * 64, 576), SCALE))
 
     # per-step queries; at a boundary step the new slot's own codes / latent
     steps = []
@@ -131,18 +154,18 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
         st = dict(p=(L0 + s).astype(np.int32))
         qi = oracle.f32_to_e4m3(synth.normal(g, (batch, HI, 128)))
         wq = synth.uniform(g, (batch, HI))
-        q = synth.normal(g, (batch, H, 576), SCALE)
+        q = synth.normal(g, (batch, H, D_MAIN), scale)
         st["boundary"] = [(int(st["p"][b]) + 1) % 4 == 0 for b in range(batch)]
         for b in range(batch):
             if st["boundary"][b]:
                 j = int(st["p"][b]) // 4
                 qi[b, :, :] = ent_i[b][0][j]
-                q[b, :, :512] = dequant_nope(ent_m[b][0][j], ent_m[b][1][j]).astype(np.float32)
+                q[b, :, :nope_m] = dequant_nope(ent_m[b][0][j], ent_m[b][1][j], nope_m).astype(np.float32)
         st["qi"], st["w"], st["q"] = qi, wq, bf16_bits(q)
         steps.append(st)
 
     # ---- GPU
-    plan = B.Plan(B.C4A, H, batch, k, Tmax, idx_heads=HI)
+    plan = B.Plan(B.C4A, H, batch, k, Tmax, idx_heads=HI, kv_layout=B.KV_V4 if v4 else B.KV_576)
     ws = plan.workspace()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     comp = torch.zeros(comp_o.size, dtype=torch.uint8, device="cuda")
@@ -153,7 +176,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
     t_ape_m, t_ape_i, t_w_m, t_w_i, t_cs = dev(ape_m), dev(ape_i), dev(w_m), dev(w_i), dev(cs)
     seqs = dev(np.arange(batch, dtype=np.int32))
     if prefill == "stream":
-        for kind, ks, ape, w, st, cache, bt in ((B.CACHE_MLA, ks_m, t_ape_m, t_w_m, st_m, comp, t_comp_bt),
+        for kind, ks, ape, w, st, cache, bt in ((kind_m, ks_m, t_ape_m, t_w_m, st_m, comp, t_comp_bt),
                                                 (B.CACHE_IDX, ks_i, t_ape_i, t_w_i, st_i, idxc, t_idx_bt)):
             rows, ps, sq = [], [], []
             for b in range(batch):
@@ -169,7 +192,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
         part_c = np.zeros_like(comp_o)
         part_i = np.zeros_like(idx_o)
         for b in range(batch):
-            oracle.page_write(0, part_c, comp_bt[b], ent_m[b][0][:n0[b]], ent_m[b][1][:n0[b]])
+            oracle.page_write(0, part_c, comp_bt[b], ent_m[b][0][:n0[b]], ent_m[b][1][:n0[b]], nope_dim=nope_m)
             oracle.page_write(1, part_i, idx_bt[b], ent_i[b][0][:n0[b]], ent_i[b][1][:n0[b]], nope_dim=64)
         comp.copy_(dev(part_c))
         idxc.copy_(dev(part_i))
@@ -183,7 +206,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
                     ring[b, t % 8, 2 * d:] = (row[2 * d:] + ape[t % 4]).astype(np.float32)
         st_m.copy_(dev(ring_m))
         st_i.copy_(dev(ring_i))
-    t_swa, t_swa_bt = bits_tensor(swa), dev(swa_bt)
+    t_swa, t_swa_bt = (dev(swa) if v4 else bits_tensor(swa)), dev(swa_bt)
     gin = []
     for s, st in enumerate(steps):
         kvm = bits_tensor(np.stack([ks_m[b][st["p"][b]] for b in range(batch)]))
@@ -193,13 +216,15 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
                         idx=torch.full((batch, k), -9, dtype=torch.int32, device="cuda"),
                         len=torch.full((batch,), -9, dtype=torch.int32, device="cuda"),
                         out=torch.zeros((batch, H, 512), dtype=torch.bfloat16, device="cuda"),
-                        lse=torch.zeros((batch, H), dtype=torch.float32, device="cuda")))
+                        lse=torch.zeros((batch, H), dtype=torch.float32, device="cuda"),
+                        codes=torch.zeros((batch, H, 512), dtype=torch.uint8, device="cuda"),
+                        scales=torch.zeros((batch, H, 4), dtype=torch.float32, device="cuda")))
     torch.cuda.synchronize()
 
     def decode_steps():
         for x in gin:
             B.compress_insert_pair(
-                dict(kind=B.CACHE_MLA, ratio=4, kv_score=x["kvm"], positions=x["pos"], seqs=seqs, ape=t_ape_m,
+                dict(kind=kind_m, ratio=4, kv_score=x["kvm"], positions=x["pos"], seqs=seqs, ape=t_ape_m,
                      rms_weight=t_w_m, rms_eps=EPS, cos_sin=t_cs, state=st_m, cache=comp, block_table=t_comp_bt,
                      num_seqs=batch, status=status),
                 dict(kind=B.CACHE_IDX, ratio=4, kv_score=x["kvi"], positions=x["pos"], seqs=seqs, ape=t_ape_i,
@@ -209,6 +234,8 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
             B.sparse_mla_decode(plan, x["q"], t_swa, t_swa_bt, x["ctx"], x["out"], ws, comp_cache=comp,
                                 comp_block_table=t_comp_bt, topk_idx=x["idx"], topk_len=x["len"], lse=x["lse"],
                                 status=status)
+            if v4:
+                B.inv_rope_fp8_quant(x["out"], x["pos"], t_cs, x["codes"], x["scales"], status=status)
 
     if graph:
         gr = torch.cuda.CUDAGraph()
@@ -229,6 +256,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
     for s, (st, x) in enumerate(zip(steps, gin)):
         gidx, glen = x["idx"].cpu().numpy(), x["len"].cpu().numpy()
         gout, glse = x["out"].float().cpu().numpy(), x["lse"].cpu().numpy()
+        gcodes, gscales = x["codes"].cpu().numpy(), x["scales"].cpu().numpy()
 
         def check(b):
             p = int(st["p"][b])
@@ -238,13 +266,23 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True):
             if st["boundary"][b]:
                 assert p // 4 in set(gidx[b][:glen[b]].tolist()), "step %d seq %d: new slot not selected" % (s, b)
             sel = gidx[b][:glen[b]].copy()
-            ref, ref_lse, _ = oracle.sparse_mla(st["q"][b], comp_o, comp_bt[b], sel, int(glen[b]), swa, swa_bt[b],
-                                                p, SCALE)
+            if v4:
+                ref, ref_lse = oracle.sparse_mla_v4(st["q"][b], comp_o, comp_bt[b], sel, int(glen[b]), swa,
+                                                    swa_bt[b], p, SCALE_V4)
+                # the step's output quantisation, bit for bit on the kernel's own bf16 output
+                o_bits = oracle.f32_to_bf16(gout[b].astype(np.float32))
+                wc, wsc = oracle.inv_rope_fp8_quant(o_bits, p, cs)
+                assert np.array_equal(gcodes[b], wc) and np.array_equal(gscales[b], wsc), \
+                    "step %d seq %d: output quant differs" % (s, b)
+            else:
+                ref, ref_lse, _ = oracle.sparse_mla(st["q"][b], comp_o, comp_bt[b], sel, int(glen[b]), swa,
+                                                    swa_bt[b], p, SCALE)
             check_attention(gout[b], ref, "step %d seq %d" % (s, b))
             np.testing.assert_allclose(glse[b], ref_lse, rtol=1e-3, atol=1e-3)
             if st["boundary"][b]:
-                # the new slot dominates: the output is close to its latent
-                lat = dequant_nope(ent_m[b][0][p // 4], ent_m[b][1][p // 4])
+                # the new slot dominates: the output is close to its latent (V4: its whole row)
+                ent = (ent_m[b][0][p // 4], ent_m[b][1][p // 4])
+                lat = dequant_row(*ent, nope_m) if v4 else dequant_nope(*ent)
                 assert np.linalg.norm(gout[b] - lat[None, :]) / np.linalg.norm(np.broadcast_to(lat, gout[b].shape)) < 0.1
             return tol
 
