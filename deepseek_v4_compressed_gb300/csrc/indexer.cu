@@ -422,30 +422,106 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     const int n_pages = (n_c + kPage - 1) / kPage;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kIdxStages; ++i) {
-            tc::mbar_init(tc::smem_u32(&full[i]), 1);
-            // MMA commit + 4 warps: the epilogue's (page ids read), FP4: the converter's (tile read)
-            tc::mbar_init(tc::smem_u32(&empty[i]), 5);
-            if (kFp4) tc::mbar_init(tc::smem_u32(&conv[i]), 4);   // the 4 warps of the tile's epilogue group
+    // the query row's block-table row (prefill rows map to their sequence's)
+    auto seq_of_row = [&]() {
+        int sq = b;
+        if (P.row_seq) {
+            sq = P.row_seq[b];
+            if (sq < 0 || sq >= P.bt_rows) {
+                if (lane == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
+                sq = 0;
+            }
         }
-        for (int i = 0; i < kAcc; ++i) {
-            tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
-            tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
+        return sq;
+    };
+    // lane l of a producer warp: page id of page l of the group of 16 tiles
+    // starting at tile i, loaded by the lanes at once
+    auto page_group = [&](int sq, int i) {
+        int pg = -1;
+        if (2 * i + lane < 2 * n_my) {
+            const int pi = min(2 * (t_begin + i) + lane, n_pages - 1);
+            pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(sq) * P.bt_stride + pi] : -1;
+            if (pg < 0 || pg >= P.num_pages) {
+                flag(P.status, DSV4_DEV_BAD_PAGE);
+                pg = -1;
+            }
         }
-        tc::mbar_init(tc::smem_u32(q_bar), 1);
-        if (kFused) {
-            // the top-k's, which the other CTAs of the cluster complete
-            tc::mbar_init(tc::smem_u32(&ctk->bar_mm), 1);
-            tc::mbar_init(tc::smem_u32(&ctk->bar_h[0]), 1);
-            tc::mbar_init(tc::smem_u32(&ctk->bar_h[1]), 1);
-            tc::mbar_init(tc::smem_u32(&ctk->bar_cnt), 1);
+        return pg;
+    };
+    // tile i's loads into its stage (a whole producer warp; v: this lane's
+    // page, lanes 0-1 the tile's two pages).  The tile's page ids go to
+    // stage_pages (the epilogue reads the scales straight from those pages)
+    // before the phase is armed.  FP8: TMA tensor loads (an unreadable page
+    // is outside the map and reads zeros); FP4: the two whole pages by 1-D
+    // bulk copies (an unreadable page, already flagged, is read as page 0).
+    auto issue_tile = [&](int i, int v) {
+        const int st = i % kIdxStages;
+        const uint32_t fb = tc::smem_u32(&full[st]);
+        if (lane < 2) stage_pages[st * 2 + lane] = v < 0 ? 0 : v;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_expect_tx(fb, kTileIn);
+        __syncwarp();
+        if (kFp4) {
+            if (lane < 2)
+                tc::bulk_g2s(tc::smem_u32(raw_tiles + st * kIdxFp4Stage + lane * kIdxFp4PageB),
+                             P.cache + static_cast<long long>(v < 0 ? 0 : v) * kIdxFp4PageB, kIdxFp4PageB, fb);
+        } else if (lane < 2) {
+            tc::tma_load_3d(tc::smem_u32(a_tiles + st * kIdxTileBytes + lane * (kIdxTileBytes / 2)), &tm_cache,
+                            fb, 0, 0, v < 0 ? P.num_pages : v);
         }
-        *abort_flag = 0;
-        tc::fence_barrier_init();
+    };
+    // This kernel may overlap the one before it (programmatic dependent
+    // launch).  When that is the library's decode compressor, it writes at
+    // most the newest entry of each sequence (slot n_c - 1, in the last tile),
+    // and every kernel before it is complete (the library's compressors let
+    // their dependents start only once those are); a caller kernel in between
+    // does not let this one start early.  So the tiles before the last are
+    // read at once, and the wait for the previous grid comes right before the
+    // last tile's loads -- and in every CTA, so that this grid completes only
+    // after it.
+    //
+    // Producer warp 8 sets up the barriers and, before the block-wide barrier,
+    // issues the query's and the first kIdxStages tiles' loads (no stage has
+    // been used yet), so that they are in flight during the set-up.
+    const int n_early = min(n_my, kIdxStages);
+    bool waited = false;
+    if (warp == 8) {
+        if (lane == 0) {
+            for (int i = 0; i < kIdxStages; ++i) {
+                tc::mbar_init(tc::smem_u32(&full[i]), 1);
+                // MMA commit + 4 warps: the epilogue's (page ids read), FP4: the converter's (tile read)
+                tc::mbar_init(tc::smem_u32(&empty[i]), 5);
+                if (kFp4) tc::mbar_init(tc::smem_u32(&conv[i]), 4);   // the 4 warps of the tile's epilogue group
+            }
+            for (int i = 0; i < kAcc; ++i) {
+                tc::mbar_init(tc::smem_u32(&acc_full[i]), 1);
+                tc::mbar_init(tc::smem_u32(&acc_empty[i]), 4);
+            }
+            tc::mbar_init(tc::smem_u32(q_bar), 1);
+            if (kFused) {
+                // the top-k's, which the other CTAs of the cluster complete
+                tc::mbar_init(tc::smem_u32(&ctk->bar_mm), 1);
+                tc::mbar_init(tc::smem_u32(&ctk->bar_h[0]), 1);
+                tc::mbar_init(tc::smem_u32(&ctk->bar_h[1]), 1);
+                tc::mbar_init(tc::smem_u32(&ctk->bar_cnt), 1);
+            }
+            *abort_flag = 0;
+            tc::fence_barrier_init();
+            tc::prefetch_tensormap(&tm_cache);
+            tc::prefetch_tensormap(&tm_q);
+            tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
+            tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
+        }
+        __syncwarp();
+        const int pg0 = page_group(seq_of_row(), 0);
+        for (int i = 0; i < n_early; ++i) {
+            if (!waited && t_begin + i == n_tiles - 1) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                waited = true;
+            }
+            issue_tile(i, __shfl_sync(0xffffffffu, pg0, 2 * i + (lane & 1)));
+        }
     }
-    if (threadIdx.x < 64) w_s[threadIdx.x] = (threadIdx.x < P.H) ? P.w[static_cast<long long>(b) * P.H + threadIdx.x] : 0.f;
-    if (kFp4 && threadIdx.x >= 64 && threadIdx.x < 64 + 18) lut_s[threadIdx.x - 64] = (&c_e2m1_lut[0][0])[threadIdx.x - 64];
     if (kFused && threadIdx.x == 0) {
         ctk->mm[0] = 0xffffffffu;
         ctk->mm[1] = 0u;
@@ -461,60 +537,22 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     if (kFused) tc::cluster_arrive_relaxed();   // this CTA has started (the top-k waits for every CTA)
-    int issued = 0;   // tiles whose loads were issued (producer only)
+    int issued = n_early;   // tiles whose loads were issued (producer only)
     int consumed = 0; // tiles whose stage the MMA released (MMA thread only)
 
     if (warp == 8 || warp == 10) {
         const int pgrp = warp == 8 ? 0 : 1;       // this producer's tiles: i = pgrp, pgrp + 2, ...
-        if (lane == 0 && pgrp == 0) {
-            tc::prefetch_tensormap(&tm_cache);
-            tc::prefetch_tensormap(&tm_q);
-            tc::mbar_arrive_expect_tx(tc::smem_u32(q_bar), P.n_pad * kIdx);
-            tc::tma_load_2d(tc::smem_u32(q_tile), &tm_q, tc::smem_u32(q_bar), 0, b * P.H);
-        }
-        // the query row's block-table row (prefill rows map to their sequence's)
-        int seq = b;
-        if (P.row_seq) {
-            seq = P.row_seq[b];
-            if (seq < 0 || seq >= P.bt_rows) {
-                if (lane == 0) flag(P.status, DSV4_DEV_BAD_INDEX);
-                seq = 0;
-            }
-        }
-        // lane l: page id of page l of the group of 16 tiles starting at tile i,
-        // loaded by the lanes at once
-        auto page_group = [&](int i) {
-            int pg = -1;
-            if (2 * i + lane < 2 * n_my) {
-                const int pi = min(2 * (t_begin + i) + lane, n_pages - 1);
-                pg = (pi < P.bt_stride) ? P.bt[static_cast<long long>(seq) * P.bt_stride + pi] : -1;
-                if (pg < 0 || pg >= P.num_pages) {
-                    flag(P.status, DSV4_DEV_BAD_PAGE);
-                    pg = -1;
-                }
-            }
-            return pg;
-        };
-        int pgl = page_group(0);
-        // This kernel may overlap the one before it (programmatic dependent
-        // launch).  When that is the library's decode compressor, it writes at
-        // most the newest entry of each sequence (slot n_c - 1, in the last
-        // tile), and every kernel before it is complete (the library's
-        // compressors let their dependents start only once those are); a
-        // caller kernel in between does not let this one start early.  So
-        // the tiles before the last are read at once, and the wait for the
-        // previous grid comes right before the last tile's loads -- and in
-        // every CTA, so that this grid completes only after it.
-        bool waited = false;
+        const int seq = seq_of_row();
+        int pgl = n_my > n_early ? page_group(seq, 0) : -1;
         for (int i = pgrp; i < n_my; i += 2) {
             if (!waited && t_begin + i == n_tiles - 1) {
                 asm volatile("griddepcontrol.wait;" ::: "memory");
                 waited = true;
             }
-            if (i >= 16 && (i & 15) < 2) pgl = page_group(i & ~15);
+            if (i < n_early) continue;                // issued before the block-wide barrier
+            if (i >= 16 && (i & 15) < 2) pgl = page_group(seq, i & ~15);
             const int v = __shfl_sync(0xffffffffu, pgl, 2 * (i & 15) + (lane & 1));   // this lane's page
             const int st = i % kIdxStages;
-            const uint32_t fb = tc::smem_u32(&full[st]);
             int go = 1;
             if (lane == 0) {
                 const uint32_t ph = (i / kIdxStages) & 1;
@@ -522,24 +560,7 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                     go = 0;
             }
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            // the tile's page ids go to stage_pages (the epilogue reads the
-            // scales straight from those pages) before the phase is armed
-            if (lane < 2) stage_pages[st * 2 + lane] = v < 0 ? 0 : v;   // scales from a valid page
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_expect_tx(fb, kTileIn);
-            __syncwarp();
-            // lanes 0-1: the two pages' rows (TMA tensor loads; an unreadable
-            // page is outside the map and reads zeros).  FP4: the two whole
-            // pages by 1-D bulk copies (an unreadable page, already flagged,
-            // is read as page 0)
-            if (kFp4) {
-                if (lane < 2)
-                    tc::bulk_g2s(tc::smem_u32(raw_tiles + st * kIdxFp4Stage + lane * kIdxFp4PageB),
-                                 P.cache + static_cast<long long>(v < 0 ? 0 : v) * kIdxFp4PageB, kIdxFp4PageB, fb);
-            } else if (lane < 2) {
-                tc::tma_load_3d(tc::smem_u32(a_tiles + st * kIdxTileBytes + lane * (kIdxTileBytes / 2)), &tm_cache,
-                                fb, 0, 0, v < 0 ? P.num_pages : v);
-            }
+            issue_tile(i, v);
             if (lane == 0) issued = i + 1;
         }
         if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -571,6 +592,12 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
         // epilogue group (warps 0-3 or 4-7) takes every other tile; the scales it
         // reads come straight from the pages, and the last tile's may be written
         // by the kernel before this one (see the producers)
+        // the head weights (FP4: and the byte-permute tables) into shared
+        // memory, loaded here so that the block-wide barrier does not wait
+        // for them; the 8 epilogue warps meet once before the first use
+        if (threadIdx.x < 64) w_s[threadIdx.x] = (threadIdx.x < P.H) ? P.w[static_cast<long long>(b) * P.H + threadIdx.x] : 0.f;
+        if (kFp4 && threadIdx.x >= 64 && threadIdx.x < 64 + 18) lut_s[threadIdx.x - 64] = (&c_e2m1_lut[0][0])[threadIdx.x - 64];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         const int grp = warp >> 2;
         const int q4 = warp & 3;
         const int row = q4 * 32 + lane;

@@ -321,6 +321,11 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int i = 0; i < kEpiParts; ++i) tc::mbar_init(tc::smem_u32(&recv_part[i]), 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
+        // the query's loads are in flight during the rest of the set-up
+        tc::prefetch_tensormap(&tm_q);
+        tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), G::kQBytes);
+        for (int c = 0; c < G::kChunks; ++c)
+            tc::tma_load_2d(tc::smem_u32(q_s + c * kTcQChunk), &tm_q, tc::smem_u32(q_full), c * 64, b * P.H + h0);
     }
     if (threadIdx.x < 64) {
         sm_m[threadIdx.x] = -INFINITY;
@@ -341,12 +346,7 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // QK(t) needs tile t loaded and S buffer t%2 read out by the
             // softmax (P(t-2) written).
             if (lane == 0) {
-                tc::prefetch_tensormap(&tm_q);
                 tc::prefetch_tensormap(&tm_swa);
-                tc::mbar_arrive_expect_tx(tc::smem_u32(q_full), G::kQBytes);
-                for (int c = 0; c < G::kChunks; ++c)
-                    tc::tma_load_2d(tc::smem_u32(q_s + c * kTcQChunk), &tm_q, tc::smem_u32(q_full), c * 64,
-                                    b * P.H + h0);
                 constexpr uint32_t id_qk = tc::idesc(64, kTcKeys, tc::kFmtBF16, tc::kFmtBF16);
                 bool ok = tc::mbar_wait(tc::smem_u32(q_full), 0, abort_flag, P.status);
                 const uint64_t qd = tc::desc_kmajor_sw128(tc::smem_u32(q_s));
