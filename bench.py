@@ -65,7 +65,8 @@ WORKLOADS = {
 # capture of this workload (one launch, cold cache), with the sha256 of the
 # sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
-    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19088896 + 0, "src_sha": "fcae9cd0963efc99"},
+    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19090432 + 0, "src_sha": "f511074a55f3f233"},
+    ("c4a_32k_b32_v4", "sparse_mla"): {"bytes_per_launch": 16450816 + 0, "src_sha": "f511074a55f3f233"},
 }
 
 
