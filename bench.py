@@ -65,8 +65,8 @@ WORKLOADS = {
 # capture of this workload (one launch, cold cache), with the sha256 of the
 # sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
-    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19090432 + 0, "src_sha": "f511074a55f3f233"},
-    ("c4a_32k_b32_v4", "sparse_mla"): {"bytes_per_launch": 16450816 + 0, "src_sha": "f511074a55f3f233"},
+    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19090432 + 0, "src_sha": "1a7cefe100b7c33c"},
+    ("c4a_32k_b32_v4", "sparse_mla"): {"bytes_per_launch": 16450816 + 0, "src_sha": "1a7cefe100b7c33c"},
 }
 
 
@@ -113,22 +113,23 @@ def algorithmic_bytes(w, ctx):
     entry = 584 if v4 else 648               # compressed entry bytes
     swa_row = 584 if v4 else 1152            # SWA token bytes (FP8 row or bf16 [576])
     mla = B * (k * entry + 128 * swa_row + k * 4 + 4 + H * d * 2 + H * 512 * 2 + H * 4 + (k + 2) * 4)
-    # V4: the output read back, codes + scales written, position and its cos/sin row
-    out_quant = B * (H * 512 * 2 + H * (512 + 16) + 4 + 256) if v4 else 0.0
+    # V4: the attention call also writes the inverse-rotated output's FP8 codes
+    # and block scales (its cos/sin row read)
+    if v4:
+        mla += B * (H * (512 + 16) + 256)
     if w["ratio"] == 128:
         # main compressor only (ratio 128, no overlap): the token's kv/score row in,
         # its state row out; at a boundary (1 token in 128) the 128 ring rows and
         # the entry.  The indices are caller metadata, read by the attention.
         comp_main = B * (2 * d * 2 + 2 * d * 4 + (128 * 2 * d * 4 + entry) / 128)
-        return dict(compress=comp_main, indexer=0.0, mla=mla, out_quant=out_quant,
-                    total=comp_main + mla + out_quant)
+        return dict(compress=comp_main, indexer=0.0, mla=mla, total=comp_main + mla)
     n_c = ctx // 4
     idx_entry = 68 if w.get("idx_fp4") else 132      # MXFP4 or FP8 indexer entries
     comp_main = B * (4 * d * 2 + 4 * d * 4 + 0.25 * (7 * 2 * d * 4 + entry))
     comp_idx = B * (512 * 2 + 512 * 4 + 0.25 * (7 * 256 * 4 + idx_entry))
     indexer = B * (n_c * idx_entry + HI * 128 + HI * 4 + k * 4 + 4 + (n_c // 64) * 4)
-    return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla, out_quant=out_quant,
-                total=comp_main + comp_idx + indexer + mla + out_quant)
+    return dict(compress=comp_main + comp_idx, indexer=indexer, mla=mla,
+                total=comp_main + comp_idx + indexer + mla)
 
 
 def src_digest(paths):
@@ -348,8 +349,7 @@ class GpuBench:
                                 window=w["window"], kv_layout=kv_layout)
             self.layers = build_layers(w, n_layers, n_pos, device)
             self.stage_names = ["compress", "indexer_topk", "sparse_mla"]
-        if self.v4:
-            self.stage_names.append("out_quant")
+
         self.idx_kind = Bd.CACHE_IDX_FP4 if w.get("idx_fp4") else Bd.CACHE_IDX
         self.ws = self.plan.workspace(device)
         self.cos_sin = Bd.rope_table(w["context"] + 1).to(device)
@@ -371,6 +371,7 @@ class GpuBench:
             self.topk_len.fill_(w["topk"])
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.info = self.plan.info()
+        # V4: the attention call launches the output quantisation after it
         self.launches_per_step = 1 + self.info["launches_indexer"] + self.info["launches_mla"] + int(self.v4)
 
     def step_inputs(self, r, j):
@@ -391,8 +392,7 @@ class GpuBench:
     def calls_for(self, L, x, j=0):
         Bd = self.Bd
         Bsz = self.w["batch"]
-        quant = [lambda: Bd.inv_rope_fp8_quant(L.out, x["pos"], self.cos_sin, L.codes, L.scales,
-                                               status=self.status)] if self.v4 else []
+        q4 = dict(out_codes=L.codes, out_scales=L.scales, cos_sin=self.cos_sin) if self.v4 else {}
         if self.c128:
             return [
                 lambda: Bd.compress_insert(self.main_kind, 128, x["kv_main"], x["pos"], L.seqs, L.ape_main,
@@ -401,8 +401,8 @@ class GpuBench:
                 lambda: Bd.sparse_mla_decode(self.plan, x["q"], L.swa, L.swa_bt, x["ctx"], L.out, self.ws,
                                              comp_cache=L.comp, comp_block_table=L.comp_bt,
                                              topk_idx=self.c128_idx[j], topk_len=self.topk_len, lse=L.lse,
-                                             status=self.status),
-            ] + quant
+                                             status=self.status, **q4),
+            ]
         return [
             lambda: Bd.compress_insert_pair(
                 dict(kind=self.main_kind, ratio=4, kv_score=x["kv_main"], positions=x["pos"], seqs=L.seqs,
@@ -415,8 +415,8 @@ class GpuBench:
                                     self.topk_len, self.ws, self.status),
             lambda: Bd.sparse_mla_decode(self.plan, x["q"], L.swa, L.swa_bt, x["ctx"], L.out, self.ws,
                                          comp_cache=L.comp, comp_block_table=L.comp_bt, topk_idx=self.topk_idx,
-                                         topk_len=self.topk_len, lse=L.lse, status=self.status),
-        ] + quant
+                                         topk_len=self.topk_len, lse=L.lse, status=self.status, **q4),
+        ]
 
     def stage_calls(self, r, j):
         return self.calls_for(self.layers[r], self.step_inputs(r, j), j)
@@ -1010,13 +1010,12 @@ def main():
     # roofline of the dominant kernel: the stage with the largest time (each
     # stage is one kernel at the c4a workloads, where the top-k runs inside the
     # logits launch when a sequence's CTAs fit one cluster)
-    stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"],
-                   "out_quant": ab["out_quant"]}
+    stage_bytes = {"compress": ab["compress"], "indexer_topk": ab["indexer"], "sparse_mla": ab["mla"]}
     kernels = {"compress": ("compress_pair_kernel / compress_kernel (dsv4_compress_insert)", "compress.cu"),
                "indexer_topk": ("indexer_logits_tc (dsv4_indexer_topk)" if bench.info["launches_indexer"] == 1 else
                                 "indexer_logits_tc + top-k kernel (dsv4_indexer_topk, 2 launches)", "indexer.cu"),
-               "sparse_mla": ("mla_decode_tc%s (dsv4_sparse_mla_decode)" % ("<V4>" if bench.v4 else ""), "mla.cu"),
-               "out_quant": ("inv_rope_fp8_quant_kernel (dsv4_inv_rope_fp8_quant)", "out_quant.cu")}
+               "sparse_mla": (("mla_decode_tc<V4> + inv_rope_fp8_quant_kernel (dsv4_sparse_mla_decode, "
+                               "2 launches)" if bench.v4 else "mla_decode_tc (dsv4_sparse_mla_decode)"), "mla.cu")}
     dom = max(bench.stage_names, key=lambda nm: stages[nm])
     achieved = stage_bytes[dom] / (stages[dom] / 1e3) / 1e9
     srcs = ["deepseek_v4_compressed_gb300/csrc/" + kernels[dom][1]]

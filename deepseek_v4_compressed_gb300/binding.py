@@ -100,7 +100,9 @@ class MlaArgs(ctypes.Structure):
                 ("topk_stride", ctypes.c_int), ("topk_len_dev", ctypes.c_void_p),
                 ("ctx_len_dev", ctypes.c_void_p), ("out_dev", ctypes.c_void_p),
                 ("lse_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p),
-                ("row_seq_dev", ctypes.c_void_p), ("bt_rows", ctypes.c_int)]
+                ("row_seq_dev", ctypes.c_void_p), ("bt_rows", ctypes.c_int),
+                ("out_codes_dev", ctypes.c_void_p), ("out_scales_dev", ctypes.c_void_p),
+                ("cos_sin_dev", ctypes.c_void_p), ("max_pos", ctypes.c_int)]
 
 
 class GatherArgs(ctypes.Structure):
@@ -378,7 +380,10 @@ def indexer_topk(plan, q_fp8, weights, idx_cache, block_table, ctx_len, out_idx,
 
 def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspace, comp_cache=None,
                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None,
-                      stream=None, row_seq=None):
+                      stream=None, row_seq=None, out_codes=None, out_scales=None, cos_sin=None):
+    """dsv4_sparse_mla_decode; V4 plans may also ask for the quantised,
+    inverse-rotated output (out_codes uint8 [B, H, 512], out_scales fp32
+    [B, H, 4], cos_sin fp32 [max_pos, 64])."""
     a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // plan.swa_page_bytes),
                 _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
                 int(_nbytes(comp_cache) // plan.comp_page_bytes) if comp_cache is not None else 0,
@@ -386,7 +391,8 @@ def sparse_mla_decode(plan, q, swa_cache, swa_block_table, ctx_len, out, workspa
                 int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
                 _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
                 _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status), _ptr(row_seq),
-                int(swa_block_table.shape[0]))
+                int(swa_block_table.shape[0]), _ptr(out_codes), _ptr(out_scales), _ptr(cos_sin),
+                int(cos_sin.shape[0]) if cos_sin is not None else 0)
     _check(lib().dsv4_sparse_mla_decode(plan.handle, ctypes.byref(a), _ptr(workspace),
                                         workspace.numel(), _stream(stream)), "sparse_mla_decode")
 

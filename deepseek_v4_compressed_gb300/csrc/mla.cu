@@ -13,6 +13,7 @@
 #include "tc_common.cuh"
 #include "tmap.h"
 #include "host_once.h"
+#include "out_quant.h"
 
 namespace dsv4 {
 
@@ -1074,6 +1075,12 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     P.row_seq = a->row_seq_dev;
     P.bt_rows = a->bt_rows;
     if (P.row_seq && P.bt_rows < 1) return DSV4_ERR_INVALID;
+    // the V4 output quantisation: a second launch after the attention (the
+    // quantisation kernel, positions from the context lengths)
+    const bool want_codes = a->out_codes_dev != nullptr;
+    if (want_codes && (!plan->kv_v4 || !a->out_scales_dev || !a->cos_sin_dev || a->max_pos < 1))
+        return DSV4_ERR_INVALID;
+    if (want_codes && (reinterpret_cast<uintptr_t>(a->out_scales_dev) & 3)) return DSV4_ERR_SHAPE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     MlaTcParams T;
     T.base = P;
@@ -1133,8 +1140,12 @@ extern "C" dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = v4 ? cudaLaunchKernelEx(&cfg, mla_decode_tc<true>, tm_q, tm_swa, T)
-                             : cudaLaunchKernelEx(&cfg, mla_decode_tc<false>, tm_q, tm_swa, T);
+    cudaError_t e = v4 ? cudaLaunchKernelEx(&cfg, mla_decode_tc<true>, tm_q, tm_swa, T)
+                       : cudaLaunchKernelEx(&cfg, mla_decode_tc<false>, tm_q, tm_swa, T);
+    if (e == cudaSuccess && want_codes)
+        e = launch_inv_rope_quant(static_cast<const uint16_t*>(a->out_dev), plan->batch, P.H, a->ctx_len_dev, true,
+                                  a->cos_sin_dev, a->max_pos, static_cast<uint8_t*>(a->out_codes_dev),
+                                  a->out_scales_dev, a->status_dev, st);
     return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }
 

@@ -12,6 +12,7 @@
 // upper half holds the 64 RoPE dims.  Pure streaming work: 1024 bytes read
 // and 528 written per row, bound by HBM.
 #include "dsv4_common.cuh"
+#include "out_quant.h"
 
 namespace dsv4 {
 
@@ -22,6 +23,7 @@ constexpr int kOqRowsPerCta = 2;                   // 8 warps: 2 rows x 4 blocks
 struct InvRopeQuantParams {
     const uint16_t* o;
     const int* pos;
+    int pos_minus;                 // subtracted from pos[t]: 1 when pos holds context lengths
     const float* cos_sin;
     int max_pos;
     int n_heads;
@@ -38,7 +40,7 @@ __global__ void __launch_bounds__(32 * 4 * kOqRowsPerCta) inv_rope_fp8_quant_ker
     if (row >= Q.rows) return;
     const int blk = warp & 3;
     const int t = static_cast<int>(row / Q.n_heads);
-    const int pos = Q.pos[t];
+    const int pos = Q.pos[t] - Q.pos_minus;
     if (pos < 0 || pos >= Q.max_pos) {
         if (lane == 0 && blk == 0) flag(Q.status, DSV4_DEV_BAD_POSITION);
         return;
@@ -67,6 +69,28 @@ __global__ void __launch_bounds__(32 * 4 * kOqRowsPerCta) inv_rope_fp8_quant_ker
     if (lane == 0) Q.scales[row * 4 + blk] = s;
 }
 
+cudaError_t launch_inv_rope_quant(const uint16_t* o, int num_tokens, int n_heads, const int* pos, bool pos_is_ctx,
+                                  const float* cos_sin, int max_pos, uint8_t* codes, float* scales, int* status,
+                                  cudaStream_t stream)
+{
+    InvRopeQuantParams Q;
+    Q.o = o;
+    Q.pos = pos;
+    Q.pos_minus = pos_is_ctx ? 1 : 0;
+    Q.cos_sin = cos_sin;
+    Q.max_pos = max_pos;
+    Q.n_heads = n_heads;
+    Q.rows = static_cast<long long>(num_tokens) * n_heads;
+    Q.codes = codes;
+    Q.scales = scales;
+    Q.status = status;
+    if (Q.rows == 0) return cudaSuccess;
+    const long long ctas = (Q.rows + kOqRowsPerCta - 1) / kOqRowsPerCta;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    inv_rope_fp8_quant_kernel<<<static_cast<unsigned>(ctas), 32 * 4 * kOqRowsPerCta, 0, stream>>>(Q);
+    return cudaGetLastError();
+}
+
 }  // namespace dsv4
 
 using namespace dsv4;
@@ -81,19 +105,10 @@ extern "C" dsv4_status dsv4_inv_rope_fp8_quant(const dsv4_inv_rope_quant_args* a
     if ((reinterpret_cast<uintptr_t>(a->o_dev) & 15) || (reinterpret_cast<uintptr_t>(a->codes_dev) & 15) ||
         (reinterpret_cast<uintptr_t>(a->scales_dev) & 3))
         return DSV4_ERR_SHAPE;
-    InvRopeQuantParams Q;
-    Q.o = static_cast<const uint16_t*>(a->o_dev);
-    Q.pos = a->positions_dev;
-    Q.cos_sin = a->cos_sin_dev;
-    Q.max_pos = a->max_pos;
-    Q.n_heads = a->n_heads;
-    Q.rows = static_cast<long long>(a->num_tokens) * a->n_heads;
-    Q.codes = static_cast<uint8_t*>(a->codes_dev);
-    Q.scales = a->scales_dev;
-    Q.status = a->status_dev;
-    const long long ctas = (Q.rows + kOqRowsPerCta - 1) / kOqRowsPerCta;
-    if (ctas > 0x7fffffffLL) return DSV4_ERR_UNSUPPORTED;
-    inv_rope_fp8_quant_kernel<<<static_cast<unsigned>(ctas), 32 * 4 * kOqRowsPerCta, 0,
-                                reinterpret_cast<cudaStream_t>(stream)>>>(Q);
-    return cudaGetLastError() == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
+    const cudaError_t e = launch_inv_rope_quant(static_cast<const uint16_t*>(a->o_dev), a->num_tokens, a->n_heads,
+                                                a->positions_dev, false, a->cos_sin_dev, a->max_pos,
+                                                static_cast<uint8_t*>(a->codes_dev), a->scales_dev, a->status_dev,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return DSV4_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? DSV4_OK : DSV4_ERR_CUDA;
 }

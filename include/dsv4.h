@@ -451,6 +451,19 @@ typedef struct dsv4_mla_args {
      * (of both tables, bt_rows rows each) of each query row. */
     const int* row_seq_dev;
     int bt_rows;
+    /* DSV4_KV_V4 plans only, optional (NULL: not produced): the attention
+     * output's inverse RoPE + FP8 quantisation as dsv4_inv_rope_fp8_quant
+     * defines it (rotation R(-p) at the row's query position p = ctx_len - 1,
+     * 128-dim blocks with fp32 scales), computed from the bf16 output and
+     * written to out_codes_dev (E4M3 [batch][n_heads][512]) and out_scales_dev
+     * (fp32 [batch][n_heads][4]); cos_sin_dev: fp32 [max_pos][64].  The
+     * call launches the quantisation kernel after the attention (stream
+     * order); out_dev is written as well.  A position outside [0, max_pos)
+     * sets DSV4_DEV_BAD_POSITION and leaves that row's codes unwritten. */
+    void* out_codes_dev;
+    float* out_scales_dev;
+    const float* cos_sin_dev;
+    int max_pos;
 } dsv4_mla_args;
 
 dsv4_status dsv4_sparse_mla_decode(const dsv4_plan* plan, const dsv4_mla_args* args,

@@ -15,7 +15,9 @@ from _util import bits_tensor, check_attention, dev, make_v4_decode_inputs, orac
 pytestmark = pytest.mark.gpu
 
 
-def run_v4(d, max_ctx=None):
+def run_v4(d, max_ctx=None, cos_sin=None, expect=B.OK):
+    """The V4 attention; with cos_sin also the output quantisation (returned
+    as codes, scales, the plan's cluster size)."""
     lt = d.layer_type
     plan = B.Plan(lt, d.n_heads, d.batch, d.topk if lt != B.SWAONLY else 0, int(max_ctx or d.ctx.max()),
                   idx_heads=8, kv_layout=B.KV_V4)
@@ -27,12 +29,20 @@ def run_v4(d, max_ctx=None):
     if lt != B.SWAONLY:
         kw = dict(comp_cache=d.t["comp"], comp_block_table=d.t["comp_bt"], topk_idx=d.t["idx"],
                   topk_len=d.t["idx_len"])
+    codes = scales = None
+    if cos_sin is not None:
+        codes = torch.full((d.batch, d.n_heads, 512), 0xAA, dtype=torch.uint8, device="cuda")
+        scales = torch.full((d.batch, d.n_heads, 4), -1.0, dtype=torch.float32, device="cuda")
+        kw.update(out_codes=codes, out_scales=scales, cos_sin=dev(cos_sin))
     B.sparse_mla_decode(plan, d.t["q"], d.t["swa"], d.t["swa_bt"], d.t["ctx"], out, ws, lse=lse, status=status,
                         **kw)
     torch.cuda.synchronize()
     st, bits = B.read_device_status(status)
-    assert st == B.OK, bits
-    return out.float().cpu().numpy(), lse.cpu().numpy()
+    assert st == expect, bits
+    res = (out.float().cpu().numpy(), lse.cpu().numpy())
+    if cos_sin is not None:
+        res += (codes.cpu().numpy(), scales.cpu().numpy(), plan.info()["mla_splits"])
+    return res
 
 
 def check_all(d, out, lse, seqs=None):
@@ -151,3 +161,40 @@ def test_v4_attention_then_output_quant():
         deq_ref = oracle.e4m3_to_f64(ref_rot[0]) * np.repeat(ref_rot[1].astype(np.float64), 128, axis=1)
         amax = np.abs(deq_ref).max()
         assert np.abs(deq - deq_ref).max() <= 2e-2 + 2 * 2.0 ** -4 * amax
+
+
+@pytest.mark.parametrize("shape", ["tiny_ragged", "c4a_32k_b32", "c128a_128k_b64", "c4a_1m_b4"])
+def test_v4_attention_with_output_quant(shape):
+    """dsv4_sparse_mla_decode asked for the quantised output (the call launches
+    the quantisation kernel after the attention, positions from the context
+    lengths): codes and scales equal the oracle's quantisation of the kernel's
+    own bf16 output bit for bit, and the attention stays within its bars."""
+    if shape == "tiny_ragged":
+        d = make_v4_decode_inputs(4, 6, [1, 63, 64, 200, 513, 1000], 8, 32, seed=13)
+    elif shape == "c4a_32k_b32":
+        d = make_v4_decode_inputs(4, 32, 32768, 64, 512, seed=14)
+    elif shape == "c128a_128k_b64":
+        d = make_v4_decode_inputs(128, 64, 131072, 64, 512, seed=15)
+    else:
+        d = make_v4_decode_inputs(4, 4, 1048576, 128, 2048, seed=16, comp_pool=4096)
+    cs = oracle.rope_table(int(d.ctx.max()), 64)
+    out, lse, codes, scales, C = run_v4(d, cos_sin=cs)
+    seqs = range(d.batch) if d.batch <= 32 else range(0, d.batch, 7)
+    check_all(d, out, lse, seqs=seqs)
+    out_bits = oracle.f32_to_bf16(out.reshape(-1, 512)).reshape(out.shape)
+    for b in seqs:
+        wc, ws = oracle.inv_rope_fp8_quant(out_bits[b], int(d.p[b]), cs)
+        assert np.array_equal(codes[b], wc), "seq %d codes" % b
+        assert np.array_equal(scales[b].view(np.uint32), ws.view(np.uint32)), "seq %d scales" % b
+
+
+def test_v4_output_quant_bad_position():
+    """A table too short for a row's position: the row is flagged and its
+    codes left unwritten; the other rows are quantised."""
+    d = make_v4_decode_inputs(4, 32, [32768] * 31 + [40000], 64, 512, seed=17)
+    cs = oracle.rope_table(32768, 64)
+    out, lse, codes, scales, C = run_v4(d, cos_sin=cs, expect=B.ERR_DEVICE_CHECK)
+    assert np.all(codes[31] == 0xAA) and np.all(scales[31] == -1.0)
+    out_bits = oracle.f32_to_bf16(out.reshape(-1, 512)).reshape(out.shape)
+    wc, ws = oracle.inv_rope_fp8_quant(out_bits[0], int(d.p[0]), cs)
+    assert np.array_equal(codes[0], wc) and np.array_equal(scales[0], ws)
