@@ -66,7 +66,6 @@ WORKLOADS = {
 # sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
     ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19090432 + 0, "src_sha": "1a7cefe100b7c33c"},
-    ("c4a_32k_b32_v4", "sparse_mla"): {"bytes_per_launch": 16450816 + 0, "src_sha": "1a7cefe100b7c33c"},
 }
 
 
