@@ -411,9 +411,11 @@ def indexer_topk_noalloc(plan, q_fp8, weights, idx_cache, block_table, ctx_len, 
 
 
 def sparse_mla_prefill(plan, q, swa_cache, swa_block_table, ctx_len, row_seq, out, workspace, comp_cache=None,
-                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None, stream=None):
+                       comp_block_table=None, topk_idx=None, topk_len=None, lse=None, status=None, stream=None,
+                       out_codes=None, out_scales=None, cos_sin=None):
     """dsv4_sparse_mla_prefill: one query row per prefill token (position
-    ctx_len - 1), row_seq mapping each row to its block-table row."""
+    ctx_len - 1), row_seq mapping each row to its block-table row; V4 plans
+    may also ask for the quantised output as in sparse_mla_decode."""
     a = MlaArgs(_ptr(q), _ptr(swa_cache), int(_nbytes(swa_cache) // plan.swa_page_bytes),
                 _ptr(swa_block_table), int(swa_block_table.shape[1]), _ptr(comp_cache),
                 int(_nbytes(comp_cache) // plan.comp_page_bytes) if comp_cache is not None else 0,
@@ -421,7 +423,8 @@ def sparse_mla_prefill(plan, q, swa_cache, swa_block_table, ctx_len, row_seq, ou
                 int(comp_block_table.shape[1]) if comp_block_table is not None else 0,
                 _ptr(topk_idx), int(topk_idx.shape[1]) if topk_idx is not None else 0,
                 _ptr(topk_len), _ptr(ctx_len), _ptr(out), _ptr(lse), _ptr(status), _ptr(row_seq),
-                int(swa_block_table.shape[0]))
+                int(swa_block_table.shape[0]), _ptr(out_codes), _ptr(out_scales), _ptr(cos_sin),
+                int(cos_sin.shape[0]) if cos_sin is not None else 0)
     _check(lib().dsv4_sparse_mla_prefill(plan.handle, ctypes.byref(a), _ptr(workspace), workspace.numel(),
                                          _stream(stream)), "sparse_mla_prefill")
 

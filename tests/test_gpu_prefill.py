@@ -141,3 +141,78 @@ def test_prefill_chunk_indexer_and_attention():
                          status=status)
     st, bits = B.read_device_status(status)
     assert st == B.ERR_DEVICE_CHECK and bits & B.DEV_BAD_INDEX
+
+
+def test_prefill_chunk_v4_geometry():
+    """The same chunk in the V4-native geometry: 584-byte rows in both caches,
+    512-dim queries, K = V attention per prefill row over its own top-k and
+    window, and the quantised, inverse-rotated output of every row at its own
+    position (codes and scales bit for bit against the oracle's quantisation
+    of the kernel's bf16 output)."""
+    from _util import SCALE_V4
+    g = synth.rng(94)
+    S, H, HI, K = 2, 64, 64, 128
+    seq_len = np.array([3000, 5000], np.int32)
+    n_q = np.array([24, 40], np.int32)
+    L = int(seq_len.max())
+    n_c = L // 4
+    cp = (n_c + 63) // 64
+    comp_bt = synth.page_tables(g, S, cp, extra_pages=1)
+    comp = np.zeros((S * cp + 1) * oracle.page_bytes(0, nope_dim=448), np.uint8)
+    for s in range(S):
+        oracle.page_write(0, comp, comp_bt[s], *oracle.quant_mla_rows(synth.normal(g, (n_c, 512), SCALE_V4),
+                                                                       nope_dim=448), nope_dim=448)
+    idx_bt = synth.page_tables(g, S, cp, extra_pages=1)
+    idxc = np.zeros((S * cp + 1) * oracle.page_bytes(1), np.uint8)
+    for s in range(S):
+        oracle.page_write(1, idxc, idx_bt[s], *oracle.quant_idx_rows(synth.normal(g, (n_c, 128), 1 / math.sqrt(128))),
+                          nope_dim=64)
+    sp = (L + 63) // 64
+    swa_bt = synth.page_tables(g, S, sp, extra_pages=1)
+    swa = np.zeros((S * sp + 1) * oracle.page_bytes(0, nope_dim=448), np.uint8)
+    for pg in range(S * sp + 1):
+        oracle.page_write(0, swa, np.array([pg], np.int32),
+                          *oracle.quant_mla_rows(synth.normal(g, (64, 512), SCALE_V4), nope_dim=448), nope_dim=448)
+    row_seq = np.repeat(np.arange(S, dtype=np.int32), n_q)
+    pos = np.concatenate([np.arange(seq_len[s] - n_q[s], seq_len[s]) for s in range(S)]).astype(np.int32)
+    T = len(pos)
+    ctx = pos + 1
+    qi = oracle.f32_to_e4m3(synth.normal(g, (T, HI, 128)))
+    wq = synth.uniform(g, (T, HI))
+    q = bf16_bits(synth.normal(g, (T, H, 512), SCALE_V4))
+    cs = oracle.rope_table(L, 64)
+    plan = B.Plan(B.C4A, H, T, K, L, idx_heads=HI, kv_layout=B.KV_V4)
+    ws = plan.workspace()
+    out_idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
+    out_len = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t_rs = dev(row_seq)
+    B.indexer_topk(plan, dev(qi), dev(wq), dev(idxc), dev(idx_bt), dev(ctx), out_idx, out_len, ws, status=status,
+                   row_seq=t_rs)
+    out = torch.zeros((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((T, H), dtype=torch.float32, device="cuda")
+    codes = torch.full((T, H, 512), 0xAA, dtype=torch.uint8, device="cuda")
+    scales = torch.full((T, H, 4), -1.0, dtype=torch.float32, device="cuda")
+    B.sparse_mla_prefill(plan, bits_tensor(q), dev(swa), dev(swa_bt), dev(ctx), t_rs, out, ws, comp_cache=dev(comp),
+                         comp_block_table=dev(comp_bt), topk_idx=out_idx, topk_len=out_len, lse=lse, status=status,
+                         out_codes=codes, out_scales=scales, cos_sin=dev(cs))
+    torch.cuda.synchronize()
+    assert B.read_device_status(status)[0] == B.OK
+    gi, gl, go, gs = out_idx.cpu().numpy(), out_len.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+    gc, gsc = codes.cpu().numpy(), scales.cpu().numpy()
+    out_bits = oracle.f32_to_bf16(go.reshape(-1, 512)).reshape(go.shape)
+
+    def check(t):
+        s = row_seq[t]
+        logits = oracle.indexer_logits(qi[t], wq[t], idxc, idx_bt[s], int(ctx[t]) // 4)
+        tol = check_topk(gi[t], int(gl[t]), logits, K)
+        ref, ref_lse = oracle.sparse_mla_v4(q[t], comp, comp_bt[s], gi[t][:gl[t]].copy(), int(gl[t]), swa, swa_bt[s],
+                                            int(pos[t]), SCALE_V4)
+        check_attention(go[t], ref, "row %d" % t)
+        np.testing.assert_allclose(gs[t], ref_lse, rtol=1e-3, atol=1e-3)
+        wc, wsc = oracle.inv_rope_fp8_quant(out_bits[t], int(pos[t]), cs)
+        assert np.array_equal(gc[t], wc) and np.array_equal(gsc[t], wsc), "row %d quant" % t
+        return tol
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=16) as ex:
+        print("near-tie slots tolerated:", sum(ex.map(check, range(T))))
