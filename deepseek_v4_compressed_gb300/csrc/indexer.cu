@@ -1318,10 +1318,25 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         for (int i = tid; i < kTkcWarps * 256; i += kTopkThreads) (&T->whist[0][0])[i] = 0;
         __syncthreads();
         int* wh = T->whist[warp];
-#pragma unroll 4
-        for (int i = tid; i < nl; i += kTopkThreads) {
-            const uint32_t o = keys[i] - base;
-            if (plo == 32 || (o >> plo) == (prefix >> plo)) atomicAdd(&wh[(o >> lo) & 255u], 1);
+        // keys in play: (key - base) >> plo == prefix >> plo, i.e. key - lo_key <
+        // 2^plo with lo_key = base + the prefix's bits at and above plo (every
+        // key in the first pass); their digit is (key - lo_key) >> lo.  Keys
+        // are read four at a time (nl4 whole groups, then the tail).
+        const uint32_t lo_key = base + (plo == 32 ? 0u : (prefix >> plo) << plo);
+        const uint32_t span_m1 = plo == 32 ? 0xffffffffu : (1u << plo) - 1u;
+        const int nl4 = nl >> 2;
+#pragma unroll 2
+        for (int i4 = tid; i4 < nl4; i4 += kTopkThreads) {
+            const uint4 kv = reinterpret_cast<const uint4*>(keys)[i4];
+            const uint32_t o0 = kv.x - lo_key, o1 = kv.y - lo_key, o2 = kv.z - lo_key, o3 = kv.w - lo_key;
+            if (o0 <= span_m1) atomicAdd(&wh[(o0 >> lo) & 255u], 1);
+            if (o1 <= span_m1) atomicAdd(&wh[(o1 >> lo) & 255u], 1);
+            if (o2 <= span_m1) atomicAdd(&wh[(o2 >> lo) & 255u], 1);
+            if (o3 <= span_m1) atomicAdd(&wh[(o3 >> lo) & 255u], 1);
+        }
+        for (int i = 4 * nl4 + tid; i < nl; i += kTopkThreads) {
+            const uint32_t o = keys[i] - lo_key;
+            if (o <= span_m1) atomicAdd(&wh[(o >> lo) & 255u], 1);
         }
         __syncthreads();
         if (tid < 256) {
