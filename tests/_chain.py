@@ -36,7 +36,7 @@ def _pool():
     return concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4))
 
 
-NOPE = {B.CACHE_MLA: 512, B.CACHE_V4: 448, B.CACHE_IDX: 64}
+NOPE = {B.CACHE_MLA: 512, B.CACHE_V4: 448, B.CACHE_IDX: 64, B.CACHE_IDX_FP4: 64}
 
 
 def oracle_entry(kind, ks, ape, w, cs, p):
@@ -45,11 +45,22 @@ def oracle_entry(kind, ks, ape, w, cs, p):
     y = oracle.compress_pool(4, ks, ape, p)
     z = oracle.rmsnorm(y, w, EPS)
     z[nope:] = oracle.rope_gptj(z[nope:], cs[(p // 4) * 4])
-    if kind != B.CACHE_IDX:
+    if kind == B.CACHE_IDX_FP4:
+        d, s = oracle.quant_idx_fp4_rows(z[None])
+    elif kind != B.CACHE_IDX:
         d, s = oracle.quant_mla_rows(z[None], nope_dim=nope)
     else:
         d, s = oracle.quant_idx_rows(z[None])
     return d[0], s[0]
+
+
+def idx_key_values(data, sc, fp4):
+    """An indexer entry's 128 key values (FP8 codes x scale, or the MXFP4
+    codes x their block exponents)."""
+    if fp4:
+        codes = np.stack([data & 15, data >> 4], axis=-1).reshape(128)
+        return oracle.e2m1_to_f64(codes) * np.repeat(2.0 ** (sc.astype(np.int64) - 127), 32)
+    return oracle.e4m3_to_f64(data) * float(sc)
 
 
 def dequant_nope(data, sc, nope=512):
@@ -62,7 +73,7 @@ def dequant_row(data, sc, nope):
     return np.concatenate([dequant_nope(data, sc, nope), rope])
 
 
-def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False):
+def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False, idx_fp4=False):
     """prefill: 'stream' runs tokens 0..L0-1 through the library's multi-token
     compressor (caches and ring built by the library, checked against the
     oracle's whole-stream entries); 'direct' writes oracle-quantised random
@@ -70,6 +81,8 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
     (the compressor state layout of dsv4.h) so that long contexts stay cheap."""
     g = synth.rng(seed)
     kind_m = B.CACHE_V4 if v4 else B.CACHE_MLA
+    kind_i = B.CACHE_IDX_FP4 if idx_fp4 else B.CACHE_IDX
+    okind_i = oracle.IDX_FP4_KIND if idx_fp4 else oracle.IDX_KIND
     D_MAIN = 512 if v4 else 576
     nope_m = NOPE[kind_m]
     scale = SCALE_V4 if v4 else SCALE
@@ -101,7 +114,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
     def entries(b):
         if prefill == "stream":
             dm, sm = oracle.compress_stream(0, 4, ks_m[b], ape_m, w_m, EPS, cs, nope_dim=nope_m)
-            di, si = oracle.compress_stream(1, 4, ks_i[b], ape_i, w_i, EPS, cs, nope_dim=64)
+            di, si = oracle.compress_stream(okind_i, 4, ks_i[b], ape_i, w_i, EPS, cs, nope_dim=64)
             return (dm, sm), (di, si)
         return None
 
@@ -117,20 +130,21 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
             n0 = int(L0[b] // 4)
             pick = g.integers(0, pool_n, size=int(n_ent[b]))
             dm, sm = pm[pick].copy(), psm[pick].copy()
-            di, si = oracle.quant_idx_rows(synth.normal(g, (int(n_ent[b]), D_IDX), 1.0))
+            rows_i = synth.normal(g, (int(n_ent[b]), D_IDX), 1.0)
+            di, si = oracle.quant_idx_fp4_rows(rows_i) if idx_fp4 else oracle.quant_idx_rows(rows_i)
             for p in range(int(L0[b]), int(T[b])):
                 if (p + 1) % 4 == 0:
                     j = p // 4
                     dm[j], sm[j] = oracle_entry(kind_m, ks_m[b], ape_m, w_m, cs, p)
-                    di[j], si[j] = oracle_entry(B.CACHE_IDX, ks_i[b], ape_i, w_i, cs, p)
+                    di[j], si[j] = oracle_entry(kind_i, ks_i[b], ape_i, w_i, cs, p)
             assert n0 <= n_ent[b]
             ent_m.append((dm, sm))
             ent_i.append((di, si))
     comp_o = np.zeros((batch * pps + 1) * oracle.page_bytes(0, nope_dim=nope_m), np.uint8)
-    idx_o = np.zeros((batch * pps + 1) * oracle.page_bytes(1), np.uint8)
+    idx_o = np.zeros((batch * pps + 1) * oracle.page_bytes(okind_i), np.uint8)
     for b in range(batch):
         oracle.page_write(0, comp_o, comp_bt[b], *ent_m[b], nope_dim=nope_m)
-        oracle.page_write(1, idx_o, idx_bt[b], *ent_i[b], nope_dim=64)
+        oracle.page_write(okind_i, idx_o, idx_bt[b], *ent_i[b], nope_dim=64)
 
     # SWA cache: rows of tokens max(0, L0 - 128) .. T - 1 (the windows of every step)
     swa_lp = (Tmax + 63) // 64
@@ -159,13 +173,16 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
         for b in range(batch):
             if st["boundary"][b]:
                 j = int(st["p"][b]) // 4
-                qi[b, :, :] = ent_i[b][0][j]
+                qi[b, :, :] = (ent_i[b][0][j] if not idx_fp4 else
+                               oracle.f32_to_e4m3(idx_key_values(ent_i[b][0][j], ent_i[b][1][j], True)
+                                                  .astype(np.float32) * 8.0))
                 q[b, :, :nope_m] = dequant_nope(ent_m[b][0][j], ent_m[b][1][j], nope_m).astype(np.float32)
         st["qi"], st["w"], st["q"] = qi, wq, bf16_bits(q)
         steps.append(st)
 
     # ---- GPU
-    plan = B.Plan(B.C4A, H, batch, k, Tmax, idx_heads=HI, kv_layout=B.KV_V4 if v4 else B.KV_576)
+    plan = B.Plan(B.C4A, H, batch, k, Tmax, idx_heads=HI, kv_layout=B.KV_V4 if v4 else B.KV_576,
+                  idx_format=B.IDX_FP4 if idx_fp4 else B.IDX_FP8)
     ws = plan.workspace()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     comp = torch.zeros(comp_o.size, dtype=torch.uint8, device="cuda")
@@ -177,7 +194,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
     seqs = dev(np.arange(batch, dtype=np.int32))
     if prefill == "stream":
         for kind, ks, ape, w, st, cache, bt in ((kind_m, ks_m, t_ape_m, t_w_m, st_m, comp, t_comp_bt),
-                                                (B.CACHE_IDX, ks_i, t_ape_i, t_w_i, st_i, idxc, t_idx_bt)):
+                                                (kind_i, ks_i, t_ape_i, t_w_i, st_i, idxc, t_idx_bt)):
             rows, ps, sq = [], [], []
             for b in range(batch):
                 rows.append(ks[b][:L0[b]])
@@ -193,7 +210,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
         part_i = np.zeros_like(idx_o)
         for b in range(batch):
             oracle.page_write(0, part_c, comp_bt[b], ent_m[b][0][:n0[b]], ent_m[b][1][:n0[b]], nope_dim=nope_m)
-            oracle.page_write(1, part_i, idx_bt[b], ent_i[b][0][:n0[b]], ent_i[b][1][:n0[b]], nope_dim=64)
+            oracle.page_write(okind_i, part_i, idx_bt[b], ent_i[b][0][:n0[b]], ent_i[b][1][:n0[b]], nope_dim=64)
         comp.copy_(dev(part_c))
         idxc.copy_(dev(part_i))
         ring_m = np.zeros((batch, 8, 4 * D_MAIN), np.float32)
@@ -227,7 +244,7 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
                 dict(kind=kind_m, ratio=4, kv_score=x["kvm"], positions=x["pos"], seqs=seqs, ape=t_ape_m,
                      rms_weight=t_w_m, rms_eps=EPS, cos_sin=t_cs, state=st_m, cache=comp, block_table=t_comp_bt,
                      num_seqs=batch, status=status),
-                dict(kind=B.CACHE_IDX, ratio=4, kv_score=x["kvi"], positions=x["pos"], seqs=seqs, ape=t_ape_i,
+                dict(kind=kind_i, ratio=4, kv_score=x["kvi"], positions=x["pos"], seqs=seqs, ape=t_ape_i,
                      rms_weight=t_w_i, rms_eps=EPS, cos_sin=t_cs, state=st_i, cache=idxc, block_table=t_idx_bt,
                      num_seqs=batch, status=status))
             B.indexer_topk(plan, x["qi"], x["w"], idxc, t_idx_bt, x["ctx"], x["idx"], x["len"], ws, status)
@@ -261,7 +278,8 @@ def run_chain(batch, L0, n_steps, H, HI, k, seed, prefill, graph=True, v4=False)
         def check(b):
             p = int(st["p"][b])
             n_c = (p + 1) // 4
-            logits = oracle.indexer_logits(st["qi"][b], st["w"][b], idx_o, idx_bt[b], n_c)
+            f = oracle.indexer_logits_fp4 if idx_fp4 else oracle.indexer_logits
+            logits = f(st["qi"][b], st["w"][b], idx_o, idx_bt[b], n_c)
             tol = check_topk(gidx[b], int(glen[b]), logits, k)
             if st["boundary"][b]:
                 assert p // 4 in set(gidx[b][:glen[b]].tolist()), "step %d seq %d: new slot not selected" % (s, b)

@@ -160,20 +160,22 @@ def test_bad_block_table_is_flagged_not_faulted():
 
 
 @pytest.mark.parametrize("case", ["b4_streamed_prefill", "c4a_32k_b32", "b4_streamed_prefill_v4",
-                                  "c4a_32k_b32_v4"])
+                                  "c4a_32k_b32_v4", "b4_streamed_prefill_fp4", "c4a_32k_b32_fp4"])
 def test_bench_call_chain_under_dependent_launch(case):
     """The benchmark's decode loop (compress pair -> indexer + top-k -> sparse
     MLA under programmatic dependent launch, captured in a CUDA graph; in the
-    V4-native geometry followed by the inverse RoPE + FP8 output quant) over
+    V4-native geometry followed by the inverse RoPE + FP8 output quant; with
+    the MXFP4 indexer cache) over
     steps that include ratio-4 boundaries: the slot a step's compressor emits
     is selected by that step's indexer and dominates its attention, and every
     cache byte, top-k set and output matches the oracle."""
     from _chain import run_chain
-    v4 = case.endswith("_v4")
+    v4, fp4 = case.endswith("_v4"), case.endswith("_fp4")
     if case.startswith("b4_streamed_prefill"):
-        tol, nb = run_chain(4, [1021, 2046, 517, 3072], 6, 64, 64, 64, seed=51, prefill="stream", v4=v4)
+        tol, nb = run_chain(4, [1021, 2046, 517, 3072], 6, 64, 64, 64, seed=51, prefill="stream", v4=v4,
+                            idx_fp4=fp4)
     else:
-        tol, nb = run_chain(32, 32763, 5, 64, 64, 512, seed=52, prefill="direct", v4=v4)
+        tol, nb = run_chain(32, 32763, 5, 64, 64, 512, seed=52, prefill="direct", v4=v4, idx_fp4=fp4)
     assert nb > 0
     print("boundary steps checked:", nb, "near-tie slots tolerated:", tol)
 
