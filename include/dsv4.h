@@ -11,7 +11,12 @@
  *       IndexCache reuse layers).  c128a layers pass precomputed indices.
  *   (3) dsv4_sparse_mla_decode : absorbed-MQA attention of every query head
  *       over (selected compressed slots) || (SWA window), one 576-dim latent
- *       KV head, value = the first 512 dims.
+ *       KV head, value = the first 512 dims (or, with the V4-native layout,
+ *       one 512-dim head that is key and value, and optionally the output's
+ *       inverse RoPE + FP8 quantisation, dsv4_inv_rope_fp8_quant).
+ *   (4) prefill: the same indexer and attention with one query row per
+ *       prefill token (dsv4_sparse_mla_prefill), plus the pages' dense-buffer
+ *       helpers (dsv4_dequant_gather, dsv4_combine_topk_swa_indices).
  *
  * Sources (page title, section):
  *   [vLLM-V4-attn]  "DeepSeek V4 attention in vLLM" (juejin): compress_ratio
@@ -38,9 +43,11 @@
  *     skip the offending access and OR a bit into the caller's device status
  *     word (int, may be NULL); dsv4_read_device_status() reads and clears it.
  *     No call traps, asserts or aborts; nothing throws across the ABI.
- *   - Geometry is fixed by this build: latent 512 (nope) + 64 (rope) = 576
- *     dims, value = 512 latent dims, pages of 64 entries / tokens, indexer
- *     head dim 128, SWA window 128.
+ *   - Geometry: latent 512 (nope) + 64 (rope) = 576 dims, value = 512 latent
+ *     dims by default, or the V4-native 448 + 64 rows with K = V per plan
+ *     (dsv4_plan_set_kv_layout); pages of 64 entries / tokens, indexer head
+ *     dim 128 (FP8 or MXFP4 entries, dsv4_plan_set_indexer_format), SWA
+ *     window 128.
  *
  * Cache layouts in HBM (all pages 64 entries; page id from a block table):
  *   compressed (main) cache page, 64 * 648 = 41472 bytes:
