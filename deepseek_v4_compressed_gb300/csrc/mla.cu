@@ -593,6 +593,13 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (lane == 0) tc::mbar_arrive(tc::smem_u32(&kv_full[kst]));
                 if (jc + 1 < n_comp_mine) fetch(jc + 1);
             }
+            // every load of the selected rows is done: a kernel launched next
+            // (programmatic dependent launch; the library's compressor, which
+            // waits for this grid's completion before it reads or writes
+            // anything) may now be scheduled while the last tile and the
+            // merge run.  Every grid before this one is complete: the
+            // producers passed griddepcontrol.wait.
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         } else {
             // ------------------------------------------- softmax + O correction
             // Head h = 16*warp + lane % 16 (S row in TMEM lane 32*warp + lane % 16);
