@@ -65,7 +65,7 @@ WORKLOADS = {
 # capture of this workload (one launch, cold cache), with the sha256 of the
 # sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
-    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19090432 + 0, "src_sha": "1a7cefe100b7c33c"},
+    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19091200 + 0, "src_sha": "ec59f41c9c3016e3"},
 }
 
 
