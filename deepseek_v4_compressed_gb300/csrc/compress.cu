@@ -361,13 +361,18 @@ __global__ void __launch_bounds__(kind_dim<MAIN_KIND>() / 2) compress_pair_kerne
             asm volatile("prefetch.global.L2 [%0];" ::"l"(Pi.bt + static_cast<long long>(b) * Pi.bt_stride +
                                                           threadIdx.x * 32));
     }
-    // launched behind the previous kernel of the stream (programmatic
-    // dependent launch): its outputs may be this kernel's inputs.  The
-    // indexer launched next may start once every CTA is past this wait: by
-    // then every earlier kernel is complete, and this one writes at most the
-    // newest entry of each sequence (the indexer reads the other slots early).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The indexer launched next may be scheduled at once: it reads only
+    // caller inputs and its cache's older slots before its own dependency
+    // wait, and this kernel writes at most the newest entry of each sequence.
+    // The kernel before this one may still be running: when it is the
+    // library's attention, it let this kernel launch only after every one of
+    // its CTAs had read its index rows and gathered its keys, and it writes
+    // nothing the indexer reads (its output and lse), so the indexer's
+    // writes (indices, logits) cannot race with it.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launched behind the previous kernel of the stream (programmatic
+    // dependent launch): its outputs may be this kernel's inputs
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (static_cast<int>(blockIdx.x) < Pm.num_tokens)
         compress_token<kind_dim<MAIN_KIND>(), RATIO, MAIN_KIND, true>(Pm, blockIdx.x);
     else if (threadIdx.x < kIdx / 2)

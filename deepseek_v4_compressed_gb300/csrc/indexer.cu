@@ -473,12 +473,13 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
     // This kernel may overlap the one before it (programmatic dependent
     // launch).  When that is the library's decode compressor, it writes at
     // most the newest entry of each sequence (slot n_c - 1, in the last tile),
-    // and every kernel before it is complete (the library's compressors let
-    // their dependents start only once those are); a caller kernel in between
-    // does not let this one start early.  So the tiles before the last are
-    // read at once, and the wait for the previous grid comes right before the
-    // last tile's loads -- and in every CTA, so that this grid completes only
-    // after it.
+    // and the kernel before it, when it may still run, is the library's
+    // attention, which writes nothing read here and had read its index rows
+    // before it let the compressor launch; a caller kernel in between does
+    // not let this one start early.  So the tiles before the last are read
+    // at once, and the wait for the previous grid (which completes only after
+    // its own predecessors) comes right before the last tile's loads -- and
+    // in every CTA, so that this grid completes only after it.
     //
     // Producer warp 8 sets up the barriers and, before the block-wide barrier,
     // issues the query's and the first kIdxStages tiles' loads (no stage has
