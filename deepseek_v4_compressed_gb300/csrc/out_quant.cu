@@ -35,6 +35,11 @@ struct InvRopeQuantParams {
 
 __global__ void __launch_bounds__(32 * 4 * kOqRowsPerCta) inv_rope_fp8_quant_kernel(InvRopeQuantParams Q)
 {
+    // launched under programmatic dependent launch behind the kernel that
+    // writes o: the next kernel may be scheduled now, and this one waits for
+    // its predecessor before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = static_cast<long long>(blockIdx.x) * kOqRowsPerCta + (warp >> 2);
     if (row >= Q.rows) return;
@@ -87,8 +92,16 @@ cudaError_t launch_inv_rope_quant(const uint16_t* o, int num_tokens, int n_heads
     if (Q.rows == 0) return cudaSuccess;
     const long long ctas = (Q.rows + kOqRowsPerCta - 1) / kOqRowsPerCta;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    inv_rope_fp8_quant_kernel<<<static_cast<unsigned>(ctas), 32 * 4 * kOqRowsPerCta, 0, stream>>>(Q);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(32 * 4 * kOqRowsPerCta, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, inv_rope_fp8_quant_kernel, Q);
 }
 
 }  // namespace dsv4
