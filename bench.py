@@ -56,6 +56,11 @@ WORKLOADS = {
                            window=128, ratio=4, v4=True),
     "c128a_128k_b64_v4": dict(name="c128a_128k_b64_v4", batch=64, context=131072, n_heads=64, idx_heads=0,
                               topk=512, window=128, ratio=128, v4=True),
+    # sparse prefill: 4 sequences, each a 256-token chunk at the end of a 32K
+    # context (1024 query rows), through the multi-token compressors, the
+    # per-row indexer + top-k and the sparse prefill attention
+    "prefill_c4a_32k_b4_c256": dict(name="prefill_c4a_32k_b4_c256", batch=4, context=32768, n_heads=64,
+                                    idx_heads=64, topk=512, window=128, ratio=4, chunk=256),
     # 60-layer stack (swaonly / c4a / c128a), IndexCache freq 2 against freq 1
     "mixed60_b16": dict(name="mixed60_b16", batch=16, context=65536, n_heads=64, idx_heads=64, topk=512,
                         window=128, ratio=0),
@@ -889,6 +894,186 @@ def mixed_stack_bench(args, w):
     return 0
 
 
+def load_tensor_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s): the burst figure and
+    its source."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def prefill_bench(args, w):
+    """Sparse prefill of one c4a layer: each of B sequences appends a chunk of
+    C tokens at the end of its context (C*B query rows).  One step = the
+    multi-token compressor insert of both streams for the chunk, the indexer
+    + top-k of every chunk token over the slots visible at its position, and
+    the sparse prefill attention of every chunk token over its own selection
+    and window (rows mapped to their sequences).  2 layer instances rotated
+    (the query rows alone are 38 MB a layer).  Prints one JSON line."""
+    from deepseek_v4_compressed_gb300 import binding as Bd
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    Bsz, L, Cn, H, HI, k = w["batch"], w["context"], w["chunk"], w["n_heads"], w["idx_heads"], w["topk"]
+    T = Bsz * Cn
+    R = 2
+    g = torch.Generator(device=device)
+    g.manual_seed(21)
+    n_c = L // 4
+    lp_c = (n_c + 63) // 64
+    lp_s = (L + 63) // 64
+    pos = torch.arange(L - Cn, L, dtype=torch.int32, device=device).repeat(Bsz)          # sequence-major rows
+    seqs = torch.arange(Bsz, dtype=torch.int32, device=device).repeat_interleave(Cn)
+    ctx = (pos + 1).contiguous()
+    cos_sin = Bd.rope_table(L + 1).to(device)
+    plan = Bd.Plan(Bd.C4A, H, T, k, L, idx_heads=HI, window=w["window"])
+    ws = plan.workspace(device)
+    layers = []
+    for li in range(R):
+        Ly = LayerInstance()
+        Ly.comp_bt = torch.randperm(Bsz * lp_c, generator=g, device=device).to(torch.int32).view(Bsz, lp_c)
+        Ly.idx_bt = torch.randperm(Bsz * lp_c, generator=g, device=device).to(torch.int32).view(Bsz, lp_c)
+        Ly.comp = torch.zeros(Bsz * lp_c * Bd.MLA_PAGE_BYTES, dtype=torch.uint8, device=device)
+        Ly.idx = torch.zeros(Bsz * lp_c * Bd.IDX_PAGE_BYTES, dtype=torch.uint8, device=device)
+        for b in range(Bsz):
+            seq = torch.full((n_c,), b, dtype=torch.int32, device=device)
+            slot = torch.arange(n_c, dtype=torch.int32, device=device)
+            Bd.cache_insert_rows(Bd.CACHE_MLA, torch.randn((n_c, 576), generator=g, device=device) / math.sqrt(576),
+                                 seq, slot, Ly.comp, Ly.comp_bt)
+            Bd.cache_insert_rows(Bd.CACHE_IDX, torch.randn((n_c, 128), generator=g, device=device) / math.sqrt(128),
+                                 seq, slot, Ly.idx, Ly.idx_bt)
+        # SWA pages for the chunk and the window before it
+        lp0 = (L - Cn - w["window"]) // 64
+        n_sp = lp_s - lp0
+        Ly.swa_bt = torch.full((Bsz, lp_s), -1, dtype=torch.int32, device=device)
+        Ly.swa_bt[:, lp0:] = torch.randperm(Bsz * n_sp, generator=g, device=device).to(torch.int32).view(Bsz, n_sp)
+        Ly.swa = (torch.randn((Bsz * n_sp * 64, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+        Ly.state_main = torch.zeros((Bsz, 8, 4 * 576), dtype=torch.float32, device=device)
+        Ly.state_idx = torch.zeros((Bsz, 8, 4 * 128), dtype=torch.float32, device=device)
+        Ly.ape_main = torch.randn((4, 2 * 576), generator=g, device=device) * 0.1
+        Ly.ape_idx = torch.randn((4, 2 * 128), generator=g, device=device) * 0.1
+        Ly.rms_main = torch.ones(576, device=device)
+        Ly.rms_idx = torch.ones(128, device=device)
+        Ly.kv_main = torch.randn((T, 4 * 576), generator=g, device=device).to(torch.bfloat16)
+        Ly.kv_idx = torch.randn((T, 4 * 128), generator=g, device=device).to(torch.bfloat16)
+        Ly.q = (torch.randn((T, H, 576), generator=g, device=device) / math.sqrt(576)).to(torch.bfloat16)
+        Ly.qi = torch.randn((T, HI, 128), generator=g, device=device).to(torch.float8_e4m3fn).view(torch.uint8)
+        Ly.wts = torch.rand((T, HI), generator=g, device=device)
+        Ly.out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+        Ly.lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        layers.append(Ly)
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
+    topk_len = torch.empty((T,), dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def stage_calls(Ly):
+        return [
+            lambda: (Bd.compress_insert(Bd.CACHE_MLA, 4, Ly.kv_main, pos, seqs, Ly.ape_main, Ly.rms_main, 1e-6, cos_sin,
+                                        Ly.state_main, Ly.comp, Ly.comp_bt, Bsz, one_token_per_seq=False,
+                                        status=status),
+                     Bd.compress_insert(Bd.CACHE_IDX, 4, Ly.kv_idx, pos, seqs, Ly.ape_idx, Ly.rms_idx, 1e-6, cos_sin,
+                                        Ly.state_idx, Ly.idx, Ly.idx_bt, Bsz, one_token_per_seq=False,
+                                        status=status)),
+            lambda: Bd.indexer_topk(plan, Ly.qi, Ly.wts, Ly.idx, Ly.idx_bt, ctx, topk_idx, topk_len, ws, status,
+                                    row_seq=seqs),
+            lambda: Bd.sparse_mla_prefill(plan, Ly.q, Ly.swa, Ly.swa_bt, ctx, seqs, Ly.out, ws, comp_cache=Ly.comp,
+                                          comp_block_table=Ly.comp_bt, topk_idx=topk_idx, topk_len=topk_len,
+                                          lse=Ly.lse, status=status),
+        ]
+
+    def run(n, which=None):
+        for i in range(n):
+            for si, c in enumerate(stage_calls(layers[i % R])):
+                if which is None or si == which:
+                    c()
+
+    W = max(args.warmup, 3)
+    run(W)
+    torch.cuda.synchronize()
+    st, bits = Bd.read_device_status(status)
+    if st != Bd.OK:
+        raise RuntimeError("device status %s (bits 0x%x)" % (Bd.status_string(st), bits))
+    K = max(4, min(args.steps, 16))
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        run(K)
+    gr.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 4
+    e0.record()
+    for _ in range(reps):
+        gr.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), device) / (reps * K)
+    t_end = time.time() + max(0.0, args.sustain_s - ms * reps * K / 1e3)
+    while time.time() < t_end:
+        gr.replay()
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    names = ["compress", "indexer_topk", "sparse_mla"]
+    stages = {}
+    for si, nm in enumerate(names):
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs):
+            run(K, si)
+        gs.replay()
+        torch.cuda.synchronize()
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gs.replay()
+        b2.record()
+        torch.cuda.synchronize()
+        stages[nm] = a.elapsed_time(b2) / K
+    st, bits = Bd.read_device_status(status)
+    if st != Bd.OK:
+        raise RuntimeError("device status %s (bits 0x%x)" % (Bd.status_string(st), bits))
+    # tensor work: the indexer's FP8 products over every row's visible slots,
+    # the attention's bf16 products (S = Q K^T over 576 dims, O = P V over 512)
+    p_rows = torch.arange(L - Cn, L, dtype=torch.float64)
+    slots = torch.floor((p_rows + 1) / 4)
+    idx_flops = float(Bsz * slots.sum() * HI * 128 * 2)
+    keys = torch.clamp(slots, max=k) + torch.clamp(p_rows + 1, max=w["window"])
+    mla_flops = float(Bsz * keys.sum() * H * (576 + 512) * 2)
+    bf16_peak, peak_kind = load_tensor_peak()
+    rooflines = {"indexer_topk": (idx_flops, 2 * bf16_peak, "fp8 (2 x the measured bf16 peak)"),
+                 "sparse_mla": (mla_flops, bf16_peak, "bf16")}
+    dom = max(["indexer_topk", "sparse_mla"], key=lambda nm: stages[nm])
+    fl, pk, pk_kind = rooflines[dom]
+    achieved = fl / (stages[dom] / 1e3) / 1e12
+    line = {
+        "metric": "prefill tokens/s per layer (C4A, 32K ctx, 4 x 256-token chunks)", "value": world * T / (ms / 1e3),
+        "unit": UNIT, "n_gpus": world, "steps": K * reps, "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8+bf16", "data": "synthetic",
+        "config": {"workload": w["name"], "sequences": Bsz, "context": L, "chunk": Cn, "query_rows": T, "heads": H,
+                   "idx_heads": HI, "topk": k, "window": w["window"], "layers_rotated": R,
+                   "timing": "CUDA graph replay of K whole steps, CUDA events", "parallelism": "replicas x%d" % world},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                     "frac": achieved / pk, "traffic": None,
+                     "peak_source": "%s %s tensor peak (MEASURED_PEAKS.json bf16_tflops)" % (peak_kind, pk_kind),
+                     "flops_per_step": fl},
+        "stages_ms": stages, "indexer_flops_per_step": idx_flops, "attention_flops_per_step": mla_flops,
+        "gpu_launches": K * reps * (4 + plan.info()["launches_indexer"] + plan.info()["launches_mla"]),
+        "clocks": clk, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def reference_arm(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -950,6 +1135,8 @@ def main():
 
     if w["name"] == "mixed60_b16":
         return mixed_stack_bench(args, w)
+    if w["name"].startswith("prefill"):
+        return prefill_bench(args, w)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
