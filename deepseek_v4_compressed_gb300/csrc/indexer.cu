@@ -1211,22 +1211,61 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_small_kernel(
 // st.async pushes on the receivers' mbarriers, keys equal to the threshold
 // taken lowest slot first, slots written in ascending order -- with warp-
 // private histograms (a pass over 32768 keys would otherwise serialise on the
-// shared-memory atomics of its most crowded bins).
+// shared-memory atomics of its most crowded bins).  Clusters of up to 4 CTAs
+// push every CTA's whole histogram to every CTA (one round, C KB in per CTA);
+// larger ones sum a pass's histograms by a reduce-scatter and an all-gather:
+// CTA q owns digits [q nb, q nb + nb), every CTA sends each owner its counts
+// of the owner's digits, and each owner sends the cluster's sums of its digits
+// to every CTA (two rounds of about 1 KB in and out per CTA).
+//
+// Candidate list: the second pass, which scans every key anyway, also writes
+// the local index of each key at or above the first pass's threshold bin (the
+// keys still in play and the ones already taken) into a per-warp list, warp w
+// covering the w-th run of the CTA's slots in slot order.  Later passes and
+// the compaction walk that list instead of all S keys; a CTA whose list would
+// overflow its capacity keeps scanning all of its keys (every count is the
+// same either way, so the CTAs of a cluster may differ in this).
 // ---------------------------------------------------------------------------
 constexpr int kTkcSlots = 32768;                 // keys per CTA at most
 constexpr int kTkcWarps = kTopkThreads / 32;     // 16
 constexpr int kTkcMaxCluster = 16;               // CTAs per query (above 8: a non-portable cluster size)
+constexpr int kTkcA2aMax = 4;                   // largest cluster that exchanges whole histograms
+// digits owned by each CTA of a cluster of C: a multiple of 4 (16-byte pushes)
+__host__ __device__ constexpr int tkc_digits_per_owner(int C) { return ((256 + C - 1) / C + 3) & ~3; }
+constexpr int tkc_rs_entries()
+{
+    int m = 0;
+    for (int c = 1; c <= kTkcMaxCluster; ++c) m = m > c * tkc_digits_per_owner(c) ? m : c * tkc_digits_per_owner(c);
+    return m;
+}
 struct TkcScratch {
-    uint64_t bar_mm, bar_h[2], bar_cnt;
+    uint64_t bar_mm, bar_rs[2], bar_ag[2], bar_cnt;
     uint32_t mm_in[kTkcMaxCluster][2];
     int cnt_in[kTkcMaxCluster][2];
-    alignas(16) int hin[2][kTkcMaxCluster][256];
+    alignas(16) int hin[2][kTkcA2aMax][256];     // CTA q's histogram (small clusters), by pass parity
+    alignas(16) int rs_in[2][tkc_rs_entries()];  // CTA r's counts of this CTA's digits at r nb, by pass parity
+    alignas(16) int ag_in[2][256];               // the cluster's count of every digit, by pass parity
+    alignas(16) int seg[256];                    // the cluster's counts of this CTA's digits
     alignas(16) int whist[kTkcWarps][256];
     alignas(16) int hist[256];
     int wsum[kTkcWarps][2];
+    int lcnt[kTkcWarps];                         // candidates found by each warp
     uint32_t mm[2];
     CtkDecision dec;
 };
+// entries of one warp's candidate list: the warp's whole run of slots up to
+// 16384 keys per CTA, half of it above (the shared-memory budget)
+__host__ __device__ constexpr int tkc_list_cap(int S)
+{
+    return S <= 16384 ? ((S + kTkcWarps - 1) / kTkcWarps + 31) & ~31
+                      : (((S + kTkcWarps - 1) / kTkcWarps + 31) & ~31) / 2;
+}
+__host__ __device__ constexpr size_t tkc_smem_bytes(int S)
+{
+    return static_cast<size_t>(S) * 4 + static_cast<size_t>(kTkcWarps) * tkc_list_cap(S) * 2 + sizeof(TkcScratch);
+}
+static_assert(tkc_smem_bytes(kTkcSlots) <= 232448 && tkc_smem_bytes(16384) <= tkc_smem_bytes(kTkcSlots),
+              "the largest S sets the shared-memory attribute");
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
     const float* logits, int row_stride, int max_slots, const int* __restrict__ ctx_len, int k, int S,
@@ -1235,13 +1274,17 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(16) uint32_t tkc_smem[];
     uint32_t* keys = tkc_smem;                                       // [S]
-    TkcScratch* T = reinterpret_cast<TkcScratch*>(tkc_smem + S);     // S is a multiple of 32
+    const int LC = tkc_list_cap(S);                                  // a multiple of 32
+    uint16_t* list = reinterpret_cast<uint16_t*>(tkc_smem + S);      // [kTkcWarps][LC]
+    TkcScratch* T = reinterpret_cast<TkcScratch*>(list + kTkcWarps * LC);   // S is a multiple of 32
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int C = static_cast<int>(gridDim.x), rank = static_cast<int>(blockIdx.x), b = blockIdx.y;
     if (tid == 0) {
         tc::mbar_init(tc::smem_u32(&T->bar_mm), 1);
-        tc::mbar_init(tc::smem_u32(&T->bar_h[0]), 1);
-        tc::mbar_init(tc::smem_u32(&T->bar_h[1]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_rs[0]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_rs[1]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_ag[0]), 1);
+        tc::mbar_init(tc::smem_u32(&T->bar_ag[1]), 1);
         tc::mbar_init(tc::smem_u32(&T->bar_cnt), 1);
         T->mm[0] = 0xffffffffu;
         T->mm[1] = 0u;
@@ -1266,7 +1309,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         }
         return;
     }
-    // keys of this CTA's slots (s0 and the row stride are multiples of 4)
+    // keys of this CTA's slots (s0, the row stride and the workspace base are
+    // 16-byte aligned)
     const float* lrow = logits + static_cast<long long>(b) * row_stride + s0;
     uint32_t mn = 0xffffffffu, mx = 0u;
     const int n4 = nl >> 2;                          // whole float4 groups, 4 loads in flight per thread
@@ -1314,49 +1358,156 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
     int plo = 32;
     uint32_t prefix = 0;
     int rem = k;
+    // warp w's run of this CTA's slots: [w0, w1)
+    const int R = ((nl + kTkcWarps - 1) / kTkcWarps + 31) & ~31;
+    const int w0 = min(nl, warp * R), w1 = min(nl, w0 + R);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint16_t* wl = list + warp * LC;
+    int wl_n = 0;                   // this warp's candidates (valid once use_list)
+    bool use_list = false;          // the same in every thread of the CTA
+    const bool a2a = C <= kTkcA2aMax;
+    const int nb = tkc_digits_per_owner(C);
+    const int my_nb = a2a ? 0 : max(0, min(256, (rank + 1) * nb) - rank * nb);   // digits this CTA owns
     for (int pass = 0;; ++pass) {
         const int p = pass & 1;
-        for (int i = tid; i < kTkcWarps * 256; i += kTopkThreads) (&T->whist[0][0])[i] = 0;
+        const bool listed = use_list;
+        const bool build = pass == 1;
+        if (listed) {
+            if (tid < 256) T->hist[tid] = 0;
+        } else {
+            for (int i = tid; i < kTkcWarps * 256; i += kTopkThreads) (&T->whist[0][0])[i] = 0;
+        }
         __syncthreads();
-        int* wh = T->whist[warp];
         // keys in play: (key - base) >> plo == prefix >> plo, i.e. key - lo_key <
         // 2^plo with lo_key = base + the prefix's bits at and above plo (every
-        // key in the first pass); their digit is (key - lo_key) >> lo.  Keys
-        // are read four at a time (nl4 whole groups, then the tail).
+        // key in the first pass); their digit is (key - lo_key) >> lo.
         const uint32_t lo_key = base + (plo == 32 ? 0u : (prefix >> plo) << plo);
         const uint32_t span_m1 = plo == 32 ? 0xffffffffu : (1u << plo) - 1u;
-        const int nl4 = nl >> 2;
-#pragma unroll 2
-        for (int i4 = tid; i4 < nl4; i4 += kTopkThreads) {
-            const uint4 kv = reinterpret_cast<const uint4*>(keys)[i4];
-            const uint32_t o0 = kv.x - lo_key, o1 = kv.y - lo_key, o2 = kv.z - lo_key, o3 = kv.w - lo_key;
-            if (o0 <= span_m1) atomicAdd(&wh[(o0 >> lo) & 255u], 1);
-            if (o1 <= span_m1) atomicAdd(&wh[(o1 >> lo) & 255u], 1);
-            if (o2 <= span_m1) atomicAdd(&wh[(o2 >> lo) & 255u], 1);
-            if (o3 <= span_m1) atomicAdd(&wh[(o3 >> lo) & 255u], 1);
-        }
-        for (int i = 4 * nl4 + tid; i < nl; i += kTopkThreads) {
-            const uint32_t o = keys[i] - lo_key;
-            if (o <= span_m1) atomicAdd(&wh[(o >> lo) & 255u], 1);
-        }
-        __syncthreads();
-        if (tid < 256) {
-            int acc = 0;
+        if (listed) {
+            // few keys: one histogram for the CTA
+            for (int j = lane; j < wl_n; j += 32) {
+                const uint32_t o = keys[wl[j]] - lo_key;
+                if (o <= span_m1) atomicAdd(&T->hist[(o >> lo) & 255u], 1);
+            }
+        } else if (build) {
+            // the warp's run 128 keys at a time (slot order = 32 u + lane):
+            // histogram of the keys in play, and every key >= lo_key appended
+            // to the warp's list in slot order
+            int* wh = T->whist[warp];
+            int cnt = 0;
+            for (int i0 = w0; i0 < w1; i0 += 128) {
+                uint32_t kk[4];
 #pragma unroll
-            for (int w = 0; w < kTkcWarps; ++w) acc += T->whist[w][tid];
-            T->hist[tid] = acc;
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + 32 * u + lane;
+                    kk[u] = i < w1 ? keys[i] : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + 32 * u + lane;
+                    const bool v = i < w1;
+                    const uint32_t o = kk[u] - lo_key;
+                    if (v && o <= span_m1) atomicAdd(&wh[(o >> lo) & 255u], 1);
+                    const uint32_t bal = __ballot_sync(0xffffffffu, v && kk[u] >= lo_key);
+                    if (bal) {
+                        const int at = cnt + __popc(bal & lt);
+                        if (((bal >> lane) & 1u) && at < LC) wl[at] = static_cast<uint16_t>(i);
+                        cnt += __popc(bal);
+                    }
+                }
+            }
+            wl_n = cnt;
+            if (lane == 0) T->lcnt[warp] = cnt;
+        } else {
+            // every key, four at a time (nl4 whole groups, then the tail)
+            int* wh = T->whist[warp];
+            const int nl4 = nl >> 2;
+#pragma unroll 2
+            for (int i4 = tid; i4 < nl4; i4 += kTopkThreads) {
+                const uint4 kv = reinterpret_cast<const uint4*>(keys)[i4];
+                const uint32_t o0 = kv.x - lo_key, o1 = kv.y - lo_key, o2 = kv.z - lo_key, o3 = kv.w - lo_key;
+                if (o0 <= span_m1) atomicAdd(&wh[(o0 >> lo) & 255u], 1);
+                if (o1 <= span_m1) atomicAdd(&wh[(o1 >> lo) & 255u], 1);
+                if (o2 <= span_m1) atomicAdd(&wh[(o2 >> lo) & 255u], 1);
+                if (o3 <= span_m1) atomicAdd(&wh[(o3 >> lo) & 255u], 1);
+            }
+            for (int i = 4 * nl4 + tid; i < nl; i += kTopkThreads) {
+                const uint32_t o = keys[i] - lo_key;
+                if (o <= span_m1) atomicAdd(&wh[(o >> lo) & 255u], 1);
+            }
         }
         __syncthreads();
-        if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_h[p]), static_cast<uint32_t>(C * 1024));
-        if (tid < 64) {
-            const uint4 h4 = *reinterpret_cast<const uint4*>(&T->hist[4 * tid]);
-            for (int q = 0; q < C; ++q)
-                tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&T->hin[p][rank][4 * tid]), q), h4,
-                                   tc::map_to_rank(tc::smem_u32(&T->bar_h[p]), q));
+        if (build) {
+            int mx_n = 0;
+#pragma unroll
+            for (int w = 0; w < kTkcWarps; ++w) mx_n = max(mx_n, T->lcnt[w]);
+            use_list = mx_n <= LC;
         }
-        if (warp == 0) {
-            const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_h[p]), (pass >> 1) & 1, status);
-            ctk_decide(T->hin[p], C, ok, prefix, lo, rem, pass, &T->dec);
+        if (!listed) {
+            if (tid < 256) {
+                int acc = 0;
+#pragma unroll
+                for (int w = 0; w < kTkcWarps; ++w) acc += T->whist[w][tid];
+                T->hist[tid] = acc;
+            }
+            __syncthreads();
+        }
+        const uint32_t ph = (pass >> 1) & 1;
+        if (a2a) {
+            if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_ag[p]), static_cast<uint32_t>(C * 1024));
+            if (tid < 64) {
+                const uint4 h4 = *reinterpret_cast<const uint4*>(&T->hist[4 * tid]);
+                for (int q = 0; q < C; ++q)
+                    tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&T->hin[p][rank][4 * tid]), q), h4,
+                                       tc::map_to_rank(tc::smem_u32(&T->bar_ag[p]), q));
+            }
+            if (warp == 0) {
+                const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&T->bar_ag[p]), ph, status);
+                ctk_decide(T->hin[p], C, ok, prefix, lo, rem, pass, &T->dec);
+            }
+        } else {
+            if (tid == 0 && my_nb > 0)
+                tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_rs[p]), static_cast<uint32_t>(C * my_nb * 4));
+            if (tid == 32) tc::mbar_arrive_expect_tx(tc::smem_u32(&T->bar_ag[p]), 1024u);
+            if (tid < 64) {
+                // digits 4 tid .. 4 tid + 3 to their owner
+                const int d0 = 4 * tid, q = d0 / nb;
+                const uint4 h4 = *reinterpret_cast<const uint4*>(&T->hist[d0]);
+                tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&T->rs_in[p][rank * nb + d0 - q * nb]), q), h4,
+                                   tc::map_to_rank(tc::smem_u32(&T->bar_rs[p]), q));
+            }
+            if (warp == 0) {
+                bool ok = true;
+                if (my_nb > 0) {
+                    ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(tc::smem_u32(&T->bar_rs[p]), ph, status));
+                    if (ok) {
+                        // the cluster's counts of this CTA's digits (four peers' loads
+                        // in flight at a time), to every CTA
+                        const int* rs = T->rs_in[p];
+                        for (int i = lane; i < my_nb; i += 32) {
+                            int s0 = 0, s1 = 0, s2 = 0, s3 = 0, r = 0;
+                            for (; r + 4 <= C; r += 4) {
+                                s0 += rs[r * nb + i];
+                                s1 += rs[(r + 1) * nb + i];
+                                s2 += rs[(r + 2) * nb + i];
+                                s3 += rs[(r + 3) * nb + i];
+                            }
+                            for (; r < C; ++r) s0 += rs[r * nb + i];
+                            T->seg[i] = (s0 + s1) + (s2 + s3);
+                        }
+                        __syncwarp();
+                        const int n4 = my_nb >> 2;
+                        for (int j = lane; j < n4 * C; j += 32) {
+                            const int dst = j / n4, part = j - dst * n4;
+                            const uint4 v = *reinterpret_cast<const uint4*>(&T->seg[4 * part]);
+                            tc::st_async_u32x4(tc::map_to_rank(tc::smem_u32(&T->ag_in[p][rank * nb + 4 * part]), dst),
+                                               v, tc::map_to_rank(tc::smem_u32(&T->bar_ag[p]), dst));
+                        }
+                    }
+                }
+                ok = ok && tc::mbar_wait_cluster(tc::smem_u32(&T->bar_ag[p]), ph, status);
+                ctk_decide(reinterpret_cast<const int (*)[256]>(T->ag_in[p]), 1, ok, prefix, lo, rem, pass, &T->dec);
+            }
         }
         __syncthreads();
         if (T->dec.failed) return;
@@ -1366,12 +1517,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         if (T->dec.done) break;
         lo = lo > 8 ? lo - 8 : 0;
     }
-    // ordered compaction: warp w walks its range of this CTA's slots 32 keys at a
-    // time; counts per warp, per CTA (pushed to every CTA), then the writes
+    // ordered compaction: warp w walks its run of this CTA's slots (or its
+    // candidate list, in the same order) 32 keys at a time; counts per warp,
+    // per CTA (pushed to every CTA), then the writes
     const uint32_t thr = prefix >> plo;
-    const int R = ((nl + kTkcWarps - 1) / kTkcWarps + 31) & ~31;
-    const int w0 = warp * R, w1 = min(nl, w0 + R);
-    // ballots of 4 consecutive 32-key groups of the warp's range (their keys read
+    // ballots of 4 consecutive 32-key groups of the warp's run (their keys read
     // at once): gb[u] = lanes whose key lies above the threshold bin, eb[u] = in it
     auto groups4 = [&](int i0, uint32_t (&gb)[4], uint32_t (&eb)[4]) {
         uint32_t d[4];
@@ -1388,14 +1538,33 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
             eb[u] = __ballot_sync(0xffffffffu, v[u] && d[u] == thr);
         }
     };
+    // the same for one 32-entry group of the list: lane's slot in i
+    auto group_l = [&](int j0, uint32_t& gb, uint32_t& eb, int& i) {
+        const int j = j0 + lane;
+        const bool v = j < wl_n;
+        i = v ? static_cast<int>(wl[j]) : 0;
+        const uint32_t d = v ? (keys[i] - base) >> plo : 0u;
+        gb = __ballot_sync(0xffffffffu, v && d > thr);
+        eb = __ballot_sync(0xffffffffu, v && d == thr);
+    };
     int wg = 0, we = 0;
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-        uint32_t gb[4], eb[4];
-        groups4(i0, gb, eb);
+    if (use_list) {
+        for (int j0 = 0; j0 < wl_n; j0 += 32) {
+            uint32_t gb, eb;
+            int i;
+            group_l(j0, gb, eb, i);
+            wg += __popc(gb);
+            we += __popc(eb);
+        }
+    } else {
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            uint32_t gb[4], eb[4];
+            groups4(i0, gb, eb);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            wg += __popc(gb[u]);
-            we += __popc(eb[u]);
+            for (int u = 0; u < 4; ++u) {
+                wg += __popc(gb[u]);
+                we += __popc(eb[u]);
+            }
         }
     }
     if (lane == 0) {
@@ -1426,18 +1595,30 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_cluster_kernel(
         g += T->cnt_in[q][0];
         e += T->cnt_in[q][1];
     }
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-        uint32_t gb[4], eb[4];
-        groups4(i0, gb, eb);
+    if (use_list) {
+        for (int j0 = 0; j0 < wl_n; j0 += 32) {
+            uint32_t gb, eb;
+            int i;
+            group_l(j0, gb, eb, i);
+            const int gr = g + __popc(gb & lt), er = e + __popc(eb & lt);
+            if ((gb >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
+            else if (((eb >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
+            g += __popc(gb);
+            e += __popc(eb);
+        }
+    } else {
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            uint32_t gb[4], eb[4];
+            groups4(i0, gb, eb);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = i0 + 32 * u + lane;
-            const int gr = g + __popc(gb[u] & lt), er = e + __popc(eb[u] & lt);
-            if ((gb[u] >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
-            else if (((eb[u] >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
-            g += __popc(gb[u]);
-            e += __popc(eb[u]);
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u + lane;
+                const int gr = g + __popc(gb[u] & lt), er = e + __popc(eb[u] & lt);
+                if ((gb[u] >> lane) & 1u) orow[gr + min(er, rem)] = s0 + i;
+                else if (((eb[u] >> lane) & 1u) && er < rem) orow[gr + er] = s0 + i;
+                g += __popc(gb[u]);
+                e += __popc(eb[u]);
+            }
         }
     }
     if (rank == 0 && tid == 0) out_len[b] = k;
@@ -1458,6 +1639,7 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         return DSV4_ERR_INVALID;
     if (a->out_stride < plan->topk || a->bt_stride < 1 || a->num_pages < 1) return DSV4_ERR_SHAPE;
     if (reinterpret_cast<uintptr_t>(a->idx_cache_dev) & 15) return DSV4_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15) return DSV4_ERR_SHAPE;
     if (a->row_seq_dev && a->bt_rows < 1) return DSV4_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_logits_off);
@@ -1564,7 +1746,7 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
         static PerDeviceOnce tkc_attr;
         if (!tkc_attr.run([] {
                 return cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(kTkcSlots * 4 + sizeof(TkcScratch))) == cudaSuccess &&
+                                            static_cast<int>(tkc_smem_bytes(kTkcSlots))) == cudaSuccess &&
                        cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
                                             1) == cudaSuccess;
             }))
@@ -1576,7 +1758,7 @@ extern "C" dsv4_status dsv4_indexer_topk(const dsv4_plan* plan, const dsv4_index
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(Cq, B, 1);
             cfg.blockDim = dim3(kTopkThreads, 1, 1);
-            cfg.dynamicSmemBytes = static_cast<size_t>(S) * 4 + sizeof(TkcScratch);
+            cfg.dynamicSmemBytes = tkc_smem_bytes(S);
             cfg.stream = st;
             cudaLaunchAttribute attr[2];
             attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -362,9 +362,11 @@ dsv4_status dsv4_cache_insert_rows(const dsv4_insert_rows_args* args, dsv4_strea
  * ctx_len_dev: int32 [batch], 1 <= L <= plan max_ctx;
  * out_idx_dev: int32 [batch][out_stride] (out_stride >= topk);
  * out_len_dev: int32 [batch].
- * workspace: dsv4_plan_workspace_bytes(plan) bytes of device memory.
- * Errors: DSV4_ERR_SHAPE if the plan is not a c4a plan or the workspace is
- *   too small; DSV4_ERR_INVALID for null pointers. */
+ * workspace: dsv4_plan_workspace_bytes(plan) bytes of device memory,
+ *   16-byte aligned.
+ * Errors: DSV4_ERR_SHAPE if the plan is not a c4a plan, the workspace is
+ *   too small or not 16-byte aligned, or idx_cache_dev is not 16-byte
+ *   aligned; DSV4_ERR_INVALID for null pointers. */
 typedef struct dsv4_indexer_args {
     const void* q_fp8_dev;
     const float* weights_dev;

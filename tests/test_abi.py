@@ -146,6 +146,23 @@ def test_fp4_format_and_prefill_entry_points_validate_on_the_host():
     assert lib.dsv4_combine_topk_swa_indices(ctypes.byref(c), None) == B.OK
 
 
+def test_indexer_rejects_misaligned_buffers_on_the_host():
+    """The indexer's cache and its workspace (the top-k bulk-copies logits rows
+    out of it) must be 16-byte aligned; the call refuses before any launch."""
+    lib = B.lib()
+    p = B.Plan(B.C4A, 8, 1, 32, 512, idx_heads=4)
+    ia = B.IndexerArgs()
+    fake = 1 << 20
+    for f in ("q_fp8_dev", "weights_dev", "idx_cache_dev", "block_table_dev", "ctx_len_dev", "out_idx_dev",
+              "out_len_dev"):
+        setattr(ia, f, fake)
+    ia.num_pages, ia.bt_stride, ia.out_stride = 1, 1, 32
+    ws_bytes = p.info()["workspace_bytes"]
+    assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), ctypes.c_void_p(fake + 4), ws_bytes, None) == B.ERR_SHAPE
+    ia.idx_cache_dev = fake + 8
+    assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), ctypes.c_void_p(fake), ws_bytes, None) == B.ERR_SHAPE
+
+
 def test_v4_layout_and_output_quant_validate_on_the_host():
     lib = B.lib()
     p = B.Plan(B.C4A, 8, 2, 32, 4096, idx_heads=8)

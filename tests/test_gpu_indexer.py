@@ -4,9 +4,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from deepseek_v4_compressed_gb300 import binding as B
+from deepseek_v4_compressed_gb300 import synth
 
-from _util import check_topk, make_decode_inputs, oracle_indexer
+from _util import check_topk, dev, make_decode_inputs, oracle_indexer
 
 pytestmark = pytest.mark.gpu
 
@@ -126,6 +128,28 @@ def test_long_rows_cluster_topk_ragged():
     idx, ln = run_indexer(d, max_ctx=131072)
     assert list(ln) == [min(512, int(c) // 4) for c in ctx]
     check_all(d, idx, ln)
+
+
+def test_long_rows_candidate_lists_and_their_overflow():
+    """A 2M-context plan (clusters of 16 CTAs with 32768 keys each, candidate
+    lists of half a warp's run).  Sequence 0 has plain scores.  In sequence 1
+    the first 2048 slots score about 8 times higher: warp 0 of the first CTA
+    finds more candidates than its list holds, so that CTA scans all of its
+    keys while the others walk their lists; the set rule holds for both."""
+    d = make_decode_inputs(4, 2, 2097152, 8, 64, 2048, seed=37, with_comp=False)
+    g = synth.rng(38)
+    n_c = int(d.n_c[1])
+    rows = synth.normal(g, (n_c, 128), 1.0 / np.sqrt(128))
+    rows[:2048] *= 8.0
+    data, sc = oracle.quant_idx_rows(rows)
+    oracle.page_write(oracle.IDX_KIND, d.idx, d.idx_bt[1], data, sc, nope_dim=64)
+    d.t["idx"] = dev(d.idx)
+    plan = B.Plan(B.C4A, d.n_heads, d.batch, d.topk, 2097152, idx_heads=d.idx_heads)
+    assert plan.info()["launches_indexer"] == 2
+    idx, ln = run_indexer(d)
+    assert np.all(ln == 2048)
+    check_all(d, idx, ln)
+    assert np.count_nonzero(idx[1] < 2048) > 1024
 
 
 def test_topk_beyond_the_cluster_range():
