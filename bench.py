@@ -482,8 +482,12 @@ def run_e2e(bench, steps, warmup):
     """The same steps through the public API with host buffers: every step copies
     its inputs host->device and its output device->host inside the timed region.
     As in a serving loop the copies run on their own streams, overlapped with the
-    previous step's kernels: a step's inputs go to one of two device blocks, its
-    kernels wait for them, and its output is read back once its kernels end."""
+    previous step's kernels: a step's inputs go to one of two device blocks, the
+    copy stream then sets that block's flag, and the step's calls start behind
+    dsv4_stream_gate on (that flag, the flag the read-back stream sets once the
+    layer instance's previous output has been read).  The kernels' stream never
+    waits on an event, so each step's first kernel keeps its programmatic launch
+    link to the previous step's last one."""
     Bd = bench.Bd
     host, layout, total, h2d, res_host = make_pinned_inputs(bench)
     dblk = [torch.empty(total, dtype=torch.uint8, device=bench.device) for _ in range(2)]
@@ -498,24 +502,26 @@ def run_e2e(bench, steps, warmup):
     d2h = sum(t.numel() * t.element_size() for t in res_host)
     s_in = torch.cuda.Stream(bench.device)
     s_out = torch.cuda.Stream(bench.device)
+    # flags: inputs landed in block 0 / 1, then per layer instance: its last
+    # output has been read back (set at the start: nothing to read yet)
+    R = len(bench.layers)
+    flags = torch.zeros(2 + R, dtype=torch.int32, device=bench.device)
+    flags[2:] = 1
+    one = torch.ones(1, dtype=torch.int32).pin_memory()
 
     def steps_fn(n):
         s_c = torch.cuda.current_stream(bench.device)   # the kernels' stream (the capture stream in a capture)
         s_in.wait_stream(s_c)
         s_out.wait_stream(s_c)
         read_done = [None, None]            # per device block: its last step's kernels
-        out_read = {}                       # per layer instance: its last read-back
         for i, (r, j) in enumerate(bench.step_order(n)):
             L, b = bench.layers[r], i % 2
             with torch.cuda.stream(s_in):
                 if read_done[b] is not None:
                     s_in.wait_event(read_done[b])
                 dblk[b].copy_(host[r][j], non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(s_in)
-            s_c.wait_event(ev_in)
-            if r in out_read:
-                s_c.wait_event(out_read[r])
+                flags[b:b + 1].copy_(one, non_blocking=True)
+            Bd.stream_gate([flags[b:b + 1], flags[2 + r:3 + r]], status=bench.status)
             for c in bench.calls_for(L, dv[b], j):
                 c()
             ev_c = torch.cuda.Event()
@@ -525,9 +531,7 @@ def run_e2e(bench, steps, warmup):
                 s_out.wait_event(ev_c)
                 for hst, t in zip(res_host, bench.result_tensors(L)):
                     hst.copy_(t, non_blocking=True)
-                ev_o = torch.cuda.Event()
-                ev_o.record(s_out)
-            out_read[r] = ev_o
+                flags[2 + r:3 + r].copy_(one, non_blocking=True)
         s_c.wait_stream(s_in)
         s_c.wait_stream(s_out)
 

@@ -37,7 +37,7 @@ EXPORTED = ["dsv4_version", "dsv4_status_string", "dsv4_layer_type_from_ratio",
             "dsv4_indexer_topk", "dsv4_sparse_mla_decode", "dsv4_selftest_bounded_wait",
             "dsv4_selftest_key_dequant", "dsv4_compress_insert_pair", "dsv4_plan_set_indexer_format",
             "dsv4_sparse_mla_prefill", "dsv4_dequant_gather", "dsv4_combine_topk_swa_indices",
-            "dsv4_plan_set_kv_layout", "dsv4_inv_rope_fp8_quant"]
+            "dsv4_plan_set_kv_layout", "dsv4_inv_rope_fp8_quant", "dsv4_stream_gate"]
 GATHER_COMP, GATHER_SWA = 0, 1
 
 
@@ -127,6 +127,10 @@ class InvRopeQuantArgs(ctypes.Structure):
                 ("codes_dev", ctypes.c_void_p), ("scales_dev", ctypes.c_void_p), ("status_dev", ctypes.c_void_p)]
 
 
+class GateArgs(ctypes.Structure):
+    _fields_ = [("flags_dev", ctypes.c_void_p * 4), ("timeout_us", ctypes.c_int), ("status_dev", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -188,6 +192,8 @@ def lib():
     L.dsv4_plan_set_kv_layout.argtypes = [vp, ctypes.c_int]
     L.dsv4_inv_rope_fp8_quant.restype = st
     L.dsv4_inv_rope_fp8_quant.argtypes = [ctypes.POINTER(InvRopeQuantArgs), vp]
+    L.dsv4_stream_gate.restype = st
+    L.dsv4_stream_gate.argtypes = [ctypes.POINTER(GateArgs), vp]
     _lib = L
     return L
 
@@ -453,3 +459,20 @@ def inv_rope_fp8_quant(o, positions, cos_sin, codes, scales, status=None, stream
     a = InvRopeQuantArgs(int(o.shape[0]), int(o.shape[1]), _ptr(o), _ptr(positions), _ptr(cos_sin),
                          int(cos_sin.shape[0]), _ptr(codes), _ptr(scales), _ptr(status))
     _check(lib().dsv4_inv_rope_fp8_quant(ctypes.byref(a), _stream(stream)), "inv_rope_fp8_quant")
+
+
+def stream_gate(flags, status=None, timeout_us=0, stream=None):
+    """dsv4_stream_gate: wait until every flag (int32 CUDA tensors of one
+    element, up to 4) is nonzero, clear them, and let the next kernel on the
+    stream launch under programmatic dependent launch."""
+    flags = list(flags)
+    if not 1 <= len(flags) <= 4:
+        raise ValueError("1 to 4 flags")
+    a = GateArgs()
+    for i, f in enumerate(flags):
+        if f.dtype != torch.int32 or f.numel() != 1:
+            raise ValueError("a flag is one int32 element")
+        a.flags_dev[i] = _ptr(f)
+    a.timeout_us = int(timeout_us)
+    a.status_dev = _ptr(status)
+    _check(lib().dsv4_stream_gate(ctypes.byref(a), _stream(stream)), "stream_gate")

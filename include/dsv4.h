@@ -583,6 +583,34 @@ typedef struct dsv4_combine_args {
 } dsv4_combine_args;
 dsv4_status dsv4_combine_topk_swa_indices(const dsv4_combine_args* args, dsv4_stream_t stream);
 
+/* ---- pipelined input staging ------------------------------------------------- */
+
+/* Stream gate for a decode loop whose inputs arrive by host-to-device copies
+ * on another stream.  Not a step of the method: serving support around it.
+ * Launches one 32-thread CTA that waits (bounded) until every non-NULL
+ * flags_dev[i] is nonzero, clears those flags to 0 and then lets the next
+ * kernel on `stream` launch under programmatic dependent launch; the gate's
+ * grid completes only after the kernel before it on `stream` has completed.
+ * Usage: on the copy stream, copy a step's inputs, then write 1 into the
+ * step's flag (a 4-byte copy, stream-ordered after the data); on the compute
+ * stream, call the gate in front of the step's calls instead of waiting on an
+ * event.  An event wait between two kernels breaks their programmatic launch
+ * link; the gate keeps the link to the previous step's last kernel.  Only work
+ * ordered after the kernels that read what a flag guards may set it again
+ * (e.g. a copy stream waiting on an event recorded after those kernels).
+ * flags_dev: up to 4 int flags (4-byte aligned; NULL entries ignored, at
+ *   least one given).  timeout_us: bound of the wait (0: 2 s); a wait that
+ *   runs out sets DSV4_DEV_TIMEOUT in *status_dev, clears no flag and lets
+ *   the next kernel launch.
+ * Errors: DSV4_ERR_INVALID (NULL args, no flag, negative timeout),
+ * DSV4_ERR_SHAPE (a misaligned flag), DSV4_ERR_CUDA (launch). */
+typedef struct dsv4_gate_args {
+    int* flags_dev[4];
+    int timeout_us;
+    int* status_dev;
+} dsv4_gate_args;
+dsv4_status dsv4_stream_gate(const dsv4_gate_args* args, dsv4_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------------- */
 
 /* Launch one CTA that waits on an mbarrier nothing arrives at, bounded by

@@ -163,6 +163,18 @@ def test_indexer_rejects_misaligned_buffers_on_the_host():
     assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), ctypes.c_void_p(fake), ws_bytes, None) == B.ERR_SHAPE
 
 
+def test_stream_gate_validates_on_the_host():
+    lib = B.lib()
+    assert lib.dsv4_stream_gate(None, None) == B.ERR_INVALID
+    a = B.GateArgs()
+    assert lib.dsv4_stream_gate(ctypes.byref(a), None) == B.ERR_INVALID          # no flag
+    a.flags_dev[1] = (1 << 20) + 2
+    assert lib.dsv4_stream_gate(ctypes.byref(a), None) == B.ERR_SHAPE            # misaligned flag
+    a.flags_dev[1] = 1 << 20
+    a.timeout_us = -1
+    assert lib.dsv4_stream_gate(ctypes.byref(a), None) == B.ERR_INVALID
+
+
 def test_v4_layout_and_output_quant_validate_on_the_host():
     lib = B.lib()
     p = B.Plan(B.C4A, 8, 2, 32, 4096, idx_heads=8)
