@@ -70,7 +70,7 @@ WORKLOADS = {
 # capture of this workload (one launch, cold cache), with the sha256 of the
 # sources it was taken on; reported as null once they change.
 TRAFFIC_RECORD = {
-    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19091200 + 0, "src_sha": "ec59f41c9c3016e3"},
+    ("c4a_32k_b32", "sparse_mla"): {"bytes_per_launch": 19091200 + 0, "src_sha": "12a50ed09123f6b8"},
 }
 
 

@@ -223,6 +223,18 @@ __device__ __forceinline__ uint32_t ldg_stream_u8_if(const uint8_t* p, bool pred
     return v;
 }
 
+__device__ __forceinline__ uint32_t ldg_stream_u32_if(const uint8_t* p, bool pred, uint32_t dflt)
+{
+    uint32_t v;
+    asm volatile("{\n\t.reg .pred q;\n\t"
+                 "setp.ne.u32 q, %2, 0;\n\t"
+                 "mov.u32 %0, %3;\n\t"
+                 "@q ld.global.nc.L1::no_allocate.u32 %0, [%1];\n\t}"
+                 : "=&r"(v)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred)), "r"(dflt));
+    return v;
+}
+
 // L2 load of an int written by the grid before this one, or dflt
 __device__ __forceinline__ int ldcg_s32_if(const int* p, bool pred, int dflt)
 {
@@ -452,12 +464,16 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             };
             // raw data of one tile, loaded one tile ahead of its use: nope unit
-            // `lane` (16 codes; V4: lanes below 28) of rows pw + 8k with its
-            // scale byte, rope unit lane % 8 of rows pw + 8 (lane / 8) and
-            // pw + 8 (lane / 8 + 4).  ent_of(k): cache entry (page * 64 + row)
-            // of row pw + 8k, -1 for none (the row then reads as zeros).
+            // `lane` (16 codes; V4: lanes below 28) of rows pw + 8k, rope unit
+            // lane % 8 of rows pw + 8 (lane / 8) and pw + 8 (lane / 8 + 4), and
+            // the scales: the 576 rows' byte lane / 4 of rows pw + 8k, one load
+            // each; the V4 rows' bytes 4 (lane / 8) .. + 3 of row pw + 8 (lane % 8)
+            // on lanes 0-15 (each nope lane takes its byte by a shuffle when it
+            // converts; measured faster for V4, slower for the 576 rows).
+            // ent_of(k): cache entry (page * 64 + row) of row pw + 8k, -1 for
+            // none (the row then reads as zeros).
             uint4 rn[8];
-            uint32_t rs[8];
+            uint32_t rs[V4 ? 1 : 8];
             uint4 rr[2];
             auto fetch_rows = [&](const uint8_t* cache, auto&& ent_of) {
                 const bool nope_lane = lane < G::kNopeLanes;
@@ -466,8 +482,15 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const int e = ent_of(k);
                     const uint8_t* page = cache + static_cast<long long>(e >> 6) * G::kPageBytes;
                     rn[k] = ldg_stream_v4_if(page + (e & 63) * G::kRowBytes + lane * 16, e >= 0 && nope_lane);
-                    rs[k] = ldg_stream_u8_if(page + kPage * G::kRowBytes + (e & 63) * 8 + (lane >> 2),
-                                             e >= 0 && nope_lane, 127);
+                    if constexpr (!V4)
+                        rs[k] = ldg_stream_u8_if(page + kPage * G::kRowBytes + (e & 63) * 8 + (lane >> 2),
+                                                 e >= 0 && nope_lane, 127);
+                }
+                if constexpr (V4) {
+                    const int e = ent_of(lane & 7);
+                    rs[0] = ldg_stream_u32_if(cache + static_cast<long long>(e >> 6) * G::kPageBytes +
+                                                  kPage * G::kRowBytes + (e & 63) * 8 + 4 * ((lane >> 3) & 1),
+                                              e >= 0 && lane < 16, 0x7f7f7f7fu);
                 }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -490,12 +513,23 @@ mla_decode_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             auto convert = [&](uint8_t* kp) {
                 const int w0 = 2 * (lane & 3);
                 const int flip = (lane >> 2) & 1;
+                // scale byte lane / 4 of row pw + 8k (V4: byte lane / 4 % 4 of the
+                // word that lane k + 8 (lane / 16) loaded)
+                uint32_t sb[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if constexpr (V4)
+                        sb[k] = (__shfl_sync(0xffffffffu, rs[0], k + 8 * (lane >> 4)) >> (8 * ((lane >> 2) & 3))) &
+                                0xffu;
+                    else
+                        sb[k] = rs[k];
+                }
                 if (lane < G::kNopeLanes) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int r = pw + 8 * k;
                         uint4 lo, hi;
-                        dequant16(rn[k], rs[k], lo, hi);
+                        dequant16(rn[k], sb[k], lo, hi);
                         uint8_t* row = kp + (lane >> 2) * kTcKChunk + r * 128;
                         const uint4 first = flip ? hi : lo;
                         const uint4 second = flip ? lo : hi;
