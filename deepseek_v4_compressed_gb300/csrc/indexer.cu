@@ -5,6 +5,8 @@
 // talk write-up), with k_s = FP8 row * fp32 scale of the indexer cache, over
 // the causal slots s < ctx_len / 4; then the k largest per query ("Indexer,
 // C4A and C128A top-k", "DeepSeek V4 attention in vLLM").
+#include <cstddef>
+
 #include "dsv4_common.cuh"
 #include "plan.h"
 #include "tc_common.cuh"
@@ -82,18 +84,23 @@ struct CtkDecision {
 struct CtkScratch {
     uint64_t bar_mm;                        // every CTA's (min, max) has landed (bytes)
     uint64_t bar_h[2];                      // every CTA's histogram of the pass has landed, by pass parity
-    uint64_t bar_cnt;                       // every CTA's compaction counts have landed
     uint32_t mm_in[kCtkMaxCluster][2];      // (min, max) key of CTA q's slots, pushed by q
-    int cnt_in[kCtkMaxCluster][2];          // CTA q's keys above / at the threshold, pushed by q
-    int hin[2][kCtkMaxCluster][256];        // CTA q's digit histogram, by pass parity, pushed by q
-    int hist[2][256];                       // this CTA's histogram, by pass parity
+    int cnt_in[kCtkMaxCluster][2];          // CTA q's keys above / at the threshold, from its histograms
+    alignas(16) int hin[2][kCtkMaxCluster][256];   // CTA q's digit histogram, by pass parity, pushed by q
+                                                   // (16-byte st.async pushes)
+    alignas(16) int hist[2][256];                  // this CTA's histogram, by pass parity (read 16 B at a time)
     uint32_t mm[2];                         // this CTA's min, max
     CtkDecision dec;                        // the decisions, for the CTA's threads
     int scan[16];
 };
+static_assert(offsetof(CtkScratch, hin) % 16 == 0 && offsetof(CtkScratch, hist) % 16 == 0 &&
+                  offsetof(CtkScratch, mm_in) % 8 == 0,
+              "vector pushes and loads of the top-k scratch");
 constexpr int kIdxSmemFused = kIdxSmem + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
 constexpr int kIdxSmem4Fused = kIdxSmem4 + kCtkSlots * 4 + static_cast<int>(sizeof(CtkScratch));
 static_assert(kIdxSmem4Fused <= 232448, "shared memory budget");
+static_assert((kIdxSmem - 1024 + kCtkSlots * 4) % 16 == 0 && (kIdxSmem4 - 1024 + kCtkSlots * 4) % 16 == 0,
+              "the top-k scratch starts 16-byte aligned");
 
 // E4M3 byte of the E2M1 magnitude with index c (0, 0.5, 1, 1.5, 2, 3, 4, 6)
 // times 2^-k, k = 0..8: every such value is an E4M3 value (normal when its
@@ -280,6 +287,12 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
     int plo = 32;                                        // the bin is (key - base) >> plo == prefix >> plo
     uint32_t prefix = 0;
     int rem = k;
+    // every CTA holds every CTA's histograms: warp q + 1 (q < rank) sums CTA
+    // q's keys above each pass's threshold digit, and takes its count in the
+    // final threshold bin, so the compaction needs no count exchange
+    const int cq = warp - 1;
+    const bool counts_peer = cq >= 0 && cq < rank;
+    int gt_q = 0, eq_q = 0;
     for (int pass = 0;; ++pass) {
         const int p = pass & 1;
 #pragma unroll
@@ -304,9 +317,25 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
         if (S->dec.failed) return;
         prefix = S->dec.prefix;
         rem = S->dec.rem;
+        if (counts_peer) {
+            // hin[p] is rewritten only by pass p + 2, after this CTA's next push
+            const uint32_t dd = (prefix >> lo) & 255u;
+            int a = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t d = 8u * lane + u;
+                a += d > dd ? S->hin[p][cq][d] : 0;
+            }
+            gt_q += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(a));
+            if (S->dec.done) eq_q = S->hin[p][cq][dd];
+        }
         plo = lo;
         if (S->dec.done) break;
         lo = lo > 8 ? lo - 8 : 0;
+    }
+    if (counts_peer && lane == 0) {
+        S->cnt_in[cq][0] = gt_q;
+        S->cnt_in[cq][1] = eq_q;
     }
     // ordered compaction: keys above the threshold bin, and the first `rem`
     // in it (lowest slot first), at their positions in the whole row
@@ -319,18 +348,8 @@ __device__ void cluster_topk(const float* lg, int s0, int s1, int n_c, int k, in
         eqn += j < nv && d == thr;
     }
     int tot;
-    const int before = ctk_excl_scan((gtn << 16) | eqn, S->scan, tot);   // counts < 2^16
-    // (c) every CTA's counts, in every CTA
-    if (tid == 0) tc::mbar_arrive_expect_tx(tc::smem_u32(&S->bar_cnt), static_cast<uint32_t>(C * 8));
-    if (tid < C)
-        tc::st_async_u32x2(tc::map_to_rank(tc::smem_u32(&S->cnt_in[rank][0]), tid), static_cast<uint32_t>(tot >> 16),
-                           static_cast<uint32_t>(tot & 0xffff), tc::map_to_rank(tc::smem_u32(&S->bar_cnt), tid));
-    if (warp == 0) {
-        const bool ok = tc::mbar_wait_cluster(tc::smem_u32(&S->bar_cnt), 0, status);
-        if (lane == 0 && !ok) S->dec.failed = 1;
-    }
-    __syncthreads();
-    if (S->dec.failed) return;
+    const int before = ctk_excl_scan((gtn << 16) | eqn, S->scan, tot);   // counts < 2^16; its barriers
+                                                                          // also publish cnt_in
     int gpos = before >> 16, epos = before & 0xffff;
     for (int q = 0; q < rank; ++q) {
         gpos += S->cnt_in[q][0];
@@ -504,7 +523,6 @@ indexer_logits_tc(const __grid_constant__ CUtensorMap tm_cache, const __grid_con
                 tc::mbar_init(tc::smem_u32(&ctk->bar_mm), 1);
                 tc::mbar_init(tc::smem_u32(&ctk->bar_h[0]), 1);
                 tc::mbar_init(tc::smem_u32(&ctk->bar_h[1]), 1);
-                tc::mbar_init(tc::smem_u32(&ctk->bar_cnt), 1);
             }
             *abort_flag = 0;
             tc::fence_barrier_init();
@@ -1264,6 +1282,10 @@ __host__ __device__ constexpr size_t tkc_smem_bytes(int S)
 {
     return static_cast<size_t>(S) * 4 + static_cast<size_t>(kTkcWarps) * tkc_list_cap(S) * 2 + sizeof(TkcScratch);
 }
+static_assert(offsetof(TkcScratch, hin) % 16 == 0 && offsetof(TkcScratch, rs_in) % 16 == 0 &&
+                  offsetof(TkcScratch, ag_in) % 16 == 0 && offsetof(TkcScratch, seg) % 16 == 0 &&
+                  offsetof(TkcScratch, hist) % 16 == 0 && offsetof(TkcScratch, mm_in) % 8 == 0,
+              "vector pushes and loads of the long-row top-k scratch");
 static_assert(tkc_smem_bytes(kTkcSlots) <= 232448 && tkc_smem_bytes(16384) <= tkc_smem_bytes(kTkcSlots),
               "the largest S sets the shared-memory attribute");
 
