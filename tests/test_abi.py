@@ -106,15 +106,16 @@ def test_entry_points_reject_null_arguments_without_gpu():
     # (type, heads, batch, topk, max_ctx, idx_heads) -> plan choices on 152 SMs
     ((B.C4A, 64, 32, 512, 32768, 64), dict(idx_ctas_per_seq=4, launches_indexer=1, mla_splits=4, mla_head_groups=1)),
     ((B.C4A, 128, 4, 2048, 1048576, 64), dict(idx_ctas_per_seq=38, launches_indexer=2, mla_splits=8, mla_head_groups=2)),
-    ((B.C4A, 64, 16, 512, 65536, 64), dict(idx_ctas_per_seq=9, launches_indexer=2, mla_splits=8, mla_head_groups=1)),
+    ((B.C4A, 64, 16, 512, 65536, 64), dict(idx_ctas_per_seq=9, launches_indexer=2, mla_splits=4, mla_head_groups=1)),
     ((B.C128A, 64, 64, 512, 131072, 64), dict(idx_ctas_per_seq=0, launches_indexer=0, mla_splits=2, mla_head_groups=1)),
-    ((B.SWAONLY, 64, 16, 0, 65536, 64), dict(launches_indexer=0, mla_splits=8, launches_mla=1)),
+    ((B.SWAONLY, 64, 16, 0, 65536, 64), dict(launches_indexer=0, mla_splits=4, launches_mla=1)),
 ])
 def test_plan_choices_on_152_sms(args, expect):
     # indexer: floor(SMs / batch) CTAs per sequence, the top-k inside the logits
     # launch when they fit one cluster (<= 8 CTAs of <= 16 tiles), else a second
-    # launch; attention: the largest cluster of 1, 2, 4, 8 CTAs per (sequence,
-    # 64-head group) that keeps every CTA on its own SM
+    # launch; attention: the largest cluster of 1, 2, 4 CTAs per (sequence,
+    # 64-head group) that keeps every CTA on its own SM, 8 when 4 would leave
+    # a CTA more than 256 keys (the 1M plan)
     import torch
     if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
         pytest.skip("the expected choices are for 152 SMs")
