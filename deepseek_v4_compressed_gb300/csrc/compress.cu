@@ -13,7 +13,16 @@
 // window of a boundary token is read from the per-sequence ring (and, in a
 // multi-token call, from this call's own inputs).  Work per entry is tiny and
 // bound by the state reads; it runs on the CUDA cores, no contraction.
+//
+// Ratio 128 (the single-stream compressor of c128a layers): a boundary pools
+// 128 ring rows, which one CTA per token reads only as fast as its one SM
+// pulls them from L2.  There a token takes a cluster of G CTAs (3 for d = 576,
+// 4 for d = 512), each owning whole 64-channel warps of the d/2 threads; the
+// RMSNorm warp totals go to every CTA of the cluster and are added in the
+// same ascending warp order, so the bytes are those of one CTA.
 #include "dsv4_common.cuh"
+#include "tc_common.cuh"
+#include "tmap.h"
 
 namespace dsv4 {
 
@@ -44,29 +53,51 @@ struct CompressParams {
 // then the warps' totals added to 0 in ascending warp order.  Double addition
 // is commutative, so every lane of a warp holds the same total, and the
 // result is the same bits wherever the order is followed.
-template <int NT>
-__device__ __forceinline__ double block_sum_d(double v, double* red)
+// NWT warps in all, NWC of them in this CTA (rank `rank` of a cluster of G
+// CTAs, global warp rank * NWC + local warp); with G > 1 each warp's total
+// is stored into every CTA of the cluster before a cluster barrier.
+template <int NWT, int NWC, int G>
+__device__ __forceinline__ double block_sum_d(double v, double* red, int rank)
 {
-    constexpr int NW = NT / 32;
     v = warp_sum_d(v);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) red[w] = v;
-    __syncthreads();
+    const int gw = rank * NWC + static_cast<int>(threadIdx.x >> 5);
+    if ((threadIdx.x & 31) == 0) {
+        if constexpr (G == 1) {
+            red[gw] = v;
+        } else {
+            const uint32_t a = tc::smem_u32(&red[gw]);
+#pragma unroll
+            for (int q = 0; q < G; ++q)
+                asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(tc::map_to_rank(a, q)), "d"(v) : "memory");
+        }
+    }
+    if constexpr (G == 1)
+        __syncthreads();
+    else
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     double s = 0.0;
 #pragma unroll
-    for (int i = 0; i < NW; ++i) s += red[i];
+    for (int i = 0; i < NWT; ++i) s += red[i];
     return s;
+}
+
+// CTAs per token of the compress kernel: the ratio-128 main streams split
+// their 64-channel warps over a cluster (see the top of this file).
+__host__ __device__ constexpr int compress_split(int D, int RATIO)
+{
+    return RATIO != 128 ? 1 : (D == 576 ? 3 : (D == 512 ? 4 : 1));
 }
 
 // Quantise the normalised, rotated vector (this thread's channels c0, c0+1)
 // into a main-cache entry: E4M3 nope with one UE8M0 byte per 64 dims, bf16
 // rope; with 448 nope dims the eighth scale byte is a zero pad.  Called by
-// all (NOPE + 64) / 2 threads.
+// the (NOPE + 64) / 2 threads of the entry (one CTA, or the CTAs of a
+// cluster): the 64-channel block and the lane follow from c0.
 template <int NOPE>
 __device__ __forceinline__ void store_mla_entry(float z0, float z1, int c0, uint8_t* data_row,
                                                 uint8_t* scale_row)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = c0 >> 6, lane = (c0 >> 1) & 31;
     if (NOPE < 512 && warp == NOPE / 64 && lane == 0) scale_row[7] = 0;
     if (warp < NOPE / 64) {
         const float amax = warp_max(fmaxf(fabsf(z0), fabsf(z1)));
@@ -151,6 +182,15 @@ __device__ __forceinline__ void store_idx_fp4_entry(float z0, float z1, int c0, 
     if ((threadIdx.x & 15) == 0) scale_row[c0 >> 5] = static_cast<uint8_t>(e + 127);
 }
 
+// Bring [p, p + bytes) into L2 without waiting (p 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %0;\n\t"
+                 "cp.async.bulk.prefetch.L2.global [g], %1;\n\t}" ::"l"(p), "r"(bytes)
+                 : "memory");
+}
+
 // Resolve the page of logical slot j of sequence seq; nullptr (and a status
 // bit) when the table entry is out of range.
 template <int KIND>
@@ -189,21 +229,23 @@ __device__ __forceinline__ void token_values(const CompressParams& P, int t, int
 // Compress kernel.  FUSED: each sequence has at most one token in the call;
 // the token's state row is written here too.  Otherwise (multi-token calls)
 // window rows inside the call come from the inputs and the ring is written
-// by state_write_kernel afterwards.
-template <int D, int RATIO, int KIND, bool FUSED>
-__device__ __forceinline__ void compress_token(const CompressParams& P, const int t)
+// by state_write_kernel afterwards.  G CTAs per token (a cluster; this one is
+// rank `rank`, owning channels [rank d/G, (rank + 1) d/G)).
+template <int D, int RATIO, int KIND, bool FUSED, int G = 1>
+__device__ __forceinline__ void compress_token(const CompressParams& P, const int t, const int rank = 0)
 {
     constexpr bool IDX = KIND == DSV4_CACHE_IDX || KIND == DSV4_CACHE_IDX_FP4;
     constexpr int COFF = (RATIO == 4) ? 2 : 1;
     constexpr int W = COFF * RATIO;
     constexpr int ROW = 2 * COFF * D;
-    constexpr int NT = D / 2;
+    constexpr int NT = D / 2 / G;                      // threads of this CTA
     constexpr int NOPE = D - kRope;
     static_assert(D == kind_dim<KIND>(), "stream dimension of the cache kind");
-    __shared__ double red_d[NT / 32];
+    static_assert(NT % 32 == 0 && (G == 1 || !IDX), "a CTA owns whole 64-channel warps");
+    __shared__ double red_d[D / 64];
     __shared__ float red_f[2];
 
-    const int c0 = 2 * threadIdx.x;
+    const int c0 = 2 * (static_cast<int>(threadIdx.x) + rank * NT);
     const int seq = P.seqs[t];
     const int p = P.positions[t];
     if (seq < 0 || seq >= P.num_seqs || p < 0) {
@@ -256,6 +298,13 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
     // two-pass ones: max, then sums in ascending s.
     constexpr int CH = W < 12 ? W : 12;
     const int s0 = (p - W + 1) < 0 ? 0 : p - W + 1;
+    if constexpr (W >= 64) {
+        // a long window: all of its ring rows into L2 at once (one bulk
+        // prefetch per row, the rows dealt round-robin over the cluster), so
+        // the two passes' chunks wait on L2, not HBM
+        for (int s = s0 + rank + G * static_cast<int>(threadIdx.x); s < p; s += G * NT)
+            prefetch_l2_bulk(ring + static_cast<long long>(s % W) * ROW, static_cast<uint32_t>(ROW * sizeof(float)));
+    }
     float m0 = -INFINITY, m1 = -INFINITY;
     for (int sb = s0; sb <= p; sb += CH) {
         float2 kv[CH], sc[CH];
@@ -291,7 +340,8 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
     const float y0 = __fdiv_rn(n0, d0), y1 = __fdiv_rn(n1, d1);
 
     // RMSNorm: mean square accumulated in double in the fixed order, rounded once.
-    const double ss = block_sum_d<NT>(static_cast<double>(y0) * y0 + static_cast<double>(y1) * y1, red_d);
+    const double ss =
+        block_sum_d<D / 64, NT / 32, G>(static_cast<double>(y0) * y0 + static_cast<double>(y1) * y1, red_d, rank);
     const float ms = __double2float_rn(ss / static_cast<double>(D));
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, P.eps)));
     const float2 w = *reinterpret_cast<const float2*>(P.rms_w + c0);
@@ -339,10 +389,15 @@ __device__ __forceinline__ void compress_token(const CompressParams& P, const in
 // launch) may be scheduled at once; it waits for this grid before reading
 // what it writes.
 template <int D, int RATIO, int KIND, bool FUSED>
-__global__ void __launch_bounds__(D / 2) compress_kernel(CompressParams P)
+__global__ void __launch_bounds__(D / 2 / compress_split(D, RATIO)) compress_kernel(CompressParams P)
 {
+    constexpr int G = compress_split(D, RATIO);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    compress_token<D, RATIO, KIND, FUSED>(P, blockIdx.x);
+    // launched behind the previous kernel of the stream (clusters: under
+    // programmatic dependent launch): touch nothing before it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // G > 1: clusters of G consecutive blocks, one token each
+    compress_token<D, RATIO, KIND, FUSED, G>(P, static_cast<int>(blockIdx.x) / G, static_cast<int>(blockIdx.x) % G);
 }
 
 // The main (d = 576, or 512 for the V4 row) and indexer (d = 128) streams of
@@ -429,16 +484,44 @@ __global__ void __launch_bounds__(D / 2) insert_rows_kernel(const float* rows, c
         store_mla_entry<kNope>(z.x, z.y, c0, page + r * kMlaData, page + kPage * kMlaData + r * 8);
 }
 
+template <int D, int RATIO, int KIND, bool FUSED>
+static cudaError_t launch_compress_kernel(const CompressParams& P, cudaStream_t st)
+{
+    constexpr int G = compress_split(D, RATIO);
+    if (G == 1) {
+        compress_kernel<D, RATIO, KIND, FUSED><<<P.num_tokens, D / 2, 0, st>>>(P);
+        return cudaGetLastError();
+    }
+    if (static_cast<long long>(P.num_tokens) * G > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(P.num_tokens * G), 1, 1);
+    cfg.blockDim = dim3(D / 2 / G, 1, 1);
+    cfg.stream = st;
+    // the small CTAs (d/2/G threads) fit beside an attention CTA, so when the
+    // grid is at most one CTA per SM they launch while the previous attention
+    // finishes (programmatic dependent launch; the kernel waits for it before
+    // touching memory).  A larger grid keeps the plain launch: at 64 tokens
+    // (192 CTAs) the early launch made a C128A 128K batch-64 step 1.1 us
+    // slower, at 16 tokens it made the c128a layers 5% faster.
+    const bool early = static_cast<long long>(P.num_tokens) * G <= sm_count();
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, compress_kernel<D, RATIO, KIND, FUSED>, P);
+}
+
 template <int D, int RATIO, int KIND>
 static cudaError_t launch_compress(const CompressParams& P, bool fused, cudaStream_t st)
 {
     if (P.num_tokens == 0) return cudaSuccess;
-    if (fused) {
-        compress_kernel<D, RATIO, KIND, true><<<P.num_tokens, D / 2, 0, st>>>(P);
-        return cudaGetLastError();
-    }
-    compress_kernel<D, RATIO, KIND, false><<<P.num_tokens, D / 2, 0, st>>>(P);
-    cudaError_t e = cudaGetLastError();
+    if (fused) return launch_compress_kernel<D, RATIO, KIND, true>(P, st);
+    cudaError_t e = launch_compress_kernel<D, RATIO, KIND, false>(P, st);
     if (e != cudaSuccess) return e;
     state_write_kernel<D, RATIO><<<P.num_tokens, D / 2, 0, st>>>(P);
     return cudaGetLastError();
@@ -468,7 +551,8 @@ static dsv4_status compress_params(const dsv4_compress_args* a, CompressParams& 
     const int coff = (a->ratio == 4) ? 2 : 1;
     if (a->num_tokens > 0 && (a->kv_score_stride < 2LL * coff * d || (a->kv_score_stride & 1)))
         return DSV4_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(a->kv_score_dev) & 3) || (reinterpret_cast<uintptr_t>(a->cache_dev) & 15))
+    if ((reinterpret_cast<uintptr_t>(a->kv_score_dev) & 3) || (reinterpret_cast<uintptr_t>(a->cache_dev) & 15) ||
+        (reinterpret_cast<uintptr_t>(a->state_dev) & 15))
         return DSV4_ERR_SHAPE;
     P.kv_score = static_cast<const uint16_t*>(a->kv_score_dev);
     P.kv_stride = a->kv_score_stride;

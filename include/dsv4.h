@@ -279,6 +279,7 @@ dsv4_status dsv4_plan_set_kv_layout(dsv4_plan* plan, dsv4_kv_layout layout);
  * state_dev: fp32 [num_seqs][coff*r][2*coff*d], a per-sequence ring: the row
  *   of position p lives at p % (coff*r).  The caller zero-fills it once; the
  *   library keeps it (rows of positions before a call are read from it).
+ *   16-byte aligned, as is cache_dev (else DSV4_ERR_SHAPE).
  * cache_dev: paged cache of `kind`, num_pages pages; block_table_dev: int32
  *   [num_seqs][bt_stride], bt_stride >= pages needed by the largest slot.
  * one_token_per_seq: 1 when every sequence has at most one token in this

@@ -14,13 +14,15 @@ The pooled vector is produced exactly by a ratio-4 compressor at its first
 boundary (position 3): the window is tokens 0..3 of the second block, all
 scores are 0 (equal softmax weights, exp(0) = 1), so y = (kv_0 + kv_1 +
 kv_2 + kv_3) / 4.  A 16-bit integer n times 2^e is kv_0 + kv_1 with both bf16
-(its high and low 8 bits), so y0 and y1 are exact.
+(its high and low 8 bits), so y0 and y1 are exact.  A ratio-128 stream gets
+the same vector at position 127 from 128 tokens (token_rows_c128).
 """
 import numpy as np
 
 # found by a seeded search over 16-bit pairs (d, n0, n1, exponent, small)
 CASES = {
     128: (48008, 38056, -15, 2.0 ** -27),
+    512: (39688, 37528, -15, 2.0 ** -27),
     576: (50580, 33216, -15, 2.0 ** -27),
 }
 
@@ -69,6 +71,22 @@ def token_rows(d):
     kv[0, 2:] = np.float32(4 * small)
     rows = np.zeros((4, 4 * d), np.uint16)
     rows[:, d:2 * d] = bf16_bits_exact(kv)
+    return rows
+
+
+def token_rows_c128(d):
+    """kv_score rows (bf16 bits) of tokens 0..127 for a ratio-128 stream of dim
+    d, [kv | score]: at its first boundary (position 127) the window is all
+    128 tokens with scores 0, so y = (sum of kv) / 128 with the same two-row
+    split of n0, n1 as the ratio-4 rows (every sum exact)."""
+    n0, n1, e, small = CASES[d]
+    kv = np.zeros((128, d), np.float32)
+    for c, n in ((0, n0), (1, n1)):
+        kv[0, c] = np.float32((n & 0xFF00) * 2.0 ** e * 128)
+        kv[1, c] = np.float32((n & 0x00FF) * 2.0 ** e * 128)
+    kv[0, 2:] = np.float32(128 * small)
+    rows = np.zeros((128, 2 * d), np.uint16)
+    rows[:, :d] = bf16_bits_exact(kv)
     return rows
 
 

@@ -164,6 +164,21 @@ def test_indexer_rejects_misaligned_buffers_on_the_host():
     assert lib.dsv4_indexer_topk(p.handle, ctypes.byref(ia), ctypes.c_void_p(fake), ws_bytes, None) == B.ERR_SHAPE
 
 
+def test_compress_rejects_a_misaligned_state_on_the_host():
+    """The ring state is read by 16-byte bulk L2 prefetches at long windows:
+    a state pointer off 16 bytes is refused before any launch."""
+    lib = B.lib()
+    a = B.CompressArgs()
+    fake = 1 << 20
+    a.kind, a.ratio, a.num_tokens, a.num_seqs, a.one_token_per_seq = B.CACHE_MLA, 128, 1, 1, 1
+    for f in ("kv_score_dev", "positions_dev", "seq_dev", "ape_dev", "rms_weight_dev", "cos_sin_dev", "cache_dev",
+              "block_table_dev"):
+        setattr(a, f, fake)
+    a.kv_score_stride, a.max_pos, a.num_pages, a.bt_stride = 2 * 576, 256, 1, 1
+    a.state_dev = fake + 8
+    assert lib.dsv4_compress_insert(ctypes.byref(a), None) == B.ERR_SHAPE
+
+
 def test_stream_gate_validates_on_the_host():
     lib = B.lib()
     assert lib.dsv4_stream_gate(None, None) == B.ERR_INVALID

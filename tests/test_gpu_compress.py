@@ -244,3 +244,26 @@ def test_rmsnorm_order_sensitive_vector_bytes_equal(kind, d):
     for chunks in (None, [[4]]):
         got = run_gpu_streams(kind, 4, [(ks, ape, w)], chunks, cs)
         assert_bytes_equal(got[0], want, "order-sensitive d=%d chunks=%s" % (d, chunks))
+
+
+
+@pytest.mark.parametrize("kind,d", [(B.CACHE_MLA, 576), (B.CACHE_V4, 512)])
+def test_rmsnorm_order_sensitive_vector_bytes_equal_ratio128(kind, d):
+    """The same order-sensitive vector through a ratio-128 stream, whose
+    boundary spreads a token's 64-channel warps over a cluster of CTAs (the
+    warp totals exchanged between them): the cache bytes equal the oracle's,
+    token by token and in one multi-token call."""
+    from _rms_case import ascending_sum, butterfly_sum, mean_square_pair, pooled_vector, token_rows_c128
+    y = pooled_vector(d)
+    assert ascending_sum(y) != butterfly_sum(y)
+    ms_asc, ms_tree = mean_square_pair(d)
+    assert ms_asc != ms_tree
+    ks = token_rows_c128(d)
+    ape = np.zeros((128, d), np.float32)
+    w = np.ones(d, np.float32)
+    cs = oracle.rope_table(128, 64)
+    want = oracle_entries(kind, 128, ks, ape, w, cs)
+    assert want[0].shape[0] == 1
+    for chunks in (None, [[128]]):
+        got = run_gpu_streams(kind, 128, [(ks, ape, w)], chunks, cs)
+        assert_bytes_equal(got[0], want, "order-sensitive ratio 128 d=%d chunks=%s" % (d, chunks))
