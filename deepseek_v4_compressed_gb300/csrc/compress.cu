@@ -5,7 +5,8 @@
 // ratio 4 vs 128" of "DeepSeek V4 attention in vLLM", and sections 5.1, 5.2,
 // 6.3 of "From MLA to CSA + HCA".
 //
-// One CTA per token, d/2 threads, thread i owns channels 2i and 2i+1
+// One CTA per token (ratio 128: a cluster, below), d/2 threads, thread i owns
+// channels 2i and 2i+1
 // (main cache d = 576: 288 threads = 9 warps, warp w < 8 owns nope block w of
 // 64 dims, warp 8 the rope dims; V4-native main cache d = 512: 8 warps, warps
 // 0-6 the 448 nope dims, warp 7 the rope dims; indexer d = 128: 64 threads).  The per-token
